@@ -1,0 +1,16 @@
+"""Double-precision CPU oracle for causal MHA/GQA attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this
+package: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` use it, to check and to time the CUDA library against a
+plain, slow, obviously correct restatement of the method.
+"""
+from .attention import (  # noqa: F401
+    split_qkv,
+    rope_cos_sin,
+    rope_rotate,
+    rope_rotate_transpose,
+    attention_forward,
+    attention_backward,
+    attention_sampled,
+)

@@ -1,0 +1,60 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case copies ``oracle/`` to a temporary directory, plants one mistake in
+the copy (a flipped sign, a wrong index, a dropped term, a transposed
+operand), and runs the pin suite against the copy in a subprocess.  The pin
+suite must fail for every planted mistake.  Nothing here touches the CUDA
+path.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "rope_rotates_backwards": ("rot[k + half, k] = -1.0", "rot[k + half, k] = 1.0"),
+    "rope_adjoint_not_transposed": ("(g * sin) @ rot.T", "(g * sin) @ rot"),
+    "rope_frequency_exponent": ("-2.0 * i * np.log(float(theta)) / hd",
+                                "-1.0 * i * np.log(float(theta)) / hd"),
+    "gqa_head_mapping_modulo": ("kh = h // grp\n            P, lse[b, h]",
+                                "kh = h % (NH // grp)\n            P, lse[b, h]"),
+    "mask_excludes_diagonal": ("np.arange(T)[None, :] <= rows[:, None]",
+                               "np.arange(T)[None, :] < rows[:, None]"),
+    "mask_anticausal": ("np.arange(T)[None, :] <= rows[:, None]",
+                        "np.arange(T)[None, :] >= rows[:, None]"),
+    "missing_score_scale": ("S = scale * (q @ k.T)", "S = (q @ k.T)"),
+    "lse_base2": ("return E / l[:, None], m + np.log(l)", "return E / l[:, None], m + np.log2(l)"),
+    "dS_drops_D": ("dS = P * (dP - D[:, None])", "dS = P * dP"),
+    "dk_transposed_operand": ("dk[b, :, kh] += scale * (dS.T @ q)", "dk[b, :, kh] += scale * (dS @ q)"),
+    "dq_missing_scale": ("dq[b, :, h] = scale * (dS @ k)", "dq[b, :, h] = (dS @ k)"),
+    "dv_not_summed_over_group": ("dv[b, :, kh] += P.T @ dO", "dv[b, :, kh] = P.T @ dO"),
+    "v_column_offset": ("V = x[:, :, C + NKV * hd:]", "V = x[:, :, C:C + NKV * hd]"),
+    "dk_not_unrotated": ("        dk = rope_rotate_transpose(dk, rope_theta)\n", ""),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src_dir = os.path.join(ROOT, "oracle")
+    dst_dir = tmp_path / "oracle"
+    shutil.copytree(src_dir, dst_dir, ignore=shutil.ignore_patterns("__pycache__"))
+    path = dst_dir / "attention.py"
+    text = path.read_text()
+    assert text.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path.write_text(text.replace(old, new))
+    mark = tmp_path / "imported.mark"
+    init = dst_dir / "__init__.py"
+    init.write_text(init.read_text() + "\nopen(%r, 'w').write('mutant')\n" % str(mark))
+    env = dict(os.environ)
+    env["PYTHONPATH"] = os.pathsep.join([str(tmp_path), ROOT, env.get("PYTHONPATH", "")])
+    res = subprocess.run(
+        [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+         "--rootdir", str(tmp_path), os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+        cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=600)
+    assert mark.exists(), "the pin suite did not import the mutant oracle"
+    assert res.returncode != 0, f"pins did not catch mutation {name}:\n{res.stdout[-2000:]}"
