@@ -1,0 +1,177 @@
+"""Python binding of the C ABI in ``include/attn_gb300.h`` (ctypes).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library.  PyTorch supplies device memory and streams.  If the shared library
+has not been built this module raises on first use; there is no fallback.
+
+The entry points keep the C names and argument order:
+
+    attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, stream=None)
+    attn_bwd_workspace_bytes(B, T, C, NH, NKV, dtype)
+    attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
+             workspace, workspace_bytes, stream=None)
+
+Tensor arguments may be torch tensors (their data pointers are passed) or
+raw integer addresses.  ``stream`` defaults to PyTorch's current stream.
+A non-zero status raises AttnError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+DTYPE_F32 = 0
+DTYPE_TF32 = 1
+DTYPE_BF16 = 2
+
+_STATUS_NAMES = {
+    0: "ATTN_OK", -1: "ATTN_ERR_NULL_POINTER", -2: "ATTN_ERR_BAD_SHAPE", -3: "ATTN_ERR_UNSUPPORTED",
+    -4: "ATTN_ERR_MISALIGNED", -5: "ATTN_ERR_WORKSPACE", -6: "ATTN_ERR_CUDA",
+    -7: "ATTN_ERR_DEVICE_TIMEOUT", -8: "ATTN_ERR_BAD_ARGUMENT",
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS_NAMES.get(status, status)} ({attn_strerror(status)})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"CUDA attention library not found at {LIB_PATH}; build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.attn_bwd_workspace_bytes.restype = sz
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_strerror.argtypes = [i]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_device_status.argtypes = [ctypes.POINTER(i), i]
+    lib.attn_device_status.restype = i
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(i)]
+    lib.attn_selftest_wait_timeout.restype = i
+    lib.attn_abi_version.argtypes = []
+    lib.attn_abi_version.restype = i
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if hasattr(x, "is_contiguous") and not x.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def attn_strerror(status: int) -> str:
+    return load().attn_strerror(int(status)).decode()
+
+
+def attn_abi_version() -> int:
+    return load().attn_abi_version()
+
+
+def attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, stream=None) -> None:
+    st = load().attn_fwd(_ptr(out), _ptr(lse), _ptr(qkv), B, T, C, NH, NKV, float(rope_theta), int(dtype),
+                         _stream(stream))
+    _check(st, "attn_fwd")
+
+
+def attn_bwd_workspace_bytes(B, T, C, NH, NKV, dtype) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, T, C, NH, NKV, int(dtype)))
+
+
+def attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, workspace, workspace_bytes,
+             stream=None) -> None:
+    st = load().attn_bwd(_ptr(dqkv), _ptr(qkv), _ptr(out), _ptr(dout), _ptr(lse), B, T, C, NH, NKV,
+                         float(rope_theta), int(dtype), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "attn_bwd")
+
+
+def attn_device_status(reset: bool = False) -> int:
+    v = ctypes.c_int(0)
+    _check(load().attn_device_status(ctypes.byref(v), 1 if reset else 0), "attn_device_status")
+    return v.value
+
+
+def attn_selftest_wait_timeout(limit_ns: int) -> int:
+    v = ctypes.c_int(0)
+    _check(load().attn_selftest_wait_timeout(int(limit_ns), ctypes.byref(v)), "attn_selftest_wait_timeout")
+    return v.value
+
+
+# ---------------------------------------------------------------------------
+# Convenience wrappers: allocate outputs with PyTorch, then call the C ABI.
+# ---------------------------------------------------------------------------
+def dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported tensor dtype {t.dtype}")
+
+
+def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None):
+    """out, lse = attention forward of packed qkv [B, T, (NH+2*NKV)*hd]."""
+    import torch
+    B, T, W = qkv.shape
+    hd = W // (NH + 2 * NKV)
+    C = NH * hd
+    out = torch.empty((B, T, C), dtype=qkv.dtype, device=qkv.device)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=qkv.device)
+    attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype_code(qkv) if dtype is None else dtype, stream)
+    return out, lse
+
+
+def backward(qkv, out, dout, lse, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None,
+             workspace=None):
+    """dqkv = attention backward; allocates the workspace unless one is given."""
+    import torch
+    B, T, W = qkv.shape
+    C = out.shape[2]
+    code = dtype_code(qkv) if dtype is None else dtype
+    nbytes = attn_bwd_workspace_bytes(B, T, C, NH, NKV, code)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
+    dqkv = torch.empty_like(qkv)
+    attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, code, workspace, workspace.numel(), stream)
+    return dqkv

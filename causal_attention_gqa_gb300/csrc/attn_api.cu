@@ -1,0 +1,281 @@
+// C ABI of the attention library (declared in include/attn_gb300.h).
+//
+// Host-side argument validation, TMA tensor-map encoding, workspace carving
+// and kernel dispatch.  Every entry point validates before it enqueues
+// anything; nothing here allocates device memory or synchronises (except the
+// explicitly synchronous status / self-test calls).
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn_gb300.h"
+#include "attn_common.cuh"
+#include "attn_kernels.h"
+#include "attn_ptx.cuh"
+
+namespace attn {
+namespace {
+
+__device__ int g_status;           // first device-side error since the last reset
+__device__ int g_selftest_status;  // result of attn_selftest_wait_timeout
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+
+int* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map over a row-major [B, T, width] array, box {64, 128, 1},
+// 128-byte swizzle; rows past T read as zeros.
+bool make_tmap(CUtensorMap* m, const void* base, int width, int T, int B) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * (cuuint64_t)T};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtype, Geometry* g) {
+  if (B < 1 || T < 1 || C < 1 || NH < 1 || NKV < 1) return ATTN_ERR_BAD_SHAPE;
+  if (C % NH != 0 || NH % NKV != 0) return ATTN_ERR_BAD_SHAPE;
+  if (!std::isfinite(rope_theta)) return ATTN_ERR_BAD_ARGUMENT;
+  const int hd = C / NH;
+  const bool rope = rope_theta > 0.f;
+  if (rope && hd % 2 != 0) return ATTN_ERR_BAD_SHAPE;
+  const long long W = (long long)(NH + 2 * NKV) * hd;
+  if ((long long)B * T > INT_MAX / 8 || (long long)B * T * NH > INT_MAX || W > INT_MAX / 4 ||
+      (long long)T > (1LL << 24))
+    return ATTN_ERR_BAD_SHAPE;
+  switch (dtype) {
+    case ATTN_DTYPE_F32:
+      if (hd > 128) return ATTN_ERR_UNSUPPORTED;
+      break;
+    case ATTN_DTYPE_BF16:
+      if (hd != 64 && hd != 128) return ATTN_ERR_UNSUPPORTED;
+      if ((long long)((T + 127) / 128) * B * NH > INT_MAX) return ATTN_ERR_BAD_SHAPE;
+      break;
+    case ATTN_DTYPE_TF32:
+      return ATTN_ERR_UNSUPPORTED;
+    default:
+      return ATTN_ERR_BAD_ARGUMENT;
+  }
+  g->B = B;
+  g->T = T;
+  g->C = C;
+  g->NH = NH;
+  g->NKV = NKV;
+  g->hd = hd;
+  g->grp = NH / NKV;
+  g->W = (int)W;
+  g->scale = (float)(1.0 / std::sqrt((double)hd));
+  g->rope_theta = rope ? rope_theta : 0.f;
+  return ATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes(const Geometry& g, int dtype) {
+  size_t bytes = align256((size_t)g.B * g.NH * g.T * sizeof(float));
+  if (dtype == ATTN_DTYPE_BF16) bytes += align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2);
+  return bytes;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// One block waits on an mbarrier nobody arrives on; the bounded wait must
+// expire, record the timeout and let the kernel exit.
+__global__ void wait_timeout_selftest_kernel(int* result, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = ptx::mbar_wait(ptx::smem_u32(&bar), 0, &abort_flag, limit_ns);
+  if (!ok && threadIdx.x == 0) record_status(result, kErrDeviceTimeout);
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_abi_version(void) { return 1; }
+
+extern "C" const char* attn_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case ATTN_ERR_BAD_SHAPE: return "invalid shape (B,T,C,NH,NKV; C%NH, NH%NKV, odd head size with RoPE, or size limits)";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported (dtype, head size) combination";
+    case ATTN_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than attn_bwd_workspace_bytes()";
+    case ATTN_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait expired";
+    case ATTN_ERR_BAD_ARGUMENT: return "invalid argument";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV,
+                        float rope_theta, int dtype, void* stream) {
+  Geometry g;
+  int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
+  if (st != ATTN_OK) return st;
+  if (!out || !lse || !qkv) return ATTN_ERR_NULL_POINTER;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_DTYPE_F32) {
+    if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(qkv)) & 3u)
+      return ATTN_ERR_MISALIGNED;
+    SimtArgs a{};
+    a.g = g;
+    a.forward = true;
+    a.out = out;
+    a.lse = lse;
+    a.qkv = qkv;
+    return from_cuda(simt_launch(a, s));
+  }
+  if (!aligned16(out) || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+  Tc05FwdArgs a{};
+  a.g = g;
+  a.out = out;
+  a.lse = lse;
+  a.status = status_word();
+  if (!a.status) return ATTN_ERR_CUDA;
+  if (!make_tmap(&a.tm_qkv, qkv, g.W, g.T, g.B)) return ATTN_ERR_CUDA;
+  return from_cuda(tc05_fwd_launch(a, s));
+}
+
+extern "C" size_t attn_bwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype) {
+  Geometry g;
+  if (check_shape(B, T, C, NH, NKV, 0.f, dtype, &g) != ATTN_OK) return 0;
+  return workspace_bytes(g, dtype);
+}
+
+extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* dout, const float* lse, int B,
+                        int T, int C, int NH, int NKV, float rope_theta, int dtype, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  Geometry g;
+  int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
+  if (st != ATTN_OK) return st;
+  if (!dqkv || !qkv || !out || !dout || !lse) return ATTN_ERR_NULL_POINTER;
+  if (!workspace || ws_bytes < workspace_bytes(g, dtype)) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* Drow = static_cast<float*>(workspace);
+  if (dtype == ATTN_DTYPE_F32) {
+    if ((reinterpret_cast<uintptr_t>(dqkv) | reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(out) |
+         reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(lse)) & 3u)
+      return ATTN_ERR_MISALIGNED;
+    cudaError_t e = launch_row_dot(Drow, out, dout, g, false, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    SimtArgs a{};
+    a.g = g;
+    a.forward = false;
+    a.lse = const_cast<float*>(lse);
+    a.qkv = qkv;
+    a.dqkv = dqkv;
+    a.dout = dout;
+    a.Drow = Drow;
+    return from_cuda(simt_launch(a, s));
+  }
+  if (!aligned16(dqkv) || !aligned16(qkv) || !aligned16(out) || !aligned16(dout) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  Tc05BwdArgs a{};
+  a.g = g;
+  a.dqkv = dqkv;
+  a.lse = lse;
+  a.Drow = Drow;
+  a.status = status_word();
+  if (!a.status) return ATTN_ERR_CUDA;
+  cudaError_t e = launch_row_dot(Drow, out, dout, g, true, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  const bool rope = g.rope_theta > 0.f;
+  const void* qk_src = qkv;
+  int qk_width = g.W;
+  if (rope) {
+    void* rot = static_cast<uint8_t*>(workspace) + align256((size_t)g.B * g.NH * g.T * sizeof(float));
+    e = launch_rope_qk_bf16(rot, qkv, g, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    qk_src = rot;
+    qk_width = (g.NH + g.NKV) * g.hd;
+  }
+  a.q_col0 = 0;
+  a.k_col0 = g.C;  // K heads follow the Q heads in both layouts
+  if (!make_tmap(&a.tm_q, qk_src, qk_width, g.T, g.B) || !make_tmap(&a.tm_k, qk_src, qk_width, g.T, g.B) ||
+      !make_tmap(&a.tm_v, qkv, g.W, g.T, g.B) || !make_tmap(&a.tm_do, dout, g.C, g.T, g.B))
+    return ATTN_ERR_CUDA;
+  e = tc05_bwd_launch(a, s);
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+extern "C" int attn_device_status(int* status, int reset) {
+  if (!status) return ATTN_ERR_NULL_POINTER;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  *status = v;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+extern "C" int attn_selftest_wait_timeout(long long limit_ns, int* status) {
+  if (!status) return ATTN_ERR_NULL_POINTER;
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 1000000000LL) limit_ns = 1000000000LL;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_selftest_status, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_selftest_status) != cudaSuccess) return ATTN_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 32>>>(static_cast<int*>(p), (unsigned long long)limit_ns);
+  if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_selftest_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  *status = v;
+  return ATTN_OK;
+}

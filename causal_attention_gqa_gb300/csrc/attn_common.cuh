@@ -1,0 +1,111 @@
+// Shared device helpers of the attention library: problem geometry, the
+// library status word, NEOX RoPE angles and bf16 conversions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Status codes (mirror attn_status_t of the public header).
+constexpr int kOk = 0;
+constexpr int kErrDeviceTimeout = -7;
+
+// Geometry of one call.  Packed qkv rows hold Q | K | V column blocks:
+// query head h at h*hd, kv head kh at C + kh*hd (K) and C + NKV*hd + kh*hd
+// (V) -- the layout of "nanoeuler -- CUDA kernels", causal GQA attention.
+struct Geometry {
+  int B, T, C, NH, NKV;
+  int hd;        // head size C / NH
+  int grp;       // query heads per kv head NH / NKV
+  int W;         // packed row width (NH + 2*NKV) * hd
+  float scale;   // 1 / sqrt(hd)
+  float rope_theta;  // <= 0: no RoPE
+};
+
+// Record the first device-side error in the library status word.
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, kOk, code);
+}
+
+// ---------------------------------------------------------------------------
+// NEOX RoPE ("nx_f32_qwen2_train_gate.nx source", build_rope / rope_node):
+// pair (i, i + hd/2) at position t turns by angle t * theta^(-2i/hd):
+//   y_i        = x_i cos(a) - x_{i+hd/2} sin(a)
+//   y_{i+hd/2} = x_{i+hd/2} cos(a) + x_i sin(a)
+// ---------------------------------------------------------------------------
+
+// Inverse frequency theta^(-2i/hd), split into a float head and tail so that
+// t * (hi + lo) can be formed with about 2^-40 relative error.  Double
+// precision is used once per frequency, never per element.
+__device__ __forceinline__ void rope_inv_freq(float theta, int i, int hd, float& hi, float& lo) {
+  double f = exp(-2.0 * (double)i * log((double)theta) / (double)hd);
+  hi = (float)f;
+  lo = (float)(f - (double)hi);
+}
+
+// The angle t * f reduced to about [-pi, pi], good to ~1e-6 rad for any
+// t < 2^24.  The product is formed error-free with an FMA (Dekker's
+// two-product), and 2*pi is subtracted in three parts (Cody & Waite, 1980):
+// C1 has 8 significant bits so k*C1 is exact for |k| < 2^16, and C2, C3 are
+// the float head and tail of 2*pi - C1.
+__device__ __forceinline__ float rope_angle(int t, float f_hi, float f_lo) {
+  const float kInv2Pi = 0.159154943091895336f;
+  const float kC1 = 6.28125f;
+  const float kC2 = 1.9353071693331003e-3f;    // float(2*pi - C1)
+  const float kC3 = 1.0253376273028358e-11f;   // float(2*pi - C1 - C2)
+  float tf = (float)t;
+  float p = tf * f_hi;
+  float e = fmaf(tf, f_hi, -p);      // exact rounding error of the product
+  float lo = fmaf(tf, f_lo, e);
+  float k = rintf(p * kInv2Pi);
+  float r = p - k * kC1;              // exact (Sterbenz)
+  r = fmaf(-k, kC2, r);
+  r = fmaf(-k, kC3, r);
+  return r + lo;
+}
+
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0, float& y1) {
+  y0 = x0 * c - x1 * s;
+  y1 = x1 * c + x0 * s;
+}
+
+// Adjoint (inverse) rotation: R^T applied to a gradient pair.
+__device__ __forceinline__ void rope_pair_transpose(float g0, float g1, float c, float s, float& y0, float& y1) {
+  y0 = g0 * c + g1 * s;
+  y1 = g1 * c - g0 * s;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace attn

@@ -1,0 +1,58 @@
+// Internal launch interfaces between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "attn_common.cuh"
+
+namespace attn {
+
+// ------------------------------------------------------------ float32 SIMT path
+struct SimtArgs {
+  Geometry g;
+  bool forward;
+  void* out;          // fwd: [B,T,C] float32
+  float* lse;         // fwd: written; bwd: read
+  const void* qkv;    // [B,T,W] float32
+  void* dqkv;         // bwd: [B,T,W] float32
+  const void* dout;   // bwd: [B,T,C] float32
+  const float* Drow;  // bwd: [B,NH,T] row dots
+};
+cudaError_t simt_launch(const SimtArgs& a, cudaStream_t stream);
+size_t simt_max_smem_bytes(int hd);
+
+// ------------------------------------------------------------ backward prologue
+// D[b,h,t] = sum_d dout[b,t,h,d] * out[b,t,h,d] (float32 accumulation).
+cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Geometry& g, bool bf16,
+                           cudaStream_t stream);
+// NEOX-rotated bf16 copy of every Q and K head: dst [B,T,(NH+NKV)*hd].
+cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream);
+
+// ------------------------------------------------------------ tcgen05 bf16 path
+struct Tc05FwdArgs {
+  Geometry g;
+  CUtensorMap tm_qkv;  // qkv [B,T,W] bf16, box {64, 128, 1}, 128-byte swizzle
+  void* out;          // [B,T,C] bf16
+  float* lse;         // [B,NH,T]
+  int* status;        // library status word
+};
+cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream);
+
+struct Tc05BwdArgs {
+  Geometry g;
+  CUtensorMap tm_q;    // Q source (qkv or rotated copy), box {64,128,1}
+  CUtensorMap tm_k;    // K source (qkv or rotated copy), box {64,128,1}
+  CUtensorMap tm_v;    // qkv (V columns), box {64,128,1}
+  CUtensorMap tm_do;   // dout, box {64,128,1}
+  int q_col0;          // column of query head 0 in the Q source
+  int k_col0;          // column of kv head 0 in the K source
+  void* dqkv;          // [B,T,W] bf16
+  const float* lse;    // [B,NH,T]
+  const float* Drow;   // [B,NH,T]
+  int* status;
+};
+cudaError_t tc05_bwd_launch(const Tc05BwdArgs& a, cudaStream_t stream);
+
+}  // namespace attn

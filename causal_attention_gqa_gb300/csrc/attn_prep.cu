@@ -1,0 +1,130 @@
+// Backward prologue kernels (HBM-bound, CUDA cores).
+//
+// Row dots: D[b,h,t] = dO[b,t,h] . O[b,t,h].  This is the identity
+// sum_s P_ts dP_ts = dO_t . O_t that "CUDA C microgpt"'s
+// attention_backward_kernel accumulates as `weighted_sum`; computing it once
+// per row up front lets the main backward form dS = P * (dP - D) tile by tile.
+//
+// Rotated Q/K copy (bf16 path with RoPE): the backward reads every Q and K
+// tile many times, so it rotates them once into the caller's workspace
+// instead of once per use.
+#include "attn_common.cuh"
+#include "attn_kernels.h"
+
+namespace attn {
+namespace {
+
+// One warp per (b, t) row of out/dout; lanes stride across the C columns in
+// 16-byte vectors and reduce per head.
+template <typename T>
+__global__ void __launch_bounds__(256) row_dot_kernel(float* __restrict__ D, const T* __restrict__ out,
+                                                      const T* __restrict__ dout, Geometry g) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  const long long rows = (long long)g.B * g.T;
+  if (warp >= rows) return;
+  const int b = warp / g.T, t = warp % g.T;
+  const T* o = out + (size_t)warp * g.C;
+  const T* d = dout + (size_t)warp * g.C;
+  for (int h = 0; h < g.NH; ++h) {
+    float acc = 0.f;
+    for (int c = lane; c < g.hd; c += 32) acc = fmaf(to_f32(o[h * g.hd + c]), to_f32(d[h * g.hd + c]), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) D[((size_t)b * g.NH + h) * g.T + t] = acc;
+  }
+}
+
+// bf16, hd a multiple of 8: lane handles 8 columns (one 16-byte vector) of a
+// head; a warp covers 256 columns = 2 heads of 128 or 4 of 64 per step.
+__global__ void __launch_bounds__(256) row_dot_bf16_vec_kernel(float* __restrict__ D, const uint4* __restrict__ out,
+                                                                const uint4* __restrict__ dout, Geometry g) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  const long long rows = (long long)g.B * g.T;
+  if (warp >= rows) return;
+  const int b = warp / g.T, t = warp % g.T;
+  const int vec_per_row = g.C / 8, vec_per_head = g.hd / 8;
+  const uint4* o = out + (size_t)warp * vec_per_row;
+  const uint4* d = dout + (size_t)warp * vec_per_row;
+  for (int v0 = 0; v0 < vec_per_row; v0 += 32) {
+    const int v = v0 + lane;
+    float acc = 0.f;
+    if (v < vec_per_row) {
+      uint4 a = o[v], c = d[v];
+      acc = bf16_lo(a.x) * bf16_lo(c.x) + bf16_hi(a.x) * bf16_hi(c.x) + bf16_lo(a.y) * bf16_lo(c.y) +
+            bf16_hi(a.y) * bf16_hi(c.y) + bf16_lo(a.z) * bf16_lo(c.z) + bf16_hi(a.z) * bf16_hi(c.z) +
+            bf16_lo(a.w) * bf16_lo(c.w) + bf16_hi(a.w) * bf16_hi(c.w);
+    }
+    // reduce within groups of vec_per_head lanes (a power of two <= 32)
+    for (int off = vec_per_head / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (v < vec_per_row && (v % vec_per_head) == 0) {
+      const int h = v / vec_per_head;
+      D[((size_t)b * g.NH + h) * g.T + t] = acc;
+    }
+  }
+}
+
+// One thread per (b, t, head, 8 consecutive pairs): heads 0..NH-1 are query
+// heads, NH..NH+NKV-1 key heads.  Writes dst[b,t,head*hd + ...].
+__global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
+                                                           const __nv_bfloat16* __restrict__ qkv, Geometry g) {
+  __shared__ float f_hi[64], f_lo[64];
+  for (int i = threadIdx.x; i < g.hd / 2; i += blockDim.x) rope_inv_freq(g.rope_theta, i, g.hd, f_hi[i], f_lo[i]);
+  __syncthreads();
+  const int half = g.hd / 2, groups = half / 8;
+  const int heads = g.NH + g.NKV;
+  const long long total = (long long)g.B * g.T * heads * groups;
+  const int dst_w = heads * g.hd;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int gi = idx % groups;
+    const long long r = idx / groups;
+    const int head = r % heads;
+    const long long bt = r / heads;
+    const int t = bt % g.T;
+    const __nv_bfloat16* src = qkv + bt * g.W + head * g.hd;  // K heads follow Q heads at column C
+    __nv_bfloat16* out = dst + bt * dst_w + head * g.hd;
+    uint4 x0 = *reinterpret_cast<const uint4*>(src + gi * 8);
+    uint4 x1 = *reinterpret_cast<const uint4*>(src + half + gi * 8);
+    uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
+    uint32_t ya[4], yc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float s0, c0, s1, c1, y00, y01, y10, y11;
+      const int i0 = gi * 8 + 2 * k;
+      __sincosf(rope_angle(t, f_hi[i0], f_lo[i0]), &s0, &c0);
+      __sincosf(rope_angle(t, f_hi[i0 + 1], f_lo[i0 + 1]), &s1, &c1);
+      rope_pair(bf16_lo(a[k]), bf16_lo(c[k]), c0, s0, y00, y10);
+      rope_pair(bf16_hi(a[k]), bf16_hi(c[k]), c1, s1, y01, y11);
+      ya[k] = pack_bf16x2(y00, y01);
+      yc[k] = pack_bf16x2(y10, y11);
+    }
+    *reinterpret_cast<uint4*>(out + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(out + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Geometry& g, bool bf16,
+                           cudaStream_t stream) {
+  const long long rows = (long long)g.B * g.T;
+  const int blocks = (int)((rows + 7) / 8);
+  if (bf16 && g.hd % 8 == 0 && (g.hd / 8) <= 32 && ((g.hd / 8) & (g.hd / 8 - 1)) == 0) {
+    row_dot_bf16_vec_kernel<<<blocks, 256, 0, stream>>>(D, (const uint4*)out, (const uint4*)dout, g);
+  } else if (bf16) {
+    row_dot_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(D, (const __nv_bfloat16*)out,
+                                                               (const __nv_bfloat16*)dout, g);
+  } else {
+    row_dot_kernel<float><<<blocks, 256, 0, stream>>>(D, (const float*)out, (const float*)dout, g);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream) {
+  const long long total = (long long)g.B * g.T * (g.NH + g.NKV) * (g.hd / 16);
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  rope_qk_bf16_kernel<<<(int)blocks, 256, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

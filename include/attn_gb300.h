@@ -1,0 +1,150 @@
+/*
+ * attn_gb300.h -- C ABI of a GB300 (sm_103a) library for fused causal
+ * multi-head / grouped-query self-attention over a packed QKV activation,
+ * forward and backward.
+ *
+ * Method.  For batch row b, query head h, position t, with hd = C/NH,
+ * grp = NH/NKV and kv head kh = h / grp (integer division):
+ *   q = R_t Q[b,t,h], k_s = R_s K[b,s,kh]     (NEOX RoPE, optional)
+ *   s_ts = q . k_s / sqrt(hd)                  for s <= t (causal)
+ *   P_ts = exp(s_ts - lse_t),  lse_t = ln sum_{s<=t} exp(s_ts)
+ *   out[b,t,h] = sum_s P_ts V[b,s,kh]
+ * Sources: "nanoeuler -- CUDA kernels" (nanoeuler_cuda.cu), section "Causal
+ * multi-head attention with GQA" -- packed layout, 1/sqrt(hs) scale, GQA map
+ * h/(NH/NKV), and the forward/backward kernel declarations with an `lse`
+ * buffer of B*NH*T floats; "nx_f32_qwen2_train_gate.nx source", build_rope /
+ * rope_node -- the NEOX rotation; "CUDA C microgpt" (microgpt.cu),
+ * attention_backward_kernel -- the row-dot D_t = dO_t . O_t used by the
+ * backward.
+ *
+ * Layouts (dense, row-major, device pointers unless stated):
+ *   qkv, dqkv : [B, T, (NH + 2*NKV)*hd]; columns [0, C) hold Q (head h at
+ *               h*hd), [C, C + NKV*hd) hold K (kv head kh at C + kh*hd),
+ *               [C + NKV*hd, ...) hold V.
+ *   out, dout : [B, T, C]; head h at columns h*hd.
+ *   lse       : float32 [B, NH, T], index (b*NH + h)*T + t; natural log of
+ *               the sum of exp of the scaled scores.
+ * Element type of qkv/out/dout/dqkv is chosen by `dtype`; lse and every
+ * accumulation are float32.
+ *
+ * RoPE: rope_theta <= 0 disables it.  Otherwise the NEOX rotation with base
+ * rope_theta is applied inside the kernels to every Q and K head at position
+ * t (0-based within each sequence): pair (i, i + hd/2) turns by angle
+ * t * rope_theta^(-2i/hd).  qkv is never modified; dqkv is the gradient with
+ * respect to the un-rotated qkv.
+ *
+ * Ownership and execution: the caller owns every buffer and the stream.  The
+ * library allocates no device memory; the backward's scratch is the
+ * caller's `workspace`.  Every call validates its arguments on the host, then
+ * enqueues kernels on `stream` (a cudaStream_t passed as void*; NULL is the
+ * legacy default stream) and returns without synchronising.  Nothing is
+ * launched when validation fails.
+ *
+ * Errors: every entry point returns ATTN_OK (0) or a negative attn_status.
+ * The library never exits the process and never traps on the device.  A
+ * kernel whose bounded wait on an on-chip barrier expires abandons its work,
+ * records ATTN_ERR_DEVICE_TIMEOUT in a library-owned device status word and
+ * returns; read it with attn_device_status() after synchronising.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  /* float32 tensors, exact float32 arithmetic on CUDA cores. */
+  ATTN_DTYPE_F32 = 0,
+  /* float32 tensors on tensor cores; reserved, currently ATTN_ERR_UNSUPPORTED. */
+  ATTN_DTYPE_TF32 = 1,
+  /* bf16 tensors, tcgen05 tensor-core MMAs with float32 accumulation. */
+  ATTN_DTYPE_BF16 = 2
+} attn_dtype_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL_POINTER = -1,    /* a required pointer is NULL */
+  ATTN_ERR_BAD_SHAPE = -2,       /* B,T,NH,NKV < 1, C % NH, NH % NKV, odd hd with RoPE, overflow */
+  ATTN_ERR_UNSUPPORTED = -3,     /* (dtype, head size) combination not implemented */
+  ATTN_ERR_MISALIGNED = -4,      /* a pointer is not 16-byte aligned (bf16 path) */
+  ATTN_ERR_WORKSPACE = -5,       /* workspace NULL or smaller than attn_bwd_workspace_bytes() */
+  ATTN_ERR_CUDA = -6,            /* a CUDA runtime call or kernel launch failed */
+  ATTN_ERR_DEVICE_TIMEOUT = -7,  /* a device-side bounded wait expired (see attn_device_status) */
+  ATTN_ERR_BAD_ARGUMENT = -8     /* any other invalid argument */
+} attn_status_t;
+
+/*
+ * attn_fwd -- causal attention forward.
+ *   out  : [B,T,C] of dtype, overwritten (every element).
+ *   lse  : float32 [B,NH,T], overwritten.
+ *   qkv  : [B,T,(NH+2*NKV)*hd] of dtype, read only.
+ * Supported: dtype F32 with any hd <= 128 (even hd when RoPE is on);
+ * dtype BF16 with hd in {64, 128}.  T >= 1, any NH divisible by NKV.
+ * bf16 pointers must be 16-byte aligned.
+ */
+ATTN_API int attn_fwd(void* out, float* lse, const void* qkv,
+             int B, int T, int C, int NH, int NKV, float rope_theta,
+             int dtype, void* stream);
+
+/*
+ * attn_bwd_workspace_bytes -- size in bytes of the scratch attn_bwd needs
+ * for this shape and dtype: the row dots D = rowsum(dO * O) as float32
+ * [B,NH,T], plus, for BF16, room for a RoPE-rotated bf16 copy of Q and K
+ * (used only when rope_theta > 0).  Returns 0 for invalid arguments.
+ */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype);
+
+/*
+ * attn_bwd -- causal attention backward.
+ *   dqkv : [B,T,(NH+2*NKV)*hd] of dtype, overwritten (every element; no need
+ *          to clear it first).  dQ at Q's columns, dK/dV (summed over the
+ *          grp query heads sharing each kv head) at K/V's columns.
+ *   qkv  : the forward's input.   out, lse : the forward's outputs.
+ *   dout : [B,T,C] of dtype, the gradient of the loss with respect to out.
+ *   workspace : device scratch of at least attn_bwd_workspace_bytes(...)
+ *          bytes, 256-byte aligned, owned by the caller; its contents on
+ *          entry do not matter and are garbage on return.
+ * Deterministic: identical inputs give bit-identical dqkv (no atomics).
+ */
+ATTN_API int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* dout,
+             const float* lse, int B, int T, int C, int NH, int NKV,
+             float rope_theta, int dtype, void* workspace, size_t workspace_bytes,
+             void* stream);
+
+/* attn_strerror -- static description of a status code; never NULL. */
+ATTN_API const char* attn_strerror(int status);
+
+/*
+ * attn_device_status -- synchronise the current device, then store in
+ * *status the first error a kernel of this library recorded on it since the
+ * last reset (ATTN_OK if none); when `reset` is non-zero clear it.
+ * Returns ATTN_OK, or ATTN_ERR_CUDA if the synchronisation failed.
+ */
+ATTN_API int attn_device_status(int* status, int reset);
+
+/*
+ * attn_selftest_wait_timeout -- failure-detection self test: launches one
+ * block that waits on an on-chip barrier nothing will ever complete, with a
+ * wait limit of `limit_ns` nanoseconds (clamped to [1e3, 1e9]).  The kernel
+ * must give up, record ATTN_ERR_DEVICE_TIMEOUT and exit; the device stays
+ * usable.  *status receives what the kernel recorded.  Synchronous.
+ */
+ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
+
+/* attn_abi_version -- ABI version of this header (currently 1). */
+ATTN_API int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,36 @@
+"""Shared helpers for the GPU parity tests: run the CUDA library through its
+C ABI on seeded inputs and measure the normalised error against the oracle."""
+import numpy as np
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def rel_err(x, ref) -> float:
+    """max |x - ref| / max |ref| (the spec error metric)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    denom = np.abs(ref).max()
+    return float(np.abs(x - ref).max() / (denom if denom > 0 else 1.0))
+
+
+def to_device(a, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(device="cuda", dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+
+
+def to_numpy(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(lib, w, qkv_np, dout_np, dtype, backward=True):
+    """Forward (and backward) through the C ABI; returns numpy float64 arrays."""
+    import torch
+    qkv = to_device(qkv_np, dtype)
+    dout = to_device(dout_np, dtype)
+    out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta)
+    res = {"out": out, "lse": lse}
+    if backward:
+        res["dqkv"] = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta)
+    torch.cuda.synchronize()
+    return {k: to_numpy(v) for k, v in res.items()}

@@ -1,0 +1,83 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol
+declared in include/*.h, and rejects invalid arguments before any CUDA work
+(no compute call is made here)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    from causal_attention_gqa_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        names.update(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_strerror"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(cdll):
+    for name in declared_symbols():
+        assert hasattr(cdll, name), name
+        assert isinstance(getattr(cdll, name), ctypes._CFuncPtr)
+
+
+def test_strerror_and_version(cdll):
+    from causal_attention_gqa_gb300 import binding
+    assert binding.attn_abi_version() == 1
+    for code in range(-8, 1):
+        assert binding.attn_strerror(code) != "unknown status"
+    assert binding.attn_strerror(-99) == "unknown status"
+
+
+def test_workspace_size(cdll):
+    from causal_attention_gqa_gb300 import binding
+    B, T, C, NH, NKV = 4, 2048, 2048, 16, 4
+    d_bytes = B * NH * T * 4
+    rot_bytes = B * T * (NH + NKV) * (C // NH) * 2
+    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == d_bytes + rot_bytes
+    assert binding.attn_bwd_workspace_bytes(1, 16, 16, 4, 4, binding.DTYPE_F32) == 256
+    assert binding.attn_bwd_workspace_bytes(1, 16, 16, 3, 4, binding.DTYPE_F32) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 16, 16, 3, 3, 0.0, 0), -2),     # C % NH
+    ((1, 16, 16, 4, 3, 0.0, 0), -2),     # NH % NKV
+    ((0, 16, 16, 4, 4, 0.0, 0), -2),     # B < 1
+    ((1, 0, 16, 4, 4, 0.0, 0), -2),      # T < 1
+    ((1, 16, 12, 4, 4, 1e4, 0), -2),     # odd head size with RoPE
+    ((1, 16, 1024, 4, 4, 0.0, 0), -3),   # hd 256 unsupported
+    ((1, 16, 128, 4, 4, 0.0, 2), -3),    # bf16 needs hd 64 or 128 (hd 32 here)
+    ((1, 16, 512, 4, 4, 0.0, 1), -3),    # TF32 reserved
+    ((1, 16, 512, 4, 4, 0.0, 7), -8),    # unknown dtype
+    ((1, 16, 512, 4, 4, float("nan"), 2), -8),
+])
+def test_forward_rejects_invalid_shapes(cdll, args, code):
+    assert cdll.attn_fwd(None, None, None, *args, None) == code
+
+
+def test_forward_rejects_null_pointers(cdll):
+    assert cdll.attn_fwd(None, None, None, 1, 16, 16, 4, 4, 0.0, 0, None) == -1
+
+
+def test_backward_rejects_missing_workspace(cdll):
+    p = 1 << 20   # never dereferenced: validation fails first
+    assert cdll.attn_bwd(p, p, p, p, p, 1, 16, 16, 4, 4, 0.0, 0, None, 0, None) == -5
+    assert cdll.attn_bwd(p, p, p, p, p, 1, 16, 16, 4, 4, 0.0, 0, p, 8, None) == -5
+    assert cdll.attn_bwd(p, p, p, p, p, 1, 16, 16, 4, 4, 0.0, 0, p + 16, 4096, None) == -4

@@ -1,0 +1,121 @@
+"""GPU parity: the CUDA library (through its C ABI) against the float64 oracle,
+element by element on the same seeded inputs.
+
+Bars (normalised max error, max|gpu - oracle| / max|oracle|): 1e-4 for the
+float32 path, 2e-2 for the bf16 path, on out, lse and dqkv (and separately
+on its dQ, dK, dV blocks).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from causal_attention_gqa_gb300.workloads import WORKLOADS, make_inputs, sample_rows, shape_workload
+from helpers import TOL, rel_err, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def check_full(lib, w, dtype, backward=True):
+    qkv, dout = make_inputs(w, dtype)
+    got = run_gpu(lib, w, qkv, dout, dtype, backward=backward)
+    tol = TOL[dtype]
+    if backward:
+        ref_dqkv, aux = oracle.attention_backward(qkv, dout, w.C, w.NH, w.NKV, w.rope_theta, return_aux=True)
+        ref_out, ref_lse = aux["out"], aux["lse"]
+    else:
+        ref_out, ref_lse = oracle.attention_forward(qkv, w.C, w.NH, w.NKV, w.rope_theta)
+    errs = {"out": rel_err(got["out"], ref_out), "lse": rel_err(got["lse"], ref_lse)}
+    lse_abs = float(np.abs(got["lse"] - ref_lse).max())
+    if backward:
+        errs["dqkv"] = rel_err(got["dqkv"], ref_dqkv)
+        gq, gk, gv = oracle.split_qkv(got["dqkv"], w.C, w.NH, w.NKV)
+        rq, rk, rv = oracle.split_qkv(ref_dqkv, w.C, w.NH, w.NKV)
+        errs.update(dq=rel_err(gq, rq), dk=rel_err(gk, rk), dv=rel_err(gv, rv))
+    assert np.isfinite(got["out"]).all() and np.isfinite(got["lse"]).all()
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{w.name} {dtype}: errors {errs} exceed {tol}"
+    assert lse_abs <= tol * max(1.0, float(np.abs(ref_lse).max())), lse_abs
+    return errs
+
+
+# ------------------------------------------------------------------ float32 path
+@pytest.mark.parametrize("name", ["microgpt_tiny", "qwen2_single_head"])
+def test_f32_tiny_workloads(lib, name):
+    check_full(lib, WORKLOADS[name], "f32")
+
+
+def test_f32_gpt2_mha_full(lib):
+    check_full(lib, WORKLOADS["gpt2_124m_mha"], "f32")
+
+
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    (1, 1, 16, 4, 4, 0.0), (2, 17, 16, 4, 2, 1e6), (1, 33, 32, 2, 1, 1e4), (3, 95, 64, 4, 1, 0.0),
+    (1, 129, 256, 2, 2, 1e6), (2, 70, 96, 3, 1, 0.0), (1, 200, 512, 8, 2, 1e6), (1, 40, 48, 8, 8, 1e6),
+])
+def test_f32_shapes(lib, B, T, C, NH, NKV, theta):
+    check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T), "f32")
+
+
+# ------------------------------------------------------------------ bf16 forward
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    (1, 1, 128, 1, 1, 0.0), (1, 128, 128, 1, 1, 0.0), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6),
+    (1, 77, 512, 4, 4, 0.0), (1, 256, 256, 4, 1, 1e4), (2, 513, 1024, 8, 8, 0.0), (1, 1000, 512, 4, 1, 1e6),
+])
+def test_bf16_forward_shapes(lib, B, T, C, NH, NKV, theta):
+    check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 7), "bf16", backward=False)
+
+
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    (1, 1, 128, 1, 1, 0.0), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6), (1, 77, 512, 4, 4, 0.0),
+    (1, 256, 256, 4, 1, 1e4), (1, 640, 1024, 8, 2, 1e6),
+])
+def test_bf16_backward_shapes(lib, B, T, C, NH, NKV, theta):
+    check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 11), "bf16")
+
+
+def test_bf16_gpt2_mha_reduced_batch(lib):
+    w = WORKLOADS["gpt2_124m_mha"].replace(B=2)
+    check_full(lib, w, "bf16")
+
+
+# ------------------------------------------------------------------ full-size, sampled
+def check_sampled(lib, w, dtype, n_rows=64, kv_groups=None):
+    """Full-size run in the benchmark's launch configuration; the oracle is
+    evaluated on seeded query rows of every head (out, lse, dQ) and on seeded
+    key rows of a few kv groups (dK, dV)."""
+    qkv, dout = make_inputs(w, dtype)
+    got = run_gpu(lib, w, qkv, dout, dtype)
+    qr = sample_rows(w.T, n_rows, w.seed + 1)
+    kr = sample_rows(w.T, n_rows, w.seed + 2)
+    if kv_groups is None:
+        kv_groups = [(0, 0), (w.B - 1, w.NKV - 1)]
+    ref = oracle.attention_sampled(qkv, dout, w.C, w.NH, w.NKV, w.rope_theta, qr, kv_groups, kr)
+    tol = TOL[dtype]
+    hd = w.hd
+    gq, gk, gv = oracle.split_qkv(got["dqkv"], w.C, w.NH, w.NKV)
+    errs = {
+        "out": rel_err(got["out"][:, qr], ref["out_rows"]),
+        "lse": rel_err(got["lse"][:, :, qr], ref["lse_rows"]),
+        "dq": rel_err(gq[:, qr], ref["dq_rows"]),
+        "dk": rel_err(np.stack([gk[b, kr, kh] for (b, kh) in kv_groups]),
+                      np.stack([ref["dk_rows"][g] for g in kv_groups])),
+        "dv": rel_err(np.stack([gv[b, kr, kh] for (b, kh) in kv_groups]),
+                      np.stack([ref["dv_rows"][g] for g in kv_groups])),
+    }
+    for k in ("out", "lse", "dqkv"):
+        assert np.isfinite(got[k]).all(), k
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{w.name} {dtype}: errors {errs} exceed {tol}"
+    return errs
+
+
+def test_bf16_gpt2_mha_full_sampled(lib):
+    check_sampled(lib, WORKLOADS["gpt2_124m_mha"], "bf16")
+
+
+def test_bf16_gqa_block_full_sampled(lib):
+    check_sampled(lib, WORKLOADS["gqa_block"], "bf16")
+
+
+def test_bf16_long_context_full_sampled(lib):
+    check_sampled(lib, WORKLOADS["long_context_gqa"], "bf16", kv_groups=[(0, 0), (0, 7)])

@@ -1,0 +1,97 @@
+"""GPU robustness: determinism, guard bands, argument errors that must launch
+nothing, and the bounded-wait failure path (a wait that nothing completes
+must expire, report ATTN_ERR_DEVICE_TIMEOUT and leave the device usable)."""
+import numpy as np
+import pytest
+
+from causal_attention_gqa_gb300.workloads import make_inputs, shape_workload
+from helpers import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype,theta", [("f32", 1e6), ("bf16", 1e6), ("bf16", 0.0)])
+def test_backward_is_deterministic(lib, dtype, theta):
+    import torch
+    w = shape_workload(2, 333, 512, 8, 2, theta, seed=21)
+    qkv_np, dout_np = make_inputs(w, dtype)
+    qkv, dout = to_device(qkv_np, dtype), to_device(dout_np, dtype)
+    out, lse = lib.forward(qkv, w.NH, w.NKV, theta)
+    out2, lse2 = lib.forward(qkv, w.NH, w.NKV, theta)
+    d1 = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, theta)
+    d2 = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, theta)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert torch.equal(d1, d2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_guard_bands_untouched(lib, dtype):
+    """Outputs live inside larger buffers filled with a canary; nothing outside
+    the output extents may change (stands in for a memory checker)."""
+    import torch
+    w = shape_workload(1, 200, 256, 4, 2, 1e6, seed=22)
+    qkv_np, dout_np = make_inputs(w, dtype)
+    qkv, dout = to_device(qkv_np, dtype), to_device(dout_np, dtype)
+    tdt = qkv.dtype
+    pad = 4096
+    canary = -12345.0
+
+    def guarded(n, dt):
+        buf = torch.full((pad + n + pad,), canary, dtype=dt, device="cuda")
+        return buf, buf[pad:pad + n]
+
+    B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
+    out_buf, out = guarded(B * T * C, tdt)
+    lse_buf, lse = guarded(B * NH * T, torch.float32)
+    dq_buf, dqkv = guarded(B * T * w.qkv_width, tdt)
+    code = lib.dtype_code(qkv)
+    lib.attn_fwd(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code)
+    nbytes = lib.attn_bwd_workspace_bytes(B, T, C, NH, NKV, code)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    lib.attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, w.rope_theta, code, ws, nbytes)
+    torch.cuda.synchronize()
+    for buf in (out_buf, lse_buf, dq_buf):
+        host = buf.float().cpu().numpy()
+        assert np.all(host[:pad] == canary) and np.all(host[-pad:] == canary)
+    assert torch.isfinite(out).all() and torch.isfinite(dqkv).all()
+
+
+def test_invalid_arguments_launch_nothing(lib):
+    import torch
+    from causal_attention_gqa_gb300.binding import AttnError
+    qkv = torch.zeros((1, 128, 3 * 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((1, 128, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda")
+    cases = [
+        (dict(C=128, NH=3, NKV=1), -2),           # C % NH
+        (dict(C=128, NH=2, NKV=3), -2),           # NH % NKV (and C/NH)
+        (dict(C=96 * 3, NH=3, NKV=3), -3),         # hd 96 unsupported on bf16
+    ]
+    for kw, code in cases:
+        with pytest.raises(AttnError) as ei:
+            lib.attn_fwd(out, lse, qkv, 1, 128, kw["C"], kw["NH"], kw["NKV"], 0.0, lib.DTYPE_BF16)
+        assert ei.value.status == code
+    with pytest.raises(AttnError) as ei:   # misaligned bf16 pointer
+        lib.attn_fwd(out.data_ptr() + 2, lse, qkv, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_BF16)
+    assert ei.value.status == -4
+    with pytest.raises(AttnError) as ei:   # TF32 reserved
+        lib.attn_fwd(out, lse, qkv, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_TF32)
+    assert ei.value.status == -3
+    with pytest.raises(AttnError) as ei:   # workspace too small
+        lib.attn_bwd(qkv, qkv, out, out, lse, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_BF16, qkv, 16)
+    assert ei.value.status == -5
+    torch.cuda.synchronize()
+    assert lib.attn_device_status() == 0
+
+
+def test_bounded_wait_expires_and_device_stays_usable(lib):
+    import torch
+    assert lib.attn_selftest_wait_timeout(2_000_000) == -7   # 2 ms limit
+    x = torch.arange(10, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 45.0
+    assert lib.attn_device_status() == 0  # the self test reports separately
+
+
+def test_no_device_errors_recorded(lib):
+    assert lib.attn_device_status(reset=True) == 0
