@@ -57,14 +57,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D bf16 tensor map over a row-major [B, T, width] array, box {64, 128, 1},
+// 3-D bf16 tensor map over a row-major [B, T, width] array, box {64, rows, 1},
 // 128-byte swizzle; rows past T read as zeros.
-bool make_tmap(CUtensorMap* m, const void* base, int width, int T, int B) {
+bool make_tmap(CUtensorMap* m, const void* base, int width, int T, int B, int rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * (cuuint64_t)T};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -107,6 +107,12 @@ int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtyp
   g->W = (int)W;
   g->scale = (float)(1.0 / std::sqrt((double)hd));
   g->rope_theta = rope ? rope_theta : 0.f;
+  for (int i = 0; i < 64; ++i) {
+    double f = 0.0;
+    if (rope && i < hd / 2) f = std::exp(-2.0 * i * std::log((double)rope_theta) / hd);
+    g->rope_f_hi[i] = (float)f;
+    g->rope_f_lo[i] = (float)(f - (double)g->rope_f_hi[i]);
+  }
   return ATTN_OK;
 }
 
@@ -229,25 +235,21 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
   a.Drow = Drow;
   a.status = status_word();
   if (!a.status) return ATTN_ERR_CUDA;
-  cudaError_t e = launch_row_dot(Drow, out, dout, g, true, s);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  // With RoPE, Q and K are read from a rotated copy in the workspace; its
+  // layout keeps query head h at column h*hd and kv head kh at C + kh*hd.
   const bool rope = g.rope_theta > 0.f;
-  const void* qk_src = qkv;
-  int qk_width = g.W;
-  if (rope) {
-    void* rot = static_cast<uint8_t*>(workspace) + align256((size_t)g.B * g.NH * g.T * sizeof(float));
-    e = launch_rope_qk_bf16(rot, qkv, g, s);
-    if (e != cudaSuccess) return ATTN_ERR_CUDA;
-    qk_src = rot;
-    qk_width = (g.NH + g.NKV) * g.hd;
+  void* rot = static_cast<uint8_t*>(workspace) + align256((size_t)g.B * g.NH * g.T * sizeof(float));
+  const void* qk_src = rope ? rot : qkv;
+  const int qk_width = rope ? (g.NH + g.NKV) * g.hd : g.W;
+  for (int r = 0; r < 2; ++r) {
+    const int rows = r ? 128 : 64;
+    if (!make_tmap(&a.tm_qk[r], qk_src, qk_width, g.T, g.B, rows) ||
+        !make_tmap(&a.tm_v[r], qkv, g.W, g.T, g.B, rows) || !make_tmap(&a.tm_do[r], dout, g.C, g.T, g.B, rows))
+      return ATTN_ERR_CUDA;
   }
-  a.q_col0 = 0;
-  a.k_col0 = g.C;  // K heads follow the Q heads in both layouts
-  if (!make_tmap(&a.tm_q, qk_src, qk_width, g.T, g.B) || !make_tmap(&a.tm_k, qk_src, qk_width, g.T, g.B) ||
-      !make_tmap(&a.tm_v, qkv, g.W, g.T, g.B) || !make_tmap(&a.tm_do, dout, g.C, g.T, g.B))
-    return ATTN_ERR_CUDA;
-  e = tc05_bwd_launch(a, s);
-  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  cudaError_t e = launch_row_dot(Drow, out, dout, g, true, s);
+  if (e == cudaSuccess && rope) e = launch_rope_qk_bf16(rot, qkv, g, s);
+  if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
 }
 

@@ -1,10 +1,628 @@
-// Causal MHA/GQA attention backward on sm_103a tensor cores (bf16).
+// Causal MHA/GQA attention backward on sm_103a tensor cores (bf16 in, f32
+// accumulation), head size 64 or 128.  Deterministic and free of atomics.
+//
+// The gradient is that of "nanoeuler -- CUDA kernels", attention_backward_kernel:
+// with P recomputed from the saved log-sum-exp, P_ts = exp(s_ts - lse_t),
+//   dP = dO V^T,  dS = P * (dP - D)  with D_t = dO_t . O_t  (the row dot of
+//   "CUDA C microgpt"'s attention_backward_kernel, computed by a prologue),
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K,
+// dK and dV summed over the query heads that share a kv head (the page's
+// atomicAdd into the shared dk/dv), and dQ/dK carried back through the RoPE
+// rotation (the page's rope_kernel with inverse=1 on dqkv).
+//
+// Two kernels split the work so that every output element has exactly one
+// writer:
+//  * dkdv: one CTA per (128-key tile j, kv head, batch row).  K_j and V_j stay
+//    in shared memory; the CTA walks every query head of the group and every
+//    64-query tile that can see tile j.  Per step: S^T = K Q^T and
+//    dP^T = V dO^T into TMEM (double-buffered), P^T and dS^T (bf16) into
+//    shared memory, then dV += P^T dO and dK += dS^T Q accumulate in TMEM.
+//  * dq:   one CTA per (128-query tile i, query head, batch row).  Q_i and dO_i
+//    stay in shared memory; the CTA walks the 64-key tiles 0..2i+1.  Per step:
+//    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
+//    dQ += dS K accumulates in TMEM.
+// Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 2-5 one TMEM lane (one key or query row) per thread for the
+// elementwise work and the epilogue.  All waits are bounded.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
 #include "attn_ptx.cuh"
 
 namespace attn {
+namespace {
 
-cudaError_t tc05_bwd_launch(const Tc05BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Store 64 bf16 values (32 packed words) as row `row` of a 64-column swizzled
+// tile (one atom column).
+__device__ __forceinline__ void store_row64(uint8_t* tile, int row, const uint32_t (&w)[32]) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    *reinterpret_cast<uint4*>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) =
+        make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const uint32_t* f, float s) {
+  return make_uint4(pack_bf16x2(__uint_as_float(f[0]) * s, __uint_as_float(f[1]) * s),
+                    pack_bf16x2(__uint_as_float(f[2]) * s, __uint_as_float(f[3]) * s),
+                    pack_bf16x2(__uint_as_float(f[4]) * s, __uint_as_float(f[5]) * s),
+                    pack_bf16x2(__uint_as_float(f[6]) * s, __uint_as_float(f[7]) * s));
+}
+
+// Epilogue of one gradient row held in TMEM (HD float32 columns at `acc`):
+// multiply by `s`, undo the RoPE rotation at position `t` if `rope`, round to
+// bf16 and store to `dst` (HD contiguous bf16; only if `store`).  Every lane of
+// the warp must call this (tcgen05.ld is warp-collective).
+template <int HD>
+__device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope, int t, const Geometry& g,
+                                               __nv_bfloat16* dst, bool store) {
+  if (!rope) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < HD; c0 += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld32(acc + c0, v);
+      ptx::tmem_wait_ld();
+      if (store) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = pack8(&v[8 * q], s);
+      }
+    }
+    return;
+  }
+  constexpr int HALF = HD / 2;
+#pragma unroll 1
+  for (int c0 = 0; c0 < HALF; c0 += 32) {
+    uint32_t lo[32], hi[32];
+    ptx::tmem_ld32(acc + c0, lo);
+    ptx::tmem_ld32(acc + HALF + c0, hi);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int i = c0 + e;
+      float sn, cs, y0, y1;
+      __sincosf(rope_angle(t, g.rope_f_hi[i], g.rope_f_lo[i]), &sn, &cs);
+      rope_pair_transpose(__uint_as_float(lo[e]) * s, __uint_as_float(hi[e]) * s, cs, sn, y0, y1);
+      lo[e] = __float_as_uint(y0);
+      hi[e] = __float_as_uint(y1);
+    }
+    if (store) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = pack8(&lo[8 * q], 1.f);
+        *reinterpret_cast<uint4*>(dst + HALF + c0 + 8 * q) = pack8(&hi[8 * q], 1.f);
+      }
+    }
+  }
+}
+
+// ===========================================================================
+// dK / dV kernel
+// ===========================================================================
+template <int HD>
+struct DkdvCfg {
+  static constexpr int kKeys = 128, kQ = 64;
+  static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
+  static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
+  static constexpr int kPTile = kKeys * kQ * 2;        // P^T or dS^T (one atom column)
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kKTile;
+  static constexpr int kQOff = kVOff + kKTile;
+  static constexpr int kDOOff = kQOff + 2 * kQTile;
+  static constexpr int kPOff = kDOOff + 2 * kQTile;
+  static constexpr int kDSOff = kPOff + 2 * kPTile;
+  static constexpr int kLseOff = kDSOff + 2 * kPTile;
+  static constexpr int kDOff = kLseOff + 2 * kQ * 4;
+  static constexpr int kBarOff = kDOff + 2 * kQ * 4;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr uint32_t kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
+};
+
+struct DkdvBarriers {
+  uint64_t kv_full, acc_done, drain;
+  uint64_t qdo_full[2], qdo_empty[2], s_full[2], s_free[2], p_full[2], pds_free[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int HD, bool ROPE>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
+                int* __restrict__ status, Geometry g) {
+  using Cfg = DkdvCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + Cfg::kKOff;
+  uint8_t* sV = smem + Cfg::kVOff;
+  uint8_t* sQ = smem + Cfg::kQOff;
+  uint8_t* sDO = smem + Cfg::kDOOff;
+  uint8_t* sP = smem + Cfg::kPOff;
+  uint8_t* sDS = smem + Cfg::kDSOff;
+  float* sLse = reinterpret_cast<float*>(smem + Cfg::kLseOff);
+  float* sD = reinterpret_cast<float*>(smem + Cfg::kDOff);
+  DkdvBarriers* bars = reinterpret_cast<DkdvBarriers*>(smem + Cfg::kBarOff);
+  volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // Heaviest key tiles (small j) first.
+  const int bk = g.B * g.NKV;
+  const int j = (int)(blockIdx.x / bk);
+  const int b = (blockIdx.x % bk) / g.NKV, kh = (blockIdx.x % bk) % g.NKV;
+  const int nq64 = (g.T + 63) / 64;
+  const int nq = nq64 - 2 * j;                  // 64-query tiles that can see key tile j
+  const int n_steps = g.grp * nq;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 2);
+      ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->pds_free[i]), 1);
+    }
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), Cfg::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    record_status(status, kErrDeviceTimeout);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    if (lane == 0) {
+      const uint32_t kvf = ptx::smem_u32(&bars->kv_full);
+      ptx::mbar_arrive_expect_tx(kvf, 2 * Cfg::kKTile);
+#pragma unroll
+      for (int a = 0; a < HD / 64; ++a) {
+        ptx::tma_load_3d(ptx::smem_u32(sK + a * Cfg::kKeys * 128), &tm_k, g.C + kh * HD + 64 * a, j * 128, b, kvf);
+        ptx::tma_load_3d(ptx::smem_u32(sV + a * Cfg::kKeys * 128), &tm_v, g.C + g.NKV * HD + kh * HD + 64 * a,
+                         j * 128, b, kvf);
+      }
+    }
+    for (int n = 0; n < n_steps; ++n) {
+      const int st = n & 1, u = n >> 1;
+      const int h = kh * g.grp + n / nq, qi = 2 * j + n % nq;
+      int ok = 1;
+      if (lane == 0 && u > 0)
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      const uint32_t full = ptx::smem_u32(&bars->qdo_full[st]);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kQTile);
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a) {
+          ptx::tma_load_3d(ptx::smem_u32(sQ + st * Cfg::kQTile + a * Cfg::kQ * 128), &tm_q, h * HD + 64 * a,
+                           qi * 64, b, full);
+          ptx::tma_load_3d(ptx::smem_u32(sDO + st * Cfg::kQTile + a * Cfg::kQ * 128), &tm_do, h * HD + 64 * a,
+                           qi * 64, b, full);
+        }
+      }
+      for (int q = lane; q < Cfg::kQ; q += 32) {
+        const int t = qi * 64 + q;
+        const size_t idx = ((size_t)b * g.NH + h) * g.T + t;
+        sLse[st * Cfg::kQ + q] = (t < g.T) ? lse[idx] * kLog2e : INFINITY;  // padding rows: P = 0
+        sD[st * Cfg::kQ + q] = (t < g.T) ? Drow[idx] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(full);
+      issued = n + 1;
+    }
+    if (lane == 0 && *abort_flag) {
+      ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, nullptr, kWaitLimitNs);
+      for (int st = 0; st < 2 && st < issued; ++st)
+        ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), ((issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
+      const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
+                     aDO = ptx::smem_u32(sDO), aP = ptx::smem_u32(sP), aDS = ptx::smem_u32(sDS);
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
+
+      auto issue_grad = [&](int m) -> bool {
+        const int st = m & 1, u = m >> 1;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kQ / 16; ++kk) {
+          const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDV, ptx::sw128_desc(aP + st * Cfg::kPTile + kk * 32, 16, 1024),
+                           ptx::sw128_desc(aDO + st * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDK, ptx::sw128_desc(aDS + st * Cfg::kPTile + kk * 32, 16, 1024),
+                           ptx::sw128_desc(aQ + st * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->pds_free[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[st]));
+        return true;
+      };
+
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n & 1, u = n >> 1;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), u & 1, abort_flag, kWaitLimitNs);
+        if (ok && n >= 2)
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t ok_ = (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
+          const uint32_t oq = st * Cfg::kQTile + (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
+          ptx::mma_bf16_ss(d_s, ptx::sw128_desc(aK + ok_, 16, 1024), ptx::sw128_desc(aQ + oq, 16, 1024), idesc_s,
+                           kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_dp, ptx::sw128_desc(aV + ok_, 16, 1024), ptx::sw128_desc(aDO + oq, 16, 1024), idesc_s,
+                           kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
+        if (n >= 1) ok = issue_grad(n - 1);
+      }
+      if (ok) ok = issue_grad(n_steps - 1);
+      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (!ok) fail();
+      ptx::mma_commit(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;           // key row within the tile
+    const int ks = j * 128 + row;
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = g.scale * kLog2e;
+    bool ok = true;
+    for (int n = 0; n < n_steps; ++n) {
+      const int st = n & 1, u = n >> 1;
+      const int qi = 2 * j + n % nq;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const bool diag = qi <= 2 * j + 1;           // this query tile overlaps the key tile
+      const float* lse2 = sLse + st * Cfg::kQ;
+      const float* dd = sD + st * Cfg::kQ;
+      uint32_t pw[32], dw[32];
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(t_lane + st * 128 + c0, sr);
+        ptx::tmem_ld32(t_lane + st * 128 + 64 + c0, dr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float p[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = c0 + c + e;
+            float pv = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -lse2[q]));
+            if (diag && qi * 64 + q < ks) pv = 0.f;  // query before key: masked
+            p[e] = pv;
+            ds[e] = pv * (__uint_as_float(dr[c + e]) - dd[q]);
+          }
+          pw[(c0 + c) / 2] = pack_bf16x2(p[0], p[1]);
+          dw[(c0 + c) / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
+      if (n >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(ptx::smem_u32(&bars->pds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+      }
+      store_row64(sP + st * Cfg::kPTile, row, pw);
+      store_row64(sDS + st * Cfg::kPTile, row, dw);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[st]));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
+    if (ok) {
+      ptx::tc_fence_after();
+      const bool store = ks < g.T;
+      __nv_bfloat16* row_ptr = dqkv + ((size_t)b * g.T + (store ? ks : 0)) * g.W;
+      store_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, row_ptr + g.C + g.NKV * HD + kh * HD, store);
+      store_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, row_ptr + g.C + kh * HD, store);
+    } else {
+      fail();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+// ===========================================================================
+// dQ kernel
+// ===========================================================================
+template <int HD>
+struct DqCfg {
+  static constexpr int kQ = 128, kKeys = 64;
+  static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
+  static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
+  static constexpr int kSTile = kQ * kKeys * 2;        // dS (one atom column)
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kQOff + kQTile;
+  static constexpr int kKOff = kDOOff + kQTile;
+  static constexpr int kVOff = kKOff + 2 * kKTile;
+  static constexpr int kDSOff = kVOff + 2 * kKTile;
+  static constexpr int kBarOff = kDSOff + 2 * kSTile;
+  // At least 116 KB so that two CTAs never share an SM: each allocates all
+  // 512 TMEM columns, and a second resident CTA would only wait for them.
+  static constexpr int kSmemBytes = (kBarOff + 256 + 1024) > 116 * 1024 ? (kBarOff + 256 + 1024) : 116 * 1024;
+  static constexpr uint32_t kTmemDQ = 256, kTmemCols = 512;
+};
+
+struct DqBarriers {
+  uint64_t q_full, acc_done, drain;
+  uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], ds_full[2], ds_free[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int HD, bool ROPE>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
+              int* __restrict__ status, Geometry g) {
+  using Cfg = DqCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + Cfg::kQOff;
+  uint8_t* sDO = smem + Cfg::kDOOff;
+  uint8_t* sK = smem + Cfg::kKOff;
+  uint8_t* sV = smem + Cfg::kVOff;
+  uint8_t* sDS = smem + Cfg::kDSOff;
+  DqBarriers* bars = reinterpret_cast<DqBarriers*>(smem + Cfg::kBarOff);
+  volatile int* abort_flag = &bars->abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // Heaviest query tiles (large i) first.
+  const int n_qt = (g.T + 127) / 128;
+  const int bh_count = g.B * g.NH;
+  const int qt = n_qt - 1 - (int)(blockIdx.x / bh_count);
+  const int b = (blockIdx.x % bh_count) / g.NH, h = (blockIdx.x % bh_count) % g.NH;
+  const int kh = h / g.grp;
+  const int nk64 = (g.T + 63) / 64;
+  const int n_steps = min(2 * qt + 2, nk64);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->ds_free[i]), 1);
+    }
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), Cfg::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    record_status(status, kErrDeviceTimeout);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t qf = ptx::smem_u32(&bars->q_full);
+      ptx::mbar_arrive_expect_tx(qf, 2 * Cfg::kQTile);
+#pragma unroll
+      for (int a = 0; a < HD / 64; ++a) {
+        ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kQ * 128), &tm_q, h * HD + 64 * a, qt * 128, b, qf);
+        ptx::tma_load_3d(ptx::smem_u32(sDO + a * Cfg::kQ * 128), &tm_do, h * HD + 64 * a, qt * 128, b, qf);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_steps; ++n) {
+        const int st = n & 1, u = n >> 1;
+        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        const uint32_t kf = ptx::smem_u32(&bars->kv_full[st]);
+        ptx::mbar_arrive_expect_tx(kf, 2 * Cfg::kKTile);
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a) {
+          ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kKTile + a * Cfg::kKeys * 128), &tm_k, g.C + kh * HD + 64 * a,
+                           n * 64, b, kf);
+          ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kKTile + a * Cfg::kKeys * 128), &tm_v,
+                           g.C + g.NKV * HD + kh * HD + 64 * a, n * 64, b, kf);
+        }
+        issued = n + 1;
+      }
+      if (*abort_flag) {
+        ptx::mbar_wait(qf, 0, nullptr, kWaitLimitNs);
+        for (int st = 0; st < 2 && st < issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
+      const uint32_t aQ = ptx::smem_u32(sQ), aDO = ptx::smem_u32(sDO), aK = ptx::smem_u32(sK),
+                     aV = ptx::smem_u32(sV), aDS = ptx::smem_u32(sDS);
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
+
+      auto issue_dq = [&](int m) -> bool {
+        const int st = m & 1, u = m >> 1;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kKeys / 16; ++kk) {
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::sw128_desc(aDS + st * Cfg::kSTile + kk * 32, 16, 1024),
+                           ptx::sw128_desc(aK + st * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
+                           (m > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->ds_free[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[st]));
+        return true;
+      };
+
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n & 1, u = n >> 1;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), u & 1, abort_flag, kWaitLimitNs);
+        if (ok && n >= 2)
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t oq = (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
+          const uint32_t ok_ = st * Cfg::kKTile + (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
+          ptx::mma_bf16_ss(d_s, ptx::sw128_desc(aQ + oq, 16, 1024), ptx::sw128_desc(aK + ok_, 16, 1024), idesc_s,
+                           kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_dp, ptx::sw128_desc(aDO + oq, 16, 1024), ptx::sw128_desc(aV + ok_, 16, 1024), idesc_s,
+                           kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
+        if (n >= 1) ok = issue_dq(n - 1);
+      }
+      if (ok) ok = issue_dq(n_steps - 1);
+      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (!ok) fail();
+      ptx::mma_commit(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;           // query row within the tile
+    const int tq = qt * 128 + row;
+    const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = g.scale * kLog2e;
+    const size_t ridx = ((size_t)b * g.NH + h) * g.T + tq;
+    const float lse2 = (tq < g.T) ? lse[ridx] * kLog2e : 0.f;   // padding rows have dO = 0, so dS = 0
+    const float drow = (tq < g.T) ? Drow[ridx] : 0.f;
+    bool ok = true;
+    for (int n = 0; n < n_steps; ++n) {
+      const int st = n & 1, u = n >> 1;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
+      uint32_t dw[32];
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld32(t_lane + st * 128 + c0, sr);
+        ptx::tmem_ld32(t_lane + st * 128 + 64 + c0, dr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float pv = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -lse2));
+            if (diag && n * 64 + c0 + c + e > tq) pv = 0.f;  // key after query: masked
+            ds[e] = pv * (__uint_as_float(dr[c + e]) - drow);
+          }
+          dw[(c0 + c) / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
+      if (n >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+      }
+      store_row64(sDS + st * Cfg::kSTile, row, dw);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full[st]));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
+    if (ok) {
+      ptx::tc_fence_after();
+      const bool store = tq < g.T;
+      __nv_bfloat16* dst = dqkv + ((size_t)b * g.T + (store ? tq : 0)) * g.W + h * HD;
+      store_grad_row<HD>(t_lane + Cfg::kTmemDQ, g.scale, ROPE, tq, g, dst, store);
+    } else {
+      fail();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int HD, bool ROPE>
+cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
+  const Geometry& g = a.g;
+  auto k1 = bwd_dkdv_kernel<HD, ROPE>;
+  auto k2 = bwd_dq_kernel<HD, ROPE>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<HD>::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<HD>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
+  k1<<<grid1, kThreads, DkdvCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_v[1], a.tm_qk[0], a.tm_do[0],
+                                                          (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
+  k2<<<grid2, kThreads, DqCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_do[1], a.tm_qk[0], a.tm_v[0],
+                                                        (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc05_bwd_launch(const Tc05BwdArgs& a, cudaStream_t stream) {
+  const bool rope = a.g.rope_theta > 0.f;
+  if (a.g.hd == 128) return rope ? launch_bwd<128, true>(a, stream) : launch_bwd<128, false>(a, stream);
+  if (a.g.hd == 64) return rope ? launch_bwd<64, true>(a, stream) : launch_bwd<64, false>(a, stream);
+  return cudaErrorInvalidValue;
+}
 
 }  // namespace attn

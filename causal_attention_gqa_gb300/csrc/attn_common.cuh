@@ -22,6 +22,10 @@ struct Geometry {
   int W;         // packed row width (NH + 2*NKV) * hd
   float scale;   // 1 / sqrt(hd)
   float rope_theta;  // <= 0: no RoPE
+  // RoPE inverse frequencies theta^(-2i/hd), i < hd/2, as float head + tail
+  // (computed once on the host in double precision).
+  float rope_f_hi[64];
+  float rope_f_lo[64];
 };
 
 // Record the first device-side error in the library status word.
@@ -35,15 +39,6 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 //   y_i        = x_i cos(a) - x_{i+hd/2} sin(a)
 //   y_{i+hd/2} = x_{i+hd/2} cos(a) + x_i sin(a)
 // ---------------------------------------------------------------------------
-
-// Inverse frequency theta^(-2i/hd), split into a float head and tail so that
-// t * (hi + lo) can be formed with about 2^-40 relative error.  Double
-// precision is used once per frequency, never per element.
-__device__ __forceinline__ void rope_inv_freq(float theta, int i, int hd, float& hi, float& lo) {
-  double f = exp(-2.0 * (double)i * log((double)theta) / (double)hd);
-  hi = (float)f;
-  lo = (float)(f - (double)hi);
-}
 
 // The angle t * f reduced to about [-pi, pi], good to ~1e-6 rad for any
 // t < 2^24.  The product is formed error-free with an FMA (Dekker's

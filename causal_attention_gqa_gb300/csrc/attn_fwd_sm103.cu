@@ -79,12 +79,13 @@ struct TileRotator {
   float f_hi[8], f_lo[8], step_c[8], step_s[8];
   int p, r0;
 
-  __device__ void init(int tid, float theta) {
+  __device__ void init(int tid, const Geometry& g) {
     p = tid % NCH;
     r0 = tid / NCH;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      rope_inv_freq(theta, 8 * p + e, HD, f_hi[e], f_lo[e]);
+      f_hi[e] = g.rope_f_hi[8 * p + e];
+      f_lo[e] = g.rope_f_lo[8 * p + e];
       __sincosf(rope_angle(RS, f_hi[e], f_lo[e]), &step_s[e], &step_c[e]);
     }
   }
@@ -387,7 +388,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
     // ------------------------------------------------------------ RoPE transform
     const int tid = threadIdx.x - kRopeWarp0 * 32;
     TileRotator<HD> rot;
-    rot.init(tid, g.rope_theta);
+    rot.init(tid, g);
     bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs));
     if (ok) {
       rot.rotate(sQ, q0);

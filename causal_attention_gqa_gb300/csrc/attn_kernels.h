@@ -42,15 +42,16 @@ cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream);
 
 struct Tc05BwdArgs {
   Geometry g;
-  CUtensorMap tm_q;    // Q source (qkv or rotated copy), box {64,128,1}
-  CUtensorMap tm_k;    // K source (qkv or rotated copy), box {64,128,1}
-  CUtensorMap tm_v;    // qkv (V columns), box {64,128,1}
-  CUtensorMap tm_do;   // dout, box {64,128,1}
-  int q_col0;          // column of query head 0 in the Q source
-  int k_col0;          // column of kv head 0 in the K source
-  void* dqkv;          // [B,T,W] bf16
-  const float* lse;    // [B,NH,T]
-  const float* Drow;   // [B,NH,T]
+  // Tensor maps with 128-byte swizzle and 64-column boxes; index 0 has 64-row
+  // boxes, index 1 128-row boxes.  Q and K come from the same source (qkv, or
+  // the rotated copy when RoPE is on); query head h starts at column h*hd and
+  // kv head kh at column C + kh*hd in both layouts.
+  CUtensorMap tm_qk[2];
+  CUtensorMap tm_v[2];   // over qkv
+  CUtensorMap tm_do[2];  // over dout
+  void* dqkv;            // [B,T,W] bf16
+  const float* lse;      // [B,NH,T]
+  const float* Drow;     // [B,NH,T]
   int* status;
 };
 cudaError_t tc05_bwd_launch(const Tc05BwdArgs& a, cudaStream_t stream);

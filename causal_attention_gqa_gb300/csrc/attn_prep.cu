@@ -67,7 +67,10 @@ __global__ void __launch_bounds__(256) row_dot_bf16_vec_kernel(float* __restrict
 __global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
                                                            const __nv_bfloat16* __restrict__ qkv, Geometry g) {
   __shared__ float f_hi[64], f_lo[64];
-  for (int i = threadIdx.x; i < g.hd / 2; i += blockDim.x) rope_inv_freq(g.rope_theta, i, g.hd, f_hi[i], f_lo[i]);
+  for (int i = threadIdx.x; i < 64; i += blockDim.x) {
+    f_hi[i] = g.rope_f_hi[i];
+    f_lo[i] = g.rope_f_lo[i];
+  }
   __syncthreads();
   const int half = g.hd / 2, groups = half / 8;
   const int heads = g.NH + g.NKV;

@@ -60,8 +60,10 @@ __device__ void load_head_tile(float* dst, const float* src, const Geometry& g, 
 }
 
 __device__ void init_rope_freqs(const Geometry& g, float* f_hi, float* f_lo) {
-  if (g.rope_theta > 0.f)
-    for (int i = threadIdx.x; i < g.hd / 2; i += blockDim.x) rope_inv_freq(g.rope_theta, i, g.hd, f_hi[i], f_lo[i]);
+  for (int i = threadIdx.x; i < 64; i += blockDim.x) {
+    f_hi[i] = g.rope_f_hi[i];
+    f_lo[i] = g.rope_f_lo[i];
+  }
 }
 
 // Write `rows` rows of a float32 gradient tile (pitch hd+1 in shared memory)
