@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Causal MHA/GQA attention forward + backward throughput on GB300.
+
+One step = attn_fwd + attn_bwd (with its prologue kernels) over one batch of
+the synthetic workload, through the library's C ABI.  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gqa_block|long_context_gqa|gpt2_124m_mha]
+
+Metric: causal attention fwd+bwd TFLOP/s with the algorithmic causal FLOP
+count (pairs = T(T+1)/2, fwd = 4*B*NH*hd*pairs, bwd = 2.5*fwd).  Under
+torchrun (N > 1) every rank runs an independent replica of the workload
+(the path shards over batch rows and kv groups with no exchange); the value is
+the work of all ranks divided by the slowest rank's time.
+
+`--impl reference` times the float64 CPU oracle instead (rank 0 only), on a
+bounded sample of the same workload: one kv group of one batch row per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd+bwd TFLOP/s on 1 GB300; % of BF16 tensor peak"
+FLUSH_BYTES = 256 << 20          # > 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "fwd_tc05": "attn_fwd_sm103.cu", "bwd_dkdv_tc05": "attn_bwd_sm103.cu", "bwd_dq_tc05": "attn_bwd_sm103.cu",
+    "bwd_row_dot": "attn_prep.cu", "bwd_rope_qk": "attn_prep.cu",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_block")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_of(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "T": w.T, "C": w.C, "NH": w.NH, "NKV": w.NKV, "hd": w.hd,
+           "rope_theta": w.rope_theta, "qkv_std": w.qkv_std, "dout_std": w.dout_std, "seed": w.seed}
+    cfg.update(extra or {})
+    return cfg
+
+
+def flops_per_step(w):
+    return w.flops_fwd() + w.flops_bwd()
+
+
+def oracle_sample(w):
+    """One kv group of batch row 0 as a standalone problem (NH = grp, NKV = 1)."""
+    import numpy as np
+    from causal_attention_gqa_gb300.workloads import make_inputs
+    qkv, dout = make_inputs(w, "bf16")
+    hd, grp = w.hd, w.NH // w.NKV
+    q = qkv[:1, :, :grp * hd]
+    k = qkv[:1, :, w.C:w.C + hd]
+    v = qkv[:1, :, w.C + w.NKV * hd:w.C + w.NKV * hd + hd]
+    sub_qkv = np.ascontiguousarray(np.concatenate([q, k, v], axis=2))
+    sub_dout = np.ascontiguousarray(dout[:1, :, :grp * hd])
+    sub = w.replace(B=1, C=grp * hd, NH=grp, NKV=1)
+    return sub, sub_qkv, sub_dout
+
+
+def time_oracle(w, min_seconds=10.0, max_reps=50):
+    """Time the oracle's forward+backward on the bounded sample; TFLOP/s."""
+    import oracle
+    sub, qkv, dout = oracle_sample(w)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_backward(qkv, dout, sub.C, sub.NH, sub.NKV, sub.rope_theta, return_aux=True)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {
+        "value": flops_per_step(sub) * reps / el / 1e12,
+        "unit": "TFLOP/s",
+        "cores": cores,
+        "kind": "oracle",
+        "sample": f"float64 NumPy oracle fwd+bwd of one kv group ({sub.NH} query heads, T={sub.T}, "
+                  f"hd={sub.hd}) of batch row 0, x{reps} in {el:.1f} s",
+        "seconds": el,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "causal_attention_gqa_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec.get("bytes_per_launch") if rec.get("source_sha256") == sha else None
+
+
+def kernel_algorithmic_flops(name, w):
+    """Algorithmic FLOPs one launch of `name` processes (causal pairs only).
+    One GEMM-unit = 2*B*NH*hd*pairs; the forward is 2 units (QK^T, PV); the
+    dK/dV kernel covers 4 (S, dP, dV, dK); the dQ kernel 1 (dQ; its S and dP
+    recomputation is extra work, not counted)."""
+    unit = 2.0 * w.B * w.NH * w.hd * w.causal_pairs
+    return {"fwd_tc05": 2 * unit, "bwd_dkdv_tc05": 4 * unit, "bwd_dq_tc05": 1 * unit}.get(name)
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    sub, qkv, dout = oracle_sample(w)
+    for _ in range(args.warmup):
+        oracle.attention_backward(qkv, dout, sub.C, sub.NH, sub.NKV, sub.rope_theta, return_aux=True)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_backward(qkv, dout, sub.C, sub.NH, sub.NKV, sub.rope_theta, return_aux=True)
+    el = time.perf_counter() - t0
+    value = flops_per_step(sub) * args.steps / el / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, {"sample": "one kv group of batch row 0 per step"}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"float64 NumPy oracle fwd+bwd of one kv group ({sub.NH} query heads, "
+                                   f"T={sub.T}, hd={sub.hd}) of batch row 0 per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from causal_attention_gqa_gb300 import binding
+    from causal_attention_gqa_gb300.workloads import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    binding.load()
+
+    B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
+    qkv_np, dout_np = make_inputs(w, "bf16")
+    qkv_host = torch.from_numpy(qkv_np).to(torch.bfloat16).pin_memory()
+    dout_host = torch.from_numpy(dout_np).to(torch.bfloat16).pin_memory()
+    qkv = qkv_host.to(dev)
+    dout = dout_host.to(dev)
+    out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
+    dqkv = torch.empty_like(qkv)
+    dqkv_host = torch.empty(dqkv.shape, dtype=torch.bfloat16).pin_memory()
+    ws_bytes = binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    code = binding.DTYPE_BF16
+
+    def step():
+        binding.attn_fwd(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, sptr)
+        binding.attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, w.rope_theta, code, ws, ws_bytes, sptr)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+    if binding.attn_device_status() != 0:
+        raise RuntimeError("device-side error recorded during warm-up")
+
+    # ---- device-resident timed region: K steps, L2 flushed between steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.15)
+    barrier()
+    binding.attn_profile_start()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    prof = binding.attn_profile_stop()
+    clocks = sampler.stop()
+    ms_steps = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_per_step = sum(ms_steps) / args.steps
+    if binding.attn_device_status() != 0:
+        raise RuntimeError("device-side error recorded during the timed region")
+
+    # ---- end to end through the C ABI with host buffers
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 50))
+    barrier()
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        qkv.copy_(qkv_host, non_blocking=True)
+        dout.copy_(dout_host, non_blocking=True)
+        step()
+        dqkv_host.copy_(dqkv, non_blocking=True)
+    e_end.record(stream)
+    barrier()
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+
+    t = torch.tensor([ms_per_step, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step, e2e_ms = float(t[0]), float(t[1])
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    fl = flops_per_step(w)
+    value = world * fl / (ms_per_step * 1e-3) / 1e12
+    e2e_value = world * fl / (e2e_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+
+    # dominant kernel by device time in the timed region
+    kernel_ms = {k: v[1] for k, v in prof.items()}
+    dom = max(kernel_ms, key=kernel_ms.get)
+    n_launch, tot_ms = prof[dom]
+    kfl = kernel_algorithmic_flops(dom, w)
+    roofline = None
+    if kfl is not None:
+        achieved = kfl / (tot_ms / n_launch * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": achieved / peak_tf, "traffic": traffic_for(dom),
+                    "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a step loop)",
+                    "avg_launch_ms": tot_ms / n_launch,
+                    "algorithmic_flop_per_launch": kfl}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                                "peak_bf16_frac": value / world / peak_tf,
+                                "wall_s_timed_region": wall}),
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": qkv_host.numel() * 2 + dout_host.numel() * 2,
+                "d2h_bytes_per_step": dqkv_host.numel() * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": int(sum(v[0] for v in prof.values())),
+        "kernels": {k: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / sum(kernel_ms.values())}
+                    for k, v in prof.items()},
+        "roofline": roofline,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in time_oracle(w).items() if k != "seconds"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from causal_attention_gqa_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

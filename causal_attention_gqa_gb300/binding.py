@@ -71,6 +71,12 @@ def load() -> ctypes.CDLL:
     lib.attn_selftest_wait_timeout.restype = i
     lib.attn_abi_version.argtypes = []
     lib.attn_abi_version.restype = i
+    lib.attn_profile_start.argtypes = []
+    lib.attn_profile_start.restype = i
+    lib.attn_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i), i]
+    lib.attn_profile_stop.restype = i
+    lib.attn_kernel_name.argtypes = [i]
+    lib.attn_kernel_name.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -136,6 +142,21 @@ def attn_selftest_wait_timeout(limit_ns: int) -> int:
     v = ctypes.c_int(0)
     _check(load().attn_selftest_wait_timeout(int(limit_ns), ctypes.byref(v)), "attn_selftest_wait_timeout")
     return v.value
+
+
+N_KERNEL_IDS = 8
+
+
+def attn_profile_start() -> None:
+    _check(load().attn_profile_start(), "attn_profile_start")
+
+
+def attn_profile_stop() -> dict:
+    """{kernel name: (launches, total ms)} for kernels launched since start."""
+    ms = (ctypes.c_double * N_KERNEL_IDS)()
+    n = (ctypes.c_int * N_KERNEL_IDS)()
+    _check(load().attn_profile_stop(ms, n, N_KERNEL_IDS), "attn_profile_stop")
+    return {load().attn_kernel_name(k).decode(): (n[k], ms[k]) for k in range(N_KERNEL_IDS) if n[k]}
 
 
 # ---------------------------------------------------------------------------

@@ -26,6 +26,7 @@
 // elementwise work and the epilogue.  All waits are bounded.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
+#include "attn_profile.h"
 #include "attn_ptx.cuh"
 
 namespace attn {
@@ -606,13 +607,17 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<HD>::kSmemBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
+  prof_begin(kKernelBwdDkdvTc05, stream);
   k1<<<grid1, kThreads, DkdvCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_v[1], a.tm_qk[0], a.tm_do[0],
                                                           (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+  prof_end(kKernelBwdDkdvTc05, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
+  prof_begin(kKernelBwdDqTc05, stream);
   k2<<<grid2, kThreads, DqCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_do[1], a.tm_qk[0], a.tm_v[0],
                                                         (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+  prof_end(kKernelBwdDqTc05, stream);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@
 // and exits.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
+#include "attn_profile.h"
 #include "attn_ptx.cuh"
 
 namespace attn {
@@ -426,7 +427,9 @@ cudaError_t launch_fwd(const Tc05FwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_qt = (a.g.T + kBM - 1) / kBM;
   const unsigned grid = (unsigned)(n_qt * a.g.B * a.g.NH);
+  prof_begin(kKernelFwdTc05, stream);
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qkv, (__nv_bfloat16*)a.out, a.lse, a.status, a.g);
+  prof_end(kKernelFwdTc05, stream);
   return cudaGetLastError();
 }
 

@@ -10,6 +10,7 @@
 // instead of once per use.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
+#include "attn_profile.h"
 
 namespace attn {
 namespace {
@@ -111,6 +112,7 @@ cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Ge
                            cudaStream_t stream) {
   const long long rows = (long long)g.B * g.T;
   const int blocks = (int)((rows + 7) / 8);
+  prof_begin(kKernelBwdRowDot, stream);
   if (bf16 && g.hd % 8 == 0 && (g.hd / 8) <= 32 && ((g.hd / 8) & (g.hd / 8 - 1)) == 0) {
     row_dot_bf16_vec_kernel<<<blocks, 256, 0, stream>>>(D, (const uint4*)out, (const uint4*)dout, g);
   } else if (bf16) {
@@ -119,6 +121,7 @@ cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Ge
   } else {
     row_dot_kernel<float><<<blocks, 256, 0, stream>>>(D, (const float*)out, (const float*)dout, g);
   }
+  prof_end(kKernelBwdRowDot, stream);
   return cudaGetLastError();
 }
 
@@ -126,7 +129,9 @@ cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, c
   const long long total = (long long)g.B * g.T * (g.NH + g.NKV) * (g.hd / 16);
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
+  prof_begin(kKernelBwdRopeQK, stream);
   rope_qk_bf16_kernel<<<(int)blocks, 256, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g);
+  prof_end(kKernelBwdRopeQK, stream);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,7 @@
 // tile and sums dQ over its key tiles.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
+#include "attn_profile.h"
 
 #include <math.h>
 
@@ -368,8 +369,10 @@ cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
     size_t smem = 3 * kTile * pitch * sizeof(float) + freq_bytes;
     cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    prof_begin(kKernelFwdSimt, stream);
     simt_fwd_kernel<DPL><<<dim3(n_tiles, g.NH, g.B), kThreads, smem, stream>>>(
         (float*)a.out, a.lse, (const float*)a.qkv, g);
+    prof_end(kKernelFwdSimt, stream);
     return cudaGetLastError();
   }
   size_t smem_kv = 4 * kTile * pitch * sizeof(float) + 2 * kTile * sizeof(float) + freq_bytes;
@@ -379,12 +382,16 @@ cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(simt_bwd_dq_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q);
   if (e != cudaSuccess) return e;
+  prof_begin(kKernelBwdDkdvSimt, stream);
   simt_bwd_dkdv_kernel<DPL><<<dim3(n_tiles, g.NKV, g.B), kThreads, smem_kv, stream>>>(
       (float*)a.dqkv, (const float*)a.qkv, (const float*)a.dout, a.lse, a.Drow, g);
+  prof_end(kKernelBwdDkdvSimt, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  prof_begin(kKernelBwdDqSimt, stream);
   simt_bwd_dq_kernel<DPL><<<dim3(n_tiles, g.NH, g.B), kThreads, smem_q, stream>>>(
       (float*)a.dqkv, (const float*)a.qkv, (const float*)a.dout, a.lse, a.Drow, g);
+  prof_end(kKernelBwdDqSimt, stream);
   return cudaGetLastError();
 }
 

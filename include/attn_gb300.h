@@ -140,6 +140,22 @@ ATTN_API int attn_device_status(int* status, int reset);
  */
 ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
 
+/*
+ * Per-kernel timing (tracing aid; not part of the attention method).
+ * attn_profile_start -- from now on, bracket every kernel this library
+ *   launches (any thread, any stream) with a pair of CUDA events recorded on
+ *   the launching stream.  Clears earlier records.
+ * attn_profile_stop -- stop recording, wait for the recorded events, and for
+ *   kernel ids 0..n-1 store the summed elapsed milliseconds in total_ms[id]
+ *   and the launch count in launches[id] (either array may be NULL).
+ * attn_kernel_name -- short name of kernel id (see attn_profile.h ids:
+ *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 bwd_rope_qk,
+ *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt); "unknown" otherwise.
+ */
+ATTN_API int attn_profile_start(void);
+ATTN_API int attn_profile_stop(double* total_ms, int* launches, int n);
+ATTN_API const char* attn_kernel_name(int id);
+
 /* attn_abi_version -- ABI version of this header (currently 1). */
 ATTN_API int attn_abi_version(void);
 
