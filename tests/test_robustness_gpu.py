@@ -35,7 +35,7 @@ def test_guard_bands_untouched(lib, dtype):
     qkv, dout = to_device(qkv_np, dtype), to_device(dout_np, dtype)
     tdt = qkv.dtype
     pad = 4096
-    canary = -12345.0
+    canary = -12288.0  # exactly representable in bf16 and float32
 
     def guarded(n, dt):
         buf = torch.full((pad + n + pad,), canary, dtype=dt, device="cuda")
