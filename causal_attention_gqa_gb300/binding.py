@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.attn_selftest_wait_timeout.restype = i
     lib.attn_abi_version.argtypes = []
     lib.attn_abi_version.restype = i
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.attn_bwd_noalloc.restype = i
     lib.attn_profile_start.argtypes = []
     lib.attn_profile_start.restype = i
     lib.attn_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i), i]
@@ -130,6 +132,15 @@ def attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, wor
     st = load().attn_bwd(_ptr(dqkv), _ptr(qkv), _ptr(out), _ptr(dout), _ptr(lse), B, T, C, NH, NKV,
                          float(rope_theta), int(dtype), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "attn_bwd")
+
+
+def attn_bwd_noalloc(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, stream=None) -> None:
+    """attn_bwd without a workspace argument, for callers that cannot allocate
+    device memory; uses the library's built-in scratch buffer (see the header
+    for its size limit and the rule that overlapping calls race)."""
+    st = load().attn_bwd_noalloc(_ptr(dqkv), _ptr(qkv), _ptr(out), _ptr(dout), _ptr(lse), B, T, C, NH, NKV,
+                                 float(rope_theta), int(dtype), _stream(stream))
+    _check(st, "attn_bwd_noalloc")
 
 
 def attn_device_status(reset: bool = False) -> int:

@@ -120,6 +120,41 @@ ATTN_API int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* 
              float rope_theta, int dtype, void* workspace, size_t workspace_bytes,
              void* stream);
 
+/*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device
+ * memory.  (The source pages have no counterpart: this is a library
+ * convenience, not part of the attention method.)
+ *
+ * Some callers cannot obtain scratch memory when they run the backward:
+ * code running inside a custom allocator or memory-pool callback (calling
+ * cudaMalloc there would re-enter the allocator), runtimes that forbid
+ * device allocation after start-up so that memory use stays fixed, and
+ * plugins that are handed only input and output pointers.  This entry point
+ * takes the same arguments as attn_bwd minus the workspace, and uses a
+ * built-in device buffer of ATTN_NOALLOC_SCRATCH_BYTES instead.  It calls no
+ * allocating routine.
+ *
+ * Limits and behaviour:
+ *  - The buffer is a fixed array in device memory: every GPU on which it is
+ *    loaded holds ATTN_NOALLOC_SCRATCH_BYTES until the process exits.
+ *  - Problems whose attn_bwd_workspace_bytes() exceeds that size are
+ *    rejected with ATTN_ERR_WORKSPACE before anything is launched (e.g. the
+ *    bf16 B=4, T=2048, NH=16, NKV=4, hd=128 case needs about 42.5 MB and
+ *    fits; B=1, T=8192, NH=32, NKV=8, hd=128 needs about 85 MB and does not).
+ *  - The first call on a device (with that device current) looks up the
+ *    buffer's device address; make that first call before any stream
+ *    capture on that device.
+ *  - All calls share the one buffer, which keeps the last call's contents.
+ *    Nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *    the GPU (different streams, or different host threads) race on it and
+ *    give wrong results: serialise them.
+ * Other arguments, results and errors are those of attn_bwd.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+ATTN_API int attn_bwd_noalloc(void* dqkv, const void* qkv, const void* out, const void* dout,
+                              const float* lse, int B, int T, int C, int NH, int NKV,
+                              float rope_theta, int dtype, void* stream);
+
 /* attn_strerror -- static description of a status code; never NULL. */
 ATTN_API const char* attn_strerror(int status);
 
