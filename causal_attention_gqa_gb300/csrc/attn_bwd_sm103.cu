@@ -22,8 +22,12 @@
 //    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
 //    dQ += dS K accumulates in TMEM.
 // Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// warps 2-5 one TMEM lane (one key or query row) per thread for the
-// elementwise work and the epilogue.  All waits are bounded.
+// and two elementwise warpgroups (warps 2-5 take the even steps, warps 6-9
+// the odd ones, each with its own TMEM and shared-memory buffers) with one
+// TMEM lane (one key or query row) per thread; they also split the epilogue.
+// Two steps are in flight at once, so one group's exp/pack/store chain runs
+// while the tensor core works on the other group's MMAs.  All waits are
+// bounded.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
 #include "attn_profile.h"
@@ -33,16 +37,17 @@ namespace attn {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Store 64 bf16 values (32 packed words) as row `row` of a 64-column swizzled
-// tile (one atom column).
-__device__ __forceinline__ void store_row64(uint8_t* tile, int row, const uint32_t (&w)[32]) {
+// Store 16 packed words (32 bf16) at columns 32*half .. 32*half+31 of row
+// `row` of a 64-column swizzled tile.
+__device__ __forceinline__ void store_row_half(uint8_t* tile, int row, int half, const uint32_t (&w)[16]) {
 #pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
+  for (int q = 0; q < 4; ++q) {
+    const int ch = half * 4 + q;
     *reinterpret_cast<uint4*>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) =
-        make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   }
 }
 
@@ -57,12 +62,14 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* f, float s) {
 // multiply by `s`, undo the RoPE rotation at position `t` if `rope`, round to
 // bf16 and store to `dst` (HD contiguous bf16; only if `store`).  Every lane of
 // the warp must call this (tcgen05.ld is warp-collective).
+// Chunks of 32 columns (32 pairs with RoPE) are dealt round-robin to
+// `nparts` callers; this caller handles part `part`.
 template <int HD>
 __device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope, int t, const Geometry& g,
-                                               __nv_bfloat16* dst, bool store) {
+                                               __nv_bfloat16* dst, bool store, int part, int nparts) {
   if (!rope) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < HD; c0 += 32) {
+    for (int c0 = 32 * part; c0 < HD; c0 += 32 * nparts) {
       uint32_t v[32];
       ptx::tmem_ld32(acc + c0, v);
       ptx::tmem_wait_ld();
@@ -75,7 +82,7 @@ __device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope,
   }
   constexpr int HALF = HD / 2;
 #pragma unroll 1
-  for (int c0 = 0; c0 < HALF; c0 += 32) {
+  for (int c0 = 32 * part; c0 < HALF; c0 += 32 * nparts) {
     uint32_t lo[32], hi[32];
     ptx::tmem_ld32(acc + c0, lo);
     ptx::tmem_ld32(acc + HALF + c0, hi);
@@ -108,22 +115,25 @@ struct DkdvCfg {
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
   static constexpr int kPTile = kKeys * kQ * 2;        // P^T or dS^T (one atom column)
+  // Q/dO ring depth: loads for step n+NQS-1 are in flight while step n runs.
+  static constexpr int kQStages = (HD == 128) ? 3 : 4;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKTile;
   static constexpr int kQOff = kVOff + kKTile;
-  static constexpr int kDOOff = kQOff + 2 * kQTile;
-  static constexpr int kPOff = kDOOff + 2 * kQTile;
+  static constexpr int kDOOff = kQOff + kQStages * kQTile;
+  static constexpr int kPOff = kDOOff + kQStages * kQTile;
   static constexpr int kDSOff = kPOff + 2 * kPTile;
   static constexpr int kLseOff = kDSOff + 2 * kPTile;
-  static constexpr int kDOff = kLseOff + 2 * kQ * 4;
-  static constexpr int kBarOff = kDOff + 2 * kQ * 4;
+  static constexpr int kDOff = kLseOff + kQStages * kQ * 4;
+  static constexpr int kBarOff = kDOff + kQStages * kQ * 4;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "dK/dV kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DkdvBarriers {
   uint64_t kv_full, acc_done, drain;
-  uint64_t qdo_full[2], qdo_empty[2], s_full[2], s_free[2], p_full[2], pds_free[2];
+  uint64_t qdo_full[4], qdo_empty[4], s_full[2], s_free[2], p_full[2], pds_free[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -135,6 +145,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
                 int* __restrict__ status, Geometry g) {
   using Cfg = DkdvCfg<HD>;
+  constexpr int NQS = Cfg::kQStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem + Cfg::kKOff;
@@ -161,9 +172,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NQS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 2);
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 4);
@@ -199,7 +212,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
     }
     for (int n = 0; n < n_steps; ++n) {
-      const int st = n & 1, u = n >> 1;
+      const int st = n % NQS, u = n / NQS;
       const int h = kh * g.grp + n / nq, qi = 2 * j + n % nq;
       int ok = 1;
       if (lane == 0 && u > 0)
@@ -232,8 +245,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     if (lane == 0 && *abort_flag) {
       ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, nullptr, kWaitLimitNs);
-      for (int st = 0; st < 2 && st < issued; ++st)
-        ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), ((issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
+      for (int st = 0; st < NQS && st < issued; ++st)
+        ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), ((issued - 1 - st) / NQS) & 1, nullptr, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -245,25 +258,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
 
       auto issue_grad = [&](int m) -> bool {
-        const int st = m & 1, u = m >> 1;
+        const int st = m & 1, u = m >> 1, qs = m % NQS;
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < Cfg::kQ / 16; ++kk) {
           const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
           ptx::mma_bf16_ss(tmem + Cfg::kTmemDV, ptx::sw128_desc(aP + st * Cfg::kPTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aDO + st * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
+                           ptx::sw128_desc(aDO + qs * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
           ptx::mma_bf16_ss(tmem + Cfg::kTmemDK, ptx::sw128_desc(aDS + st * Cfg::kPTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aQ + st * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
+                           ptx::sw128_desc(aQ + qs * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->pds_free[st]));
-        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
         return true;
       };
 
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, u = n >> 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), u & 1, abort_flag, kWaitLimitNs);
+        const int st = n & 1, u = n >> 1, qs = n % NQS;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
         if (ok && n >= 2)
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
@@ -272,7 +285,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t ok_ = (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
-          const uint32_t oq = st * Cfg::kQTile + (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
+          const uint32_t oq = qs * Cfg::kQTile + (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
           ptx::mma_bf16_ss(d_s, ptx::sw128_desc(aK + ok_, 16, 1024), ptx::sw128_desc(aQ + oq, 16, 1024), idesc_s,
                            kk > 0 ? 1u : 0u);
           ptx::mma_bf16_ss(d_dp, ptx::sw128_desc(aV + ok_, 16, 1024), ptx::sw128_desc(aDO + oq, 16, 1024), idesc_s,
@@ -289,25 +302,30 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
+    const int wg = (warp - 2) >> 2;                // this group takes steps n = wg, wg+2, ...
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;           // key row within the tile
     const int ks = j * 128 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = g.scale * kLog2e;
     bool ok = true;
-    for (int n = 0; n < n_steps; ++n) {
-      const int st = n & 1, u = n >> 1;
+    for (int n = wg; n < n_steps; n += 2) {
+      const int st = wg, u = n >> 1;
       const int qi = 2 * j + n % nq;
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
+      // P/dS buffer `st` is free once the MMAs of step n-2 retired (they were
+      // issued before this step's S and dP, so this returns at once).
+      if (ok && n >= 2)
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(ptx::smem_u32(&bars->pds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       const bool diag = qi <= 2 * j + 1;           // this query tile overlaps the key tile
-      const float* lse2 = sLse + st * Cfg::kQ;
-      const float* dd = sD + st * Cfg::kQ;
-      uint32_t pw[32], dw[32];
+      const float* lse2 = sLse + (n % NQS) * Cfg::kQ;
+      const float* dd = sD + (n % NQS) * Cfg::kQ;
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32], dr[32], pw[16], dw[16];
         ptx::tmem_ld32(t_lane + st * 128 + c0, sr);
         ptx::tmem_ld32(t_lane + st * 128 + 64 + c0, dr);
         ptx::tmem_wait_ld();
@@ -322,20 +340,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             p[e] = pv;
             ds[e] = pv * (__uint_as_float(dr[c + e]) - dd[q]);
           }
-          pw[(c0 + c) / 2] = pack_bf16x2(p[0], p[1]);
-          dw[(c0 + c) / 2] = pack_bf16x2(ds[0], ds[1]);
+          pw[c / 2] = pack_bf16x2(p[0], p[1]);
+          dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
+        if (c0 == 32) {  // both chunks of S and dP are in registers: release the TMEM buffer
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
+        }
+        store_row_half(sP + st * Cfg::kPTile, row, c0 / 32, pw);
+        store_row_half(sDS + st * Cfg::kPTile, row, c0 / 32, dw);
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
-      if (n >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        ptx::mbar_wait(ptx::smem_u32(&bars->pds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
-        if (!ok) break;
-      }
-      store_row64(sP + st * Cfg::kPTile, row, pw);
-      store_row64(sDS + st * Cfg::kPTile, row, dw);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[st]));
@@ -345,8 +360,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       ptx::tc_fence_after();
       const bool store = ks < g.T;
       __nv_bfloat16* row_ptr = dqkv + ((size_t)b * g.T + (store ? ks : 0)) * g.W;
-      store_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, row_ptr + g.C + g.NKV * HD + kh * HD, store);
-      store_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, row_ptr + g.C + kh * HD, store);
+      store_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, row_ptr + g.C + g.NKV * HD + kh * HD, store,
+                         wg, 2);
+      store_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, row_ptr + g.C + kh * HD, store, wg, 2);
     } else {
       fail();
     }
@@ -370,21 +386,23 @@ struct DqCfg {
   static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kSTile = kQ * kKeys * 2;        // dS (one atom column)
+  static constexpr int kKStages = 4;                   // K/V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kQOff + kQTile;
   static constexpr int kKOff = kDOOff + kQTile;
-  static constexpr int kVOff = kKOff + 2 * kKTile;
-  static constexpr int kDSOff = kVOff + 2 * kKTile;
+  static constexpr int kVOff = kKOff + kKStages * kKTile;
+  static constexpr int kDSOff = kVOff + kKStages * kKTile;
   static constexpr int kBarOff = kDSOff + 2 * kSTile;
   // At least 116 KB so that two CTAs never share an SM: each allocates all
   // 512 TMEM columns, and a second resident CTA would only wait for them.
   static constexpr int kSmemBytes = (kBarOff + 256 + 1024) > 116 * 1024 ? (kBarOff + 256 + 1024) : 116 * 1024;
   static constexpr uint32_t kTmemDQ = 256, kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "dQ kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DqBarriers {
   uint64_t q_full, acc_done, drain;
-  uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], ds_full[2], ds_free[2];
+  uint64_t kv_full[4], kv_empty[4], s_full[2], s_free[2], ds_full[2], ds_free[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -396,6 +414,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
               int* __restrict__ status, Geometry g) {
   using Cfg = DqCfg<HD>;
+  constexpr int NKS = Cfg::kKStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
@@ -420,9 +439,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NKS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->kv_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 4);
@@ -456,7 +477,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       int issued = 0;
       for (int n = 0; n < n_steps; ++n) {
-        const int st = n & 1, u = n >> 1;
+        const int st = n % NKS, u = n / NKS;
         if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)) {
           fail();
           break;
@@ -474,8 +495,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       if (*abort_flag) {
         ptx::mbar_wait(qf, 0, nullptr, kWaitLimitNs);
-        for (int st = 0; st < 2 && st < issued; ++st)
-          ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
+        for (int st = 0; st < NKS && st < issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -488,23 +509,23 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
 
       auto issue_dq = [&](int m) -> bool {
-        const int st = m & 1, u = m >> 1;
+        const int st = m & 1, u = m >> 1, ks = m % NKS;
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < Cfg::kKeys / 16; ++kk) {
           ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::sw128_desc(aDS + st * Cfg::kSTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aK + st * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
+                           ptx::sw128_desc(aK + ks * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
                            (m > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->ds_free[st]));
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[ks]));
         return true;
       };
 
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, u = n >> 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), u & 1, abort_flag, kWaitLimitNs);
+        const int st = n & 1, u = n >> 1, ks = n % NKS;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[ks]), (n / NKS) & 1, abort_flag, kWaitLimitNs);
         if (ok && n >= 2)
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
@@ -513,7 +534,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
-          const uint32_t ok_ = st * Cfg::kKTile + (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
+          const uint32_t ok_ = ks * Cfg::kKTile + (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
           ptx::mma_bf16_ss(d_s, ptx::sw128_desc(aQ + oq, 16, 1024), ptx::sw128_desc(aK + ok_, 16, 1024), idesc_s,
                            kk > 0 ? 1u : 0u);
           ptx::mma_bf16_ss(d_dp, ptx::sw128_desc(aDO + oq, 16, 1024), ptx::sw128_desc(aV + ok_, 16, 1024), idesc_s,
@@ -530,6 +551,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
+    const int wg = (warp - 2) >> 2;                // this group takes steps n = wg, wg+2, ...
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;           // query row within the tile
     const int tq = qt * 128 + row;
@@ -539,16 +561,18 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float lse2 = (tq < g.T) ? lse[ridx] * kLog2e : 0.f;   // padding rows have dO = 0, so dS = 0
     const float drow = (tq < g.T) ? Drow[ridx] : 0.f;
     bool ok = true;
-    for (int n = 0; n < n_steps; ++n) {
-      const int st = n & 1, u = n >> 1;
+    for (int n = wg; n < n_steps; n += 2) {
+      const int st = wg, u = n >> 1;
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
+      if (ok && n >= 2)
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
-      uint32_t dw[32];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32], dr[32], dw[16];
         ptx::tmem_ld32(t_lane + st * 128 + c0, sr);
         ptx::tmem_ld32(t_lane + st * 128 + 64 + c0, dr);
         ptx::tmem_wait_ld();
@@ -561,18 +585,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (diag && n * 64 + c0 + c + e > tq) pv = 0.f;  // key after query: masked
             ds[e] = pv * (__uint_as_float(dr[c + e]) - drow);
           }
-          dw[(c0 + c) / 2] = pack_bf16x2(ds[0], ds[1]);
+          dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
+        if (c0 == 32) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
+        }
+        store_row_half(sDS + st * Cfg::kSTile, row, c0 / 32, dw);
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
-      if (n >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
-        if (!ok) break;
-      }
-      store_row64(sDS + st * Cfg::kSTile, row, dw);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full[st]));
@@ -582,7 +603,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::tc_fence_after();
       const bool store = tq < g.T;
       __nv_bfloat16* dst = dqkv + ((size_t)b * g.T + (store ? tq : 0)) * g.W + h * HD;
-      store_grad_row<HD>(t_lane + Cfg::kTmemDQ, g.scale, ROPE, tq, g, dst, store);
+      store_grad_row<HD>(t_lane + Cfg::kTmemDQ, g.scale, ROPE, tq, g, dst, store, wg, 2);
     } else {
       fail();
     }
