@@ -4,7 +4,8 @@
 // One CTA owns a 128-query tile of one (batch row, query head) and walks the
 // key tiles 0..qt (causal tile skipping: tiles entirely above the diagonal are
 // never loaded).  Warp roles:
-//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of stages.
+//   warp 0      TMA producer: Q once, then K_j and V_j into separate rings;
+//               K runs two tiles ahead of V so that S_j never waits on a load.
 //   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one
 //               of two TMEM score buffers, O += P_j V_j into the TMEM output.
 //   warps 2-5   softmax: thread = query row = TMEM lane.  Reads S_j, keeps the
@@ -41,14 +42,16 @@ template <int HD, bool ROPE>
 struct FwdCfg {
   static constexpr int kAtomBytes = kBM * 128;              // 128 rows x 128 B swizzle-atom column
   static constexpr int kTileBytes = kBM * HD * 2;           // Q / K / V tile
-  static constexpr int kStages = (HD == 128) ? 2 : 4;
+  static constexpr int kKStages = (HD == 128) ? 3 : 4;      // K ring depth
+  static constexpr int kVStages = (HD == 128) ? 2 : 4;      // V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kPOff = kQOff + kTileBytes;
   static constexpr int kPBytes = kBM * kBN * 2;
   static constexpr int kKOff = kPOff + kPBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // barriers + alignment slack
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + alignment slack
+  static_assert(kSmemBytes <= 232448, "forward kernel exceeds the 227 KB shared-memory limit");
   static constexpr int kThreads = ROPE ? 320 : 192;
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemCols = 512;
 };
@@ -56,7 +59,7 @@ struct FwdCfg {
 struct FwdBarriers {
   uint64_t q_full, q_ready, pv_done, p_full, drain;
   uint64_t s_full[2], s_free[2];
-  uint64_t k_full[4], v_full[4], k_ready[4], kv_empty[4];
+  uint64_t k_full[4], k_ready[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t tmem_base;
   int abort;
 };
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(FwdCfg<HD, ROPE>::kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
            int* __restrict__ status, Geometry g) {
   using Cfg = FwdCfg<HD, ROPE>;
-  constexpr int NS = Cfg::kStages;
+  constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
@@ -159,11 +162,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
     }
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < NK; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->v_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->k_ready[i]), 4);
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[i]), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->v_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[i]), 1);
     }
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -192,36 +198,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a)
         ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kAtomBytes), &tm_qkv, q_col + 64 * a, q0, b, q_full);
-      int issued = 0;
+      // Issue order: K_0, K_1, then V_j, K_{j+2} for j = 0, 1, ...
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % NS, u = j / NS;
-        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[s]), (u - 1) & 1, abort_flag, kWaitLimitNs)) {
-          fail();
-          ok = false;
-          break;
-        }
-        const uint32_t kf = ptx::smem_u32(&bars->k_full[s]), vf = ptx::smem_u32(&bars->v_full[s]);
-        uint8_t* k_dst = sK + s * Cfg::kTileBytes;
-        uint8_t* v_dst = sV + s * Cfg::kTileBytes;
+      auto load_k = [&](int j) -> bool {
+        const int st = j % NK, u = j / NK;
+        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs))
+          return false;
+        const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
         ptx::mbar_arrive_expect_tx(kf, Cfg::kTileBytes);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(k_dst + a * Cfg::kAtomBytes), &tm_qkv, k_col + 64 * a, j * kBN, b, kf);
+          ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv, k_col + 64 * a,
+                           j * kBN, b, kf);
+        k_issued = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j % NV, u = j / NV;
+        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs))
+          return false;
+        const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
         ptx::mbar_arrive_expect_tx(vf, Cfg::kTileBytes);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(v_dst + a * Cfg::kAtomBytes), &tm_qkv, v_col + 64 * a, j * kBN, b, vf);
-        issued = j + 1;
+          ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv, v_col + 64 * a,
+                           j * kBN, b, vf);
+        v_issued = j + 1;
+        return true;
+      };
+      for (int j = 0; j < 2 && j < n_kv && ok; ++j) ok = load_k(j);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        ok = load_v(j);
+        if (ok && j + 2 < n_kv) ok = load_k(j + 2);
       }
+      if (!ok) fail();
       if (*abort_flag) {
         // Let every copy already in flight land before shared memory is released.
         ptx::mbar_wait(q_full, 0, nullptr, kWaitLimitNs);
-        for (int s = 0; s < NS && s < issued; ++s) {
-          const int last_u = (issued - 1 - s) / NS;
-          ptx::mbar_wait(ptx::smem_u32(&bars->k_full[s]), last_u & 1, nullptr, kWaitLimitNs);
-          ptx::mbar_wait(ptx::smem_u32(&bars->v_full[s]), last_u & 1, nullptr, kWaitLimitNs);
-        }
+        for (int st = 0; st < NK && st < k_issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / NK) & 1, nullptr, kWaitLimitNs);
+        for (int st = 0; st < NV && st < v_issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / NV) & 1, nullptr, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -234,9 +252,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
       bool ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->q_ready : &bars->q_full), 0, abort_flag, kWaitLimitNs);
 
       auto issue_pv = [&](int i) -> bool {
-        const int sp = i % NS;
+        const int sp = i % NV;
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full), i & 1, abort_flag, kWaitLimitNs)) return false;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->v_full[sp]), (i / NS) & 1, abort_flag, kWaitLimitNs)) return false;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->v_full[sp]), (i / NV) & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
         const uint32_t v_base = sVa + sp * Cfg::kTileBytes;
 #pragma unroll
@@ -246,13 +264,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
           ptx::mma_bf16_ss(tmem + Cfg::kTmemO, a, bdesc, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->pv_done));
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[sp]));
+        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[sp]));
         return true;
       };
 
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % NS, sb = j & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->k_ready[s] : &bars->k_full[s]), (j / NS) & 1, abort_flag,
+        const int s = j % NK, sb = j & 1;
+        ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->k_ready[s] : &bars->k_full[s]), (j / NK) & 1, abort_flag,
                             kWaitLimitNs);
         if (ok && j >= 2) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[sb]), ((j >> 1) - 1) & 1, abort_flag,
                                               kWaitLimitNs);
@@ -267,6 +285,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
                            idesc_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
+        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[s]));
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) ok = issue_pv(n_kv - 1);
@@ -398,8 +417,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->q_ready));
     }
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j % NS;
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->k_full[s]), (j / NS) & 1, abort_flag,
+      const int s = j % NK;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->k_full[s]), (j / NK) & 1, abort_flag,
                                                     kWaitLimitNs));
       if (!ok) break;
       rot.rotate(sK + s * Cfg::kTileBytes, j * kBN);
