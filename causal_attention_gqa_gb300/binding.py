@@ -155,7 +155,7 @@ def attn_selftest_wait_timeout(limit_ns: int) -> int:
     return v.value
 
 
-N_KERNEL_IDS = 8
+N_KERNEL_IDS = 9
 
 
 def attn_profile_start() -> None:

@@ -39,6 +39,21 @@ int* status_word() {
   return g_status_ptr[dev];
 }
 
+int g_num_sms[kMaxDevices] = {};
+
+// Streaming multiprocessors of the current device (persistent grid size).
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -187,7 +202,8 @@ extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, in
   a.out = out;
   a.lse = lse;
   a.status = status_word();
-  if (!a.status) return ATTN_ERR_CUDA;
+  a.num_sms = num_sms();
+  if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
   if (!make_tmap(&a.tm_qkv, qkv, g.W, g.T, g.B)) return ATTN_ERR_CUDA;
   return from_cuda(tc05_fwd_launch(a, s));
 }
@@ -234,7 +250,8 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
   a.lse = lse;
   a.Drow = Drow;
   a.status = status_word();
-  if (!a.status) return ATTN_ERR_CUDA;
+  a.num_sms = num_sms();
+  if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
   // With RoPE, Q and K are read from a rotated copy in the workspace; its
   // layout keeps query head h at column h*hd and kv head kh at C + kh*hd.
   const bool rope = g.rope_theta > 0.f;
@@ -247,8 +264,7 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
         !make_tmap(&a.tm_v[r], qkv, g.W, g.T, g.B, rows) || !make_tmap(&a.tm_do[r], dout, g.C, g.T, g.B, rows))
       return ATTN_ERR_CUDA;
   }
-  cudaError_t e = launch_row_dot(Drow, out, dout, g, true, s);
-  if (e == cudaSuccess && rope) e = launch_rope_qk_bf16(rot, qkv, g, s);
+  cudaError_t e = launch_bwd_prologue_bf16(Drow, rot, out, dout, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
 }

@@ -133,7 +133,7 @@ struct DkdvCfg {
 
 struct DkdvBarriers {
   uint64_t kv_full, acc_done, drain;
-  uint64_t qdo_full[4], qdo_empty[4], s_full[2], s_free[2], p_full[2], pds_free[2];
+  uint64_t qdo_full[4], qdo_empty[4], s_full[2], p_full[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -178,9 +178,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 4);
-      ptx::mbar_init(ptx::smem_u32(&bars->pds_free[i]), 1);
     }
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -269,16 +267,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           ptx::mma_bf16_ss(tmem + Cfg::kTmemDK, ptx::sw128_desc(aDS + st * Cfg::kPTile + kk * 32, 16, 1024),
                            ptx::sw128_desc(aQ + qs * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->pds_free[st]));
         ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
         return true;
       };
 
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, u = n >> 1, qs = n % NQS;
+        const int st = n & 1, qs = n % NQS;
+        // TMEM buffer st was last read by step n-2's elementwise group before
+        // it arrived on p_full(n-2), which issue_grad(n-2) already observed.
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
-        if (ok && n >= 2)
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
@@ -312,12 +309,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     for (int n = wg; n < n_steps; n += 2) {
       const int st = wg, u = n >> 1;
       const int qi = 2 * j + n % nq;
+      // s_full(n) is committed after the MMAs of step n-2 were issued, so it
+      // also means those MMAs no longer read P/dS buffer st.
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
-      // P/dS buffer `st` is free once the MMAs of step n-2 retired (they were
-      // issued before this step's S and dP, so this returns at once).
-      if (ok && n >= 2)
-        ok = __all_sync(0xffffffffu,
-                        ptx::mbar_wait(ptx::smem_u32(&bars->pds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       const bool diag = qi <= 2 * j + 1;           // this query tile overlaps the key tile
@@ -343,15 +337,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           pw[c / 2] = pack_bf16x2(p[0], p[1]);
           dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
-        if (c0 == 32) {  // both chunks of S and dP are in registers: release the TMEM buffer
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
-        }
         store_row_half(sP + st * Cfg::kPTile, row, c0 / 32, pw);
         store_row_half(sDS + st * Cfg::kPTile, row, c0 / 32, dw);
       }
       ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[st]));
     }
@@ -402,7 +392,7 @@ struct DqCfg {
 
 struct DqBarriers {
   uint64_t q_full, acc_done, drain;
-  uint64_t kv_full[4], kv_empty[4], s_full[2], s_free[2], ds_full[2], ds_free[2];
+  uint64_t kv_full[4], kv_empty[4], s_full[2], ds_full[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -445,9 +435,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 4);
-      ptx::mbar_init(ptx::smem_u32(&bars->ds_free[i]), 1);
     }
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -518,16 +506,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                            ptx::sw128_desc(aK + ks * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
                            (m > 0 || kk > 0) ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->ds_free[st]));
         ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[ks]));
         return true;
       };
 
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, u = n >> 1, ks = n % NKS;
+        const int st = n & 1, ks = n % NKS;
+        // TMEM buffer st: free once ds_full(n-2) was observed (see dK/dV kernel).
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[ks]), (n / NKS) & 1, abort_flag, kWaitLimitNs);
-        if (ok && n >= 2)
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
@@ -564,9 +550,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int n = wg; n < n_steps; n += 2) {
       const int st = wg, u = n >> 1;
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
-      if (ok && n >= 2)
-        ok = __all_sync(0xffffffffu,
-                        ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
@@ -587,14 +570,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
-        if (c0 == 32) {
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
-        }
         store_row_half(sDS + st * Cfg::kSTile, row, c0 / 32, dw);
       }
       ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full[st]));
     }

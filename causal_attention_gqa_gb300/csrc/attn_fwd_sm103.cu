@@ -1,20 +1,32 @@
 // Causal MHA/GQA attention forward on sm_103a tensor cores (bf16 in, f32
 // accumulation), head size 64 or 128.
 //
-// One CTA owns a 128-query tile of one (batch row, query head) and walks the
-// key tiles 0..qt (causal tile skipping: tiles entirely above the diagonal are
-// never loaded).  Warp roles:
-//   warp 0      TMA producer: Q once, then K_j and V_j into separate rings;
-//               K runs two tiles ahead of V so that S_j never waits on a load.
-//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one
-//               of two TMEM score buffers, O += P_j V_j into the TMEM output.
+// Persistent kernel: one CTA per SM walks a strided list of work items, one
+// item = a 128-query tile of one (batch row, query head), heaviest (longest
+// causal row range) first; query heads that share a kv head are adjacent in
+// the list, so concurrently running CTAs reuse K/V tiles through L2.  Every
+// role runs one continuous stream of key tiles across its items, so the next
+// item's loads and first MMAs overlap the current item's last softmax and
+// epilogue; barriers and TMEM are set up once per CTA.  Within an item the
+// key tiles 0..qt are visited (causal tile skipping).  Warp roles:
+//   warp 0      TMA producer: Q (double-buffered across items), then K_j and
+//               V_j into separate rings; K runs two tiles ahead of V so that
+//               the score MMA never waits on a load.
+//   warp 1      TMEM owner and score-MMA issuer (one thread): S_j = Q K_j^T
+//               into one of two TMEM score buffers.
+//   warp 6      PV-MMA issuer (one thread): O += P_j V_j with P_j read from
+//               tensor memory (A operand) and V_j from shared memory.
+//               Two issuers keep the tensor core fed: each one's barrier
+//               checks and commits overlap the other's queued MMAs.
 //   warps 2-5   softmax: thread = query row = TMEM lane.  Reads S_j, keeps the
-//               running max m and sum l, writes P_j (bf16) to shared memory in
-//               the MMA's swizzled layout, rescales O in TMEM when m grows
-//               past a threshold (exact: l and O share the stale max), and in
-//               the epilogue writes out = O / l and lse = m + ln l.
-//   warps 6-9   (RoPE only) rotate Q and every landed K tile in shared memory
-//               before the MMA warp may read them.
+//               running max m and sum l, writes P_j (bf16) into one of two
+//               TMEM P buffers, rescales O in TMEM when m grows past a
+//               threshold (exact: l and O share the stale max), and at the end
+//               of an item writes out = O / l and lse = m + ln l.
+//   warps 7-10  (RoPE only) rotate each item's Q and every landed K tile in
+//               shared memory before the score MMA may read them.
+// TMEM columns: S0, S1 (128 each), P0, P1 (64 each, bf16 pairs), then O (one
+// buffer at head size 128, two at 64).
 // The math is that of "nanoeuler -- CUDA kernels", attention_forward_kernel
 // (scale 1/sqrt(hd), kv head h/(NH/NKV), causal mask, row softmax, PV), with
 // the softmax evaluated online over key tiles; lse follows the forward kernel
@@ -36,7 +48,8 @@ constexpr int kBN = 128;                      // keys per tile
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: P may reach 2^8 before O is rescaled
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kRopeWarp0 = 6;
+constexpr int kPvWarp = 6;
+constexpr int kRopeWarp0 = 7;
 
 template <int HD, bool ROPE>
 struct FwdCfg {
@@ -44,25 +57,45 @@ struct FwdCfg {
   static constexpr int kTileBytes = kBM * HD * 2;           // Q / K / V tile
   static constexpr int kKStages = (HD == 128) ? 3 : 4;      // K ring depth
   static constexpr int kVStages = (HD == 128) ? 2 : 4;      // V ring depth
-  static constexpr int kQOff = 0;
-  static constexpr int kPOff = kQOff + kTileBytes;
-  static constexpr int kPBytes = kBM * kBN * 2;
-  static constexpr int kKOff = kPOff + kPBytes;
+  static constexpr int kQOff = 0;                           // two Q buffers (items in flight)
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + alignment slack
   static_assert(kSmemBytes <= 232448, "forward kernel exceeds the 227 KB shared-memory limit");
-  static constexpr int kThreads = ROPE ? 320 : 192;
-  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemCols = 512;
+  static constexpr int kThreads = ROPE ? 352 : 224;
+  static constexpr int kOBuffers = (HD == 128) ? 1 : 2;
+  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemP0 = 256, kTmemP1 = 320, kTmemO0 = 384,
+                            kTmemO1 = 384 + HD, kTmemCols = 512;
 };
 
 struct FwdBarriers {
-  uint64_t q_full, q_ready, pv_done, p_full, drain;
+  uint64_t q_full[2], q_ready[2], q_empty[2], o_free[2];
+  uint64_t pv_done[2], p_full[2], drain, drain2;
   uint64_t s_full[2], s_free[2];
   uint64_t k_full[4], k_ready[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t tmem_base;
   int abort;
 };
+
+// Work item w -> (batch row, query head, query tile).  Items are ordered by
+// decreasing query tile (longest causal range first); within a tile, the
+// heads of one batch row are consecutive.
+struct FwdItem {
+  int b, h, kh, qt;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(int w, const Geometry& g) {
+  const int n_qt = (g.T + kBM - 1) / kBM;
+  const int bh_count = g.B * g.NH;
+  FwdItem it;
+  it.qt = n_qt - 1 - w / bh_count;
+  const int bh = w % bh_count;
+  it.b = bh / g.NH;
+  it.h = bh % g.NH;
+  it.kh = it.h / g.grp;
+  return it;
+}
 
 // Byte offset of element (row, col) inside a 128-row bf16 tile stored as
 // 128-byte-swizzled atom columns of 64 elements.
@@ -128,40 +161,33 @@ struct TileRotator {
 template <int HD, bool ROPE>
 __global__ void __launch_bounds__(FwdCfg<HD, ROPE>::kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-           int* __restrict__ status, Geometry g) {
+           int* __restrict__ status, Geometry g, int n_items) {
   using Cfg = FwdCfg<HD, ROPE>;
-  constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages;
+  constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages, NO = Cfg::kOBuffers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
-  uint8_t* sP = smem + Cfg::kPOff;
   uint8_t* sK = smem + Cfg::kKOff;
   uint8_t* sV = smem + Cfg::kVOff;
   FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(smem + Cfg::kBarOff);
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  // Tile order: heaviest query tiles first; heads sharing a kv head adjacent.
-  const int n_qt = (g.T + kBM - 1) / kBM;
-  const int bh_count = g.B * g.NH;
-  const int qt = n_qt - 1 - (int)(blockIdx.x / bh_count);
-  const int bh = blockIdx.x % bh_count;
-  const int b = bh / g.NH, h = bh % g.NH;
-  const int kh = h / g.grp;
-  const int q0 = qt * kBM;
-  const int n_kv = qt + 1;
+  const int w0 = blockIdx.x, dw = gridDim.x;   // this CTA's items: w0, w0 + dw, ...
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->q_ready), 4);
-    ptx::mbar_init(ptx::smem_u32(&bars->pv_done), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->p_full), 4);
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
     for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->q_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->q_ready[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->q_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->o_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->pv_done[i]), 1);
     }
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain2), 1);
     for (int i = 0; i < NK; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->k_ready[i]), 4);
@@ -192,50 +218,65 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_qkv);
-      const int q_col = h * HD, k_col = g.C + kh * HD, v_col = g.C + g.NKV * HD + kh * HD;
-      const uint32_t q_full = ptx::smem_u32(&bars->q_full);
-      ptx::mbar_arrive_expect_tx(q_full, Cfg::kTileBytes);
-#pragma unroll
-      for (int a = 0; a < HD / 64; ++a)
-        ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kAtomBytes), &tm_qkv, q_col + 64 * a, q0, b, q_full);
-      // Issue order: K_0, K_1, then V_j, K_{j+2} for j = 0, 1, ...
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 0, v_issued = 0, q_issued = 0;  // global sequence counters
       bool ok = true;
-      auto load_k = [&](int j) -> bool {
-        const int st = j % NK, u = j / NK;
-        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs))
-          return false;
-        const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
-        ptx::mbar_arrive_expect_tx(kf, Cfg::kTileBytes);
+      for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+        const FwdItem item = fwd_item(w, g);
+        const int n_kv = item.qt + 1;
+        const int k_col = g.C + item.kh * HD, v_col = g.C + g.NKV * HD + item.kh * HD;
+        // Q of this item into buffer it & 1 once item it-2 issued its last S.
+        const int qb = it & 1;
+        if (it >= 2 && !ptx::mbar_wait(ptx::smem_u32(&bars->q_empty[qb]), ((it >> 1) - 1) & 1, abort_flag,
+                                       kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
+        ptx::mbar_arrive_expect_tx(qf, Cfg::kTileBytes);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv, k_col + 64 * a,
-                           j * kBN, b, kf);
-        k_issued = j + 1;
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int st = j % NV, u = j / NV;
-        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs))
-          return false;
-        const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
-        ptx::mbar_arrive_expect_tx(vf, Cfg::kTileBytes);
+          ptx::tma_load_3d(ptx::smem_u32(sQ + qb * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv,
+                           item.h * HD + 64 * a, item.qt * kBM, item.b, qf);
+        q_issued = it + 1;
+        const int kbase = k_issued;  // global index of this item's key tile 0
+        auto load_k = [&](int j) -> bool {
+          const int gi = kbase + j, st = gi % NK, u = gi / NK;
+          if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs))
+            return false;
+          const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
+          ptx::mbar_arrive_expect_tx(kf, Cfg::kTileBytes);
 #pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv, v_col + 64 * a,
-                           j * kBN, b, vf);
-        v_issued = j + 1;
-        return true;
-      };
-      for (int j = 0; j < 2 && j < n_kv && ok; ++j) ok = load_k(j);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        ok = load_v(j);
-        if (ok && j + 2 < n_kv) ok = load_k(j + 2);
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv,
+                             k_col + 64 * a, j * kBN, item.b, kf);
+          k_issued = gi + 1;
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          const int gi = kbase + j, st = gi % NV, u = gi / NV;
+          if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs))
+            return false;
+          const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
+          ptx::mbar_arrive_expect_tx(vf, Cfg::kTileBytes);
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv,
+                             v_col + 64 * a, j * kBN, item.b, vf);
+          v_issued = gi + 1;
+          return true;
+        };
+        // Issue order within an item: K_0, K_1, then V_j, K_{j+2}.
+        for (int j = 0; j < 2 && j < n_kv && ok; ++j) ok = load_k(j);
+        for (int j = 0; j < n_kv && ok; ++j) {
+          ok = load_v(j);
+          if (ok && j + 2 < n_kv) ok = load_k(j + 2);
+        }
       }
       if (!ok) fail();
       if (*abort_flag) {
         // Let every copy already in flight land before shared memory is released.
-        ptx::mbar_wait(q_full, 0, nullptr, kWaitLimitNs);
+        for (int qb = 0; qb < 2 && qb < q_issued; ++qb)
+          ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]), ((q_issued - 1 - qb) >> 1) & 1, nullptr, kWaitLimitNs);
         for (int st = 0; st < NK && st < k_issued; ++st)
           ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / NK) & 1, nullptr, kWaitLimitNs);
         for (int st = 0; st < NV && st < v_issued; ++st)
@@ -243,188 +284,257 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score-MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kBM, HD, false, true);
-      const uint32_t sQa = ptx::smem_u32(sQ), sPa = ptx::smem_u32(sP);
-      const uint32_t sKa = ptx::smem_u32(sK), sVa = ptx::smem_u32(sV);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->q_ready : &bars->q_full), 0, abort_flag, kWaitLimitNs);
-
-      auto issue_pv = [&](int i) -> bool {
-        const int sp = i % NV;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full), i & 1, abort_flag, kWaitLimitNs)) return false;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->v_full[sp]), (i / NV) & 1, abort_flag, kWaitLimitNs)) return false;
-        ptx::tc_fence_after();
-        const uint32_t v_base = sVa + sp * Cfg::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t a = ptx::sw128_desc(sPa + (kk >> 2) * Cfg::kAtomBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, Cfg::kAtomBytes, 1024);
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemO, a, bdesc, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(ptx::smem_u32(&bars->pv_done));
-        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[sp]));
-        return true;
-      };
-
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % NK, sb = j & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->k_ready[s] : &bars->k_full[s]), (j / NK) & 1, abort_flag,
+      const uint32_t sQa = ptx::smem_u32(sQ), sKa = ptx::smem_u32(sK);
+      bool ok = true;
+      int gi = 0;  // global key-tile index of this CTA's stream
+      for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+        const FwdItem item = fwd_item(w, g);
+        const int n_kv = item.qt + 1, qb = it & 1;
+        ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->q_ready[qb] : &bars->q_full[qb]), (it >> 1) & 1, abort_flag,
                             kWaitLimitNs);
-        if (ok && j >= 2) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free[sb]), ((j >> 1) - 1) & 1, abort_flag,
-                                              kWaitLimitNs);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t k_base = sKa + s * Cfg::kTileBytes;
-        const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+        for (int j = 0; j < n_kv && ok; ++j, ++gi) {
+          const int s = gi % NK, sb = gi & 1;
+          const uint32_t kb = ptx::smem_u32(ROPE ? &bars->k_ready[s] : &bars->k_full[s]);
+          const uint32_t fb = ptx::smem_u32(&bars->s_free[sb]);
+          // K_j landed (and rotated); score buffer sb read out by the softmax of tile gi-2.
+          if (!(ptx::mbar_ready(kb, (gi / NK) & 1) & (gi < 2 ? 1u : ptx::mbar_ready(fb, ((gi >> 1) - 1) & 1)))) {
+            ok = ptx::mbar_wait(kb, (gi / NK) & 1, abort_flag, kWaitLimitNs);
+            if (ok && gi >= 2) ok = ptx::mbar_wait(fb, ((gi >> 1) - 1) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t k_base = sKa + s * Cfg::kTileBytes;
+          const uint32_t q_base = sQa + qb * Cfg::kTileBytes;
+          const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kAtomBytes + (kk & 3) * 32;
-          ptx::mma_bf16_ss(d_s, ptx::sw128_desc(sQa + off, 16, 1024), ptx::sw128_desc(k_base + off, 16, 1024),
-                           idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kAtomBytes + (kk & 3) * 32;
+            ptx::mma_bf16_ss(d_s, ptx::sw128_desc(q_base + off, 16, 1024), ptx::sw128_desc(k_base + off, 16, 1024),
+                             idesc_s, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
+          ptx::mma_commit(ptx::smem_u32(&bars->k_empty[s]));
+          if (j == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qb]));
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
-        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[s]));
-        if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok) ok = issue_pv(n_kv - 1);
       if (!ok) fail();
       // Drain: every MMA this thread issued has finished before TMEM is freed.
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
-  } else if (warp < kSoftmaxWarp0 + 4) {
-    // ------------------------------------------------------------ softmax
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV-MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kBM, HD, false, true);
+      const uint32_t sVa = ptx::smem_u32(sV);
+      bool ok = true;
+      int gi = 0;
+      for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+        const FwdItem item = fwd_item(w, g);
+        const int n_kv = item.qt + 1, ob = (NO == 2) ? (it & 1) : 0;
+        // The first PV of an item overwrites its O buffer: the epilogue of the
+        // item that last used it must have read it out.
+        if (it >= NO)
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_free[ob]), (((it - NO) / NO)) & 1, abort_flag, kWaitLimitNs);
+        for (int j = 0; j < n_kv && ok; ++j, ++gi) {
+          const int pb = gi & 1, sp = gi % NV;
+          const uint32_t pf = ptx::smem_u32(&bars->p_full[pb]), vf = ptx::smem_u32(&bars->v_full[sp]);
+          if (!(ptx::mbar_ready(pf, (gi >> 1) & 1) & ptx::mbar_ready(vf, (gi / NV) & 1))) {
+            ok = ptx::mbar_wait(pf, (gi >> 1) & 1, abort_flag, kWaitLimitNs);
+            if (ok) ok = ptx::mbar_wait(vf, (gi / NV) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t v_base = sVa + sp * Cfg::kTileBytes;
+          const uint32_t d_o = tmem + (ob ? Cfg::kTmemO1 : Cfg::kTmemO0);
+          const uint32_t a_p = tmem + (pb ? Cfg::kTmemP1 : Cfg::kTmemP0);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, Cfg::kAtomBytes, 1024);
+            ptx::mma_bf16_ts(d_o, a_p + kk * 8, bdesc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->pv_done[pb]));
+          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[sp]));
+        }
+      }
+      if (!ok) fail();
+      ptx::mma_commit(ptx::smem_u32(&bars->drain2));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain2), 0, nullptr, kWaitLimitNs);
+    }
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+    // ------------------------------------------------------------ softmax + epilogue
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
-    const int tq = q0 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = g.scale * 1.4426950408889634f;  // scale * log2(e)
-    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sb]), (j >> 1) & 1, abort_flag,
-                                                    kWaitLimitNs));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      uint32_t sr[kBN];
-      const uint32_t s_addr = t_lane + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
-      ptx::tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      ptx::tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-      ptx::tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-      ptx::tmem_wait_ld();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[sb]));
-
-      if (j == n_kv - 1) {  // diagonal tile: key c is visible to row `row` iff c <= row
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c > row) sr[c] = __float_as_uint(-INFINITY);
-      }
-      float mt = __uint_as_float(sr[0]);
-#pragma unroll
-      for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
-      const float m_cand = mt * sl2;
-      const bool grow = m_cand > m + kRescaleThreshold;   // always true on the first tile
-      const float m_new = grow ? m_cand : m;
-      const float corr = grow ? ptx::ex2_approx(m - m_new) : 1.f;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const float p = ptx::ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -m_new));
-        sr[c] = __float_as_uint(p);
-        rs += p;
-      }
-      l = l * corr + rs;
-      m = m_new;
-
-      // P_j may overwrite P_{j-1} and O may be rescaled only after PV_{j-1}.
-      if (j >= 1) {
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done), (j - 1) & 1, abort_flag,
+    int gi = 0;
+    for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+      const FwdItem item = fwd_item(w, g);
+      const int n_kv = item.qt + 1;
+      const int tq = item.qt * kBM + row;
+      const int ob = (NO == 2) ? (it & 1) : 0;
+      const uint32_t o_addr = t_lane + (ob ? Cfg::kTmemO1 : Cfg::kTmemO0);
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_kv; ++j, ++gi) {
+        const int sb = gi & 1;
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sb]), (gi >> 1) & 1, abort_flag,
                                                       kWaitLimitNs));
         if (!ok) break;
         ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {
+        uint32_t sr[kBN];
+        const uint32_t s_addr = t_lane + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
+        ptx::tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        ptx::tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        ptx::tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[sb]));
+
+        if (j == n_kv - 1) {  // diagonal tile: key c is visible to row `row` iff c <= row
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c > row) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // Row max with 8 independent partial maxima (no 128-long dependency chain).
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_cand = mt * sl2;
+        const bool grow = m_cand > m + kRescaleThreshold;   // always true on an item's first tile
+        const float m_new = grow ? m_cand : m;
+        const float corr = grow ? ptx::ex2_approx(m - m_new) : 1.f;
+        // p = 2^(s * scale * log2(e) - m): exponent arguments two at a time
+        // (packed FMA), row sum in 8 independent partial sums (packed adds).
+        const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(-m_new, -m_new);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2);
+          const float2 p = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+          sr[c] = __float_as_uint(p.x);
+          sr[c + 1] = __float_as_uint(p.y);
+          acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], p);
+        }
+        const float2 acc01 = __fadd2_rn(acc[0], acc[1]), acc23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 acc4 = __fadd2_rn(acc01, acc23);
+        const float rs = acc4.x + acc4.y;
+        l = l * corr + rs;
+        m = m_new;
+
+        // P buffer gi&1 was read by PV(gi-2); O may be rescaled only once
+        // PV(gi-1) (same item) has finished.
+        const int pb = gi & 1;
+        const bool rescale = (j >= 1) && __any_sync(0xffffffffu, grow);
+        if (gi >= 2) {
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[pb]), ((gi - 2) >> 1) & 1,
+                                                        abort_flag, kWaitLimitNs));
+          if (!ok) break;
+        }
+        if (rescale) {
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[pb ^ 1]), ((gi - 1) >> 1) & 1,
+                                                        abort_flag, kWaitLimitNs));
+          if (!ok) break;
+          ptx::tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < HD; c0 += 32) {
             uint32_t o[32];
-            ptx::tmem_ld32(t_lane + Cfg::kTmemO + c0, o);
+            ptx::tmem_ld32(o_addr + c0, o);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
-            ptx::tmem_st32(t_lane + Cfg::kTmemO + c0, o);
+            ptx::tmem_st32(o_addr + c0, o);
           }
+        } else {
+          ptx::tc_fence_after();
+        }
+        // P (bf16, two keys per 32-bit column) into TMEM P buffer pb.
+        {
+          const uint32_t p_addr = t_lane + (pb ? Cfg::kTmemP1 : Cfg::kTmemP0);
+          uint32_t pw[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pw[c] = pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+          ptx::tmem_st32(p_addr, pw);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            pw[c] = pack_bf16x2(__uint_as_float(sr[64 + 2 * c]), __uint_as_float(sr[64 + 2 * c + 1]));
+          ptx::tmem_st32(p_addr + 32, pw);
           ptx::tmem_wait_st();
         }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[pb]));
       }
-#pragma unroll
-      for (int ch = 0; ch < kBN / 8; ++ch) {
-        const uint32_t* q = &sr[8 * ch];
-        const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(q[0]), __uint_as_float(q[1])),
-                                   pack_bf16x2(__uint_as_float(q[2]), __uint_as_float(q[3])),
-                                   pack_bf16x2(__uint_as_float(q[4]), __uint_as_float(q[5])),
-                                   pack_bf16x2(__uint_as_float(q[6]), __uint_as_float(q[7])));
-        *reinterpret_cast<uint4*>(sP + sw128_offset(row, 8 * ch)) = v;
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full));
-    }
-    if (ok) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done), (n_kv - 1) & 1, abort_flag,
-                                                    kWaitLimitNs));
-    }
-    if (ok) {
+      if (!ok) break;
+      // Epilogue of this item: O is complete once its last PV has finished.
+      const int last = gi - 1;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[last & 1]), (last >> 1) & 1,
+                                                    abort_flag, kWaitLimitNs));
+      if (!ok) break;
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = out + ((size_t)b * g.T + tq) * g.C + h * HD;
+      __nv_bfloat16* orow = out + ((size_t)item.b * g.T + (tq < g.T ? tq : 0)) * g.C + item.h * HD;
 #pragma unroll 1
       for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t o[32];
-        ptx::tmem_ld32(t_lane + Cfg::kTmemO + c0, o);
+        ptx::tmem_ld32(o_addr + c0, o);
         ptx::tmem_wait_ld();
         if (tq < g.T) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const uint4 w = make_uint4(
+            const uint4 w4 = make_uint4(
                 pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
                 pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
                 pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
                 pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
-            *reinterpret_cast<uint4*>(orow + c0 + 8 * v) = w;
+            *reinterpret_cast<uint4*>(orow + c0 + 8 * v) = w4;
           }
         }
       }
-      if (tq < g.T) lse[((size_t)b * g.NH + h) * g.T + tq] = (m + log2f(l)) * 0.6931471805599453f;
-    } else {
-      fail();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->o_free[ob]));
+      if (tq < g.T) lse[((size_t)item.b * g.NH + item.h) * g.T + tq] = (m + log2f(l)) * 0.6931471805599453f;
     }
-  } else if (ROPE) {
+    if (!ok) fail();
+  } else if (ROPE && warp >= kRopeWarp0) {
     // ------------------------------------------------------------ RoPE transform
     const int tid = threadIdx.x - kRopeWarp0 * 32;
     TileRotator<HD> rot;
     rot.init(tid, g);
-    bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs));
-    if (ok) {
-      rot.rotate(sQ, q0);
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->q_ready));
-    }
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j % NK;
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->k_full[s]), (j / NK) & 1, abort_flag,
+    bool ok = true;
+    int gi = 0;
+    for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+      const FwdItem item = fwd_item(w, g);
+      const int qb = it & 1;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]), (it >> 1) & 1, abort_flag,
                                                     kWaitLimitNs));
       if (!ok) break;
-      rot.rotate(sK + s * Cfg::kTileBytes, j * kBN);
+      rot.rotate(sQ + qb * Cfg::kTileBytes, item.qt * kBM);
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->k_ready[s]));
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->q_ready[qb]));
+      for (int j = 0; j <= item.qt && ok; ++j, ++gi) {
+        const int s = gi % NK;
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->k_full[s]), (gi / NK) & 1, abort_flag,
+                                                      kWaitLimitNs));
+        if (!ok) break;
+        rot.rotate(sK + s * Cfg::kTileBytes, j * kBN);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->k_ready[s]));
+      }
     }
     if (!ok) fail();
   }
@@ -445,9 +555,11 @@ cudaError_t launch_fwd(const Tc05FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_qt = (a.g.T + kBM - 1) / kBM;
-  const unsigned grid = (unsigned)(n_qt * a.g.B * a.g.NH);
+  const int n_items = n_qt * a.g.B * a.g.NH;
+  const unsigned grid = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelFwdTc05, stream);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qkv, (__nv_bfloat16*)a.out, a.lse, a.status, a.g);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qkv, (__nv_bfloat16*)a.out, a.lse, a.status, a.g,
+                                                        n_items);
   prof_end(kKernelFwdTc05, stream);
   return cudaGetLastError();
 }

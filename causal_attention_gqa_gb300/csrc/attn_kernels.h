@@ -29,6 +29,10 @@ cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Ge
                            cudaStream_t stream);
 // NEOX-rotated bf16 copy of every Q and K head: dst [B,T,(NH+NKV)*hd].
 cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream);
+// bf16 (hd a multiple of 16): row dots D and, when RoPE is on, the rotated
+// Q/K copy in one launch.
+cudaError_t launch_bwd_prologue_bf16(float* D, void* rot, const void* out, const void* dout, const void* qkv,
+                                     const Geometry& g, cudaStream_t stream);
 
 // ------------------------------------------------------------ tcgen05 bf16 path
 struct Tc05FwdArgs {
@@ -37,6 +41,7 @@ struct Tc05FwdArgs {
   void* out;          // [B,T,C] bf16
   float* lse;         // [B,NH,T]
   int* status;        // library status word
+  int num_sms;        // persistent grid size
 };
 cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream);
 
@@ -53,6 +58,7 @@ struct Tc05BwdArgs {
   const float* lse;      // [B,NH,T]
   const float* Drow;     // [B,NH,T]
   int* status;
+  int num_sms;           // persistent grid size
 };
 cudaError_t tc05_bwd_launch(const Tc05BwdArgs& a, cudaStream_t stream);
 

@@ -106,7 +106,86 @@ __global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __rest
   }
 }
 
+// bf16 backward prologue in one launch over a flat index space:
+//  * the first n_dot threads (rounded up to whole warps) each multiply one
+//    16-byte chunk of out and dout; the hd/8 threads of a head-row sum their
+//    partials with shuffles and one of them writes D[b,h,t];
+//  * the remaining threads (RoPE only) each rotate 8 NEOX pairs of one Q or K
+//    head-row into the workspace copy.
+// One load per thread per tensor keeps many requests in flight.
+__global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float* __restrict__ D, const uint4* __restrict__ out,
+                                                                 const uint4* __restrict__ dout,
+                                                                 __nv_bfloat16* __restrict__ rot,
+                                                                 const __nv_bfloat16* __restrict__ qkv, Geometry g,
+                                                                 long long n_dot_padded, long long n_rope) {
+  const int vec_per_head = g.hd / 8;  // 8 or 16, divides 32
+  const long long n_dot = (long long)g.B * g.T * g.NH * vec_per_head;
+  const long long total = n_dot_padded + n_rope;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    if (idx < n_dot_padded) {  // warp-uniform: n_dot_padded is a multiple of 32
+      float acc = 0.f;
+      if (idx < n_dot) {
+        const uint4 a = out[idx], c = dout[idx];
+        acc = bf16_lo(a.x) * bf16_lo(c.x) + bf16_hi(a.x) * bf16_hi(c.x) + bf16_lo(a.y) * bf16_lo(c.y) +
+              bf16_hi(a.y) * bf16_hi(c.y) + bf16_lo(a.z) * bf16_lo(c.z) + bf16_hi(a.z) * bf16_hi(c.z) +
+              bf16_lo(a.w) * bf16_lo(c.w) + bf16_hi(a.w) * bf16_hi(c.w);
+      }
+      for (int off = vec_per_head / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (idx < n_dot && (idx % vec_per_head) == 0) {
+        const long long r = idx / vec_per_head;  // ((b*T + t)*NH + h)
+        const int h = (int)(r % g.NH);
+        const long long bt = r / g.NH;
+        const int t = (int)(bt % g.T), b = (int)(bt / g.T);
+        D[((size_t)b * g.NH + h) * g.T + t] = acc;
+      }
+      continue;
+    }
+    const long long k = idx - n_dot_padded;
+    const int groups = g.hd / 16, heads = g.NH + g.NKV, half = g.hd / 2;
+    const int gi = (int)(k % groups);
+    const long long r = k / groups;
+    const int head = (int)(r % heads);
+    const long long bt = r / heads;
+    const int t = (int)(bt % g.T);
+    const __nv_bfloat16* src = qkv + bt * g.W + head * g.hd;
+    __nv_bfloat16* dst = rot + bt * (long long)heads * g.hd + head * g.hd;
+    const uint4 x0 = *reinterpret_cast<const uint4*>(src + gi * 8);
+    const uint4 x1 = *reinterpret_cast<const uint4*>(src + half + gi * 8);
+    const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
+    uint32_t ya[4], yc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float s0, c0, s1, c1, y00, y01, y10, y11;
+      const int i0 = gi * 8 + 2 * q;
+      __sincosf(rope_angle(t, g.rope_f_hi[i0], g.rope_f_lo[i0]), &s0, &c0);
+      __sincosf(rope_angle(t, g.rope_f_hi[i0 + 1], g.rope_f_lo[i0 + 1]), &s1, &c1);
+      rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
+      rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
+      ya[q] = pack_bf16x2(y00, y01);
+      yc[q] = pack_bf16x2(y10, y11);
+    }
+    *reinterpret_cast<uint4*>(dst + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(dst + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_prologue_bf16(float* D, void* rot, const void* out, const void* dout, const void* qkv,
+                                     const Geometry& g, cudaStream_t stream) {
+  const long long n_dot = (long long)g.B * g.T * g.NH * (g.hd / 8);
+  const long long n_dot_padded = (n_dot + 31) / 32 * 32;
+  const long long n_rope = (g.rope_theta > 0.f) ? (long long)g.B * g.T * (g.NH + g.NKV) * (g.hd / 16) : 0;
+  long long blocks = (n_dot_padded + n_rope + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  prof_begin(kKernelBwdPrologue, stream);
+  bwd_prologue_bf16_kernel<<<(int)blocks, 256, 0, stream>>>(D, (const uint4*)out, (const uint4*)dout,
+                                                            (__nv_bfloat16*)rot, (const __nv_bfloat16*)qkv, g,
+                                                            n_dot_padded, n_rope);
+  prof_end(kKernelBwdPrologue, stream);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Geometry& g, bool bf16,
                            cudaStream_t stream) {

@@ -16,7 +16,8 @@ enum KernelId {
   kKernelFwdSimt = 5,
   kKernelBwdDkdvSimt = 6,
   kKernelBwdDqSimt = 7,
-  kKernelCount = 8
+  kKernelBwdPrologue = 8,
+  kKernelCount = 9
 };
 
 // Record the start / end of a launch of kernel `id` on `stream` (no-ops while

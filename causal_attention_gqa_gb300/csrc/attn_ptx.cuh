@@ -64,6 +64,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Single non-looping check (one try_wait).  Several independent checks
+// issued back to back overlap their latency, unlike a chain of mbar_wait calls
+// that each branch on their own result.
+__device__ __forceinline__ uint32_t mbar_ready(uint32_t bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity) ? 1u : 0u;
+}
+
 // Wait until the barrier phase with the given parity completes.  Gives up
 // (returns false) when `*abort` becomes non-zero or after `limit_ns`
 // nanoseconds; never spins forever.
@@ -137,6 +144,21 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
       "}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D(tmem) (+)= A(tmem) * B(smem desc), kind::f16.  A is M x K with row m in
+// TMEM lane m and two consecutive K elements packed per 32-bit column, so one
+// K=16 step consumes 8 columns starting at a_tmem.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

@@ -185,7 +185,8 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
  *   and the launch count in launches[id] (either array may be NULL).
  * attn_kernel_name -- short name of kernel id (see attn_profile.h ids:
  *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 bwd_rope_qk,
- *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt); "unknown" otherwise.
+ *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt, 8 bwd_prologue); "unknown"
+ *   otherwise.
  */
 ATTN_API int attn_profile_start(void);
 ATTN_API int attn_profile_stop(double* total_ms, int* launches, int n);
