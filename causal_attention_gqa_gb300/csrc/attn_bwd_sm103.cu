@@ -21,12 +21,14 @@
 //    stay in shared memory; the CTA walks the 64-key tiles 0..2i+1.  Per step:
 //    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
 //    dQ += dS K accumulates in TMEM.
-// Warp roles in both: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
-// and two elementwise warpgroups (warps 2-5 take the even steps, warps 6-9
-// the odd ones, each with its own TMEM and shared-memory buffers) with one
-// TMEM lane (one key or query row) per thread; they also split the epilogue.
-// Two steps are in flight at once, so one group's exp/pack/store chain runs
-// while the tensor core works on the other group's MMAs.  All waits are
+// Warp roles in both: warp 0 TMA producer; warp 1 TMEM owner and MMA issuer;
+// two elementwise warpgroups (warps 2-5 take the even steps, warps 6-9 the
+// odd ones, each with its own TMEM and shared-memory buffers) with one TMEM
+// lane (one key or query row) per thread, which also split the epilogue.  Two
+// steps are in flight at once.  In the dQ kernel warp 1 issues only the score
+// MMAs (S, dP) and warp 10 the dQ MMAs, so the two streams feed the tensor
+// core independently (measured faster there; in the dK/dV kernel one issuer
+// that alternates score and gradient groups measured faster).  All waits are
 // bounded.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
@@ -37,7 +39,9 @@ namespace attn {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kThreads = 320;
+constexpr int kThreadsDkdv = 320;   // producer, MMA issuer, two elementwise warpgroups
+constexpr int kThreadsDq = 352;     // + a separate dQ-MMA issuer warp
+constexpr int kGradWarp = 10;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Store 16 packed words (32 bf16) at columns 32*half .. 32*half+31 of row
@@ -139,7 +143,7 @@ struct DkdvBarriers {
 };
 
 template <int HD, bool ROPE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsDkdv, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                 __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
@@ -392,13 +396,14 @@ struct DqCfg {
 
 struct DqBarriers {
   uint64_t q_full, acc_done, drain;
-  uint64_t kv_full[4], kv_empty[4], s_full[2], ds_full[2];
+  uint64_t drain2;
+  uint64_t kv_full[4], kv_empty[4], s_full[2], s_free[2], ds_full[2], ds_free[2];
   uint32_t tmem_base;
   int abort;
 };
 
 template <int HD, bool ROPE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsDq, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
@@ -435,8 +440,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->ds_free[i]), 1);
     }
+    ptx::mbar_init(ptx::smem_u32(&bars->drain2), 1);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -488,33 +496,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S / dP issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
       const uint32_t aQ = ptx::smem_u32(sQ), aDO = ptx::smem_u32(sDO), aK = ptx::smem_u32(sK),
-                     aV = ptx::smem_u32(sV), aDS = ptx::smem_u32(sDS);
+                     aV = ptx::smem_u32(sV);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
-
-      auto issue_dq = [&](int m) -> bool {
-        const int st = m & 1, u = m >> 1, ks = m % NKS;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < Cfg::kKeys / 16; ++kk) {
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::sw128_desc(aDS + st * Cfg::kSTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aK + ks * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
-                           (m > 0 || kk > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[ks]));
-        return true;
-      };
-
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, ks = n % NKS;
-        // TMEM buffer st: free once ds_full(n-2) was observed (see dK/dV kernel).
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[ks]), (n / NKS) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
+        const int st = n & 1, u = n >> 1, ks = n % NKS;
+        // K_n/V_n landed; TMEM buffer st read out by step n-2's elementwise group.
+        const uint32_t kf = ptx::smem_u32(&bars->kv_full[ks]), sf = ptx::smem_u32(&bars->s_free[st]);
+        if (!(ptx::mbar_ready(kf, (n / NKS) & 1) & (n < 2 ? 1u : ptx::mbar_ready(sf, (u - 1) & 1)))) {
+          ok = ptx::mbar_wait(kf, (n / NKS) & 1, abort_flag, kWaitLimitNs);
+          if (ok && n >= 2) ok = ptx::mbar_wait(sf, (u - 1) & 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+        }
         ptx::tc_fence_after();
         const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
 #pragma unroll
@@ -527,13 +523,36 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                            kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
-        if (n >= 1) ok = issue_dq(n - 1);
       }
-      if (ok) ok = issue_dq(n_steps - 1);
-      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
       if (!ok) fail();
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+    }
+  } else if (warp == kGradWarp) {
+    // ------------------------------------------------------------ dQ issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
+      const uint32_t aK = ptx::smem_u32(sK), aDS = ptx::smem_u32(sDS);
+      bool ok = true;
+      for (int m = 0; m < n_steps && ok; ++m) {
+        const int st = m & 1, u = m >> 1, ks = m % NKS;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full[st]), u & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kKeys / 16; ++kk) {
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::sw128_desc(aDS + st * Cfg::kSTile + kk * 32, 16, 1024),
+                           ptx::sw128_desc(aK + ks * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
+                           (m > 0 || kk > 0) ? 1u : 0u);
+        }
+        // S_m and dP_m finished before ds_full(m), so K_m/V_m are free after this.
+        ptx::mma_commit(ptx::smem_u32(&bars->ds_free[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[ks]));
+      }
+      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (!ok) fail();
+      ptx::mma_commit(ptx::smem_u32(&bars->drain2));
+      ptx::mbar_wait(ptx::smem_u32(&bars->drain2), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
@@ -553,6 +572,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!ok) break;
       ptx::tc_fence_after();
       const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
+      uint32_t dw0[16];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t sr[32], dr[32], dw[16];
@@ -570,8 +590,25 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
-        store_row_half(sDS + st * Cfg::kSTile, row, c0 / 32, dw);
+        if (c0 == 32) {
+          // S and dP are in registers: release the TMEM buffer, then make sure
+          // the dQ MMAs of step n-2 are done with dS buffer st.
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
+          if (n >= 2) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag,
+                                                          kWaitLimitNs));
+            if (!ok) break;
+          }
+          store_row_half(sDS + st * Cfg::kSTile, row, 0, dw0);
+          store_row_half(sDS + st * Cfg::kSTile, row, 1, dw);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) dw0[q] = dw[q];
+        }
       }
+      if (!ok) break;
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
@@ -608,14 +645,14 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
   prof_begin(kKernelBwdDkdvTc05, stream);
-  k1<<<grid1, kThreads, DkdvCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_v[1], a.tm_qk[0], a.tm_do[0],
+  k1<<<grid1, kThreadsDkdv, DkdvCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_v[1], a.tm_qk[0], a.tm_do[0],
                                                           (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
   prof_end(kKernelBwdDkdvTc05, stream);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
   prof_begin(kKernelBwdDqTc05, stream);
-  k2<<<grid2, kThreads, DqCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_do[1], a.tm_qk[0], a.tm_v[0],
+  k2<<<grid2, kThreadsDq, DqCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_do[1], a.tm_qk[0], a.tm_v[0],
                                                         (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
   return cudaGetLastError();
