@@ -107,13 +107,16 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
 // Rotate a 128-row tile in shared memory (NEOX pairs (i, i+HD/2)).  128
 // threads: thread tid owns pairs 8p..8p+7 (p = tid % NCH) for rows
 // r0, r0 + RS, ..., r0 = tid / NCH.  Angles advance by RS rows with the
-// angle-addition recurrence, from an accurately reduced start per tile.
+// angle-addition recurrence, from an accurately reduced start per tile.  The
+// two pairs held in one 32-bit bf16x2 word are processed together with
+// packed FP32 (f32x2) arithmetic.
 template <int HD>
 struct TileRotator {
   static constexpr int NCH = HD / 16;        // 8-pair groups per row
   static constexpr int RS = 128 / NCH;       // row stride between a thread's rows
   static constexpr int ROWS = 128 / RS;      // rows per thread
-  float f_hi[8], f_lo[8], step_c[8], step_s[8];
+  float f_hi[8], f_lo[8];
+  float2 step_c[4], step_s[4];               // cos/sin of RS * f for pairs (2q, 2q+1)
   int p, r0;
 
   __device__ void init(int tid, const Geometry& g) {
@@ -123,36 +126,54 @@ struct TileRotator {
     for (int e = 0; e < 8; ++e) {
       f_hi[e] = g.rope_f_hi[8 * p + e];
       f_lo[e] = g.rope_f_lo[8 * p + e];
-      __sincosf(rope_angle(RS, f_hi[e], f_lo[e]), &step_s[e], &step_c[e]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float s0, c0, s1, c1;
+      __sincosf(rope_angle(RS, f_hi[2 * q], f_lo[2 * q]), &s0, &c0);
+      __sincosf(rope_angle(RS, f_hi[2 * q + 1], f_lo[2 * q + 1]), &s1, &c1);
+      step_c[q] = make_float2(c0, c1);
+      step_s[q] = make_float2(s0, s1);
     }
   }
 
   __device__ void rotate(uint8_t* tile, int pos0) {
-    float c[8], s[8];
+    float2 c[4], sn[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) __sincosf(rope_angle(pos0 + r0, f_hi[e], f_lo[e]), &s[e], &c[e]);
+    for (int q = 0; q < 4; ++q) {
+      float s0, c0, s1, c1;
+      __sincosf(rope_angle(pos0 + r0, f_hi[2 * q], f_lo[2 * q]), &s0, &c0);
+      __sincosf(rope_angle(pos0 + r0, f_hi[2 * q + 1], f_lo[2 * q + 1]), &s1, &c1);
+      c[q] = make_float2(c0, c1);
+      sn[q] = make_float2(s0, s1);
+    }
 #pragma unroll 1
     for (int k = 0; k < ROWS; ++k) {
       const int r = r0 + k * RS;
       uint4* a_ptr = reinterpret_cast<uint4*>(tile + sw128_offset(r, 8 * p));
       uint4* b_ptr = reinterpret_cast<uint4*>(tile + sw128_offset(r, 8 * p + HD / 2));
-      uint4 a = *a_ptr, b = *b_ptr;
-      uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const uint4 a = *a_ptr, b = *b_ptr;
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      uint32_t ya[4], yb[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        float y0l, y1l, y0h, y1h;
-        rope_pair(bf16_lo(av[q]), bf16_lo(bv[q]), c[2 * q], s[2 * q], y0l, y1l);
-        rope_pair(bf16_hi(av[q]), bf16_hi(bv[q]), c[2 * q + 1], s[2 * q + 1], y0h, y1h);
-        av[q] = pack_bf16x2(y0l, y0h);
-        bv[q] = pack_bf16x2(y1l, y1h);
+        // x0 = first elements of pairs (2q, 2q+1), x1 = their partners.
+        const float2 x0 = make_float2(bf16_lo(av[q]), bf16_hi(av[q]));
+        const float2 x1 = make_float2(bf16_lo(bv[q]), bf16_hi(bv[q]));
+        const float2 ns = make_float2(-sn[q].x, -sn[q].y);
+        const float2 y0 = __ffma2_rn(x0, c[q], __fmul2_rn(x1, ns));     // x0 cos - x1 sin
+        const float2 y1 = __ffma2_rn(x1, c[q], __fmul2_rn(x0, sn[q]));  // x1 cos + x0 sin
+        ya[q] = pack_bf16x2(y0.x, y0.y);
+        yb[q] = pack_bf16x2(y1.x, y1.y);
       }
-      *a_ptr = make_uint4(av[0], av[1], av[2], av[3]);
-      *b_ptr = make_uint4(bv[0], bv[1], bv[2], bv[3]);
+      *a_ptr = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+      *b_ptr = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {  // advance the angle by RS positions
-        const float cn = c[e] * step_c[e] - s[e] * step_s[e];
-        s[e] = s[e] * step_c[e] + c[e] * step_s[e];
-        c[e] = cn;
+      for (int q = 0; q < 4; ++q) {  // advance the angles by RS positions
+        const float2 nss = make_float2(-step_s[q].x, -step_s[q].y);
+        const float2 cn = __ffma2_rn(c[q], step_c[q], __fmul2_rn(sn[q], nss));
+        sn[q] = __ffma2_rn(sn[q], step_c[q], __fmul2_rn(c[q], step_s[q]));
+        c[q] = cn;
       }
     }
   }
