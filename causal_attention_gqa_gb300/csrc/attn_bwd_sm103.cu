@@ -195,6 +195,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Everything above overlapped the prologue's tail; its outputs (row dots,
+  // rotated Q/K) are read below.  Once every CTA of this grid is past this
+  // point the dQ kernel may start: it depends on the prologue only, which has
+  // then completed.
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   auto fail = [&]() {
     *abort_flag = 1;
     record_status(status, kErrDeviceTimeout);
@@ -456,6 +462,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Launched as a programmatic dependent of the dK/dV kernel, whose CTAs all
+  // waited for the prologue before allowing this grid to start; this kernel
+  // reads only the prologue's outputs and the inputs, and writes dqkv columns
+  // the dK/dV kernel does not touch, so it needs no wait of its own.
   auto fail = [&]() {
     *abort_flag = 1;
     record_status(status, kErrDeviceTimeout);
@@ -625,6 +635,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
   }
 
+  // Finish only after the dK/dV kernel this grid overlapped has completed, so
+  // that work later in the stream (which waits for this grid only) never
+  // overwrites the workspace while the dK/dV kernel still reads it.
+  ptx::grid_dep_wait();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -645,17 +659,16 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
   prof_begin(kKernelBwdDkdvTc05, stream);
-  k1<<<grid1, kThreadsDkdv, DkdvCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_v[1], a.tm_qk[0], a.tm_do[0],
-                                                          (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+  e = launch_pdl(k1, dim3(grid1), dim3(kThreadsDkdv), DkdvCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_v[1],
+                 a.tm_qk[0], a.tm_do[0], (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
   prof_end(kKernelBwdDkdvTc05, stream);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
   prof_begin(kKernelBwdDqTc05, stream);
-  k2<<<grid2, kThreadsDq, DqCfg<HD>::kSmemBytes, stream>>>(a.tm_qk[1], a.tm_do[1], a.tm_qk[0], a.tm_v[0],
-                                                        (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+  e = launch_pdl(k2, dim3(grid2), dim3(kThreadsDq), DqCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_do[1],
+                 a.tm_qk[0], a.tm_v[0], (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

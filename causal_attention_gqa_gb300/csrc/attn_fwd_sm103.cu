@@ -229,6 +229,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // A following backward prologue may get resident now; it waits for this
+  // grid to complete before reading out.
+  ptx::grid_dep_launch();
 
   auto fail = [&]() {
     *abort_flag = 1;

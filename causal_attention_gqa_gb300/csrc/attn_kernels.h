@@ -5,9 +5,31 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "attn_common.cuh"
 
 namespace attn {
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream is still running; it must call
+// griddepcontrol.wait before touching anything that kernel writes, unless
+// an earlier grid already guarantees it (see the backward kernels).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------ float32 SIMT path
 struct SimtArgs {

@@ -11,6 +11,7 @@
 #include "attn_common.cuh"
 #include "attn_kernels.h"
 #include "attn_profile.h"
+#include "attn_ptx.cuh"
 
 namespace attn {
 namespace {
@@ -118,6 +119,10 @@ __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float* __restric
                                                                  __nv_bfloat16* __restrict__ rot,
                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
                                                                  long long n_dot_padded, long long n_rope) {
+  // out is written by the forward that may still be finishing (programmatic
+  // launch): wait for it, then let the dK/dV kernel get resident.
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int vec_per_head = g.hd / 8;  // 8 or 16, divides 32
   const long long n_dot = (long long)g.B * g.T * g.NH * vec_per_head;
   const long long total = n_dot_padded + n_rope;
@@ -180,11 +185,11 @@ cudaError_t launch_bwd_prologue_bf16(float* D, void* rot, const void* out, const
   long long blocks = (n_dot_padded + n_rope + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;   // grid-stride beyond 32 blocks per SM (measured faster)
   prof_begin(kKernelBwdPrologue, stream);
-  bwd_prologue_bf16_kernel<<<(int)blocks, 256, 0, stream>>>(D, (const uint4*)out, (const uint4*)dout,
-                                                            (__nv_bfloat16*)rot, (const __nv_bfloat16*)qkv, g,
-                                                            n_dot_padded, n_rope);
+  cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, D,
+                             (const uint4*)out, (const uint4*)dout, (__nv_bfloat16*)rot,
+                             (const __nv_bfloat16*)qkv, g, n_dot_padded, n_rope);
   prof_end(kKernelBwdPrologue, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Geometry& g, bool bf16,
