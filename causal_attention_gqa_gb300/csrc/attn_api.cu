@@ -133,8 +133,15 @@ int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtyp
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Leading part of the workspace: float32 row dots [B,NH,T] (F32), or the
+// bf16 path's row table of float pairs [B,NH,Tp].
+size_t row_part_bytes(const Geometry& g, int dtype) {
+  if (dtype == ATTN_DTYPE_BF16) return align256((size_t)g.B * g.NH * row_table_rows(g.T) * sizeof(float2));
+  return align256((size_t)g.B * g.NH * g.T * sizeof(float));
+}
+
 size_t workspace_bytes(const Geometry& g, int dtype) {
-  size_t bytes = align256((size_t)g.B * g.NH * g.T * sizeof(float));
+  size_t bytes = row_part_bytes(g, dtype);
   if (dtype == ATTN_DTYPE_BF16) bytes += align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2);
   return bytes;
 }
@@ -247,15 +254,14 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
   Tc05BwdArgs a{};
   a.g = g;
   a.dqkv = dqkv;
-  a.lse = lse;
-  a.Drow = Drow;
+  a.LD = static_cast<const float2*>(workspace);
   a.status = status_word();
   a.num_sms = num_sms();
   if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
   // With RoPE, Q and K are read from a rotated copy in the workspace; its
   // layout keeps query head h at column h*hd and kv head kh at C + kh*hd.
   const bool rope = g.rope_theta > 0.f;
-  void* rot = static_cast<uint8_t*>(workspace) + align256((size_t)g.B * g.NH * g.T * sizeof(float));
+  void* rot = static_cast<uint8_t*>(workspace) + row_part_bytes(g, dtype);
   const void* qk_src = rope ? rot : qkv;
   const int qk_width = rope ? (g.NH + g.NKV) * g.hd : g.W;
   for (int r = 0; r < 2; ++r) {
@@ -264,7 +270,7 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
         !make_tmap(&a.tm_v[r], qkv, g.W, g.T, g.B, rows) || !make_tmap(&a.tm_do[r], dout, g.C, g.T, g.B, rows))
       return ATTN_ERR_CUDA;
   }
-  cudaError_t e = launch_bwd_prologue_bf16(Drow, rot, out, dout, qkv, g, s);
+  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float2*>(workspace), rot, out, dout, lse, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
 }

@@ -22,14 +22,15 @@
 //    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
 //    dQ += dS K accumulates in TMEM.
 // Warp roles in both: warp 0 TMA producer; warp 1 TMEM owner and MMA issuer;
-// two elementwise warpgroups (warps 2-5 take the even steps, warps 6-9 the
-// odd ones, each with its own TMEM and shared-memory buffers) with one TMEM
-// lane (one key or query row) per thread, which also split the epilogue.  Two
-// steps are in flight at once.  In the dQ kernel warp 1 issues only the score
-// MMAs (S, dP) and warp 10 the dQ MMAs, so the two streams feed the tensor
-// core independently (measured faster there; in the dK/dV kernel one issuer
-// that alternates score and gradient groups measured faster).  All waits are
-// bounded.
+// two elementwise warpgroups with one TMEM lane (one key or query row) per
+// thread, which also split the epilogue.  In the dK/dV kernel they take
+// alternate steps; in the dQ kernel each takes half of every step's 64
+// columns.  Score results are double-buffered in TMEM, so two steps are in
+// flight at once.  In the dQ kernel warp 1
+// issues only the score MMAs (S, dP) and warp 10 the dQ MMAs, so the two
+// streams feed the tensor core independently (measured faster there; in the
+// dK/dV kernel one issuer that alternates score and gradient groups measured
+// faster).  All waits are bounded.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
 #include "attn_profile.h"
@@ -127,9 +128,8 @@ struct DkdvCfg {
   static constexpr int kDOOff = kQOff + kQStages * kQTile;
   static constexpr int kPOff = kDOOff + kQStages * kQTile;
   static constexpr int kDSOff = kPOff + 2 * kPTile;
-  static constexpr int kLseOff = kDSOff + 2 * kPTile;
-  static constexpr int kDOff = kLseOff + kQStages * kQ * 4;
-  static constexpr int kBarOff = kDOff + kQStages * kQ * 4;
+  static constexpr int kLDOff = kDSOff + 2 * kPTile;       // row-table tiles (float2 per query)
+  static constexpr int kBarOff = kLDOff + kQStages * kQ * 8;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "dK/dV kernel exceeds the 227 KB shared-memory limit");
@@ -146,8 +146,8 @@ template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDkdv, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
-                int* __restrict__ status, Geometry g) {
+                __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ LD, int* __restrict__ status,
+                Geometry g) {
   using Cfg = DkdvCfg<HD>;
   constexpr int NQS = Cfg::kQStages;
   extern __shared__ uint8_t smem_raw[];
@@ -158,8 +158,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   uint8_t* sDO = smem + Cfg::kDOOff;
   uint8_t* sP = smem + Cfg::kPOff;
   uint8_t* sDS = smem + Cfg::kDSOff;
-  float* sLse = reinterpret_cast<float*>(smem + Cfg::kLseOff);
-  float* sD = reinterpret_cast<float*>(smem + Cfg::kDOff);
+  float2* sLD = reinterpret_cast<float2*>(smem + Cfg::kLDOff);
   DkdvBarriers* bars = reinterpret_cast<DkdvBarriers*>(smem + Cfg::kBarOff);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -171,13 +170,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const int nq64 = (g.T + 63) / 64;
   const int nq = nq64 - 2 * j;                  // 64-query tiles that can see key tile j
   const int n_steps = g.grp * nq;
+  const int Tp = row_table_rows(g.T);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
     for (int i = 0; i < NQS; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 2);
+      ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -208,6 +208,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Per step: Q_i and dO_i (TMA) and the 64 row-table entries of the step's
+    // queries (one bulk copy; the table is padded to whole 64-row tiles with
+    // zeros, and padding query rows have zero Q and dO, so they add nothing).
     int issued = 0;
     if (lane == 0) {
       const uint32_t kvf = ptx::smem_u32(&bars->kv_full);
@@ -218,21 +221,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ptx::tma_load_3d(ptx::smem_u32(sV + a * Cfg::kKeys * 128), &tm_v, g.C + g.NKV * HD + kh * HD + 64 * a,
                          j * 128, b, kvf);
       }
-    }
-    for (int n = 0; n < n_steps; ++n) {
-      const int st = n % NQS, u = n / NQS;
-      const int h = kh * g.grp + n / nq, qi = 2 * j + n % nq;
-      int ok = 1;
-      if (lane == 0 && u > 0)
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) fail();
-        break;
-      }
-      const uint32_t full = ptx::smem_u32(&bars->qdo_full[st]);
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kQTile);
+      int h = kh * g.grp, qi = 2 * j;             // step n's query head and 64-query tile
+      for (int n = 0; n < n_steps; ++n) {
+        const int st = n % NQS, u = n / NQS;
+        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->qdo_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        const uint32_t full = ptx::smem_u32(&bars->qdo_full[st]);
+        ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kQTile + Cfg::kQ * 8);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a) {
           ptx::tma_load_3d(ptx::smem_u32(sQ + st * Cfg::kQTile + a * Cfg::kQ * 128), &tm_q, h * HD + 64 * a,
@@ -240,16 +237,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           ptx::tma_load_3d(ptx::smem_u32(sDO + st * Cfg::kQTile + a * Cfg::kQ * 128), &tm_do, h * HD + 64 * a,
                            qi * 64, b, full);
         }
+        ptx::bulk_load(ptx::smem_u32(sLD + st * Cfg::kQ), LD + ((size_t)b * g.NH + h) * Tp + qi * 64, Cfg::kQ * 8,
+                       full);
+        issued = n + 1;
+        if (++qi == nq64) {
+          qi = 2 * j;
+          ++h;
+        }
       }
-      for (int q = lane; q < Cfg::kQ; q += 32) {
-        const int t = qi * 64 + q;
-        const size_t idx = ((size_t)b * g.NH + h) * g.T + t;
-        sLse[st * Cfg::kQ + q] = (t < g.T) ? lse[idx] * kLog2e : INFINITY;  // padding rows: P = 0
-        sD[st * Cfg::kQ + q] = (t < g.T) ? Drow[idx] : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(full);
-      issued = n + 1;
     }
     if (lane == 0 && *abort_flag) {
       ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, nullptr, kWaitLimitNs);
@@ -261,21 +256,29 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
-      const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
-                     aDO = ptx::smem_u32(sDO), aP = ptx::smem_u32(sP), aDS = ptx::smem_u32(sDS);
+      const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
+      const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), 16, 1024);
+      const uint64_t dQk = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
+      const uint64_t dDOk = ptx::sw128_desc(ptx::smem_u32(sDO), 16, 1024);
+      const uint64_t dQm = ptx::sw128_desc(ptx::smem_u32(sQ), Cfg::kQ * 128, 1024);
+      const uint64_t dDOm = ptx::sw128_desc(ptx::smem_u32(sDO), Cfg::kQ * 128, 1024);
+      const uint64_t dP = ptx::sw128_desc(ptx::smem_u32(sP), 16, 1024);
+      const uint64_t dDS = ptx::sw128_desc(ptx::smem_u32(sDS), 16, 1024);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
 
       auto issue_grad = [&](int m) -> bool {
         const int st = m & 1, u = m >> 1, qs = m % NQS;
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
+        const uint64_t ap = ptx::desc_advance(dP, st * Cfg::kPTile), ads = ptx::desc_advance(dDS, st * Cfg::kPTile);
+        const uint64_t bdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile), bq = ptx::desc_advance(dQm, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kQ / 16; ++kk) {
           const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDV, ptx::sw128_desc(aP + st * Cfg::kPTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aDO + qs * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDK, ptx::sw128_desc(aDS + st * Cfg::kPTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aQ + qs * Cfg::kQTile + kk * 2048, Cfg::kQ * 128, 1024), idesc_g, acc);
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDV, ptx::desc_advance(ap, kk * 32), ptx::desc_advance(bdo, kk * 2048),
+                           idesc_g, acc);
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDK, ptx::desc_advance(ads, kk * 32), ptx::desc_advance(bq, kk * 2048),
+                           idesc_g, acc);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
         return true;
@@ -289,14 +292,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
+        const uint64_t bq = ptx::desc_advance(dQk, qs * Cfg::kQTile), bdo = ptx::desc_advance(dDOk, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t ok_ = (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
-          const uint32_t oq = qs * Cfg::kQTile + (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
-          ptx::mma_bf16_ss(d_s, ptx::sw128_desc(aK + ok_, 16, 1024), ptx::sw128_desc(aQ + oq, 16, 1024), idesc_s,
-                           kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_dp, ptx::sw128_desc(aV + ok_, 16, 1024), ptx::sw128_desc(aDO + oq, 16, 1024), idesc_s,
-                           kk > 0 ? 1u : 0u);
+          const uint32_t oq = (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dK, ok_), ptx::desc_advance(bq, oq), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_dp, ptx::desc_advance(dV, ok_), ptx::desc_advance(bdo, oq), idesc_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
         if (n >= 1) ok = issue_grad(n - 1);
@@ -325,30 +327,38 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       if (!ok) break;
       ptx::tc_fence_after();
       const bool diag = qi <= 2 * j + 1;           // this query tile overlaps the key tile
-      const float* lse2 = sLse + (n % NQS) * Cfg::kQ;
-      const float* dd = sD + (n % NQS) * Cfg::kQ;
+      const int qk = qi * 64 - ks;                 // query column c is before this key iff c + qk < 0
+      // Row-table pairs of two consecutive queries: (-lse2_c, -D_c, -lse2_c+1, -D_c+1).
+      const float4* ld4 = reinterpret_cast<const float4*>(sLD + (n % NQS) * Cfg::kQ);
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      // Two halves of 32 query columns (all 64 at once would spill registers
+      // in this 10-warp kernel).
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      for (int half = 0; half < 2; ++half) {
         uint32_t sr[32], dr[32], pw[16], dw[16];
-        ptx::tmem_ld32(t_lane + st * 128 + c0, sr);
-        ptx::tmem_ld32(t_lane + st * 128 + 64 + c0, dr);
+        ptx::tmem_ld32(t_lane + st * 128 + 32 * half, sr);
+        ptx::tmem_ld32(t_lane + st * 128 + 64 + 32 * half, dr);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          float p[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = c0 + c + e;
-            float pv = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -lse2[q]));
-            if (diag && qi * 64 + q < ks) pv = 0.f;  // query before key: masked
-            p[e] = pv;
-            ds[e] = pv * (__uint_as_float(dr[c + e]) - dd[q]);
+          const int q = 32 * half + c;
+          const float4 L = ld4[q >> 1];
+          // p = 2^(s * scale * log2(e) - lse * log2(e)); dS = p * (dP - D)
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                                      make_float2(L.x, L.z));
+          float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
+          if (diag) {                              // query before key: masked
+            if (q + qk < 0) p0 = 0.f;
+            if (q + 1 + qk < 0) p1 = 0.f;
           }
-          pw[c / 2] = pack_bf16x2(p[0], p[1]);
-          dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
+          const float2 ds = __fmul2_rn(make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(dr[c]),
+                                                                                   __uint_as_float(dr[c + 1])),
+                                                                       make_float2(L.y, L.w)));
+          pw[c >> 1] = pack_bf16x2(p0, p1);
+          dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
         }
-        store_row_half(sP + st * Cfg::kPTile, row, c0 / 32, pw);
-        store_row_half(sDS + st * Cfg::kPTile, row, c0 / 32, dw);
+        store_row_half(sP + st * Cfg::kPTile, row, half, pw);
+        store_row_half(sDS + st * Cfg::kPTile, row, half, dw);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -412,8 +422,8 @@ template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDq, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-              __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ lse, const float* __restrict__ Drow,
-              int* __restrict__ status, Geometry g) {
+              __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ LD, int* __restrict__ status,
+              Geometry g) {
   using Cfg = DqCfg<HD>;
   constexpr int NKS = Cfg::kKStages;
   extern __shared__ uint8_t smem_raw[];
@@ -446,8 +456,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
-      ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 8);
+      ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 8);
       ptx::mbar_init(ptx::smem_u32(&bars->ds_free[i]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->drain2), 1);
@@ -509,8 +519,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // ------------------------------------------------------------ S / dP issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
-      const uint32_t aQ = ptx::smem_u32(sQ), aDO = ptx::smem_u32(sDO), aK = ptx::smem_u32(sK),
-                     aV = ptx::smem_u32(sV);
+      const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
+      const uint64_t dDO = ptx::sw128_desc(ptx::smem_u32(sDO), 16, 1024);
+      const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
+      const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), 16, 1024);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n & 1, u = n >> 1, ks = n % NKS;
@@ -523,14 +535,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         ptx::tc_fence_after();
         const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
+        const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, ks * Cfg::kKTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t oq = (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
-          const uint32_t ok_ = ks * Cfg::kKTile + (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
-          ptx::mma_bf16_ss(d_s, ptx::sw128_desc(aQ + oq, 16, 1024), ptx::sw128_desc(aK + ok_, 16, 1024), idesc_s,
-                           kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_dp, ptx::sw128_desc(aDO + oq, 16, 1024), ptx::sw128_desc(aV + ok_, 16, 1024), idesc_s,
-                           kk > 0 ? 1u : 0u);
+          const uint32_t ok_ = (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQ, oq), ptx::desc_advance(bk, ok_), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_dp, ptx::desc_advance(dDO, oq), ptx::desc_advance(bv, ok_), idesc_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
       }
@@ -542,18 +553,19 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // ------------------------------------------------------------ dQ issuer
     if (lane == 0) {
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
-      const uint32_t aK = ptx::smem_u32(sK), aDS = ptx::smem_u32(sDS);
+      const uint64_t dKm = ptx::sw128_desc(ptx::smem_u32(sK), Cfg::kKeys * 128, 1024);
+      const uint64_t dDS = ptx::sw128_desc(ptx::smem_u32(sDS), 16, 1024);
       bool ok = true;
       for (int m = 0; m < n_steps && ok; ++m) {
         const int st = m & 1, u = m >> 1, ks = m % NKS;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full[st]), u & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
+        const uint64_t a_ds = ptx::desc_advance(dDS, st * Cfg::kSTile), bk = ptx::desc_advance(dKm, ks * Cfg::kKTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kKeys / 16; ++kk) {
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::sw128_desc(aDS + st * Cfg::kSTile + kk * 32, 16, 1024),
-                           ptx::sw128_desc(aK + ks * Cfg::kKTile + kk * 2048, Cfg::kKeys * 128, 1024), idesc_g,
-                           (m > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::desc_advance(a_ds, kk * 32), ptx::desc_advance(bk, kk * 2048),
+                           idesc_g, (m > 0 || kk > 0) ? 1u : 0u);
         }
         // S_m and dP_m finished before ds_full(m), so K_m/V_m are free after this.
         ptx::mma_commit(ptx::smem_u32(&bars->ds_free[st]));
@@ -566,59 +578,56 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int wg = (warp - 2) >> 2;                // this group takes steps n = wg, wg+2, ...
+    // Both groups work on every step, group wg on key columns 32*wg ..
+    // 32*wg+31 (half the per-step latency of one group doing all 64).
+    const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;           // query row within the tile
     const int tq = qt * 128 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = g.scale * kLog2e;
-    const size_t ridx = ((size_t)b * g.NH + h) * g.T + tq;
-    const float lse2 = (tq < g.T) ? lse[ridx] * kLog2e : 0.f;   // padding rows have dO = 0, so dS = 0
-    const float drow = (tq < g.T) ? Drow[ridx] : 0.f;
+    // This row's table entry (-lse * log2(e), -D); padding rows have zero Q
+    // and dO, hence dP = 0 and dS = 0.
+    const float2 ldr =
+        (tq < g.T) ? LD[((size_t)b * g.NH + h) * row_table_rows(g.T) + tq] : make_float2(0.f, 0.f);
+    const float2 nl2 = make_float2(ldr.x, ldr.x), nd2 = make_float2(ldr.y, ldr.y);
+    const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
-    for (int n = wg; n < n_steps; n += 2) {
-      const int st = wg, u = n >> 1;
+    for (int n = 0; n < n_steps; ++n) {
+      const int st = n & 1, u = n >> 1;
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
+      uint32_t sr[32], dr[32];
+      ptx::tmem_ld32(t_lane + st * 128 + 32 * wg, sr);
+      ptx::tmem_ld32(t_lane + st * 128 + 64 + 32 * wg, dr);
+      ptx::tmem_wait_ld();
+      // This group's S and dP columns are in registers: release them.
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
       const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
-      uint32_t dw0[16];
+      const int kq = n * 64 + 32 * wg - tq;        // key column c is after this query iff c + kq > 0
+      uint32_t dw[16];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t sr[32], dr[32], dw[16];
-        ptx::tmem_ld32(t_lane + st * 128 + c0, sr);
-        ptx::tmem_ld32(t_lane + st * 128 + 64 + c0, dr);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float pv = ptx::ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -lse2));
-            if (diag && n * 64 + c0 + c + e > tq) pv = 0.f;  // key after query: masked
-            ds[e] = pv * (__uint_as_float(dr[c + e]) - drow);
-          }
-          dw[c / 2] = pack_bf16x2(ds[0], ds[1]);
+      for (int c = 0; c < 32; c += 2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl2);
+        float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
+        if (diag) {                                // key after query: masked
+          if (c + kq > 0) p0 = 0.f;
+          if (c + 1 + kq > 0) p1 = 0.f;
         }
-        if (c0 == 32) {
-          // S and dP are in registers: release the TMEM buffer, then make sure
-          // the dQ MMAs of step n-2 are done with dS buffer st.
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
-          if (n >= 2) {
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag,
-                                                          kWaitLimitNs));
-            if (!ok) break;
-          }
-          store_row_half(sDS + st * Cfg::kSTile, row, 0, dw0);
-          store_row_half(sDS + st * Cfg::kSTile, row, 1, dw);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) dw0[q] = dw[q];
-        }
+        const float2 ds = __fmul2_rn(
+            make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd2));
+        dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
       }
-      if (!ok) break;
+      // The dQ MMAs of step n-2 must be done with dS buffer st.
+      if (n >= 2) {
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag,
+                                                      kWaitLimitNs));
+        if (!ok) break;
+      }
+      store_row_half(sDS + st * Cfg::kSTile, row, wg, dw);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
@@ -660,13 +669,13 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
   prof_begin(kKernelBwdDkdvTc05, stream);
   e = launch_pdl(k1, dim3(grid1), dim3(kThreadsDkdv), DkdvCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_v[1],
-                 a.tm_qk[0], a.tm_do[0], (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+                 a.tm_qk[0], a.tm_do[0], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDkdvTc05, stream);
   if (e != cudaSuccess) return e;
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
   prof_begin(kKernelBwdDqTc05, stream);
   e = launch_pdl(k2, dim3(grid2), dim3(kThreadsDq), DqCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_do[1],
-                 a.tm_qk[0], a.tm_v[0], (__nv_bfloat16*)a.dqkv, a.lse, a.Drow, a.status, g);
+                 a.tm_qk[0], a.tm_v[0], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
   return e;
 }

@@ -311,7 +311,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
     // ------------------------------------------------------------ score-MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
-      const uint32_t sQa = ptx::smem_u32(sQ), sKa = ptx::smem_u32(sK);
+      const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
+      const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
       bool ok = true;
       int gi = 0;  // global key-tile index of this CTA's stream
       for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
@@ -330,14 +331,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
             if (!ok) break;
           }
           ptx::tc_fence_after();
-          const uint32_t k_base = sKa + s * Cfg::kTileBytes;
-          const uint32_t q_base = sQa + qb * Cfg::kTileBytes;
+          const uint64_t bk = ptx::desc_advance(dK, s * Cfg::kTileBytes);
+          const uint64_t aq = ptx::desc_advance(dQ, qb * Cfg::kTileBytes);
           const uint32_t d_s = tmem + (sb ? Cfg::kTmemS1 : Cfg::kTmemS0);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kAtomBytes + (kk & 3) * 32;
-            ptx::mma_bf16_ss(d_s, ptx::sw128_desc(q_base + off, 16, 1024), ptx::sw128_desc(k_base + off, 16, 1024),
-                             idesc_s, kk > 0 ? 1u : 0u);
+            ptx::mma_bf16_ss(d_s, ptx::desc_advance(aq, off), ptx::desc_advance(bk, off), idesc_s, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
           ptx::mma_commit(ptx::smem_u32(&bars->k_empty[s]));
@@ -353,7 +353,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
     // ------------------------------------------------------------ PV-MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kBM, HD, false, true);
-      const uint32_t sVa = ptx::smem_u32(sV);
+      const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), Cfg::kAtomBytes, 1024);
       bool ok = true;
       int gi = 0;
       for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
@@ -372,14 +372,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
             if (!ok) break;
           }
           ptx::tc_fence_after();
-          const uint32_t v_base = sVa + sp * Cfg::kTileBytes;
+          const uint64_t bv = ptx::desc_advance(dV, sp * Cfg::kTileBytes);
           const uint32_t d_o = tmem + (ob ? Cfg::kTmemO1 : Cfg::kTmemO0);
           const uint32_t a_p = tmem + (pb ? Cfg::kTmemP1 : Cfg::kTmemP0);
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, Cfg::kAtomBytes, 1024);
-            ptx::mma_bf16_ts(d_o, a_p + kk * 8, bdesc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            ptx::mma_bf16_ts(d_o, a_p + kk * 8, ptx::desc_advance(bv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_commit(ptx::smem_u32(&bars->pv_done[pb]));
           ptx::mma_commit(ptx::smem_u32(&bars->v_empty[sp]));
         }

@@ -110,22 +110,30 @@ __global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __rest
 // bf16 backward prologue in one launch over a flat index space:
 //  * the first n_dot threads (rounded up to whole warps) each multiply one
 //    16-byte chunk of out and dout; the hd/8 threads of a head-row sum their
-//    partials with shuffles and one of them writes D[b,h,t];
+//    partials with shuffles and one of them writes the row-table entry
+//    LD[b,h,t] = (-lse[b,h,t] * log2(e), -D[b,h,t]): the two per-row values
+//    the backward's elementwise steps use, side by side, already in the form
+//    they enter the exponent and the dS difference;
+//  * the next n_pad threads clear the table rows T..Tp-1 of every (b, h), so
+//    that whole 64-row tiles of the table can be copied;
 //  * the remaining threads (RoPE only) each rotate 8 NEOX pairs of one Q or K
 //    head-row into the workspace copy.
 // One load per thread per tensor keeps many requests in flight.
-__global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float* __restrict__ D, const uint4* __restrict__ out,
+__global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float2* __restrict__ LD, const uint4* __restrict__ out,
                                                                  const uint4* __restrict__ dout,
+                                                                 const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
-                                                                 long long n_dot_padded, long long n_rope) {
+                                                                 long long n_dot_padded, long long n_pad,
+                                                                 long long n_rope) {
   // out is written by the forward that may still be finishing (programmatic
   // launch): wait for it, then let the dK/dV kernel get resident.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int vec_per_head = g.hd / 8;  // 8 or 16, divides 32
   const long long n_dot = (long long)g.B * g.T * g.NH * vec_per_head;
-  const long long total = n_dot_padded + n_rope;
+  const long long total = n_dot_padded + n_pad + n_rope;
+  const int Tp = row_table_rows(g.T);
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     if (idx < n_dot_padded) {  // warp-uniform: n_dot_padded is a multiple of 32
@@ -142,11 +150,18 @@ __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float* __restric
         const int h = (int)(r % g.NH);
         const long long bt = r / g.NH;
         const int t = (int)(bt % g.T), b = (int)(bt / g.T);
-        D[((size_t)b * g.NH + h) * g.T + t] = acc;
+        const size_t bh = (size_t)b * g.NH + h;
+        LD[bh * Tp + t] = make_float2(-lse[bh * g.T + t] * 1.4426950408889634f, -acc);
       }
       continue;
     }
-    const long long k = idx - n_dot_padded;
+    if (idx < n_dot_padded + n_pad) {
+      const long long k = idx - n_dot_padded;
+      const int pad = Tp - g.T;
+      LD[(k / pad) * Tp + g.T + k % pad] = make_float2(0.f, 0.f);
+      continue;
+    }
+    const long long k = idx - n_dot_padded - n_pad;
     const int groups = g.hd / 16, heads = g.NH + g.NKV, half = g.hd / 2;
     const int gi = (int)(k % groups);
     const long long r = k / groups;
@@ -177,17 +192,18 @@ __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float* __restric
 
 }  // namespace
 
-cudaError_t launch_bwd_prologue_bf16(float* D, void* rot, const void* out, const void* dout, const void* qkv,
-                                     const Geometry& g, cudaStream_t stream) {
+cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, const void* dout, const float* lse,
+                                     const void* qkv, const Geometry& g, cudaStream_t stream) {
   const long long n_dot = (long long)g.B * g.T * g.NH * (g.hd / 8);
   const long long n_dot_padded = (n_dot + 31) / 32 * 32;
+  const long long n_pad = (long long)g.B * g.NH * (row_table_rows(g.T) - g.T);
   const long long n_rope = (g.rope_theta > 0.f) ? (long long)g.B * g.T * (g.NH + g.NKV) * (g.hd / 16) : 0;
-  long long blocks = (n_dot_padded + n_rope + 255) / 256;
+  long long blocks = (n_dot_padded + n_pad + n_rope + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;   // grid-stride beyond 32 blocks per SM (measured faster)
   prof_begin(kKernelBwdPrologue, stream);
-  cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, D,
-                             (const uint4*)out, (const uint4*)dout, (__nv_bfloat16*)rot,
-                             (const __nv_bfloat16*)qkv, g, n_dot_padded, n_rope);
+  cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
+                             (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot,
+                             (const __nv_bfloat16*)qkv, g, n_dot_padded, n_pad, n_rope);
   prof_end(kKernelBwdPrologue, stream);
   return e;
 }

@@ -97,9 +97,11 @@ ATTN_API int attn_fwd(void* out, float* lse, const void* qkv,
 
 /*
  * attn_bwd_workspace_bytes -- size in bytes of the scratch attn_bwd needs
- * for this shape and dtype: the row dots D = rowsum(dO * O) as float32
- * [B,NH,T], plus, for BF16, room for a RoPE-rotated bf16 copy of Q and K
- * (used only when rope_theta > 0).  Returns 0 for invalid arguments.
+ * for this shape and dtype: the row dots D = rowsum(dO * O) (float32
+ * [B,NH,T]; for BF16 stored next to the rescaled lse as float pairs over T
+ * rounded up to 64 rows), plus, for BF16, room for a RoPE-rotated bf16 copy
+ * of Q and K (used only when rope_theta > 0).  Returns 0 for invalid
+ * arguments.
  */
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype);
 

@@ -49,9 +49,13 @@ def test_strerror_and_version(cdll):
 def test_workspace_size(cdll):
     from causal_attention_gqa_gb300 import binding
     B, T, C, NH, NKV = 4, 2048, 2048, 16, 4
-    d_bytes = B * NH * T * 4
+    # bf16: (lse, D) float pairs per (b, h) row over T rounded up to 64, then
+    # the rotated Q/K copy; each part rounded up to 256 bytes.
+    row_bytes = B * NH * T * 8
     rot_bytes = B * T * (NH + NKV) * (C // NH) * 2
-    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == d_bytes + rot_bytes
+    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == row_bytes + rot_bytes
+    ragged = binding.attn_bwd_workspace_bytes(1, 100, 256, 2, 1, binding.DTYPE_BF16)
+    assert ragged == 2 * 128 * 8 + 100 * 3 * 128 * 2 + (256 - (100 * 3 * 128 * 2) % 256) % 256
     assert binding.attn_bwd_workspace_bytes(1, 16, 16, 4, 4, binding.DTYPE_F32) == 256
     assert binding.attn_bwd_workspace_bytes(1, 16, 16, 3, 4, binding.DTYPE_F32) == 0
 
