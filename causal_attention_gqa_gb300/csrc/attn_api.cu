@@ -211,7 +211,7 @@ extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, in
   a.status = status_word();
   a.num_sms = num_sms();
   if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
-  if (!make_tmap(&a.tm_qkv, qkv, g.W, g.T, g.B)) return ATTN_ERR_CUDA;
+  if (!make_tmap(&a.tm_qkv, qkv, g.W, g.T, g.B) || !make_tmap(&a.tm_out, out, g.C, g.T, g.B)) return ATTN_ERR_CUDA;
   return from_cuda(tc05_fwd_launch(a, s));
 }
 

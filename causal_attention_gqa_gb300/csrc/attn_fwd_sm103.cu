@@ -71,7 +71,7 @@ struct FwdCfg {
 
 struct FwdBarriers {
   uint64_t q_full[2], q_ready[2], q_empty[2], o_free[2];
-  uint64_t pv_done[2], p_full[2], drain, drain2;
+  uint64_t pv_done[2], p_full[2], drain, drain2, o_staged;
   uint64_t s_full[2], s_free[2];
   uint64_t k_full[4], k_ready[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t tmem_base;
@@ -181,7 +181,7 @@ struct TileRotator {
 
 template <int HD, bool ROPE>
 __global__ void __launch_bounds__(FwdCfg<HD, ROPE>::kThreads, 1)
-fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out, float* __restrict__ lse,
            int* __restrict__ status, Geometry g, int n_items) {
   using Cfg = FwdCfg<HD, ROPE>;
   constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages, NO = Cfg::kOBuffers;
@@ -200,7 +200,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->q_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->q_ready[i]), 4);
-      ptx::mbar_init(ptx::smem_u32(&bars->q_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->q_empty[i]), 2);  // last score MMA + epilogue store
       ptx::mbar_init(ptx::smem_u32(&bars->o_free[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 4);
@@ -209,6 +209,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
     }
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain2), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->o_staged), 4);
     for (int i = 0; i < NK; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->k_ready[i]), 4);
@@ -417,6 +418,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[sb]));
+        // Non-blocking checks issued now and consumed after the math: P
+        // buffer gi&1 was read by PV(gi-2); O may be rescaled only once
+        // PV(gi-1) (same item) has finished.
+        const int pb = gi & 1;
+        const uint32_t pfree_now = gi < 2 ? 1u : ptx::mbar_test(ptx::smem_u32(&bars->pv_done[pb]), ((gi - 2) >> 1) & 1);
+        const uint32_t prev_now =
+            j < 1 ? 1u : ptx::mbar_test(ptx::smem_u32(&bars->pv_done[pb ^ 1]), ((gi - 1) >> 1) & 1);
 
         if (j == n_kv - 1) {  // diagonal tile: key c is visible to row `row` iff c <= row
 #pragma unroll
@@ -455,19 +463,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
         l = l * corr + rs;
         m = m_new;
 
-        // P buffer gi&1 was read by PV(gi-2); O may be rescaled only once
-        // PV(gi-1) (same item) has finished.
-        const int pb = gi & 1;
         const bool rescale = (j >= 1) && __any_sync(0xffffffffu, grow);
-        if (gi >= 2) {
+        if (!__all_sync(0xffffffffu, pfree_now)) {
           ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[pb]), ((gi - 2) >> 1) & 1,
                                                         abort_flag, kWaitLimitNs));
           if (!ok) break;
         }
         if (rescale) {
-          ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[pb ^ 1]), ((gi - 1) >> 1) & 1,
-                                                        abort_flag, kWaitLimitNs));
-          if (!ok) break;
+          if (!__all_sync(0xffffffffu, prev_now)) {
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[pb ^ 1]), ((gi - 1) >> 1) & 1,
+                                                          abort_flag, kWaitLimitNs));
+            if (!ok) break;
+          }
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -500,35 +507,58 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict
       }
       if (!ok) break;
       // Epilogue of this item: O is complete once its last PV has finished.
+      // out = O / l is staged in this item's Q buffer (every score MMA of the
+      // item has completed) in the tensor-map layout and written with TMA
+      // stores (rows past T are clipped), instead of one scattered 16-byte
+      // store per thread and chunk.
       const int last = gi - 1;
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[last & 1]), (last >> 1) & 1,
                                                     abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = out + ((size_t)item.b * g.T + (tq < g.T ? tq : 0)) * g.C + item.h * HD;
+      uint8_t* stile = sQ + (it & 1) * Cfg::kTileBytes;
 #pragma unroll 1
       for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t o[32];
         ptx::tmem_ld32(o_addr + c0, o);
         ptx::tmem_wait_ld();
-        if (tq < g.T) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 w4 = make_uint4(
-                pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
-            *reinterpret_cast<uint4*>(orow + c0 + 8 * v) = w4;
-          }
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w4 = make_uint4(
+              pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+          *reinterpret_cast<uint4*>(stile + sw128_offset(row, c0 + 8 * v)) = w4;
         }
       }
       ptx::tc_fence_before();
+      ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->o_free[ob]));
+      if (lane == 0) {
+        ptx::mbar_arrive(ptx::smem_u32(&bars->o_free[ob]));
+        ptx::mbar_arrive(ptx::smem_u32(&bars->o_staged));
+      }
       if (tq < g.T) lse[((size_t)item.b * g.NH + item.h) * g.T + tq] = (m + log2f(l)) * 0.6931471805599453f;
+      if (warp == kSoftmaxWarp0 && lane == 0) {
+        // All four warps staged their rows: store the tile, and release the
+        // Q buffer once the TMA engine has read it.
+        if (ptx::mbar_wait(ptx::smem_u32(&bars->o_staged), it & 1, abort_flag, kWaitLimitNs)) {
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_store_3d(&tm_out, ptx::smem_u32(stile + a * Cfg::kAtomBytes), item.h * HD + 64 * a,
+                              item.qt * kBM, item.b);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read();
+        } else {
+          fail();
+        }
+        ptx::mbar_arrive(ptx::smem_u32(&bars->q_empty[it & 1]));
+      }
     }
+    // Every tile store has landed in global memory before the CTA exits.
+    if (warp == kSoftmaxWarp0 && lane == 0) ptx::bulk_wait();
     if (!ok) fail();
   } else if (ROPE && warp >= kRopeWarp0) {
     // ------------------------------------------------------------ RoPE transform
@@ -580,8 +610,7 @@ cudaError_t launch_fwd(const Tc05FwdArgs& a, cudaStream_t stream) {
   const int n_items = n_qt * a.g.B * a.g.NH;
   const unsigned grid = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelFwdTc05, stream);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qkv, (__nv_bfloat16*)a.out, a.lse, a.status, a.g,
-                                                        n_items);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qkv, a.tm_out, a.lse, a.status, a.g, n_items);
   prof_end(kKernelFwdTc05, stream);
   return cudaGetLastError();
 }

@@ -64,6 +64,7 @@ cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, con
 struct Tc05FwdArgs {
   Geometry g;
   CUtensorMap tm_qkv;  // qkv [B,T,W] bf16, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_out;  // out [B,T,C] bf16, same box and swizzle (tile stores)
   void* out;          // [B,T,C] bf16
   float* lse;         // [B,NH,T]
   int* status;        // library status word

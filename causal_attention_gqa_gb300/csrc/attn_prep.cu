@@ -107,86 +107,81 @@ __global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __rest
   }
 }
 
-// bf16 backward prologue in one launch over a flat index space:
-//  * the first n_dot threads (rounded up to whole warps) each multiply one
-//    16-byte chunk of out and dout; the hd/8 threads of a head-row sum their
-//    partials with shuffles and one of them writes the row-table entry
-//    LD[b,h,t] = (-lse[b,h,t] * log2(e), -D[b,h,t]): the two per-row values
-//    the backward's elementwise steps use, side by side, already in the form
-//    they enter the exponent and the dS difference;
-//  * the next n_pad threads clear the table rows T..Tp-1 of every (b, h), so
-//    that whole 64-row tiles of the table can be copied;
-//  * the remaining threads (RoPE only) each rotate 8 NEOX pairs of one Q or K
-//    head-row into the workspace copy.
-// One load per thread per tensor keeps many requests in flight.
+// bf16 backward prologue, one launch.  Block-stride over the B*T token rows
+// (b, t); for each row:
+//  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout; the
+//    hd/8 lanes of a head sum their partials with shuffles and one of them
+//    writes the row-table entry LD[b,h,t] = (-lse[b,h,t] * log2(e), -D[b,h,t])
+//    with D = dO . O: the two per-row values the backward's elementwise steps
+//    use, side by side, already in the form they enter the exponent and the
+//    dS difference;
+//  * (RoPE only) threads 0..(NH+NKV)*hd/16-1 each rotate 8 NEOX pairs of one
+//    Q or K head of the row into the workspace copy.
+// Afterwards the table rows T..Tp-1 of every (b, h) are cleared, so that whole
+// 64-row tiles of the table can be copied.  All index arithmetic is 32-bit
+// with shifts: hd/8 and hd/16 are powers of two.
 __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float2* __restrict__ LD, const uint4* __restrict__ out,
                                                                  const uint4* __restrict__ dout,
                                                                  const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
-                                                                 long long n_dot_padded, long long n_pad,
-                                                                 long long n_rope) {
+                                                                 int vph_log2, int rope) {
   // out is written by the forward that may still be finishing (programmatic
   // launch): wait for it, then let the dK/dV kernel get resident.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  const int vec_per_head = g.hd / 8;  // 8 or 16, divides 32
-  const long long n_dot = (long long)g.B * g.T * g.NH * vec_per_head;
-  const long long total = n_dot_padded + n_pad + n_rope;
-  const int Tp = row_table_rows(g.T);
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    if (idx < n_dot_padded) {  // warp-uniform: n_dot_padded is a multiple of 32
+  const int vph = 1 << vph_log2;                  // 16-byte chunks per head (hd / 8)
+  const int dot_units = g.C >> 3;                 // chunks per token row
+  const int dot_threads = (dot_units + 31) & ~31;  // whole warps take part in the shuffles
+  const int gph_log2 = vph_log2 - 1;              // 8-pair groups per head (hd / 16), log2
+  const int heads = g.NH + g.NKV, half = g.hd >> 1;
+  const int rope_units = rope ? heads << gph_log2 : 0;
+  const int rows = g.B * g.T, Tp = row_table_rows(g.T);
+  const int rot_w = heads * g.hd;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int b = row / g.T, t = row - b * g.T;
+    for (int c = threadIdx.x; c < dot_threads; c += blockDim.x) {
       float acc = 0.f;
-      if (idx < n_dot) {
-        const uint4 a = out[idx], c = dout[idx];
-        acc = bf16_lo(a.x) * bf16_lo(c.x) + bf16_hi(a.x) * bf16_hi(c.x) + bf16_lo(a.y) * bf16_lo(c.y) +
-              bf16_hi(a.y) * bf16_hi(c.y) + bf16_lo(a.z) * bf16_lo(c.z) + bf16_hi(a.z) * bf16_hi(c.z) +
-              bf16_lo(a.w) * bf16_lo(c.w) + bf16_hi(a.w) * bf16_hi(c.w);
+      if (c < dot_units) {
+        const uint4 a = out[(size_t)row * dot_units + c], d = dout[(size_t)row * dot_units + c];
+        acc = bf16_lo(a.x) * bf16_lo(d.x) + bf16_hi(a.x) * bf16_hi(d.x) + bf16_lo(a.y) * bf16_lo(d.y) +
+              bf16_hi(a.y) * bf16_hi(d.y) + bf16_lo(a.z) * bf16_lo(d.z) + bf16_hi(a.z) * bf16_hi(d.z) +
+              bf16_lo(a.w) * bf16_lo(d.w) + bf16_hi(a.w) * bf16_hi(d.w);
       }
-      for (int off = vec_per_head / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (idx < n_dot && (idx % vec_per_head) == 0) {
-        const long long r = idx / vec_per_head;  // ((b*T + t)*NH + h)
-        const int h = (int)(r % g.NH);
-        const long long bt = r / g.NH;
-        const int t = (int)(bt % g.T), b = (int)(bt / g.T);
-        const size_t bh = (size_t)b * g.NH + h;
-        LD[bh * Tp + t] = make_float2(-lse[bh * g.T + t] * 1.4426950408889634f, -acc);
+      for (int off = vph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (c < dot_units && (c & (vph - 1)) == 0) {
+        const int bh = b * g.NH + (c >> vph_log2);
+        LD[(size_t)bh * Tp + t] = make_float2(-lse[(size_t)bh * g.T + t] * 1.4426950408889634f, -acc);
       }
-      continue;
     }
-    if (idx < n_dot_padded + n_pad) {
-      const long long k = idx - n_dot_padded;
-      const int pad = Tp - g.T;
-      LD[(k / pad) * Tp + g.T + k % pad] = make_float2(0.f, 0.f);
-      continue;
-    }
-    const long long k = idx - n_dot_padded - n_pad;
-    const int groups = g.hd / 16, heads = g.NH + g.NKV, half = g.hd / 2;
-    const int gi = (int)(k % groups);
-    const long long r = k / groups;
-    const int head = (int)(r % heads);
-    const long long bt = r / heads;
-    const int t = (int)(bt % g.T);
-    const __nv_bfloat16* src = qkv + bt * g.W + head * g.hd;
-    __nv_bfloat16* dst = rot + bt * (long long)heads * g.hd + head * g.hd;
-    const uint4 x0 = *reinterpret_cast<const uint4*>(src + gi * 8);
-    const uint4 x1 = *reinterpret_cast<const uint4*>(src + half + gi * 8);
-    const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
-    uint32_t ya[4], yc[4];
+    for (int u = threadIdx.x; u < rope_units; u += blockDim.x) {
+      const int head = u >> gph_log2, gi = u & ((1 << gph_log2) - 1);
+      const __nv_bfloat16* src = qkv + (size_t)row * g.W + head * g.hd;  // K heads follow Q heads at column C
+      __nv_bfloat16* dst = rot + (size_t)row * rot_w + head * g.hd;
+      const uint4 x0 = *reinterpret_cast<const uint4*>(src + gi * 8);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(src + half + gi * 8);
+      const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
+      uint32_t ya[4], yc[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float s0, c0, s1, c1, y00, y01, y10, y11;
-      const int i0 = gi * 8 + 2 * q;
-      __sincosf(rope_angle(t, g.rope_f_hi[i0], g.rope_f_lo[i0]), &s0, &c0);
-      __sincosf(rope_angle(t, g.rope_f_hi[i0 + 1], g.rope_f_lo[i0 + 1]), &s1, &c1);
-      rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
-      rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
-      ya[q] = pack_bf16x2(y00, y01);
-      yc[q] = pack_bf16x2(y10, y11);
+      for (int q = 0; q < 4; ++q) {
+        float s0, c0, s1, c1, y00, y01, y10, y11;
+        const int i0 = gi * 8 + 2 * q;
+        __sincosf(rope_angle(t, g.rope_f_hi[i0], g.rope_f_lo[i0]), &s0, &c0);
+        __sincosf(rope_angle(t, g.rope_f_hi[i0 + 1], g.rope_f_lo[i0 + 1]), &s1, &c1);
+        rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
+        rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
+        ya[q] = pack_bf16x2(y00, y01);
+        yc[q] = pack_bf16x2(y10, y11);
+      }
+      *reinterpret_cast<uint4*>(dst + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+      *reinterpret_cast<uint4*>(dst + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
     }
-    *reinterpret_cast<uint4*>(dst + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-    *reinterpret_cast<uint4*>(dst + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+  }
+  // Table padding rows T..Tp-1 of every (b, h).
+  const int pad = Tp - g.T, n_pad = g.B * g.NH * pad;
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n_pad; k += gridDim.x * blockDim.x) {
+    const int bh = k / pad;
+    LD[(size_t)bh * Tp + g.T + (k - bh * pad)] = make_float2(0.f, 0.f);
   }
 }
 
@@ -194,16 +189,15 @@ __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float2* __restri
 
 cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, const void* dout, const float* lse,
                                      const void* qkv, const Geometry& g, cudaStream_t stream) {
-  const long long n_dot = (long long)g.B * g.T * g.NH * (g.hd / 8);
-  const long long n_dot_padded = (n_dot + 31) / 32 * 32;
-  const long long n_pad = (long long)g.B * g.NH * (row_table_rows(g.T) - g.T);
-  const long long n_rope = (g.rope_theta > 0.f) ? (long long)g.B * g.T * (g.NH + g.NKV) * (g.hd / 16) : 0;
-  long long blocks = (n_dot_padded + n_pad + n_rope + 255) / 256;
-  if (blocks > 152 * 32) blocks = 152 * 32;   // grid-stride beyond 32 blocks per SM (measured faster)
+  const int vph = g.hd / 8;  // 8 or 16
+  int vph_log2 = 0;
+  while ((1 << vph_log2) < vph) ++vph_log2;
+  const int rows = g.B * g.T;
+  const int blocks = rows < 152 * 8 ? rows : 152 * 8;  // 8 resident 256-thread blocks per SM
   prof_begin(kKernelBwdPrologue, stream);
   cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
                              (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot,
-                             (const __nv_bfloat16*)qkv, g, n_dot_padded, n_pad, n_rope);
+                             (const __nv_bfloat16*)qkv, g, vph_log2, g.rope_theta > 0.f ? 1 : 0);
   prof_end(kKernelBwdPrologue, stream);
   return e;
 }
