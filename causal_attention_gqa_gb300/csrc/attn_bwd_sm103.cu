@@ -606,6 +606,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
+      // Non-blocking check, consumed after the math: the dQ MMAs of step n-2
+      // are done with dS buffer st.
+      const uint32_t dsfree_now = n < 2 ? 1u : ptx::mbar_test(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1);
       const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
       const int kq = n * 64 + 32 * wg - tq;        // key column c is after this query iff c + kq > 0
       uint32_t dw[16];
@@ -621,8 +624,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd2));
         dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
       }
-      // The dQ MMAs of step n-2 must be done with dS buffer st.
-      if (n >= 2) {
+      if (!__all_sync(0xffffffffu, dsfree_now)) {
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag,
                                                       kWaitLimitNs));
         if (!ok) break;
