@@ -14,16 +14,16 @@
 //               the score MMA never waits on a load.
 //   warp 1      TMEM owner and score-MMA issuer (one thread): S_j = Q K_j^T
 //               into one of two TMEM score buffers.
-//   warp 6      PV-MMA issuer (one thread): O += P_j V_j with P_j read from
+//   warp 2      PV-MMA issuer (one thread): O += P_j V_j with P_j read from
 //               tensor memory (A operand) and V_j from shared memory.
 //               Two issuers keep the tensor core fed: each one's barrier
 //               checks and commits overlap the other's queued MMAs.
-//   warps 2-5   softmax: thread = query row = TMEM lane.  Reads S_j, keeps the
+//   warps 4-7   softmax: thread = query row = TMEM lane.  Reads S_j, keeps the
 //               running max m and sum l, writes P_j (bf16) into one of two
 //               TMEM P buffers, rescales O in TMEM when m grows past a
 //               threshold (exact: l and O share the stale max), and at the end
 //               of an item writes out = O / l and lse = m + ln l.
-//   warps 7-10  (RoPE only) rotate each item's Q and every landed K tile in
+//   warps 8-11  (RoPE only) rotate each item's Q and every landed K tile in
 //               shared memory before the score MMA may read them.
 // TMEM columns: S0, S1 (128 each), P0, P1 (64 each, bf16 pairs), then O (one
 // buffer at head size 128, two at 64).
@@ -47,9 +47,9 @@ constexpr int kBM = 128;                      // queries per tile
 constexpr int kBN = 128;                      // keys per tile
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: P may reach 2^8 before O is rescaled
-constexpr int kSoftmaxWarp0 = 2;
-constexpr int kPvWarp = 6;
-constexpr int kRopeWarp0 = 7;
+constexpr int kPvWarp = 2;
+constexpr int kSoftmaxWarp0 = 4;              // warpgroup 1
+constexpr int kRopeWarp0 = 8;                 // warpgroup 2 (RoPE only)
 
 template <int HD, bool ROPE>
 struct FwdCfg {
@@ -63,7 +63,7 @@ struct FwdCfg {
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // barriers + alignment slack
   static_assert(kSmemBytes <= 232448, "forward kernel exceeds the 227 KB shared-memory limit");
-  static constexpr int kThreads = ROPE ? 352 : 224;
+  static constexpr int kThreads = ROPE ? 384 : 256;
   static constexpr int kOBuffers = (HD == 128) ? 1 : 2;
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemP0 = 256, kTmemP1 = 320, kTmemO0 = 384,
                             kTmemO1 = 384 + HD, kTmemCols = 512;
@@ -431,35 +431,33 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           for (int c = 0; c < kBN; ++c)
             if (c > row) sr[c] = __float_as_uint(-INFINITY);
         }
-        // Row max with 8 independent partial maxima (no 128-long dependency chain).
-        float mx[8];
+        // Row max with 4 independent partial maxima (no 128-long dependency chain).
+        float mx[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+        for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sr[k]);
 #pragma unroll
-        for (int c = 8; c < kBN; c += 8)
+        for (int c = 4; c < kBN; c += 4)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         const float m_cand = mt * sl2;
         const bool grow = m_cand > m + kRescaleThreshold;   // always true on an item's first tile
         const float m_new = grow ? m_cand : m;
         const float corr = grow ? ptx::ex2_approx(m - m_new) : 1.f;
         // p = 2^(s * scale * log2(e) - m): exponent arguments two at a time
-        // (packed FMA), row sum in 8 independent partial sums (packed adds).
+        // (packed FMA), row sum in 4 independent partial sums (packed adds).
         const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(-m_new, -m_new);
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < kBN; c += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2);
           const float2 p = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
           sr[c] = __float_as_uint(p.x);
           sr[c + 1] = __float_as_uint(p.y);
-          acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], p);
+          acc[(c >> 1) & 1] = __fadd2_rn(acc[(c >> 1) & 1], p);
         }
-        const float2 acc01 = __fadd2_rn(acc[0], acc[1]), acc23 = __fadd2_rn(acc[2], acc[3]);
-        const float2 acc4 = __fadd2_rn(acc01, acc23);
-        const float rs = acc4.x + acc4.y;
+        const float2 acc2 = __fadd2_rn(acc[0], acc[1]);
+        const float rs = acc2.x + acc2.y;
         l = l * corr + rs;
         m = m_new;
 
@@ -468,6 +466,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done[pb]), ((gi - 2) >> 1) & 1,
                                                         abort_flag, kWaitLimitNs));
           if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        // P (bf16, two keys per 32-bit column) into TMEM P buffer pb.  Packed
+        // first, so that the 128 score registers are dead before the O rescale
+        // below needs its own 32.
+        {
+          const uint32_t p_addr = t_lane + (pb ? Cfg::kTmemP1 : Cfg::kTmemP0);
+          uint32_t pw[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pw[c] = pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+          ptx::tmem_st32(p_addr, pw);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            pw[c] = pack_bf16x2(__uint_as_float(sr[64 + 2 * c]), __uint_as_float(sr[64 + 2 * c + 1]));
+          ptx::tmem_st32(p_addr + 32, pw);
         }
         if (rescale) {
           if (!__all_sync(0xffffffffu, prev_now)) {
@@ -485,22 +498,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
             ptx::tmem_st32(o_addr + c0, o);
           }
-        } else {
-          ptx::tc_fence_after();
         }
-        // P (bf16, two keys per 32-bit column) into TMEM P buffer pb.
-        {
-          const uint32_t p_addr = t_lane + (pb ? Cfg::kTmemP1 : Cfg::kTmemP0);
-          uint32_t pw[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) pw[c] = pack_bf16x2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
-          ptx::tmem_st32(p_addr, pw);
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            pw[c] = pack_bf16x2(__uint_as_float(sr[64 + 2 * c]), __uint_as_float(sr[64 + 2 * c + 1]));
-          ptx::tmem_st32(p_addr + 32, pw);
-          ptx::tmem_wait_st();
-        }
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[pb]));

@@ -107,20 +107,23 @@ __global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __rest
   }
 }
 
-// bf16 backward prologue, one launch.  Block-stride over the B*T token rows
-// (b, t); for each row:
-//  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout; the
-//    hd/8 lanes of a head sum their partials with shuffles and one of them
-//    writes the row-table entry LD[b,h,t] = (-lse[b,h,t] * log2(e), -D[b,h,t])
-//    with D = dO . O: the two per-row values the backward's elementwise steps
-//    use, side by side, already in the form they enter the exponent and the
-//    dS difference;
+// bf16 backward prologue, one launch.  Block-stride over pairs of token rows
+// (b, t), (b, t+1) of the flattened B*T rows; for each pair:
+//  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout of both
+//    rows; the hd/8 lanes of a head sum their partials with shuffles and one
+//    of them writes the row-table entry LD[b,h,t] = (-lse[b,h,t] * log2(e),
+//    -D[b,h,t]) with D = dO . O: the two per-row values the backward's
+//    elementwise steps use, side by side, already in the form they enter the
+//    exponent and the dS difference;
 //  * (RoPE only) threads 0..(NH+NKV)*hd/16-1 each rotate 8 NEOX pairs of one
-//    Q or K head of the row into the workspace copy.
+//    Q or K head of both rows into the workspace copy.
+// Every load of a pair of rows is issued before the first of them is used,
+// so that each thread keeps several 16-byte loads in flight (the kernel is
+// bound by HBM latency and bandwidth, not arithmetic).
 // Afterwards the table rows T..Tp-1 of every (b, h) are cleared, so that whole
 // 64-row tiles of the table can be copied.  All index arithmetic is 32-bit
 // with shifts: hd/8 and hd/16 are powers of two.
-__global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float2* __restrict__ LD, const uint4* __restrict__ out,
+__global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float2* __restrict__ LD, const uint4* __restrict__ out,
                                                                  const uint4* __restrict__ dout,
                                                                  const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float2* __restri
   // launch): wait for it, then let the dK/dV kernel get resident.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
+  constexpr int R = 2;                            // token rows per iteration
   const int vph = 1 << vph_log2;                  // 16-byte chunks per head (hd / 8)
   const int dot_units = g.C >> 3;                 // chunks per token row
   const int dot_threads = (dot_units + 31) & ~31;  // whole warps take part in the shuffles
@@ -138,43 +142,69 @@ __global__ void __launch_bounds__(256) bwd_prologue_bf16_kernel(float2* __restri
   const int rope_units = rope ? heads << gph_log2 : 0;
   const int rows = g.B * g.T, Tp = row_table_rows(g.T);
   const int rot_w = heads * g.hd;
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int b = row / g.T, t = row - b * g.T;
+  const int n_groups = (rows + R - 1) / R;
+  for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
+    const int row0 = grp * R;
+    const int nr = min(R, rows - row0);
     for (int c = threadIdx.x; c < dot_threads; c += blockDim.x) {
-      float acc = 0.f;
-      if (c < dot_units) {
-        const uint4 a = out[(size_t)row * dot_units + c], d = dout[(size_t)row * dot_units + c];
-        acc = bf16_lo(a.x) * bf16_lo(d.x) + bf16_hi(a.x) * bf16_hi(d.x) + bf16_lo(a.y) * bf16_lo(d.y) +
-              bf16_hi(a.y) * bf16_hi(d.y) + bf16_lo(a.z) * bf16_lo(d.z) + bf16_hi(a.z) * bf16_hi(d.z) +
-              bf16_lo(a.w) * bf16_lo(d.w) + bf16_hi(a.w) * bf16_hi(d.w);
+      uint4 a[R], d[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        a[r] = make_uint4(0u, 0u, 0u, 0u);
+        d[r] = a[r];
+        if (c < dot_units && r < nr) {
+          a[r] = out[(size_t)(row0 + r) * dot_units + c];
+          d[r] = dout[(size_t)(row0 + r) * dot_units + c];
+        }
       }
-      for (int off = vph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (c < dot_units && (c & (vph - 1)) == 0) {
-        const int bh = b * g.NH + (c >> vph_log2);
-        LD[(size_t)bh * Tp + t] = make_float2(-lse[(size_t)bh * g.T + t] * 1.4426950408889634f, -acc);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float acc = bf16_lo(a[r].x) * bf16_lo(d[r].x) + bf16_hi(a[r].x) * bf16_hi(d[r].x) +
+                    bf16_lo(a[r].y) * bf16_lo(d[r].y) + bf16_hi(a[r].y) * bf16_hi(d[r].y) +
+                    bf16_lo(a[r].z) * bf16_lo(d[r].z) + bf16_hi(a[r].z) * bf16_hi(d[r].z) +
+                    bf16_lo(a[r].w) * bf16_lo(d[r].w) + bf16_hi(a[r].w) * bf16_hi(d[r].w);
+        for (int off = vph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (c < dot_units && r < nr && (c & (vph - 1)) == 0) {
+          const int row = row0 + r;
+          const int b = row / g.T, t = row - b * g.T;
+          const int bh = b * g.NH + (c >> vph_log2);
+          LD[(size_t)bh * Tp + t] = make_float2(-lse[(size_t)bh * g.T + t] * 1.4426950408889634f, -acc);
+        }
       }
     }
     for (int u = threadIdx.x; u < rope_units; u += blockDim.x) {
       const int head = u >> gph_log2, gi = u & ((1 << gph_log2) - 1);
-      const __nv_bfloat16* src = qkv + (size_t)row * g.W + head * g.hd;  // K heads follow Q heads at column C
-      __nv_bfloat16* dst = rot + (size_t)row * rot_w + head * g.hd;
-      const uint4 x0 = *reinterpret_cast<const uint4*>(src + gi * 8);
-      const uint4 x1 = *reinterpret_cast<const uint4*>(src + half + gi * 8);
-      const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
-      uint32_t ya[4], yc[4];
+      uint4 x0[R], x1[R];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float s0, c0, s1, c1, y00, y01, y10, y11;
-        const int i0 = gi * 8 + 2 * q;
-        __sincosf(rope_angle(t, g.rope_f_hi[i0], g.rope_f_lo[i0]), &s0, &c0);
-        __sincosf(rope_angle(t, g.rope_f_hi[i0 + 1], g.rope_f_lo[i0 + 1]), &s1, &c1);
-        rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
-        rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
-        ya[q] = pack_bf16x2(y00, y01);
-        yc[q] = pack_bf16x2(y10, y11);
+      for (int r = 0; r < R; ++r) {
+        if (r < nr) {
+          const __nv_bfloat16* src = qkv + (size_t)(row0 + r) * g.W + head * g.hd;  // K heads follow Q heads
+          x0[r] = *reinterpret_cast<const uint4*>(src + gi * 8);
+          x1[r] = *reinterpret_cast<const uint4*>(src + half + gi * 8);
+        }
       }
-      *reinterpret_cast<uint4*>(dst + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-      *reinterpret_cast<uint4*>(dst + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (r >= nr) break;
+        const int row = row0 + r;
+        const int t = row % g.T;
+        const uint32_t a[4] = {x0[r].x, x0[r].y, x0[r].z, x0[r].w}, c[4] = {x1[r].x, x1[r].y, x1[r].z, x1[r].w};
+        uint32_t ya[4], yc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float s0, c0, s1, c1, y00, y01, y10, y11;
+          const int i0 = gi * 8 + 2 * q;
+          __sincosf(rope_angle(t, g.rope_f_hi[i0], g.rope_f_lo[i0]), &s0, &c0);
+          __sincosf(rope_angle(t, g.rope_f_hi[i0 + 1], g.rope_f_lo[i0 + 1]), &s1, &c1);
+          rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
+          rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
+          ya[q] = pack_bf16x2(y00, y01);
+          yc[q] = pack_bf16x2(y10, y11);
+        }
+        __nv_bfloat16* dst = rot + (size_t)row * rot_w + head * g.hd;
+        *reinterpret_cast<uint4*>(dst + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+        *reinterpret_cast<uint4*>(dst + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+      }
     }
   }
   // Table padding rows T..Tp-1 of every (b, h).
@@ -192,8 +222,8 @@ cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, con
   const int vph = g.hd / 8;  // 8 or 16
   int vph_log2 = 0;
   while ((1 << vph_log2) < vph) ++vph_log2;
-  const int rows = g.B * g.T;
-  const int blocks = rows < 152 * 8 ? rows : 152 * 8;  // 8 resident 256-thread blocks per SM
+  const int groups = (g.B * g.T + 1) / 2;           // pairs of token rows
+  const int blocks = groups < 152 * 4 ? groups : 152 * 4;  // 4 resident 256-thread blocks per SM
   prof_begin(kKernelBwdPrologue, stream);
   cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
                              (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot,
