@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Causal MHA/GQA attention forward + backward throughput on GB300.
 
-One step = attn_fwd + attn_bwd (with its prologue kernels) over one batch of
-the synthetic workload, through the library's C ABI.  Prints ONE JSON line.
+One step = attn_fwd_ws (the forward with its RoPE pass over Q/K into a
+workspace) + attn_bwd (with its prologue kernel) over one batch of the
+synthetic workload, through the library's C ABI.  Prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload gqa_block|long_context_gqa|gpt2_124m_mha]
@@ -36,7 +37,7 @@ FLUSH_BYTES = 256 << 20          # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fwd_tc05": "attn_fwd_sm103.cu", "bwd_dkdv_tc05": "attn_bwd_sm103.cu", "bwd_dq_tc05": "attn_bwd_sm103.cu",
-    "bwd_row_dot": "attn_prep.cu", "bwd_rope_qk": "attn_prep.cu", "bwd_prologue": "attn_prep.cu",
+    "bwd_row_dot": "attn_prep.cu", "rope_qk": "attn_prep.cu", "bwd_prologue": "attn_prep.cu",
 }
 
 
@@ -242,13 +243,15 @@ def run_ours(args, w):
     dqkv_host = torch.empty(dqkv.shape, dtype=torch.bfloat16).pin_memory()
     ws_bytes = binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    fws_bytes = binding.attn_fwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16)
+    fws = torch.empty(max(fws_bytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
     code = binding.DTYPE_BF16
 
     def step():
-        binding.attn_fwd(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, sptr)
+        binding.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, fws, fws_bytes, sptr)
         binding.attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, w.rope_theta, code, ws, ws_bytes, sptr)
 
     def barrier():

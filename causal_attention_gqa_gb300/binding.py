@@ -7,6 +7,9 @@ has not been built this module raises on first use; there is no fallback.
 The entry points keep the C names and argument order:
 
     attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, stream=None)
+    attn_fwd_workspace_bytes(B, T, C, NH, NKV, dtype)
+    attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype,
+                workspace, workspace_bytes, stream=None)
     attn_bwd_workspace_bytes(B, T, C, NH, NKV, dtype)
     attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
              workspace, workspace_bytes, stream=None)
@@ -59,6 +62,10 @@ def load() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.attn_fwd.restype = i
+    lib.attn_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.attn_fwd_workspace_bytes.restype = sz
+    lib.attn_fwd_ws.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.attn_fwd_ws.restype = i
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -123,6 +130,16 @@ def attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, stream=None) ->
     _check(st, "attn_fwd")
 
 
+def attn_fwd_workspace_bytes(B, T, C, NH, NKV, dtype) -> int:
+    return int(load().attn_fwd_workspace_bytes(B, T, C, NH, NKV, int(dtype)))
+
+
+def attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, workspace, workspace_bytes, stream=None) -> None:
+    st = load().attn_fwd_ws(_ptr(out), _ptr(lse), _ptr(qkv), B, T, C, NH, NKV, float(rope_theta), int(dtype),
+                            _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "attn_fwd_ws")
+
+
 def attn_bwd_workspace_bytes(B, T, C, NH, NKV, dtype) -> int:
     return int(load().attn_bwd_workspace_bytes(B, T, C, NH, NKV, int(dtype)))
 
@@ -182,15 +199,25 @@ def dtype_code(t) -> int:
     raise TypeError(f"unsupported tensor dtype {t.dtype}")
 
 
-def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None):
-    """out, lse = attention forward of packed qkv [B, T, (NH+2*NKV)*hd]."""
+def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None, workspace=None):
+    """out, lse = attention forward of packed qkv [B, T, (NH+2*NKV)*hd].
+
+    With ``workspace`` (a uint8 tensor, or True to allocate one of
+    attn_fwd_workspace_bytes) the call goes through attn_fwd_ws, else attn_fwd."""
     import torch
     B, T, W = qkv.shape
     hd = W // (NH + 2 * NKV)
     C = NH * hd
+    code = dtype_code(qkv) if dtype is None else dtype
     out = torch.empty((B, T, C), dtype=qkv.dtype, device=qkv.device)
     lse = torch.empty((B, NH, T), dtype=torch.float32, device=qkv.device)
-    attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype_code(qkv) if dtype is None else dtype, stream)
+    if workspace is None:
+        attn_fwd(out, lse, qkv, B, T, C, NH, NKV, rope_theta, code, stream)
+    else:
+        if workspace is True:
+            nbytes = attn_fwd_workspace_bytes(B, T, C, NH, NKV, code)
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
+        attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, rope_theta, code, workspace, workspace.numel(), stream)
     return out, lse
 
 

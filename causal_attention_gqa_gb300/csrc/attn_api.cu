@@ -177,7 +177,7 @@ extern "C" const char* attn_strerror(int status) {
     case ATTN_ERR_BAD_SHAPE: return "invalid shape (B,T,C,NH,NKV; C%NH, NH%NKV, odd head size with RoPE, or size limits)";
     case ATTN_ERR_UNSUPPORTED: return "unsupported (dtype, head size) combination";
     case ATTN_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
-    case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than attn_bwd_workspace_bytes()";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than the *_workspace_bytes() size";
     case ATTN_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait expired";
     case ATTN_ERR_BAD_ARGUMENT: return "invalid argument";
@@ -185,8 +185,14 @@ extern "C" const char* attn_strerror(int status) {
   }
 }
 
-extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV,
-                        float rope_theta, int dtype, void* stream) {
+namespace {
+
+// Forward shared by attn_fwd (workspace == NULL: RoPE rotated inside the
+// attention kernel) and attn_fwd_ws (bf16 with RoPE: one rotation pass writes
+// the rotated Q/K copy into the workspace, and the attention kernel reads Q
+// and K from there).
+int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV, float rope_theta,
+             int dtype, void* workspace, size_t ws_bytes, void* stream) {
   Geometry g;
   int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
   if (st != ATTN_OK) return st;
@@ -204,15 +210,51 @@ extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, in
     return from_cuda(simt_launch(a, s));
   }
   if (!aligned16(out) || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+  const bool pre_rotate = workspace != nullptr && g.rope_theta > 0.f;
+  if (pre_rotate && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
   Tc05FwdArgs a{};
   a.g = g;
   a.out = out;
   a.lse = lse;
   a.status = status_word();
   a.num_sms = num_sms();
+  a.pre_rotated = pre_rotate;
   if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
-  if (!make_tmap(&a.tm_qkv, qkv, g.W, g.T, g.B) || !make_tmap(&a.tm_out, out, g.C, g.T, g.B)) return ATTN_ERR_CUDA;
+  const void* qk_src = pre_rotate ? workspace : qkv;
+  const int qk_width = pre_rotate ? (g.NH + g.NKV) * g.hd : g.W;
+  if (!make_tmap(&a.tm_qk, qk_src, qk_width, g.T, g.B) || !make_tmap(&a.tm_v, qkv, g.W, g.T, g.B) ||
+      !make_tmap(&a.tm_out, out, g.C, g.T, g.B))
+    return ATTN_ERR_CUDA;
+  if (pre_rotate) {
+    cudaError_t e = launch_rope_qk_bf16(workspace, qkv, g, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  }
   return from_cuda(tc05_fwd_launch(a, s));
+}
+
+}  // namespace
+
+extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV,
+                        float rope_theta, int dtype, void* stream) {
+  return fwd_impl(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, nullptr, 0, stream);
+}
+
+extern "C" size_t attn_fwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype) {
+  Geometry g;
+  if (check_shape(B, T, C, NH, NKV, 0.f, dtype, &g) != ATTN_OK) return 0;
+  if (dtype != ATTN_DTYPE_BF16) return 0;
+  return align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2);
+}
+
+extern "C" int attn_fwd_ws(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV,
+                           float rope_theta, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  Geometry g;
+  int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
+  if (st != ATTN_OK) return st;
+  const size_t need = attn_fwd_workspace_bytes(B, T, C, NH, NKV, dtype);
+  if (need > 0 && (!workspace || ws_bytes < need)) return ATTN_ERR_WORKSPACE;
+  return fwd_impl(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, need > 0 ? workspace : nullptr, ws_bytes,
+                  stream);
 }
 
 extern "C" size_t attn_bwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype) {

@@ -181,7 +181,8 @@ struct TileRotator {
 
 template <int HD, bool ROPE>
 __global__ void __launch_bounds__(FwdCfg<HD, ROPE>::kThreads, 1)
-fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out, float* __restrict__ lse,
+fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_v,
+           const __grid_constant__ CUtensorMap tm_out, float* __restrict__ lse,
            int* __restrict__ status, Geometry g, int n_items) {
   using Cfg = FwdCfg<HD, ROPE>;
   constexpr int NK = Cfg::kKStages, NV = Cfg::kVStages, NO = Cfg::kOBuffers;
@@ -242,7 +243,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      ptx::tma_prefetch_desc(&tm_qkv);
+      ptx::tma_prefetch_desc(&tm_qk);
+      ptx::tma_prefetch_desc(&tm_v);
       int k_issued = 0, v_issued = 0, q_issued = 0;  // global sequence counters
       bool ok = true;
       for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
@@ -260,7 +262,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
         ptx::mbar_arrive_expect_tx(qf, Cfg::kTileBytes);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(sQ + qb * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv,
+          ptx::tma_load_3d(ptx::smem_u32(sQ + qb * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qk,
                            item.h * HD + 64 * a, item.qt * kBM, item.b, qf);
         q_issued = it + 1;
         const int kbase = k_issued;  // global index of this item's key tile 0
@@ -272,7 +274,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           ptx::mbar_arrive_expect_tx(kf, Cfg::kTileBytes);
 #pragma unroll
           for (int a = 0; a < HD / 64; ++a)
-            ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv,
+            ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qk,
                              k_col + 64 * a, j * kBN, item.b, kf);
           k_issued = gi + 1;
           return true;
@@ -285,7 +287,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ C
           ptx::mbar_arrive_expect_tx(vf, Cfg::kTileBytes);
 #pragma unroll
           for (int a = 0; a < HD / 64; ++a)
-            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_qkv,
+            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtomBytes), &tm_v,
                              v_col + 64 * a, j * kBN, item.b, vf);
           v_issued = gi + 1;
           return true;
@@ -609,7 +611,7 @@ cudaError_t launch_fwd(const Tc05FwdArgs& a, cudaStream_t stream) {
   const int n_items = n_qt * a.g.B * a.g.NH;
   const unsigned grid = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelFwdTc05, stream);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qkv, a.tm_out, a.lse, a.status, a.g, n_items);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(a.tm_qk, a.tm_v, a.tm_out, a.lse, a.status, a.g, n_items);
   prof_end(kKernelFwdTc05, stream);
   return cudaGetLastError();
 }
@@ -617,7 +619,7 @@ cudaError_t launch_fwd(const Tc05FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream) {
-  const bool rope = a.g.rope_theta > 0.f;
+  const bool rope = a.g.rope_theta > 0.f && !a.pre_rotated;
   if (a.g.hd == 128) return rope ? launch_fwd<128, true>(a, stream) : launch_fwd<128, false>(a, stream);
   if (a.g.hd == 64) return rope ? launch_fwd<64, true>(a, stream) : launch_fwd<64, false>(a, stream);
   return cudaErrorInvalidValue;

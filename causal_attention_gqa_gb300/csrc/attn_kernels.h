@@ -49,7 +49,9 @@ size_t simt_max_smem_bytes(int hd);
 // D[b,h,t] = sum_d dout[b,t,h,d] * out[b,t,h,d] (float32 accumulation).
 cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Geometry& g, bool bf16,
                            cudaStream_t stream);
-// NEOX-rotated bf16 copy of every Q and K head: dst [B,T,(NH+NKV)*hd].
+// NEOX-rotated bf16 copy of every Q and K head: dst [B,T,(NH+NKV)*hd], query
+// head h at column h*hd and kv head kh at C + kh*hd (the columns they have
+// in qkv).  hd must be a multiple of 16.
 cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream);
 // Rows of the per-(b, h) row table the bf16 backward reads: T rounded up to
 // whole 64-row query tiles.
@@ -63,7 +65,13 @@ cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, con
 // ------------------------------------------------------------ tcgen05 bf16 path
 struct Tc05FwdArgs {
   Geometry g;
-  CUtensorMap tm_qkv;  // qkv [B,T,W] bf16, box {64, 128, 1}, 128-byte swizzle
+  // Q and K come from tm_qk (qkv itself, or the RoPE-rotated copy written by
+  // launch_rope_qk_bf16), V from tm_v (qkv); query head h starts at column
+  // h*hd and kv head kh at column C + kh*hd in both layouts.  Box {64, 128, 1},
+  // 128-byte swizzle.
+  CUtensorMap tm_qk;
+  CUtensorMap tm_v;
+  bool pre_rotated;    // RoPE on, Q/K already rotated: no rotation in the kernel
   CUtensorMap tm_out;  // out [B,T,C] bf16, same box and swizzle (tile stores)
   void* out;          // [B,T,C] bf16
   float* lse;         // [B,NH,T]

@@ -64,46 +64,65 @@ __global__ void __launch_bounds__(256) row_dot_bf16_vec_kernel(float* __restrict
   }
 }
 
-// One thread per (b, t, head, 8 consecutive pairs): heads 0..NH-1 are query
-// heads, NH..NH+NKV-1 key heads.  Writes dst[b,t,head*hd + ...].
-__global__ void __launch_bounds__(256) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
-                                                           const __nv_bfloat16* __restrict__ qkv, Geometry g) {
-  __shared__ float f_hi[64], f_lo[64];
-  for (int i = threadIdx.x; i < 64; i += blockDim.x) {
-    f_hi[i] = g.rope_f_hi[i];
-    f_lo[i] = g.rope_f_lo[i];
-  }
-  __syncthreads();
-  const int half = g.hd / 2, groups = half / 8;
+// Rotated Q/K copy.  Thread u of a block owns unit u of a token row: 8
+// consecutive NEOX pairs of one head (heads 0..NH-1 are query heads,
+// NH..NH+NKV-1 kv heads; K heads follow Q heads at column C in qkv, so head
+// `head` sits at column head*hd in both arrays).  The block walks groups of
+// R consecutive token rows with a block stride; all 2R loads of a group are
+// issued before the first is used (the kernel is HBM-bound).
+// dst[b,t,head*hd + ...] = rotated qkv[b,t,head*hd + ...].
+__global__ void __launch_bounds__(512) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
+                                                            const __nv_bfloat16* __restrict__ qkv, Geometry g,
+                                                            int gph_log2) {
+  constexpr int R = 4;
+  const int half = g.hd >> 1;
   const int heads = g.NH + g.NKV;
-  const long long total = (long long)g.B * g.T * heads * groups;
-  const int dst_w = heads * g.hd;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int gi = idx % groups;
-    const long long r = idx / groups;
-    const int head = r % heads;
-    const long long bt = r / heads;
-    const int t = bt % g.T;
-    const __nv_bfloat16* src = qkv + bt * g.W + head * g.hd;  // K heads follow Q heads at column C
-    __nv_bfloat16* out = dst + bt * dst_w + head * g.hd;
-    uint4 x0 = *reinterpret_cast<const uint4*>(src + gi * 8);
-    uint4 x1 = *reinterpret_cast<const uint4*>(src + half + gi * 8);
-    uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
-    uint32_t ya[4], yc[4];
+  const int upr = heads << gph_log2;               // units per token row
+  const int rows = g.B * g.T, dst_w = heads * g.hd;
+  const int n_groups = (rows + R - 1) / R;
+  for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
+    const int row0 = grp * R;
+    const int nr = min(R, rows - row0);
+    for (int u = threadIdx.x; u < upr; u += blockDim.x) {
+      const int head = u >> gph_log2, gi = u & ((1 << gph_log2) - 1);
+      const int col = head * g.hd + gi * 8;
+      uint4 x0[R], x1[R];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float s0, c0, s1, c1, y00, y01, y10, y11;
-      const int i0 = gi * 8 + 2 * k;
-      __sincosf(rope_angle(t, f_hi[i0], f_lo[i0]), &s0, &c0);
-      __sincosf(rope_angle(t, f_hi[i0 + 1], f_lo[i0 + 1]), &s1, &c1);
-      rope_pair(bf16_lo(a[k]), bf16_lo(c[k]), c0, s0, y00, y10);
-      rope_pair(bf16_hi(a[k]), bf16_hi(c[k]), c1, s1, y01, y11);
-      ya[k] = pack_bf16x2(y00, y01);
-      yc[k] = pack_bf16x2(y10, y11);
+      for (int r = 0; r < R; ++r) {
+        if (r < nr) {
+          const __nv_bfloat16* src = qkv + (size_t)(row0 + r) * g.W + col;
+          x0[r] = *reinterpret_cast<const uint4*>(src);
+          x1[r] = *reinterpret_cast<const uint4*>(src + half);
+        }
+      }
+      float f_hi[8], f_lo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        f_hi[e] = g.rope_f_hi[gi * 8 + e];
+        f_lo[e] = g.rope_f_lo[gi * 8 + e];
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (r >= nr) break;
+        const int row = row0 + r;
+        const int t = row % g.T;
+        const uint32_t a[4] = {x0[r].x, x0[r].y, x0[r].z, x0[r].w}, c[4] = {x1[r].x, x1[r].y, x1[r].z, x1[r].w};
+        uint32_t ya[4], yc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float s0, c0, s1, c1, y00, y01, y10, y11;
+          __sincosf(rope_angle(t, f_hi[2 * q], f_lo[2 * q]), &s0, &c0);
+          __sincosf(rope_angle(t, f_hi[2 * q + 1], f_lo[2 * q + 1]), &s1, &c1);
+          rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
+          rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
+          ya[q] = pack_bf16x2(y00, y01);
+          yc[q] = pack_bf16x2(y10, y11);
+        }
+        __nv_bfloat16* out = dst + (size_t)row * dst_w + col;
+        *reinterpret_cast<uint4*>(out) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+        *reinterpret_cast<uint4*>(out + half) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
+      }
     }
-    *reinterpret_cast<uint4*>(out + gi * 8) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-    *reinterpret_cast<uint4*>(out + half + gi * 8) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
   }
 }
 
@@ -250,12 +269,17 @@ cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Ge
 }
 
 cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream) {
-  const long long total = (long long)g.B * g.T * (g.NH + g.NKV) * (g.hd / 16);
-  long long blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  prof_begin(kKernelBwdRopeQK, stream);
-  rope_qk_bf16_kernel<<<(int)blocks, 256, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g);
-  prof_end(kKernelBwdRopeQK, stream);
+  int gph_log2 = 0;                                   // log2(hd / 16)
+  while ((16 << gph_log2) < g.hd) ++gph_log2;
+  const int upr = (g.NH + g.NKV) << gph_log2;
+  const int threads = upr >= 512 ? 512 : (upr + 31) / 32 * 32;
+  const int groups = (g.B * g.T + 3) / 4;
+  const int per_sm = 2048 / threads;                  // resident blocks per SM by thread count
+  const int cap = 152 * (per_sm > 0 ? per_sm : 1);
+  const int blocks = groups < cap ? groups : cap;
+  prof_begin(kKernelRopeQK, stream);
+  rope_qk_bf16_kernel<<<blocks, threads, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g, gph_log2);
+  prof_end(kKernelRopeQK, stream);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,7 @@ enum KernelId {
   kKernelBwdDkdvTc05 = 1,
   kKernelBwdDqTc05 = 2,
   kKernelBwdRowDot = 3,
-  kKernelBwdRopeQK = 4,
+  kKernelRopeQK = 4,
   kKernelFwdSimt = 5,
   kKernelBwdDkdvSimt = 6,
   kKernelBwdDqSimt = 7,

@@ -34,8 +34,8 @@
  * respect to the un-rotated qkv.
  *
  * Ownership and execution: the caller owns every buffer and the stream.  The
- * library allocates no device memory; the backward's scratch is the
- * caller's `workspace`.  Every call validates its arguments on the host, then
+ * library allocates no device memory; scratch is the caller's `workspace`
+ * (attn_bwd, attn_fwd_ws).  Every call validates its arguments on the host, then
  * enqueues kernels on `stream` (a cudaStream_t passed as void*; NULL is the
  * legacy default stream) and returns without synchronising.  Nothing is
  * launched when validation fails.
@@ -76,7 +76,7 @@ typedef enum {
   ATTN_ERR_BAD_SHAPE = -2,       /* B,T,NH,NKV < 1, C % NH, NH % NKV, odd hd with RoPE, overflow */
   ATTN_ERR_UNSUPPORTED = -3,     /* (dtype, head size) combination not implemented */
   ATTN_ERR_MISALIGNED = -4,      /* a pointer is not 16-byte aligned (bf16 path) */
-  ATTN_ERR_WORKSPACE = -5,       /* workspace NULL or smaller than attn_bwd_workspace_bytes() */
+  ATTN_ERR_WORKSPACE = -5,       /* workspace NULL or smaller than the *_workspace_bytes() size */
   ATTN_ERR_CUDA = -6,            /* a CUDA runtime call or kernel launch failed */
   ATTN_ERR_DEVICE_TIMEOUT = -7,  /* a device-side bounded wait expired (see attn_device_status) */
   ATTN_ERR_BAD_ARGUMENT = -8     /* any other invalid argument */
@@ -94,6 +94,32 @@ typedef enum {
 ATTN_API int attn_fwd(void* out, float* lse, const void* qkv,
              int B, int T, int C, int NH, int NKV, float rope_theta,
              int dtype, void* stream);
+
+/*
+ * attn_fwd_workspace_bytes -- size in bytes of the scratch attn_fwd_ws
+ * uses for this shape and dtype: room for a RoPE-rotated copy of Q and K,
+ * [B,T,(NH+NKV)*hd] of dtype, for BF16; 0 for F32 (which needs none) and
+ * for invalid arguments.
+ *
+ * attn_fwd_ws -- attn_fwd with caller-provided scratch.  Same arguments,
+ * results and supported shapes as attn_fwd, plus
+ *   workspace : device scratch of at least attn_fwd_workspace_bytes(...)
+ *          bytes (may be NULL when that is 0), 256-byte aligned, owned by the
+ *          caller; its contents on entry do not matter and are garbage on
+ *          return.
+ * With BF16 and rope_theta > 0 it first rotates every Q and K head once into
+ * the workspace (one HBM-bound pass over Q and K, the rotation the source
+ * pages apply to qkv in place before attention) and then runs the attention
+ * kernel on the rotated copy; attn_fwd instead rotates Q and every K tile
+ * inside the attention kernel, once per use, which costs more for long
+ * sequences because each K tile is used by many query tiles.  Without RoPE,
+ * or for F32, it is attn_fwd.  The two give the same results up to the
+ * rounding of the rotated values to dtype (both round them once).
+ */
+ATTN_API size_t attn_fwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype);
+ATTN_API int attn_fwd_ws(void* out, float* lse, const void* qkv,
+             int B, int T, int C, int NH, int NKV, float rope_theta,
+             int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_bwd_workspace_bytes -- size in bytes of the scratch attn_bwd needs
@@ -186,7 +212,7 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
  *   kernel ids 0..n-1 store the summed elapsed milliseconds in total_ms[id]
  *   and the launch count in launches[id] (either array may be NULL).
  * attn_kernel_name -- short name of kernel id (see attn_profile.h ids:
- *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 bwd_rope_qk,
+ *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 rope_qk,
  *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt, 8 bwd_prologue); "unknown"
  *   otherwise.
  */

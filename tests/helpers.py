@@ -23,12 +23,14 @@ def to_numpy(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(lib, w, qkv_np, dout_np, dtype, backward=True):
-    """Forward (and backward) through the C ABI; returns numpy float64 arrays."""
+def run_gpu(lib, w, qkv_np, dout_np, dtype, backward=True, fwd_ws=False):
+    """Forward (and backward) through the C ABI; returns numpy float64 arrays.
+    fwd_ws: run the forward through attn_fwd_ws (pre-rotated Q/K) instead of
+    attn_fwd."""
     import torch
     qkv = to_device(qkv_np, dtype)
     dout = to_device(dout_np, dtype)
-    out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta)
+    out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta, workspace=True if fwd_ws else None)
     res = {"out": out, "lse": lse}
     if backward:
         res["dqkv"] = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta)

@@ -28,7 +28,8 @@ def declared_symbols():
 
 def test_header_declares_entry_points():
     names = declared_symbols()
-    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_strerror"):
+    for required in ("attn_fwd", "attn_fwd_ws", "attn_fwd_workspace_bytes", "attn_bwd", "attn_bwd_workspace_bytes",
+                     "attn_strerror"):
         assert required in names
 
 
@@ -85,3 +86,20 @@ def test_backward_rejects_missing_workspace(cdll):
     assert cdll.attn_bwd(p, p, p, p, p, 1, 16, 16, 4, 4, 0.0, 0, None, 0, None) == -5
     assert cdll.attn_bwd(p, p, p, p, p, 1, 16, 16, 4, 4, 0.0, 0, p, 8, None) == -5
     assert cdll.attn_bwd(p, p, p, p, p, 1, 16, 16, 4, 4, 0.0, 0, p + 16, 4096, None) == -4
+
+
+def test_forward_workspace_size_and_validation(cdll):
+    from causal_attention_gqa_gb300 import binding
+    B, T, C, NH, NKV = 4, 2048, 2048, 16, 4
+    # bf16: the rotated Q/K copy [B, T, (NH+NKV)*hd], rounded up to 256 bytes.
+    assert binding.attn_fwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == B * T * (NH + NKV) * 128 * 2
+    assert binding.attn_fwd_workspace_bytes(1, 100, 256, 2, 1, binding.DTYPE_BF16) == (100 * 3 * 128 * 2 + 255) // 256 * 256
+    assert binding.attn_fwd_workspace_bytes(1, 99, 256, 2, 1, binding.DTYPE_BF16) == (99 * 3 * 128 * 2 + 255) // 256 * 256
+    assert binding.attn_fwd_workspace_bytes(1, 16, 16, 4, 4, binding.DTYPE_F32) == 0
+    assert binding.attn_fwd_workspace_bytes(1, 16, 16, 3, 4, binding.DTYPE_BF16) == 0
+    p = 1 << 20   # never dereferenced: validation fails first
+    args = (1, 128, 512, 4, 1, 1e6, binding.DTYPE_BF16)
+    assert cdll.attn_fwd_ws(p, p, p, *args, None, 0, None) == -5
+    assert cdll.attn_fwd_ws(p, p, p, *args, p, 64, None) == -5
+    assert cdll.attn_fwd_ws(p, p, p, 1, 16, 16, 3, 3, 0.0, 0, None, 0, None) == -2
+    assert cdll.attn_fwd_ws(None, None, None, 1, 16, 16, 4, 4, 0.0, 0, None, 0, None) == -1

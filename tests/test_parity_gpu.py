@@ -15,9 +15,9 @@ from helpers import TOL, rel_err, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-def check_full(lib, w, dtype, backward=True):
+def check_full(lib, w, dtype, backward=True, fwd_ws=False):
     qkv, dout = make_inputs(w, dtype)
-    got = run_gpu(lib, w, qkv, dout, dtype, backward=backward)
+    got = run_gpu(lib, w, qkv, dout, dtype, backward=backward, fwd_ws=fwd_ws)
     tol = TOL[dtype]
     if backward:
         ref_dqkv, aux = oracle.attention_backward(qkv, dout, w.C, w.NH, w.NKV, w.rope_theta, return_aux=True)
@@ -66,6 +66,15 @@ def test_bf16_forward_shapes(lib, B, T, C, NH, NKV, theta):
 
 
 @pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    (1, 1, 128, 1, 1, 1e6), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6), (1, 256, 256, 4, 1, 1e4),
+    (1, 1000, 512, 4, 1, 1e6), (1, 77, 512, 4, 4, 0.0),
+])
+def test_bf16_forward_workspace_shapes(lib, B, T, C, NH, NKV, theta):
+    """attn_fwd_ws: Q/K rotated once into the workspace, then attention."""
+    check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 9), "bf16", fwd_ws=True)
+
+
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
     (1, 1, 128, 1, 1, 0.0), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6), (1, 77, 512, 4, 4, 0.0),
     (1, 256, 256, 4, 1, 1e4), (1, 640, 1024, 8, 2, 1e6),
 ])
@@ -79,12 +88,13 @@ def test_bf16_gpt2_mha_reduced_batch(lib):
 
 
 # ------------------------------------------------------------------ full-size, sampled
-def check_sampled(lib, w, dtype, n_rows=64, kv_groups=None):
-    """Full-size run in the benchmark's launch configuration; the oracle is
+def check_sampled(lib, w, dtype, n_rows=64, kv_groups=None, fwd_ws=False):
+    """Full-size run in the benchmark's launch configuration (fwd_ws: the
+    forward through attn_fwd_ws, as bench.py calls it); the oracle is
     evaluated on seeded query rows of every head (out, lse, dQ) and on seeded
     key rows of a few kv groups (dK, dV)."""
     qkv, dout = make_inputs(w, dtype)
-    got = run_gpu(lib, w, qkv, dout, dtype)
+    got = run_gpu(lib, w, qkv, dout, dtype, fwd_ws=fwd_ws)
     qr = sample_rows(w.T, n_rows, w.seed + 1)
     kr = sample_rows(w.T, n_rows, w.seed + 2)
     if kv_groups is None:
@@ -114,8 +124,12 @@ def test_bf16_gpt2_mha_full_sampled(lib):
 
 
 def test_bf16_gqa_block_full_sampled(lib):
-    check_sampled(lib, WORKLOADS["gqa_block"], "bf16")
+    check_sampled(lib, WORKLOADS["gqa_block"], "bf16", fwd_ws=True)
+
+
+def test_bf16_gqa_block_full_sampled_in_kernel_rope(lib):
+    check_sampled(lib, WORKLOADS["gqa_block"], "bf16", fwd_ws=False)
 
 
 def test_bf16_long_context_full_sampled(lib):
-    check_sampled(lib, WORKLOADS["long_context_gqa"], "bf16", kv_groups=[(0, 0), (0, 7)])
+    check_sampled(lib, WORKLOADS["long_context_gqa"], "bf16", kv_groups=[(0, 0), (0, 7)], fwd_ws=True)
