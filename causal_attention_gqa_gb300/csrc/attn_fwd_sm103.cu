@@ -1,9 +1,10 @@
 // Causal MHA/GQA attention forward on sm_103a tensor cores (bf16 in, f32
 // accumulation), head size 64 or 128.
 //
-// Persistent kernel: one CTA per SM walks a strided list of work items, one
-// item = a 128-query tile of one (batch row, query head), heaviest (longest
-// causal row range) first; query heads that share a kv head are adjacent in
+// Persistent kernel: one CTA per SM walks its share of a list of work items
+// (dealt back and forth across the CTAs, see snake_item), one item = a
+// 128-query tile of one (batch row, query head), heaviest (longest causal row
+// range) first; query heads that share a kv head are adjacent in
 // the list, so concurrently running CTAs reuse K/V tiles through L2.  Every
 // role runs one continuous stream of key tiles across its items, so the next
 // item's loads and first MMAs overlap the current item's last softmax and
@@ -95,6 +96,16 @@ __device__ __forceinline__ FwdItem fwd_item(int w, const Geometry& g) {
   it.h = bh % g.NH;
   it.kh = it.h / g.grp;
   return it;
+}
+
+// The it-th item of the CTA with index w0 in a grid of dw CTAs.  Items are
+// dealt in rounds of dw, forward in even rounds and backward in odd ones
+// (boustrophedon), so that the CTA that took the heaviest item of one round
+// takes the lightest of the next: with items sorted by decreasing weight this
+// keeps the per-CTA totals within a few percent of each other, where a plain
+// stride leaves the first CTAs with up to ~25 % more work.
+__device__ __forceinline__ int snake_item(int it, int w0, int dw) {
+  return it * dw + ((it & 1) ? dw - 1 - w0 : w0);
 }
 
 // Byte offset of element (row, col) inside a 128-row bf16 tile stored as
@@ -195,7 +206,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int w0 = blockIdx.x, dw = gridDim.x;   // this CTA's items: w0, w0 + dw, ...
+  const int w0 = blockIdx.x, dw = gridDim.x;   // this CTA's items: snake_item(0..., w0, dw)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -247,7 +258,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
       ptx::tma_prefetch_desc(&tm_v);
       int k_issued = 0, v_issued = 0, q_issued = 0;  // global sequence counters
       bool ok = true;
-      for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+      for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake_item(it, w0, dw)) {
         const FwdItem item = fwd_item(w, g);
         const int n_kv = item.qt + 1;
         const int k_col = g.C + item.kh * HD, v_col = g.C + g.NKV * HD + item.kh * HD;
@@ -318,7 +329,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
       bool ok = true;
       int gi = 0;  // global key-tile index of this CTA's stream
-      for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+      for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake_item(it, w0, dw)) {
         const FwdItem item = fwd_item(w, g);
         const int n_kv = item.qt + 1, qb = it & 1;
         ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->q_ready[qb] : &bars->q_full[qb]), (it >> 1) & 1, abort_flag,
@@ -359,7 +370,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
       const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), Cfg::kAtomBytes, 1024);
       bool ok = true;
       int gi = 0;
-      for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+      for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake_item(it, w0, dw)) {
         const FwdItem item = fwd_item(w, g);
         const int n_kv = item.qt + 1, ob = (NO == 2) ? (it & 1) : 0;
         // The first PV of an item overwrites its O buffer: the epilogue of the
@@ -397,7 +408,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
     const float sl2 = g.scale * 1.4426950408889634f;  // scale * log2(e)
     bool ok = true;
     int gi = 0;
-    for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+    for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake_item(it, w0, dw)) {
       const FwdItem item = fwd_item(w, g);
       const int n_kv = item.qt + 1;
       const int tq = item.qt * kBM + row;
@@ -568,7 +579,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
     rot.init(tid, g);
     bool ok = true;
     int gi = 0;
-    for (int it = 0, w = w0; w < n_items && ok; ++it, w += dw) {
+    for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake_item(it, w0, dw)) {
       const FwdItem item = fwd_item(w, g);
       const int qb = it & 1;
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]), (it >> 1) & 1, abort_flag,
