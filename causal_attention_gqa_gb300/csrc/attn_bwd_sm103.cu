@@ -329,8 +329,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       const bool diag = qi <= 2 * j + 1;           // this query tile overlaps the key tile
       const int qk = qi * 64 - ks;                 // query column c is before this key iff c + qk < 0
       // Row-table pairs of two consecutive queries: (-lse2_c, -D_c, -lse2_c+1, -D_c+1).
+      // Every thread reads all 32 pairs of the step (broadcast loads); they are
+      // fetched four pairs ahead of their use, the first four before the TMEM
+      // loads complete, so that their latency overlaps the math instead of
+      // stalling each column pair.
       const float4* ld4 = reinterpret_cast<const float4*>(sLD + (n % NQS) * Cfg::kQ);
       const float2 sl2x2 = make_float2(sl2, sl2);
+      float4 Lw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) Lw[k] = ld4[k];
       // Two halves of 32 query columns (all 64 at once would spill registers
       // in this 10-warp kernel).
 #pragma unroll
@@ -341,8 +348,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const int q = 32 * half + c;
-          const float4 L = ld4[q >> 1];
+          const int q = 32 * half + c, k = q >> 1;
+          const float4 L = Lw[k & 3];
+          if (k + 4 < 32) Lw[k & 3] = ld4[k + 4];
           // p = 2^(s * scale * log2(e) - lse * log2(e)); dS = p * (dP - D)
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
                                       make_float2(L.x, L.z));
