@@ -15,8 +15,9 @@
 //  * dkdv: one CTA per (128-key tile j, kv head, batch row).  K_j and V_j stay
 //    in shared memory; the CTA walks every query head of the group and every
 //    64-query tile that can see tile j.  Per step: S^T = K Q^T and
-//    dP^T = V dO^T into TMEM (double-buffered), P^T and dS^T (bf16) into
-//    shared memory, then dV += P^T dO and dK += dS^T Q accumulate in TMEM.
+//    dP^T = V dO^T into TMEM (double-buffered), P^T and dS^T (bf16) back
+//    into TMEM over the score columns already read, then dV += P^T dO and
+//    dK += dS^T Q (A operand from TMEM) accumulate in TMEM.
 //  * dq:   one CTA per (128-query tile i, query head, batch row).  Q_i and dO_i
 //    stay in shared memory; the CTA walks the 64-key tiles 0..2i+1.  Per step:
 //    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
@@ -119,25 +120,27 @@ struct DkdvCfg {
   static constexpr int kKeys = 128, kQ = 64;
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
-  static constexpr int kPTile = kKeys * kQ * 2;        // P^T or dS^T (one atom column)
   // Q/dO ring depth: loads for step n+NQS-1 are in flight while step n runs.
-  static constexpr int kQStages = (HD == 128) ? 3 : 4;
+  // The ring recycles a slot only after the step's gradient MMAs, so its
+  // depth must cover load latency + score MMAs + elementwise + gradient MMAs.
+  static constexpr int kQStages = (HD == 128) ? 4 : 8;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKTile;
   static constexpr int kQOff = kVOff + kKTile;
   static constexpr int kDOOff = kQOff + kQStages * kQTile;
-  static constexpr int kPOff = kDOOff + kQStages * kQTile;
-  static constexpr int kDSOff = kPOff + 2 * kPTile;
-  static constexpr int kLDOff = kDSOff + 2 * kPTile;       // row-table tiles (float2 per query)
+  static constexpr int kLDOff = kDOOff + kQStages * kQTile;  // row-table tiles (float2 per query)
   static constexpr int kBarOff = kLDOff + kQStages * kQ * 8;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  // TMEM: two score buffers of 128 columns (S^T at +0, dP^T at +64; P^T and
+  // dS^T, bf16 pairs, overwrite the first 32 columns of each once read), then
+  // the dK and dV accumulators.
   static constexpr uint32_t kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "dK/dV kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DkdvBarriers {
   uint64_t kv_full, acc_done, drain;
-  uint64_t qdo_full[4], qdo_empty[4], s_full[2], p_full[2];
+  uint64_t qdo_full[8], qdo_empty[8], s_full[2], p_full[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -156,8 +159,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   uint8_t* sV = smem + Cfg::kVOff;
   uint8_t* sQ = smem + Cfg::kQOff;
   uint8_t* sDO = smem + Cfg::kDOOff;
-  uint8_t* sP = smem + Cfg::kPOff;
-  uint8_t* sDS = smem + Cfg::kDSOff;
   float2* sLD = reinterpret_cast<float2*>(smem + Cfg::kLDOff);
   DkdvBarriers* bars = reinterpret_cast<DkdvBarriers*>(smem + Cfg::kBarOff);
   volatile int* abort_flag = &bars->abort;
@@ -262,23 +263,23 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       const uint64_t dDOk = ptx::sw128_desc(ptx::smem_u32(sDO), 16, 1024);
       const uint64_t dQm = ptx::sw128_desc(ptx::smem_u32(sQ), Cfg::kQ * 128, 1024);
       const uint64_t dDOm = ptx::sw128_desc(ptx::smem_u32(sDO), Cfg::kQ * 128, 1024);
-      const uint64_t dP = ptx::sw128_desc(ptx::smem_u32(sP), 16, 1024);
-      const uint64_t dDS = ptx::sw128_desc(ptx::smem_u32(sDS), 16, 1024);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
 
+      // Gradient MMAs of step m with A from TMEM: P^T and dS^T (bf16 pairs)
+      // sit in the first 32 columns of the step's S^T and dP^T halves.  The
+      // next score MMAs into the same buffer (step m+2) are issued after
+      // these, and MMAs issued by one thread execute in order.
       auto issue_grad = [&](int m) -> bool {
         const int st = m & 1, u = m >> 1, qs = m % NQS;
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        const uint64_t ap = ptx::desc_advance(dP, st * Cfg::kPTile), ads = ptx::desc_advance(dDS, st * Cfg::kPTile);
+        const uint32_t ap = tmem + st * 128, ads = tmem + st * 128 + 64;
         const uint64_t bdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile), bq = ptx::desc_advance(dQm, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kQ / 16; ++kk) {
           const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDV, ptx::desc_advance(ap, kk * 32), ptx::desc_advance(bdo, kk * 2048),
-                           idesc_g, acc);
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDK, ptx::desc_advance(ads, kk * 32), ptx::desc_advance(bq, kk * 2048),
-                           idesc_g, acc);
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDV, ap + kk * 8, ptx::desc_advance(bdo, kk * 2048), idesc_g, acc);
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDK, ads + kk * 8, ptx::desc_advance(bq, kk * 2048), idesc_g, acc);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
         return true;
@@ -365,10 +366,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           pw[c >> 1] = pack_bf16x2(p0, p1);
           dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
         }
-        store_row_half(sP + st * Cfg::kPTile, row, half, pw);
-        store_row_half(sDS + st * Cfg::kPTile, row, half, dw);
+        // P^T and dS^T of these 32 queries over the S^T / dP^T columns this
+        // thread has already read.
+        ptx::tmem_st16(t_lane + st * 128 + 16 * half, pw);
+        ptx::tmem_st16(t_lane + st * 128 + 64 + 16 * half, dw);
       }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[st]));
