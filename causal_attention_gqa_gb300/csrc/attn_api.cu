@@ -134,9 +134,9 @@ int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtyp
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Leading part of the workspace: float32 row dots [B,NH,T] (F32), or the
-// bf16 path's row table of float pairs [B,NH,Tp].
+// bf16 path's two row tables per (b, h), Tp floats each.
 size_t row_part_bytes(const Geometry& g, int dtype) {
-  if (dtype == ATTN_DTYPE_BF16) return align256((size_t)g.B * g.NH * row_table_rows(g.T) * sizeof(float2));
+  if (dtype == ATTN_DTYPE_BF16) return align256((size_t)g.B * g.NH * row_table_rows(g.T) * 2 * sizeof(float));
   return align256((size_t)g.B * g.NH * g.T * sizeof(float));
 }
 
@@ -296,7 +296,7 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
   Tc05BwdArgs a{};
   a.g = g;
   a.dqkv = dqkv;
-  a.LD = static_cast<const float2*>(workspace);
+  a.LD = static_cast<const float*>(workspace);
   a.status = status_word();
   a.num_sms = num_sms();
   if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
@@ -312,7 +312,7 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
         !make_tmap(&a.tm_v[r], qkv, g.W, g.T, g.B, rows) || !make_tmap(&a.tm_do[r], dout, g.C, g.T, g.B, rows))
       return ATTN_ERR_CUDA;
   }
-  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float2*>(workspace), rot, out, dout, lse, qkv, g, s);
+  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rot, out, dout, lse, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
 }

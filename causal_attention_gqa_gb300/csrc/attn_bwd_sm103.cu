@@ -14,10 +14,10 @@
 // writer:
 //  * dkdv: one CTA per (128-key tile j, kv head, batch row).  K_j and V_j stay
 //    in shared memory; the CTA walks every query head of the group and every
-//    64-query tile that can see tile j.  Per step: S^T = K Q^T and
-//    dP^T = V dO^T into TMEM (double-buffered), P^T and dS^T (bf16) back
-//    into TMEM over the score columns already read, then dV += P^T dO and
-//    dK += dS^T Q (A operand from TMEM) accumulate in TMEM.
+//    128-query tile that can see tile j.  Per step: S^T = K Q^T and
+//    dP^T = V dO^T into TMEM, P^T and dS^T (bf16) back into TMEM over the
+//    score columns already read, then dV += P^T dO and dK += dS^T Q (A
+//    operand from TMEM) accumulate in TMEM.
 //  * dq:   one CTA per (128-query tile i, query head, batch row).  Q_i and dO_i
 //    stay in shared memory; the CTA walks the 64-key tiles 0..2i+1.  Per step:
 //    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
@@ -115,41 +115,53 @@ __device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope,
 // ===========================================================================
 // dK / dV kernel
 // ===========================================================================
+// One step = 128 queries of one query head of the group, so that every MMA
+// has N = 128 (full tensor-core rate; N = 64 runs at about two thirds).  TMEM:
+// S^T [0, 128), dP^T [128, 256), dK and dV accumulators from column 256.  The
+// step's four MMA groups run in order S^T, dP^T, dV, dK; the elementwise
+// groups turn S^T into P^T while dP^T is computed, and dP^T into dS^T while
+// dV is accumulated, writing P^T / dS^T (bf16 pairs) back into TMEM over
+// score columns they have already read.  The gradient MMAs take their A
+// operand from there.  The next step's S^T and dP^T overwrite those columns;
+// they are issued after this step's gradient MMAs, and MMAs issued by one
+// thread execute in order.
 template <int HD>
 struct DkdvCfg {
-  static constexpr int kKeys = 128, kQ = 64;
+  static constexpr int kKeys = 128, kQ = 128;
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
-  // Q/dO ring depth: loads for step n+NQS-1 are in flight while step n runs.
-  // The ring recycles a slot only after the step's gradient MMAs, so its
-  // depth must cover load latency + score MMAs + elementwise + gradient MMAs.
-  static constexpr int kQStages = (HD == 128) ? 4 : 8;
+  static constexpr int kAtom = 128 * 128;              // one 64-column atom column of a 128-row tile
+  // Q/dO ring depth: a slot is recycled after the step's gradient MMAs.
+  static constexpr int kQStages = (HD == 128) ? 2 : 4;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKTile;
   static constexpr int kQOff = kVOff + kKTile;
   static constexpr int kDOOff = kQOff + kQStages * kQTile;
-  static constexpr int kLDOff = kDOOff + kQStages * kQTile;  // row-table tiles (float2 per query)
+  static constexpr int kLDOff = kDOOff + kQStages * kQTile;  // per stage: lse2[128], then D[128] (float)
   static constexpr int kBarOff = kLDOff + kQStages * kQ * 8;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
-  // TMEM: two score buffers of 128 columns (S^T at +0, dP^T at +64; P^T and
-  // dS^T, bf16 pairs, overwrite the first 32 columns of each once read), then
-  // the dK and dV accumulators.
-  static constexpr uint32_t kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "dK/dV kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DkdvBarriers {
   uint64_t kv_full, acc_done, drain;
-  uint64_t qdo_full[8], qdo_empty[8], s_full[2], p_full[2];
+  uint64_t qdo_full[4], qdo_empty[4];
+  uint64_t s_full, dp_full, p_full, ds_full;
   uint32_t tmem_base;
   int abort;
 };
+
+// TMEM column (relative to a score block) of the bf16 pairs of queries
+// 16*kk .. 16*kk+15: elementwise group w writes the 32 columns of its queries
+// 64w .. 64w+63 at 64w.
+__device__ __forceinline__ uint32_t pair_col(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
 
 template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDkdv, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ LD, int* __restrict__ status,
+                __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ LD, int* __restrict__ status,
                 Geometry g) {
   using Cfg = DkdvCfg<HD>;
   constexpr int NQS = Cfg::kQStages;
@@ -159,7 +171,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   uint8_t* sV = smem + Cfg::kVOff;
   uint8_t* sQ = smem + Cfg::kQOff;
   uint8_t* sDO = smem + Cfg::kDOOff;
-  float2* sLD = reinterpret_cast<float2*>(smem + Cfg::kLDOff);
+  float* sLD = reinterpret_cast<float*>(smem + Cfg::kLDOff);
   DkdvBarriers* bars = reinterpret_cast<DkdvBarriers*>(smem + Cfg::kBarOff);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -168,8 +180,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const int bk = g.B * g.NKV;
   const int j = (int)(blockIdx.x / bk);
   const int b = (blockIdx.x % bk) / g.NKV, kh = (blockIdx.x % bk) % g.NKV;
-  const int nq64 = (g.T + 63) / 64;
-  const int nq = nq64 - 2 * j;                  // 64-query tiles that can see key tile j
+  const int nq128 = (g.T + 127) / 128;
+  const int nq = nq128 - j;                     // 128-query tiles that can see key tile j
   const int n_steps = g.grp * nq;
   const int Tp = row_table_rows(g.T);
 
@@ -181,10 +193,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 4);
-    }
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->p_full), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -196,7 +208,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // Everything above overlapped the prologue's tail; its outputs (row dots,
+  // Everything above overlapped the prologue's tail; its outputs (row table,
   // rotated Q/K) are read below.  Once every CTA of this grid is past this
   // point the dQ kernel may start: it depends on the prologue only, which has
   // then completed.
@@ -209,20 +221,21 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per step: Q_i and dO_i (TMA) and the 64 row-table entries of the step's
-    // queries (one bulk copy; the table is padded to whole 64-row tiles with
-    // zeros, and padding query rows have zero Q and dO, so they add nothing).
+    // Per step: Q_i and dO_i (TMA, 128 rows) and the step's 128 row-table
+    // entries of each kind (two bulk copies; the table is padded to whole
+    // 128-row tiles with zeros, and padding query rows have zero Q and dO, so
+    // they add nothing).
     int issued = 0;
     if (lane == 0) {
       const uint32_t kvf = ptx::smem_u32(&bars->kv_full);
       ptx::mbar_arrive_expect_tx(kvf, 2 * Cfg::kKTile);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) {
-        ptx::tma_load_3d(ptx::smem_u32(sK + a * Cfg::kKeys * 128), &tm_k, g.C + kh * HD + 64 * a, j * 128, b, kvf);
-        ptx::tma_load_3d(ptx::smem_u32(sV + a * Cfg::kKeys * 128), &tm_v, g.C + g.NKV * HD + kh * HD + 64 * a,
-                         j * 128, b, kvf);
+        ptx::tma_load_3d(ptx::smem_u32(sK + a * Cfg::kAtom), &tm_k, g.C + kh * HD + 64 * a, j * 128, b, kvf);
+        ptx::tma_load_3d(ptx::smem_u32(sV + a * Cfg::kAtom), &tm_v, g.C + g.NKV * HD + kh * HD + 64 * a, j * 128, b,
+                         kvf);
       }
-      int h = kh * g.grp, qi = 2 * j;             // step n's query head and 64-query tile
+      int h = kh * g.grp, qi = j;                  // step n's query head and 128-query tile
       for (int n = 0; n < n_steps; ++n) {
         const int st = n % NQS, u = n / NQS;
         if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->qdo_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)) {
@@ -233,16 +246,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ptx::mbar_arrive_expect_tx(full, 2 * Cfg::kQTile + Cfg::kQ * 8);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a) {
-          ptx::tma_load_3d(ptx::smem_u32(sQ + st * Cfg::kQTile + a * Cfg::kQ * 128), &tm_q, h * HD + 64 * a,
-                           qi * 64, b, full);
-          ptx::tma_load_3d(ptx::smem_u32(sDO + st * Cfg::kQTile + a * Cfg::kQ * 128), &tm_do, h * HD + 64 * a,
-                           qi * 64, b, full);
+          ptx::tma_load_3d(ptx::smem_u32(sQ + st * Cfg::kQTile + a * Cfg::kAtom), &tm_q, h * HD + 64 * a, qi * 128, b,
+                           full);
+          ptx::tma_load_3d(ptx::smem_u32(sDO + st * Cfg::kQTile + a * Cfg::kAtom), &tm_do, h * HD + 64 * a, qi * 128,
+                           b, full);
         }
-        ptx::bulk_load(ptx::smem_u32(sLD + st * Cfg::kQ), LD + ((size_t)b * g.NH + h) * Tp + qi * 64, Cfg::kQ * 8,
-                       full);
+        const float* tab = LD + (size_t)(2 * (b * g.NH + h)) * Tp + qi * 128;
+        ptx::bulk_load(ptx::smem_u32(sLD + st * 256), tab, Cfg::kQ * 4, full);
+        ptx::bulk_load(ptx::smem_u32(sLD + st * 256 + 128), tab + Tp, Cfg::kQ * 4, full);
         issued = n + 1;
-        if (++qi == nq64) {
-          qi = 2 * j;
+        if (++qi == nq128) {
+          qi = j;
           ++h;
         }
       }
@@ -255,56 +269,54 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
       const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), 16, 1024);
       const uint64_t dQk = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
       const uint64_t dDOk = ptx::sw128_desc(ptx::smem_u32(sDO), 16, 1024);
-      const uint64_t dQm = ptx::sw128_desc(ptx::smem_u32(sQ), Cfg::kQ * 128, 1024);
-      const uint64_t dDOm = ptx::sw128_desc(ptx::smem_u32(sDO), Cfg::kQ * 128, 1024);
+      const uint64_t dQm = ptx::sw128_desc(ptx::smem_u32(sQ), Cfg::kAtom, 1024);
+      const uint64_t dDOm = ptx::sw128_desc(ptx::smem_u32(sDO), Cfg::kAtom, 1024);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
-
-      // Gradient MMAs of step m with A from TMEM: P^T and dS^T (bf16 pairs)
-      // sit in the first 32 columns of the step's S^T and dP^T halves.  The
-      // next score MMAs into the same buffer (step m+2) are issued after
-      // these, and MMAs issued by one thread execute in order.
-      auto issue_grad = [&](int m) -> bool {
-        const int st = m & 1, u = m >> 1, qs = m % NQS;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->p_full[st]), u & 1, abort_flag, kWaitLimitNs)) return false;
-        ptx::tc_fence_after();
-        const uint32_t ap = tmem + st * 128, ads = tmem + st * 128 + 64;
-        const uint64_t bdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile), bq = ptx::desc_advance(dQm, qs * Cfg::kQTile);
-#pragma unroll
-        for (int kk = 0; kk < Cfg::kQ / 16; ++kk) {
-          const uint32_t acc = (m > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDV, ap + kk * 8, ptx::desc_advance(bdo, kk * 2048), idesc_g, acc);
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDK, ads + kk * 8, ptx::desc_advance(bq, kk * 2048), idesc_g, acc);
-        }
-        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
-        return true;
-      };
-
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, qs = n % NQS;
-        // TMEM buffer st was last read by step n-2's elementwise group before
-        // it arrived on p_full(n-2), which issue_grad(n-2) already observed.
+        const int qs = n % NQS;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
         const uint64_t bq = ptx::desc_advance(dQk, qs * Cfg::kQTile), bdo = ptx::desc_advance(dDOk, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t ok_ = (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
-          const uint32_t oq = (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dK, ok_), ptx::desc_advance(bq, oq), idesc_s, kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_dp, ptx::desc_advance(dV, ok_), ptx::desc_advance(bdo, oq), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemS, ptx::desc_advance(dK, off), ptx::desc_advance(bq, off), idesc_s,
+                           kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
-        if (n >= 1) ok = issue_grad(n - 1);
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDP, ptx::desc_advance(dV, off), ptx::desc_advance(bdo, off), idesc_s,
+                           kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+        // dV += P^T dO once both groups wrote P^T.
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint64_t gdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile), gq = ptx::desc_advance(dQm, qs * Cfg::kQTile);
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk), ptx::desc_advance(gdo, kk * 2048),
+                           idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q once both groups wrote dS^T.
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), n & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(gq, kk * 2048),
+                           idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
       }
-      if (ok) ok = issue_grad(n_steps - 1);
       if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
       if (!ok) fail();
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
@@ -312,69 +324,96 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int wg = (warp - 2) >> 2;                // this group takes steps n = wg, wg+2, ...
+    // Group wg owns queries 64*wg .. 64*wg+63 of every step (TMEM columns
+    // 64*wg .. of each score block); thread = key row = TMEM lane.
+    const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;           // key row within the tile
     const int ks = j * 128 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t t_s = t_lane + Cfg::kTmemS + 64 * wg, t_dp = t_lane + Cfg::kTmemDP + 64 * wg;
     const float sl2 = g.scale * kLog2e;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
-    for (int n = wg; n < n_steps; n += 2) {
-      const int st = wg, u = n >> 1;
-      const int qi = 2 * j + n % nq;
-      // s_full(n) is committed after the MMAs of step n-2 were issued, so it
-      // also means those MMAs no longer read P/dS buffer st.
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
+    for (int n = 0; n < n_steps; ++n) {
+      const int qi = j + n % nq;
+      const bool diag = qi == j;                   // query tile == key tile: query q is before key row iff q < row
+      const int q0 = 64 * wg;                      // first query (within the tile) of this group
+      // This group's row-table entries: -lse * log2(e) and -D of its 64 queries.
+      const float4* lse4 = reinterpret_cast<const float4*>(sLD + (n % NQS) * 256 + q0);
+      const float4* d4 = reinterpret_cast<const float4*>(sLD + (n % NQS) * 256 + 128 + q0);
+      // ---- P^T = exp2(S^T * scale * log2(e) - lse * log2(e)), while dP^T is computed.
+      float p[64];
+      float4 Lw[2];
+      // s_full(n) also means the step's loads (table included) have landed:
+      // the issuer waited for them before the score MMAs.
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
-      const bool diag = qi <= 2 * j + 1;           // this query tile overlaps the key tile
-      const int qk = qi * 64 - ks;                 // query column c is before this key iff c + qk < 0
-      // Row-table pairs of two consecutive queries: (-lse2_c, -D_c, -lse2_c+1, -D_c+1).
-      // Every thread reads all 32 pairs of the step (broadcast loads); they are
-      // fetched four pairs ahead of their use, the first four before the TMEM
-      // loads complete, so that their latency overlaps the math instead of
-      // stalling each column pair.
-      const float4* ld4 = reinterpret_cast<const float4*>(sLD + (n % NQS) * Cfg::kQ);
-      const float2 sl2x2 = make_float2(sl2, sl2);
-      float4 Lw[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) Lw[k] = ld4[k];
-      // Two halves of 32 query columns (all 64 at once would spill registers
-      // in this 10-warp kernel).
+      Lw[0] = lse4[0];
+      Lw[1] = lse4[1];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32], pw[16], dw[16];
-        ptx::tmem_ld32(t_lane + st * 128 + 32 * half, sr);
-        ptx::tmem_ld32(t_lane + st * 128 + 64 + 32 * half, dr);
+        uint32_t sr[32], pw[16];
+        ptx::tmem_ld32(t_s + 32 * half, sr);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int q = 32 * half + c, k = q >> 1;
-          const float4 L = Lw[k & 3];
-          if (k + 4 < 32) Lw[k & 3] = ld4[k + 4];
-          // p = 2^(s * scale * log2(e) - lse * log2(e)); dS = p * (dP - D)
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
-                                      make_float2(L.x, L.z));
-          float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
-          if (diag) {                              // query before key: masked
-            if (q + qk < 0) p0 = 0.f;
-            if (q + 1 + qk < 0) p1 = 0.f;
+        for (int c = 0; c < 32; c += 4) {
+          const int k = (32 * half + c) >> 2;       // float4 index 0..15
+          const float4 L = Lw[k & 1];
+          if (k + 2 < 16) Lw[k & 1] = lse4[k + 2];
+          const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2,
+                                       make_float2(L.x, L.y));
+          const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2x2,
+                                       make_float2(L.z, L.w));
+          float e[4] = {ptx::ex2_approx(x0.x), ptx::ex2_approx(x0.y), ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y)};
+          if (diag) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (q0 + 32 * half + c + t < row) e[t] = 0.f;
           }
-          const float2 ds = __fmul2_rn(make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(dr[c]),
-                                                                                   __uint_as_float(dr[c + 1])),
-                                                                       make_float2(L.y, L.w)));
-          pw[c >> 1] = pack_bf16x2(p0, p1);
-          dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) p[32 * half + c + t] = e[t];
+          pw[c >> 1] = pack_bf16x2(e[0], e[1]);
+          pw[(c >> 1) + 1] = pack_bf16x2(e[2], e[3]);
         }
-        // P^T and dS^T of these 32 queries over the S^T / dP^T columns this
-        // thread has already read.
-        ptx::tmem_st16(t_lane + st * 128 + 16 * half, pw);
-        ptx::tmem_st16(t_lane + st * 128 + 64 + 16 * half, dw);
+        ptx::tmem_st16(t_s + 16 * half, pw);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[st]));
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full));
+      // ---- dS^T = P^T * (dP^T - D), while dV is accumulated.
+      Lw[0] = d4[0];
+      Lw[1] = d4[1];
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), n & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dr[32], dw[16];
+        ptx::tmem_ld32(t_dp + 32 * half, dr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const int k = (32 * half + c) >> 2;
+          const float4 L = Lw[k & 1];
+          if (k + 2 < 16) Lw[k & 1] = d4[k + 2];
+          const float2 a0 = __fmul2_rn(make_float2(p[32 * half + c], p[32 * half + c + 1]),
+                                       __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                                                  make_float2(L.x, L.y)));
+          const float2 a1 = __fmul2_rn(make_float2(p[32 * half + c + 2], p[32 * half + c + 3]),
+                                       __fadd2_rn(make_float2(__uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3])),
+                                                  make_float2(L.z, L.w)));
+          dw[c >> 1] = pack_bf16x2(a0.x, a0.y);
+          dw[(c >> 1) + 1] = pack_bf16x2(a1.x, a1.y);
+        }
+        ptx::tmem_st16(t_dp + 16 * half, dw);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
     }
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
     if (ok) {
@@ -433,7 +472,7 @@ template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDq, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-              __nv_bfloat16* __restrict__ dqkv, const float2* __restrict__ LD, int* __restrict__ status,
+              __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ LD, int* __restrict__ status,
               Geometry g) {
   using Cfg = DqCfg<HD>;
   constexpr int NKS = Cfg::kKStages;
@@ -599,8 +638,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float sl2 = g.scale * kLog2e;
     // This row's table entry (-lse * log2(e), -D); padding rows have zero Q
     // and dO, hence dP = 0 and dS = 0.
-    const float2 ldr =
-        (tq < g.T) ? LD[((size_t)b * g.NH + h) * row_table_rows(g.T) + tq] : make_float2(0.f, 0.f);
+    const int Tp = row_table_rows(g.T);
+    const float2 ldr = (tq < g.T) ? make_float2(LD[(size_t)(2 * (b * g.NH + h)) * Tp + tq],
+                                                LD[(size_t)(2 * (b * g.NH + h) + 1) * Tp + tq])
+                                  : make_float2(0.f, 0.f);
     const float2 nl2 = make_float2(ldr.x, ldr.x), nd2 = make_float2(ldr.y, ldr.y);
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
@@ -682,7 +723,7 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
   prof_begin(kKernelBwdDkdvTc05, stream);
   e = launch_pdl(k1, dim3(grid1), dim3(kThreadsDkdv), DkdvCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_v[1],
-                 a.tm_qk[0], a.tm_do[0], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
+                 a.tm_qk[1], a.tm_do[1], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDkdvTc05, stream);
   if (e != cudaSuccess) return e;
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);

@@ -53,13 +53,14 @@ cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Ge
 // head h at column h*hd and kv head kh at C + kh*hd (the columns they have
 // in qkv).  hd must be a multiple of 16.
 cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream);
-// Rows of the per-(b, h) row table the bf16 backward reads: T rounded up to
-// whole 64-row query tiles.
-__host__ __device__ inline int row_table_rows(int T) { return (T + 63) / 64 * 64; }
-// bf16 (hd a multiple of 16): the row table LD[(b*NH + h)*Tp + t] =
-// (-lse * log2(e), -D) with D = dO . O (zeros for t >= T) and, when RoPE is
-// on, the rotated Q/K copy, in one launch.
-cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, const void* dout, const float* lse,
+// Rows of each per-(b, h) row table the bf16 backward reads: T rounded up to
+// whole 128-row query tiles.
+__host__ __device__ inline int row_table_rows(int T) { return (T + 127) / 128 * 128; }
+// bf16 (hd a multiple of 16): the row tables, two float arrays of Tp rows per
+// (b, h): LD[(2*(b*NH + h))*Tp + t] = -lse * log2(e) and
+// LD[(2*(b*NH + h) + 1)*Tp + t] = -D with D = dO . O (zeros for t >= T); and,
+// when RoPE is on, the rotated Q/K copy; in one launch.
+cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, const void* dout, const float* lse,
                                      const void* qkv, const Geometry& g, cudaStream_t stream);
 
 // ------------------------------------------------------------ tcgen05 bf16 path
@@ -90,7 +91,7 @@ struct Tc05BwdArgs {
   CUtensorMap tm_v[2];   // over qkv
   CUtensorMap tm_do[2];  // over dout
   void* dqkv;            // [B,T,W] bf16
-  const float2* LD;      // row table [B,NH,Tp]: (-lse * log2(e), -D), see launch_bwd_prologue_bf16
+  const float* LD;       // row tables: -lse * log2(e) and -D per (b, h), see launch_bwd_prologue_bf16
   int* status;
   int num_sms;           // persistent grid size
 };

@@ -130,9 +130,9 @@ __global__ void __launch_bounds__(512) rope_qk_bf16_kernel(__nv_bfloat16* __rest
 // (b, t), (b, t+1) of the flattened B*T rows; for each pair:
 //  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout of both
 //    rows; the hd/8 lanes of a head sum their partials with shuffles and one
-//    of them writes the row-table entry LD[b,h,t] = (-lse[b,h,t] * log2(e),
-//    -D[b,h,t]) with D = dO . O: the two per-row values the backward's
-//    elementwise steps use, side by side, already in the form they enter the
+//    of them writes the row-table entries -lse[b,h,t] * log2(e) and -D[b,h,t]
+//    with D = dO . O (two tables per (b, h)): the two per-row values the
+//    backward's elementwise steps use, already in the form they enter the
 //    exponent and the dS difference;
 //  * (RoPE only) threads 0..(NH+NKV)*hd/16-1 each rotate 8 NEOX pairs of one
 //    Q or K head of both rows into the workspace copy.
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(512) rope_qk_bf16_kernel(__nv_bfloat16* __rest
 // Afterwards the table rows T..Tp-1 of every (b, h) are cleared, so that whole
 // 64-row tiles of the table can be copied.  All index arithmetic is 32-bit
 // with shifts: hd/8 and hd/16 are powers of two.
-__global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float2* __restrict__ LD, const uint4* __restrict__ out,
+__global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float* __restrict__ LD, const uint4* __restrict__ out,
                                                                  const uint4* __restrict__ dout,
                                                                  const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float2* __res
           const int row = row0 + r;
           const int b = row / g.T, t = row - b * g.T;
           const int bh = b * g.NH + (c >> vph_log2);
-          LD[(size_t)bh * Tp + t] = make_float2(-lse[(size_t)bh * g.T + t] * 1.4426950408889634f, -acc);
+          LD[(size_t)(2 * bh) * Tp + t] = -lse[(size_t)bh * g.T + t] * 1.4426950408889634f;
+          LD[(size_t)(2 * bh + 1) * Tp + t] = -acc;
         }
       }
     }
@@ -226,17 +227,17 @@ __global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float2* __res
       }
     }
   }
-  // Table padding rows T..Tp-1 of every (b, h).
-  const int pad = Tp - g.T, n_pad = g.B * g.NH * pad;
+  // Table padding rows T..Tp-1 of both tables of every (b, h).
+  const int pad = Tp - g.T, n_pad = 2 * g.B * g.NH * pad;
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n_pad; k += gridDim.x * blockDim.x) {
-    const int bh = k / pad;
-    LD[(size_t)bh * Tp + g.T + (k - bh * pad)] = make_float2(0.f, 0.f);
+    const int tab = k / pad;
+    LD[(size_t)tab * Tp + g.T + (k - tab * pad)] = 0.f;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_prologue_bf16(float2* LD, void* rot, const void* out, const void* dout, const float* lse,
+cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, const void* dout, const float* lse,
                                      const void* qkv, const Geometry& g, cudaStream_t stream) {
   const int vph = g.hd / 8;  // 8 or 16
   int vph_log2 = 0;
