@@ -118,13 +118,10 @@ __device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope,
 // One step = 128 queries of one query head of the group, so that every MMA
 // has N = 128 (full tensor-core rate; N = 64 runs at about two thirds).  TMEM:
 // S^T [0, 128), dP^T [128, 256), dK and dV accumulators from column 256.  The
-// step's four MMA groups run in order S^T, dP^T, dV, dK; the elementwise
-// groups turn S^T into P^T while dP^T is computed, and dP^T into dS^T while
-// dV is accumulated, writing P^T / dS^T (bf16 pairs) back into TMEM over
-// score columns they have already read.  The gradient MMAs take their A
-// operand from there.  The next step's S^T and dP^T overwrite those columns;
-// they are issued after this step's gradient MMAs, and MMAs issued by one
-// thread execute in order.
+// elementwise groups write P^T / dS^T (bf16 pairs) back into TMEM over score
+// columns they have already read, and the gradient MMAs take their A operand
+// from there; the MMA issue order (see the issuer) keeps the tensor core busy
+// with the previous step's dK while P^T is formed.
 template <int HD>
 struct DkdvCfg {
   static constexpr int kKeys = 128, kQ = 128;
@@ -278,6 +275,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       const uint64_t dQm = ptx::sw128_desc(ptx::smem_u32(sQ), Cfg::kAtom, 1024);
       const uint64_t dDOm = ptx::sw128_desc(ptx::smem_u32(sDO), Cfg::kAtom, 1024);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
+      // dK += dS^T Q of step m once both groups wrote dS^T(m); frees the
+      // step's ring slot.
+      auto issue_dk = [&](int m) -> bool {
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), m & 1, abort_flag, kWaitLimitNs)) return false;
+        ptx::tc_fence_after();
+        const int ms = m % NQS;
+        const uint64_t gq = ptx::desc_advance(dQm, ms * Cfg::kQTile);
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(gq, kk * 2048),
+                           idesc_g, (m > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[ms]));
+        return true;
+      };
+      // Issue order S^T(n), dK(n-1), dP^T(n), dV(n): the tensor core works on
+      // dK(n-1) and dP^T(n) while the elementwise groups turn S^T(n) into
+      // P^T(n), and on dV(n) and S^T(n+1) while they form dS^T(n).  dP^T(n)
+      // overwrites dS^T(n-1) after dK(n-1) has been issued, S^T(n+1)
+      // overwrites P^T(n) after dV(n): MMAs from one thread run in order.
       for (int n = 0; n < n_steps && ok; ++n) {
         const int qs = n % NQS;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
@@ -291,6 +307,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                            kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+        if (n > 0 && !(ok = issue_dk(n - 1))) break;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
@@ -302,21 +319,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint64_t gdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile), gq = ptx::desc_advance(dQm, qs * Cfg::kQTile);
+        const uint64_t gdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
           ptx::mma_bf16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk), ptx::desc_advance(gdo, kk * 2048),
                            idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q once both groups wrote dS^T.
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), n & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(gq, kk * 2048),
-                           idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[qs]));
       }
+      if (ok && n_steps > 0) ok = issue_dk(n_steps - 1);
       if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
       if (!ok) fail();
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
