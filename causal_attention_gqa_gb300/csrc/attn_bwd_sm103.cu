@@ -19,19 +19,14 @@
 //    score columns already read, then dV += P^T dO and dK += dS^T Q (A
 //    operand from TMEM) accumulate in TMEM.
 //  * dq:   one CTA per (128-query tile i, query head, batch row).  Q_i and dO_i
-//    stay in shared memory; the CTA walks the 64-key tiles 0..2i+1.  Per step:
-//    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into shared memory, then
-//    dQ += dS K accumulates in TMEM.
-// Warp roles in both: warp 0 TMA producer; warp 1 TMEM owner and MMA issuer;
-// two elementwise warpgroups with one TMEM lane (one key or query row) per
-// thread, which also split the epilogue.  In the dK/dV kernel they take
-// alternate steps; in the dQ kernel each takes half of every step's 64
-// columns.  Score results are double-buffered in TMEM, so two steps are in
-// flight at once.  In the dQ kernel warp 1
-// issues only the score MMAs (S, dP) and warp 10 the dQ MMAs, so the two
-// streams feed the tensor core independently (measured faster there; in the
-// dK/dV kernel one issuer that alternates score and gradient groups measured
-// faster).  All waits are bounded.
+//    stay in shared memory; the CTA walks the 128-key tiles 0..i.  Per step:
+//    S = Q K^T and dP = dO V^T into TMEM, dS (bf16) back into TMEM over the
+//    dP columns already read, then dQ += dS K (A operand from TMEM)
+//    accumulates in TMEM.
+// Warp roles in both: warp 0 TMA producer; warp 1 TMEM owner and the single
+// MMA issuer; two elementwise warpgroups with one TMEM lane (one key or query
+// row) per thread, each owning half of every step's 128 columns, which also
+// split the epilogue.  Every MMA has N = 128.  All waits are bounded.
 #include "attn_common.cuh"
 #include "attn_kernels.h"
 #include "attn_profile.h"
@@ -42,20 +37,8 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kThreadsDkdv = 320;   // producer, MMA issuer, two elementwise warpgroups
-constexpr int kThreadsDq = 352;     // + a separate dQ-MMA issuer warp
-constexpr int kGradWarp = 10;
+constexpr int kThreadsDq = 320;     // producer, MMA issuer, two elementwise warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
-
-// Store 16 packed words (32 bf16) at columns 32*half .. 32*half+31 of row
-// `row` of a 64-column swizzled tile.
-__device__ __forceinline__ void store_row_half(uint8_t* tile, int row, int half, const uint32_t (&w)[16]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int ch = half * 4 + q;
-    *reinterpret_cast<uint4*>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) =
-        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-  }
-}
 
 __device__ __forceinline__ uint4 pack8(const uint32_t* f, float s) {
   return make_uint4(pack_bf16x2(__uint_as_float(f[0]) * s, __uint_as_float(f[1]) * s),
@@ -449,30 +432,34 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // ===========================================================================
 // dQ kernel
 // ===========================================================================
+// One CTA per (128-query tile, query head, batch row); Q_i and dO_i stay in
+// shared memory and the CTA walks the 128-key tiles 0..i (every MMA N = 128).
+// TMEM: S [0, 128), dP [128, 256), dQ accumulator from 256.  The elementwise
+// groups turn S into P (kept in registers) while dP is computed, then dP into
+// dS, written (bf16 pairs) into TMEM over the dP columns they have read; the
+// dQ MMA takes its A operand from there.  Issue order S(n), dQ(n-1), dP(n):
+// the tensor core works on dQ(n-1) and dP(n) while P(n) is formed.
 template <int HD>
 struct DqCfg {
-  static constexpr int kQ = 128, kKeys = 64;
+  static constexpr int kQ = 128, kKeys = 128;
   static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
-  static constexpr int kSTile = kQ * kKeys * 2;        // dS (one atom column)
-  static constexpr int kKStages = 4;                   // K/V ring depth
+  static constexpr int kAtom = 128 * 128;              // one 64-column atom column of a 128-row tile
+  static constexpr int kKStages = (HD == 128) ? 2 : 4; // K ring and V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kQOff + kQTile;
   static constexpr int kKOff = kDOOff + kQTile;
   static constexpr int kVOff = kKOff + kKStages * kKTile;
-  static constexpr int kDSOff = kVOff + kKStages * kKTile;
-  static constexpr int kBarOff = kDSOff + 2 * kSTile;
-  // At least 116 KB so that two CTAs never share an SM: each allocates all
-  // 512 TMEM columns, and a second resident CTA would only wait for them.
-  static constexpr int kSmemBytes = (kBarOff + 256 + 1024) > 116 * 1024 ? (kBarOff + 256 + 1024) : 116 * 1024;
-  static constexpr uint32_t kTmemDQ = 256, kTmemCols = 512;
+  static constexpr int kBarOff = kVOff + kKStages * kKTile;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256, kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "dQ kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DqBarriers {
   uint64_t q_full, acc_done, drain;
-  uint64_t drain2;
-  uint64_t kv_full[4], kv_empty[4], s_full[2], s_free[2], ds_full[2], ds_free[2];
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full, s_free, dp_full, ds_full;
   uint32_t tmem_base;
   int abort;
 };
@@ -491,7 +478,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* sDO = smem + Cfg::kDOOff;
   uint8_t* sK = smem + Cfg::kKOff;
   uint8_t* sV = smem + Cfg::kVOff;
-  uint8_t* sDS = smem + Cfg::kDSOff;
   DqBarriers* bars = reinterpret_cast<DqBarriers*>(smem + Cfg::kBarOff);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -502,24 +488,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int qt = n_qt - 1 - (int)(blockIdx.x / bh_count);
   const int b = (blockIdx.x % bh_count) / g.NH, h = (blockIdx.x % bh_count) % g.NH;
   const int kh = h / g.grp;
-  const int nk64 = (g.T + 63) / 64;
-  const int n_steps = min(2 * qt + 2, nk64);
+  const int n_steps = qt + 1;                    // 128-key tiles 0..qt
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
     for (int i = 0; i < NKS; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->s_free[i]), 8);
-      ptx::mbar_init(ptx::smem_u32(&bars->ds_full[i]), 8);
-      ptx::mbar_init(ptx::smem_u32(&bars->ds_free[i]), 1);
-    }
-    ptx::mbar_init(ptx::smem_u32(&bars->drain2), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_free), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -547,106 +531,113 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_arrive_expect_tx(qf, 2 * Cfg::kQTile);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) {
-        ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kQ * 128), &tm_q, h * HD + 64 * a, qt * 128, b, qf);
-        ptx::tma_load_3d(ptx::smem_u32(sDO + a * Cfg::kQ * 128), &tm_do, h * HD + 64 * a, qt * 128, b, qf);
+        ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kAtom), &tm_q, h * HD + 64 * a, qt * 128, b, qf);
+        ptx::tma_load_3d(ptx::smem_u32(sDO + a * Cfg::kAtom), &tm_do, h * HD + 64 * a, qt * 128, b, qf);
       }
-      int issued = 0;
-      for (int n = 0; n < n_steps; ++n) {
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % NKS, u = n / NKS;
-        if (u > 0 && !ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)) {
-          fail();
+        if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)))
           break;
-        }
-        const uint32_t kf = ptx::smem_u32(&bars->kv_full[st]);
-        ptx::mbar_arrive_expect_tx(kf, 2 * Cfg::kKTile);
+        const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
+        ptx::mbar_arrive_expect_tx(kf, Cfg::kKTile);
 #pragma unroll
-        for (int a = 0; a < HD / 64; ++a) {
-          ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kKTile + a * Cfg::kKeys * 128), &tm_k, g.C + kh * HD + 64 * a,
-                           n * 64, b, kf);
-          ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kKTile + a * Cfg::kKeys * 128), &tm_v,
-                           g.C + g.NKV * HD + kh * HD + 64 * a, n * 64, b, kf);
-        }
-        issued = n + 1;
+        for (int a = 0; a < HD / 64; ++a)
+          ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kKTile + a * Cfg::kAtom), &tm_k, g.C + kh * HD + 64 * a,
+                           n * 128, b, kf);
+        k_issued = n + 1;
+        if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)))
+          break;
+        const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
+        ptx::mbar_arrive_expect_tx(vf, Cfg::kKTile);
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a)
+          ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kKTile + a * Cfg::kAtom), &tm_v,
+                           g.C + g.NKV * HD + kh * HD + 64 * a, n * 128, b, vf);
+        v_issued = n + 1;
       }
+      if (!ok) fail();
       if (*abort_flag) {
         ptx::mbar_wait(qf, 0, nullptr, kWaitLimitNs);
-        for (int st = 0; st < NKS && st < issued; ++st)
-          ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
+        for (int st = 0; st < NKS && st < k_issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
+        for (int st = 0; st < NKS && st < v_issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ S / dP issuer
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
       const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
       const uint64_t dDO = ptx::sw128_desc(ptx::smem_u32(sDO), 16, 1024);
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
       const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), 16, 1024);
+      const uint64_t dKm = ptx::sw128_desc(ptx::smem_u32(sK), Cfg::kAtom, 1024);
       bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
-      for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1, u = n >> 1, ks = n % NKS;
-        // K_n/V_n landed; TMEM buffer st read out by step n-2's elementwise group.
-        const uint32_t kf = ptx::smem_u32(&bars->kv_full[ks]), sf = ptx::smem_u32(&bars->s_free[st]);
-        if (!(ptx::mbar_ready(kf, (n / NKS) & 1) & (n < 2 ? 1u : ptx::mbar_ready(sf, (u - 1) & 1)))) {
-          ok = ptx::mbar_wait(kf, (n / NKS) & 1, abort_flag, kWaitLimitNs);
-          if (ok && n >= 2) ok = ptx::mbar_wait(sf, (u - 1) & 1, abort_flag, kWaitLimitNs);
-          if (!ok) break;
-        }
+      // dQ += dS K of step m once both groups wrote dS(m); frees K_m.
+      auto issue_dq = [&](int m) -> bool {
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), m & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        const uint32_t d_s = tmem + st * 128, d_dp = tmem + st * 128 + 64;
+        const int ms = m % NKS;
+        const uint64_t bk = ptx::desc_advance(dKm, ms * Cfg::kKTile);
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kKeys / 16; ++kk)
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDQ, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(bk, kk * 2048),
+                           idesc_g, (m > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ms]));
+        return true;
+      };
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int ks = n % NKS, u = n / NKS;
+        // K_n landed; the groups have read S(n-1) out of TMEM.
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), u & 1, abort_flag, kWaitLimitNs);
+        if (ok && n > 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free), (n - 1) & 1, abort_flag, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
         const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, ks * Cfg::kKTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t oq = (kk >> 2) * Cfg::kQ * 128 + (kk & 3) * 32;
-          const uint32_t ok_ = (kk >> 2) * Cfg::kKeys * 128 + (kk & 3) * 32;
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQ, oq), ptx::desc_advance(bk, ok_), idesc_s, kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_dp, ptx::desc_advance(dDO, oq), ptx::desc_advance(bv, ok_), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemS, ptx::desc_advance(dQ, off), ptx::desc_advance(bk, off), idesc_s,
+                           kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+        // dQ(n-1) reads dS(n-1) in the dP columns: issued before dP(n)
+        // overwrites them (MMAs from one thread run in order).
+        if (n > 0 && !(ok = issue_dq(n - 1))) break;
+        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[ks]), u & 1, abort_flag, kWaitLimitNs))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
+          ptx::mma_bf16_ss(tmem + Cfg::kTmemDP, ptx::desc_advance(dDO, off), ptx::desc_advance(bv, off), idesc_s,
+                           kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[ks]));
       }
+      if (ok && n_steps > 0) ok = issue_dq(n_steps - 1);
+      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
       if (!ok) fail();
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
-  } else if (warp == kGradWarp) {
-    // ------------------------------------------------------------ dQ issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
-      const uint64_t dKm = ptx::sw128_desc(ptx::smem_u32(sK), Cfg::kKeys * 128, 1024);
-      const uint64_t dDS = ptx::sw128_desc(ptx::smem_u32(sDS), 16, 1024);
-      bool ok = true;
-      for (int m = 0; m < n_steps && ok; ++m) {
-        const int st = m & 1, u = m >> 1, ks = m % NKS;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full[st]), u & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint64_t a_ds = ptx::desc_advance(dDS, st * Cfg::kSTile), bk = ptx::desc_advance(dKm, ks * Cfg::kKTile);
-#pragma unroll
-        for (int kk = 0; kk < Cfg::kKeys / 16; ++kk) {
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDQ, ptx::desc_advance(a_ds, kk * 32), ptx::desc_advance(bk, kk * 2048),
-                           idesc_g, (m > 0 || kk > 0) ? 1u : 0u);
-        }
-        // S_m and dP_m finished before ds_full(m), so K_m/V_m are free after this.
-        ptx::mma_commit(ptx::smem_u32(&bars->ds_free[st]));
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[ks]));
-      }
-      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
-      if (!ok) fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain2));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain2), 0, nullptr, kWaitLimitNs);
-    }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    // Both groups work on every step, group wg on key columns 32*wg ..
-    // 32*wg+31 (half the per-step latency of one group doing all 64).
+    // Group wg owns keys 64*wg .. 64*wg+63 of every step (TMEM columns 64*wg
+    // .. of each score block); thread = query row = TMEM lane.
     const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;           // query row within the tile
     const int tq = qt * 128 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t t_s = t_lane + Cfg::kTmemS + 64 * wg, t_dp = t_lane + Cfg::kTmemDP + 64 * wg;
     const float sl2 = g.scale * kLog2e;
-    // This row's table entry (-lse * log2(e), -D); padding rows have zero Q
-    // and dO, hence dP = 0 and dS = 0.
+    // This row's table entries -lse * log2(e) and -D; padding rows have zero
+    // Q and dO, hence dP = 0 and dS = 0.
     const int Tp = row_table_rows(g.T);
     const float2 ldr = (tq < g.T) ? make_float2(LD[(size_t)(2 * (b * g.NH + h)) * Tp + tq],
                                                 LD[(size_t)(2 * (b * g.NH + h) + 1) * Tp + tq])
@@ -655,46 +646,55 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
-      const int st = n & 1, u = n >> 1;
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[st]), u & 1, abort_flag, kWaitLimitNs));
+      const bool diag = n == qt;                   // key tile == query tile: key k is after row iff k > row
+      const int k0 = 64 * wg;                      // first key (within the tile) of this group
+      // ---- P = exp2(S * scale * log2(e) - lse * log2(e)), while dP is computed.
+      float p[64];
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
-      uint32_t sr[32], dr[32];
-      ptx::tmem_ld32(t_lane + st * 128 + 32 * wg, sr);
-      ptx::tmem_ld32(t_lane + st * 128 + 64 + 32 * wg, dr);
-      ptx::tmem_wait_ld();
-      // This group's S and dP columns are in registers: release them.
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free[st]));
-      // Non-blocking check, consumed after the math: the dQ MMAs of step n-2
-      // are done with dS buffer st.
-      const uint32_t dsfree_now = n < 2 ? 1u : ptx::mbar_test(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1);
-      const bool diag = n >= 2 * qt;               // key tile overlaps the query tile
-      const int kq = n * 64 + 32 * wg - tq;        // key column c is after this query iff c + kq > 0
-      uint32_t dw[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl2);
-        float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
-        if (diag) {                                // key after query: masked
-          if (c + kq > 0) p0 = 0.f;
-          if (c + 1 + kq > 0) p1 = 0.f;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[32];
+        ptx::tmem_ld32(t_s + 32 * half, sr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl2);
+          float e0 = ptx::ex2_approx(x.x), e1 = ptx::ex2_approx(x.y);
+          if (diag) {
+            if (k0 + 32 * half + c > row) e0 = 0.f;
+            if (k0 + 32 * half + c + 1 > row) e1 = 0.f;
+          }
+          p[32 * half + c] = e0;
+          p[32 * half + c + 1] = e1;
         }
-        const float2 ds = __fmul2_rn(
-            make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd2));
-        dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
       }
-      if (!__all_sync(0xffffffffu, dsfree_now)) {
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->ds_free[st]), (u - 1) & 1, abort_flag,
-                                                      kWaitLimitNs));
-        if (!ok) break;
-      }
-      store_row_half(sDS + st * Cfg::kSTile, row, wg, dw);
-      ptx::fence_proxy_async_smem();
+      // S is in registers: the next score MMA may overwrite it.
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full[st]));
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free));
+      // ---- dS = P * (dP - D), while dQ(n-1) is accumulated.
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), n & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dr[32], dw[16];
+        ptx::tmem_ld32(t_dp + 32 * half, dr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 ds = __fmul2_rn(make_float2(p[32 * half + c], p[32 * half + c + 1]),
+                                       __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd2));
+          dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
+        }
+        ptx::tmem_st16(t_dp + 16 * half, dw);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
     }
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
     if (ok) {
@@ -738,7 +738,7 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
   prof_begin(kKernelBwdDqTc05, stream);
   e = launch_pdl(k2, dim3(grid2), dim3(kThreadsDq), DqCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_do[1],
-                 a.tm_qk[0], a.tm_v[0], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
+                 a.tm_qk[1], a.tm_v[1], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
   return e;
 }
