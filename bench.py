@@ -2,8 +2,9 @@
 """Causal MHA/GQA attention forward + backward throughput on GB300.
 
 One step = attn_fwd_ws (the forward with its RoPE pass over Q/K into a
-workspace) + attn_bwd (with its prologue kernel) over one batch of the
-synthetic workload, through the library's C ABI.  Prints ONE JSON line.
+workspace) + attn_bwd_rot (the backward with its prologue kernel, reading the
+forward's rotated Q/K) over one batch of the synthetic workload, through the
+library's C ABI.  Prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload gqa_block|long_context_gqa|gpt2_124m_mha]
@@ -252,7 +253,8 @@ def run_ours(args, w):
 
     def step():
         binding.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, fws, fws_bytes, sptr)
-        binding.attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, w.rope_theta, code, ws, ws_bytes, sptr)
+        binding.attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, w.rope_theta, code, fws, ws, ws_bytes,
+                             sptr)
 
     def barrier():
         if world > 1:

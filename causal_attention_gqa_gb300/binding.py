@@ -13,6 +13,8 @@ The entry points keep the C names and argument order:
     attn_bwd_workspace_bytes(B, T, C, NH, NKV, dtype)
     attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
              workspace, workspace_bytes, stream=None)
+    attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
+                 qk_rot, workspace, workspace_bytes, stream=None)
 
 Tensor arguments may be torch tensors (their data pointers are passed) or
 raw integer addresses.  ``stream`` defaults to PyTorch's current stream.
@@ -70,6 +72,8 @@ def load() -> ctypes.CDLL:
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     lib.attn_bwd.restype = i
+    lib.attn_bwd_rot.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, sz, vp]
+    lib.attn_bwd_rot.restype = i
     lib.attn_strerror.argtypes = [i]
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_device_status.argtypes = [ctypes.POINTER(i), i]
@@ -151,6 +155,15 @@ def attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, wor
     _check(st, "attn_bwd")
 
 
+def attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, qk_rot, workspace, workspace_bytes,
+                 stream=None) -> None:
+    """attn_bwd reading the RoPE-rotated Q/K from the forward's attn_fwd_ws workspace `qk_rot`."""
+    st = load().attn_bwd_rot(_ptr(dqkv), _ptr(qkv), _ptr(out), _ptr(dout), _ptr(lse), B, T, C, NH, NKV,
+                             float(rope_theta), int(dtype), _ptr(qk_rot), _ptr(workspace), int(workspace_bytes),
+                             _stream(stream))
+    _check(st, "attn_bwd_rot")
+
+
 def attn_bwd_noalloc(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, stream=None) -> None:
     """attn_bwd without a workspace argument, for callers that cannot allocate
     device memory; uses the library's built-in scratch buffer (see the header
@@ -221,9 +234,24 @@ def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=
     return out, lse
 
 
+def forward_ws(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None):
+    """(out, lse, workspace) through attn_fwd_ws; the workspace holds the
+    rotated Q/K that backward(..., qk_rot=workspace) can reuse."""
+    import torch
+    B, T, W = qkv.shape
+    hd = W // (NH + 2 * NKV)
+    code = dtype_code(qkv) if dtype is None else dtype
+    nbytes = attn_fwd_workspace_bytes(B, T, NH * hd, NH, NKV, code)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
+    out, lse = forward(qkv, NH, NKV, rope_theta, dtype, stream, workspace=ws)
+    return out, lse, ws
+
+
 def backward(qkv, out, dout, lse, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None,
-             workspace=None):
-    """dqkv = attention backward; allocates the workspace unless one is given."""
+             workspace=None, qk_rot=None):
+    """dqkv = attention backward; allocates the workspace unless one is given.
+    With ``qk_rot`` (the workspace of the attn_fwd_ws call that made out/lse)
+    the call goes through attn_bwd_rot, else attn_bwd."""
     import torch
     B, T, W = qkv.shape
     C = out.shape[2]
@@ -232,5 +260,9 @@ def backward(qkv, out, dout, lse, NH: int, NKV: int, rope_theta: float = 0.0, dt
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
     dqkv = torch.empty_like(qkv)
-    attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, code, workspace, workspace.numel(), stream)
+    if qk_rot is None:
+        attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, code, workspace, workspace.numel(), stream)
+    else:
+        attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, code, qk_rot, workspace,
+                     workspace.numel(), stream)
     return dqkv

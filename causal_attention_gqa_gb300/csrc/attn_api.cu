@@ -263,9 +263,14 @@ extern "C" size_t attn_bwd_workspace_bytes(int B, int T, int C, int NH, int NKV,
   return workspace_bytes(g, dtype);
 }
 
-extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* dout, const float* lse, int B,
-                        int T, int C, int NH, int NKV, float rope_theta, int dtype, void* workspace,
-                        size_t ws_bytes, void* stream) {
+namespace {
+
+// Backward shared by attn_bwd (qk_rot == NULL: with RoPE the prologue rotates
+// Q/K into the workspace) and attn_bwd_rot (qk_rot: the rotated copy an
+// attn_fwd_ws call left in its workspace).
+int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, const float* lse, int B, int T, int C,
+             int NH, int NKV, float rope_theta, int dtype, const void* qk_rot, void* workspace, size_t ws_bytes,
+             void* stream) {
   Geometry g;
   int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
   if (st != ATTN_OK) return st;
@@ -293,6 +298,9 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
   if (!aligned16(dqkv) || !aligned16(qkv) || !aligned16(out) || !aligned16(dout) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return ATTN_ERR_MISALIGNED;
+  const bool rope = g.rope_theta > 0.f;
+  const bool reuse = rope && qk_rot != nullptr;
+  if (reuse && (reinterpret_cast<uintptr_t>(qk_rot) & 255u)) return ATTN_ERR_MISALIGNED;
   Tc05BwdArgs a{};
   a.g = g;
   a.dqkv = dqkv;
@@ -300,11 +308,11 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
   a.status = status_word();
   a.num_sms = num_sms();
   if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
-  // With RoPE, Q and K are read from a rotated copy in the workspace; its
-  // layout keeps query head h at column h*hd and kv head kh at C + kh*hd.
-  const bool rope = g.rope_theta > 0.f;
+  // With RoPE, Q and K are read from a rotated copy (the caller's, or one the
+  // prologue writes into the workspace); its layout keeps query head h at
+  // column h*hd and kv head kh at C + kh*hd.
   void* rot = static_cast<uint8_t*>(workspace) + row_part_bytes(g, dtype);
-  const void* qk_src = rope ? rot : qkv;
+  const void* qk_src = !rope ? qkv : (reuse ? qk_rot : rot);
   const int qk_width = rope ? (g.NH + g.NKV) * g.hd : g.W;
   for (int r = 0; r < 2; ++r) {
     const int rows = r ? 128 : 64;
@@ -312,9 +320,26 @@ extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void
         !make_tmap(&a.tm_v[r], qkv, g.W, g.T, g.B, rows) || !make_tmap(&a.tm_do[r], dout, g.C, g.T, g.B, rows))
       return ATTN_ERR_CUDA;
   }
-  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rot, out, dout, lse, qkv, g, s);
+  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rope && !reuse ? rot : nullptr, out, dout,
+                                           lse, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* dout, const float* lse, int B,
+                        int T, int C, int NH, int NKV, float rope_theta, int dtype, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  return bwd_impl(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, nullptr, workspace, ws_bytes,
+                  stream);
+}
+
+extern "C" int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const void* dout, const float* lse, int B,
+                            int T, int C, int NH, int NKV, float rope_theta, int dtype, const void* qk_rot,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  return bwd_impl(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, qk_rot, workspace, ws_bytes,
+                  stream);
 }
 
 extern "C" int attn_device_status(int* status, int reset) {

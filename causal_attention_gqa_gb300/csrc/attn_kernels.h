@@ -59,7 +59,7 @@ __host__ __device__ inline int row_table_rows(int T) { return (T + 127) / 128 * 
 // bf16 (hd a multiple of 16): the row tables, two float arrays of Tp rows per
 // (b, h): LD[(2*(b*NH + h))*Tp + t] = -lse * log2(e) and
 // LD[(2*(b*NH + h) + 1)*Tp + t] = -D with D = dO . O (zeros for t >= T); and,
-// when RoPE is on, the rotated Q/K copy; in one launch.
+// when `rot` is not NULL, the RoPE-rotated Q/K copy; in one launch.
 cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, const void* dout, const float* lse,
                                      const void* qkv, const Geometry& g, cudaStream_t stream);
 

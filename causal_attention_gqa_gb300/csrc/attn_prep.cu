@@ -247,7 +247,7 @@ cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, cons
   prof_begin(kKernelBwdPrologue, stream);
   cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
                              (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot,
-                             (const __nv_bfloat16*)qkv, g, vph_log2, g.rope_theta > 0.f ? 1 : 0);
+                             (const __nv_bfloat16*)qkv, g, vph_log2, rot != nullptr ? 1 : 0);
   prof_end(kKernelBwdPrologue, stream);
   return e;
 }

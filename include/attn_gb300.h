@@ -149,6 +149,23 @@ ATTN_API int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* 
              void* stream);
 
 /*
+ * attn_bwd_rot -- attn_bwd that reuses the rotated Q/K copy of the forward.
+ * Same arguments, results and errors as attn_bwd, plus
+ *   qk_rot : the workspace of the attn_fwd_ws call that produced out and lse
+ *          from this qkv, left unchanged since (it holds Q and K rotated by
+ *          RoPE, [B,T,(NH+NKV)*hd] of dtype; 256-byte aligned).
+ * With BF16 and rope_theta > 0 the backward then reads Q and K from qk_rot
+ * instead of rotating them again into its own workspace (one HBM pass fewer);
+ * otherwise qk_rot is ignored and it is attn_bwd.  A qk_rot that does not
+ * hold the rotation of this qkv gives wrong gradients: the library cannot
+ * check it.
+ */
+ATTN_API int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const void* dout,
+             const float* lse, int B, int T, int C, int NH, int NKV,
+             float rope_theta, int dtype, const void* qk_rot, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device
  * memory.  (The source pages have no counterpart: this is a library
  * convenience, not part of the attention method.)

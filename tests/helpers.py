@@ -26,13 +26,20 @@ def to_numpy(t):
 def run_gpu(lib, w, qkv_np, dout_np, dtype, backward=True, fwd_ws=False):
     """Forward (and backward) through the C ABI; returns numpy float64 arrays.
     fwd_ws: run the forward through attn_fwd_ws (pre-rotated Q/K) instead of
-    attn_fwd."""
+    attn_fwd, and the backward through attn_bwd_rot on the forward's rotated
+    copy instead of attn_bwd."""
     import torch
     qkv = to_device(qkv_np, dtype)
     dout = to_device(dout_np, dtype)
-    out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta, workspace=True if fwd_ws else None)
+    if fwd_ws:
+        # The benchmark's configuration: attn_fwd_ws, then attn_bwd_rot reusing
+        # the forward's rotated Q/K.
+        out, lse, fws = lib.forward_ws(qkv, w.NH, w.NKV, w.rope_theta)
+    else:
+        out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta)
+        fws = None
     res = {"out": out, "lse": lse}
     if backward:
-        res["dqkv"] = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta)
+        res["dqkv"] = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta, qk_rot=fws)
     torch.cuda.synchronize()
     return {k: to_numpy(v) for k, v in res.items()}

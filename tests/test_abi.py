@@ -103,3 +103,11 @@ def test_forward_workspace_size_and_validation(cdll):
     assert cdll.attn_fwd_ws(p, p, p, *args, p, 64, None) == -5
     assert cdll.attn_fwd_ws(p, p, p, 1, 16, 16, 3, 3, 0.0, 0, None, 0, None) == -2
     assert cdll.attn_fwd_ws(None, None, None, 1, 16, 16, 4, 4, 0.0, 0, None, 0, None) == -1
+
+
+def test_backward_rot_validation(cdll):
+    p = 1 << 20   # never dereferenced: validation fails first
+    args = (1, 128, 512, 4, 1, 1e6, 2)
+    assert cdll.attn_bwd_rot(p, p, p, p, p, *args, p, None, 0, None) == -5
+    assert cdll.attn_bwd_rot(p, p, p, p, p, *args, p + 16, p, 1 << 24, None) == -4
+    assert cdll.attn_bwd_rot(None, p, p, p, p, *args, p, p, 1 << 24, None) == -1

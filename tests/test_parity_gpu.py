@@ -70,7 +70,8 @@ def test_bf16_forward_shapes(lib, B, T, C, NH, NKV, theta):
     (1, 1000, 512, 4, 1, 1e6), (1, 77, 512, 4, 4, 0.0),
 ])
 def test_bf16_forward_workspace_shapes(lib, B, T, C, NH, NKV, theta):
-    """attn_fwd_ws: Q/K rotated once into the workspace, then attention."""
+    """attn_fwd_ws (Q/K rotated once into the workspace, then attention) and
+    attn_bwd_rot reading that rotated copy."""
     check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 9), "bf16", fwd_ws=True)
 
 
