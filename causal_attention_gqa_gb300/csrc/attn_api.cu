@@ -320,6 +320,7 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
         !make_tmap(&a.tm_v[r], qkv, g.W, g.T, g.B, rows) || !make_tmap(&a.tm_do[r], dout, g.C, g.T, g.B, rows))
       return ATTN_ERR_CUDA;
   }
+  if (!make_tmap(&a.tm_dqkv, dqkv, g.W, g.T, g.B, 128)) return ATTN_ERR_CUDA;
   cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rope && !reuse ? rot : nullptr, out, dout,
                                            lse, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);

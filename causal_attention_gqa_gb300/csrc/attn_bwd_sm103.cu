@@ -47,25 +47,32 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* f, float s) {
                     pack_bf16x2(__uint_as_float(f[6]) * s, __uint_as_float(f[7]) * s));
 }
 
+// Byte offset of the 16-byte chunk holding columns col..col+7 (col a multiple
+// of 8) of row `row` in a 128-row bf16 tile stored as 128-byte-swizzled atom
+// columns of 64 elements: the layout of the tensor maps' 64 x 128 boxes.
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int col) {
+  return (uint32_t)((col >> 6) * (128 * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
 // Epilogue of one gradient row held in TMEM (HD float32 columns at `acc`):
 // multiply by `s`, undo the RoPE rotation at position `t` if `rope`, round to
-// bf16 and store to `dst` (HD contiguous bf16; only if `store`).  Every lane of
-// the warp must call this (tcgen05.ld is warp-collective).
-// Chunks of 32 columns (32 pairs with RoPE) are dealt round-robin to
-// `nparts` callers; this caller handles part `part`.
+// bf16 and write row `row` of the swizzled staging tile `stile` (HD columns),
+// from which one thread then writes the whole tile with TMA stores (coalesced;
+// one 16-byte store per thread and row would not be).  Every lane of the warp
+// must call this (tcgen05.ld is warp-collective).  Chunks of 32 columns (32
+// pairs with RoPE) are dealt round-robin to `nparts` callers; this caller
+// handles part `part`.
 template <int HD>
-__device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope, int t, const Geometry& g,
-                                               __nv_bfloat16* dst, bool store, int part, int nparts) {
+__device__ __forceinline__ void stage_grad_row(uint32_t acc, float s, bool rope, int t, const Geometry& g,
+                                               uint8_t* stile, int row, int part, int nparts) {
   if (!rope) {
 #pragma unroll 1
     for (int c0 = 32 * part; c0 < HD; c0 += 32 * nparts) {
       uint32_t v[32];
       ptx::tmem_ld32(acc + c0, v);
       ptx::tmem_wait_ld();
-      if (store) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = pack8(&v[8 * q], s);
-      }
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(stile + sw128_chunk(row, c0 + 8 * q)) = pack8(&v[8 * q], s);
     }
     return;
   }
@@ -85,12 +92,10 @@ __device__ __forceinline__ void store_grad_row(uint32_t acc, float s, bool rope,
       lo[e] = __float_as_uint(y0);
       hi[e] = __float_as_uint(y1);
     }
-    if (store) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = pack8(&lo[8 * q], 1.f);
-        *reinterpret_cast<uint4*>(dst + HALF + c0 + 8 * q) = pack8(&hi[8 * q], 1.f);
-      }
+    for (int q = 0; q < 4; ++q) {
+      *reinterpret_cast<uint4*>(stile + sw128_chunk(row, c0 + 8 * q)) = pack8(&lo[8 * q], 1.f);
+      *reinterpret_cast<uint4*>(stile + sw128_chunk(row, HALF + c0 + 8 * q)) = pack8(&hi[8 * q], 1.f);
     }
   }
 }
@@ -125,7 +130,7 @@ struct DkdvCfg {
 };
 
 struct DkdvBarriers {
-  uint64_t kv_full, acc_done, drain;
+  uint64_t kv_full, acc_done, drain, staged;
   uint64_t qdo_full[4], qdo_empty[4];
   uint64_t s_full, dp_full, p_full, ds_full;
   uint32_t tmem_base;
@@ -141,8 +146,8 @@ template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDkdv, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ LD, int* __restrict__ status,
-                Geometry g) {
+                const __grid_constant__ CUtensorMap tm_dqkv, const float* __restrict__ LD,
+                int* __restrict__ status, Geometry g) {
   using Cfg = DkdvCfg<HD>;
   constexpr int NQS = Cfg::kQStages;
   extern __shared__ uint8_t smem_raw[];
@@ -169,6 +174,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     ptx::mbar_init(ptx::smem_u32(&bars->kv_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->staged), 8);
     for (int i = 0; i < NQS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[i]), 1);
@@ -408,15 +414,34 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
     }
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
+    // Every MMA has completed: the first Q and dO ring stages are free and
+    // stage the dV and dK tiles; rows past T are clipped by the TMA store.
+    uint8_t* stV = sQ;
+    uint8_t* stK = sDO;
     if (ok) {
       ptx::tc_fence_after();
-      const bool store = ks < g.T;
-      __nv_bfloat16* row_ptr = dqkv + ((size_t)b * g.T + (store ? ks : 0)) * g.W;
-      store_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, row_ptr + g.C + g.NKV * HD + kh * HD, store,
-                         wg, 2);
-      store_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, row_ptr + g.C + kh * HD, store, wg, 2);
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, stV, row, wg, 2);
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, stK, row, wg, 2);
     } else {
       fail();
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->staged));
+    if (warp == 2 && lane == 0) {
+      if (ptx::mbar_wait(ptx::smem_u32(&bars->staged), 0, abort_flag, kWaitLimitNs) && !*abort_flag) {
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a) {
+          ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(stV + a * Cfg::kAtom), g.C + g.NKV * HD + kh * HD + 64 * a,
+                            j * 128, b);
+          ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(stK + a * Cfg::kAtom), g.C + kh * HD + 64 * a, j * 128, b);
+        }
+        ptx::bulk_commit();
+        ptx::bulk_wait();
+      } else {
+        fail();
+      }
     }
   }
 
@@ -457,7 +482,7 @@ struct DqCfg {
 };
 
 struct DqBarriers {
-  uint64_t q_full, acc_done, drain;
+  uint64_t q_full, acc_done, drain, staged;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, ds_full;
   uint32_t tmem_base;
@@ -468,8 +493,8 @@ template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDq, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-              __nv_bfloat16* __restrict__ dqkv, const float* __restrict__ LD, int* __restrict__ status,
-              Geometry g) {
+              const __grid_constant__ CUtensorMap tm_dqkv, const float* __restrict__ LD,
+              int* __restrict__ status, Geometry g) {
   using Cfg = DqCfg<HD>;
   constexpr int NKS = Cfg::kKStages;
   extern __shared__ uint8_t smem_raw[];
@@ -494,6 +519,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->staged), 8);
     for (int i = 0; i < NKS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->k_empty[i]), 1);
@@ -697,13 +723,28 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
     }
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
+    // Every MMA has completed: the Q buffer is free and stages the dQ tile;
+    // rows past T are clipped by the TMA store.
     if (ok) {
       ptx::tc_fence_after();
-      const bool store = tq < g.T;
-      __nv_bfloat16* dst = dqkv + ((size_t)b * g.T + (store ? tq : 0)) * g.W + h * HD;
-      store_grad_row<HD>(t_lane + Cfg::kTmemDQ, g.scale, ROPE, tq, g, dst, store, wg, 2);
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ, g.scale, ROPE, tq, g, sQ, row, wg, 2);
     } else {
       fail();
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->staged));
+    if (warp == 2 && lane == 0) {
+      if (ptx::mbar_wait(ptx::smem_u32(&bars->staged), 0, abort_flag, kWaitLimitNs) && !*abort_flag) {
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a)
+          ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(sQ + a * Cfg::kAtom), h * HD + 64 * a, qt * 128, b);
+        ptx::bulk_commit();
+        ptx::bulk_wait();
+      } else {
+        fail();
+      }
     }
   }
 
@@ -732,13 +773,13 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   const unsigned grid1 = (unsigned)(((g.T + 127) / 128) * g.B * g.NKV);
   prof_begin(kKernelBwdDkdvTc05, stream);
   e = launch_pdl(k1, dim3(grid1), dim3(kThreadsDkdv), DkdvCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_v[1],
-                 a.tm_qk[1], a.tm_do[1], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
+                 a.tm_qk[1], a.tm_do[1], a.tm_dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDkdvTc05, stream);
   if (e != cudaSuccess) return e;
   const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
   prof_begin(kKernelBwdDqTc05, stream);
   e = launch_pdl(k2, dim3(grid2), dim3(kThreadsDq), DqCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_do[1],
-                 a.tm_qk[1], a.tm_v[1], (__nv_bfloat16*)a.dqkv, a.LD, a.status, g);
+                 a.tm_qk[1], a.tm_v[1], a.tm_dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
   return e;
 }

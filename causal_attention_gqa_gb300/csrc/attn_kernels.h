@@ -90,6 +90,7 @@ struct Tc05BwdArgs {
   CUtensorMap tm_qk[2];
   CUtensorMap tm_v[2];   // over qkv
   CUtensorMap tm_do[2];  // over dout
+  CUtensorMap tm_dqkv;   // over dqkv, 128-row boxes (tile stores of the gradients)
   void* dqkv;            // [B,T,W] bf16
   const float* LD;       // row tables: -lse * log2(e) and -D per (b, h), see launch_bwd_prologue_bf16
   int* status;
