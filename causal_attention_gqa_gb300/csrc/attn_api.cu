@@ -140,9 +140,13 @@ size_t row_part_bytes(const Geometry& g, int dtype) {
   return align256((size_t)g.B * g.NH * g.T * sizeof(float));
 }
 
+// bf16: row tables, then the rotated Q/K copy, then 256 bytes for the dQ
+// kernel's work-item counter.
+size_t rot_part_bytes(const Geometry& g) { return align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2); }
+
 size_t workspace_bytes(const Geometry& g, int dtype) {
   size_t bytes = row_part_bytes(g, dtype);
-  if (dtype == ATTN_DTYPE_BF16) bytes += align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2);
+  if (dtype == ATTN_DTYPE_BF16) bytes += rot_part_bytes(g) + 256;
   return bytes;
 }
 
@@ -312,6 +316,7 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
   // prologue writes into the workspace); its layout keeps query head h at
   // column h*hd and kv head kh at C + kh*hd.
   void* rot = static_cast<uint8_t*>(workspace) + row_part_bytes(g, dtype);
+  a.item_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(rot) + rot_part_bytes(g));
   const void* qk_src = !rope ? qkv : (reuse ? qk_rot : rot);
   const int qk_width = rope ? (g.NH + g.NKV) * g.hd : g.W;
   for (int r = 0; r < 2; ++r) {
@@ -321,8 +326,8 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
       return ATTN_ERR_CUDA;
   }
   if (!make_tmap(&a.tm_dqkv, dqkv, g.W, g.T, g.B, 128)) return ATTN_ERR_CUDA;
-  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rope && !reuse ? rot : nullptr, out, dout,
-                                           lse, qkv, g, s);
+  cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rope && !reuse ? rot : nullptr,
+                                           a.item_counter, out, dout, lse, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
 }

@@ -457,69 +457,89 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // ===========================================================================
 // dQ kernel
 // ===========================================================================
-// One CTA per (128-query tile, query head, batch row); Q_i and dO_i stay in
-// shared memory and the CTA walks the 128-key tiles 0..i (every MMA N = 128).
-// TMEM: S [0, 128), dP [128, 256), dQ accumulator from 256.  The elementwise
-// groups turn S into P (kept in registers) while dP is computed, then dP into
-// dS, written (bf16 pairs) into TMEM over the dP columns they have read; the
-// dQ MMA takes its A operand from there.  Issue order S(n), dQ(n-1), dP(n):
-// the tensor core works on dQ(n-1) and dP(n) while P(n) is formed.
+// Persistent: one CTA per SM claims work items (128-query tile, query head,
+// batch row), heaviest (longest causal key range) first, from a counter in
+// the workspace that the prologue clears: CTAs that become resident early
+// (the kernel starts while the dK/dV kernel drains) take more items.  Per
+// item, Q_i and dO_i stay in shared memory and the CTA walks the 128-key
+// tiles 0..i (every MMA N = 128).  The next item's Q and dO are loaded as
+// soon as the current item's last score MMAs have read them, and its first
+// MMAs overlap the current item's epilogue.
+// TMEM: S [0, 128), dP [128, 256), two dQ accumulators from 256 (items
+// alternate).  The elementwise groups turn S into P (kept in registers) while
+// dP is computed, then dP into dS, written (bf16 pairs) into TMEM over the dP
+// columns they have read; the dQ MMA takes its A operand from there.  Issue
+// order S(n), dQ(n-1), dP(n): the tensor core works on dQ(n-1) and dP(n)
+// while P(n) is formed.
 template <int HD>
 struct DqCfg {
   static constexpr int kQ = 128, kKeys = 128;
-  static constexpr int kQTile = kQ * HD * 2;           // Q_i or dO_i
+  static constexpr int kQTile = kQ * HD * 2;           // Q_i, dO_i or the staged dQ tile
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kAtom = 128 * 128;              // one 64-column atom column of a 128-row tile
   static constexpr int kKStages = (HD == 128) ? 2 : 4; // K ring and V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kQOff + kQTile;
-  static constexpr int kKOff = kDOOff + kQTile;
+  static constexpr int kStOff = kDOOff + kQTile;       // dQ staging tile (TMA store source)
+  static constexpr int kKOff = kStOff + kQTile;
   static constexpr int kVOff = kKOff + kKStages * kKTile;
   static constexpr int kBarOff = kVOff + kKStages * kKTile;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256, kTmemCols = 512;
+  static constexpr int kItemSlots = 4;                 // claimed-item queue depth
   static_assert(kSmemBytes <= 232448, "dQ kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DqBarriers {
-  uint64_t q_full, acc_done, drain, staged;
+  uint64_t q_full, q_empty, do_full, do_empty, drain;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, ds_full;
+  uint64_t acc_done[2], dq_free[2], staged, stage_free;
+  uint64_t item_full[4], item_empty[4];
+  int item[4];
   uint32_t tmem_base;
   int abort;
 };
+
+// Work item w -> (batch row, query head, 128-query tile); heaviest first.
+struct DqItem {
+  int b, h, qt;
+};
+__device__ __forceinline__ DqItem dq_item(int w, const Geometry& g) {
+  const int n_qt = (g.T + 127) / 128, bh_count = g.B * g.NH;
+  DqItem it;
+  it.qt = n_qt - 1 - w / bh_count;
+  const int bh = w % bh_count;
+  it.b = bh / g.NH;
+  it.h = bh % g.NH;
+  return it;
+}
 
 template <int HD, bool ROPE>
 __global__ void __launch_bounds__(kThreadsDq, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_dqkv, const float* __restrict__ LD,
-              int* __restrict__ status, Geometry g) {
+              int* __restrict__ item_counter, int n_items, int* __restrict__ status, Geometry g) {
   using Cfg = DqCfg<HD>;
-  constexpr int NKS = Cfg::kKStages;
+  constexpr int NKS = Cfg::kKStages, NIS = Cfg::kItemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
   uint8_t* sDO = smem + Cfg::kDOOff;
+  uint8_t* sSt = smem + Cfg::kStOff;
   uint8_t* sK = smem + Cfg::kKOff;
   uint8_t* sV = smem + Cfg::kVOff;
   DqBarriers* bars = reinterpret_cast<DqBarriers*>(smem + Cfg::kBarOff);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  // Heaviest query tiles (large i) first.
-  const int n_qt = (g.T + 127) / 128;
-  const int bh_count = g.B * g.NH;
-  const int qt = n_qt - 1 - (int)(blockIdx.x / bh_count);
-  const int b = (blockIdx.x % bh_count) / g.NH, h = (blockIdx.x % bh_count) % g.NH;
-  const int kh = h / g.grp;
-  const int n_steps = qt + 1;                    // 128-key tiles 0..qt
-
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->do_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->do_empty), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->staged), 8);
     for (int i = 0; i < NKS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->k_empty[i]), 1);
@@ -530,6 +550,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     ptx::mbar_init(ptx::smem_u32(&bars->s_free), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->acc_done[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->dq_free[i]), 8);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->staged), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->stage_free), 1);
+    for (int i = 0; i < NIS; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars->item_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->item_empty[i]), 9);   // MMA issuer + 8 elementwise warps
+    }
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -543,49 +573,96 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t tmem = bars->tmem_base;
   // Launched as a programmatic dependent of the dK/dV kernel, whose CTAs all
   // waited for the prologue before allowing this grid to start; this kernel
-  // reads only the prologue's outputs and the inputs, and writes dqkv columns
-  // the dK/dV kernel does not touch, so it needs no wait of its own.
+  // reads only the prologue's outputs (row tables, rotated Q/K, the cleared
+  // item counter) and the inputs, and writes dqkv columns the dK/dV kernel
+  // does not touch, so it needs no wait of its own.
   auto fail = [&]() {
     *abort_flag = 1;
     record_status(status, kErrDeviceTimeout);
+  };
+  // Claimed item `it` of this CTA (-1: no more work), published by the producer.
+  auto next_item = [&](int it, bool* okp) -> int {
+    const int slot = it % NIS;
+    if (!ptx::mbar_wait(ptx::smem_u32(&bars->item_full[slot]), (it / NIS) & 1, abort_flag, kWaitLimitNs)) {
+      *okp = false;
+      return -1;
+    }
+    return *reinterpret_cast<volatile int*>(&bars->item[slot]);
   };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint32_t qf = ptx::smem_u32(&bars->q_full);
-      ptx::mbar_arrive_expect_tx(qf, 2 * Cfg::kQTile);
-#pragma unroll
-      for (int a = 0; a < HD / 64; ++a) {
-        ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kAtom), &tm_q, h * HD + 64 * a, qt * 128, b, qf);
-        ptx::tma_load_3d(ptx::smem_u32(sDO + a * Cfg::kAtom), &tm_do, h * HD + 64 * a, qt * 128, b, qf);
-      }
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 0, v_issued = 0, q_issued = 0;  // global sequence counters
+      int gs = 0;                                    // global index of the item's first key step
       bool ok = true;
-      for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n % NKS, u = n / NKS;
-        if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)))
+      for (int it = 0; ok; ++it) {
+        const int slot = it % NIS;
+        if (it >= NIS &&
+            !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->item_empty[slot]), (it / NIS - 1) & 1, abort_flag,
+                                  kWaitLimitNs)))
           break;
-        const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
-        ptx::mbar_arrive_expect_tx(kf, Cfg::kKTile);
+        int w = atomicAdd(item_counter, 1);
+        if (w >= n_items) w = -1;
+        bars->item[slot] = w;
+        ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[slot]));
+        if (w < 0) break;
+        const DqItem item = dq_item(w, g);
+        const int kh = item.h / g.grp, n_steps = item.qt + 1;
+        // Q and dO of this item once the previous item's last score MMAs read them.
+        if (it > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty), (it - 1) & 1, abort_flag, kWaitLimitNs)))
+          break;
+        const uint32_t qf = ptx::smem_u32(&bars->q_full);
+        ptx::mbar_arrive_expect_tx(qf, Cfg::kQTile);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kKTile + a * Cfg::kAtom), &tm_k, g.C + kh * HD + 64 * a,
-                           n * 128, b, kf);
-        k_issued = n + 1;
-        if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag, kWaitLimitNs)))
-          break;
-        const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
-        ptx::mbar_arrive_expect_tx(vf, Cfg::kKTile);
+          ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kAtom), &tm_q, item.h * HD + 64 * a, item.qt * 128, item.b, qf);
+        q_issued = it + 1;
+        bool do_loaded = false;
+        for (int n = 0; n < n_steps && ok; ++n) {
+          const int gi = gs + n, st = gi % NKS, u = gi / NKS;
+          if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), (u - 1) & 1, abort_flag,
+                                             kWaitLimitNs)))
+            break;
+          const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
+          ptx::mbar_arrive_expect_tx(kf, Cfg::kKTile);
 #pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kKTile + a * Cfg::kAtom), &tm_v,
-                           g.C + g.NKV * HD + kh * HD + 64 * a, n * 128, b, vf);
-        v_issued = n + 1;
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kKTile + a * Cfg::kAtom), &tm_k, g.C + kh * HD + 64 * a,
+                             n * 128, item.b, kf);
+          k_issued = gi + 1;
+          if (!do_loaded) {
+            if (it > 0 &&
+                !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->do_empty), (it - 1) & 1, abort_flag, kWaitLimitNs)))
+              break;
+            const uint32_t df = ptx::smem_u32(&bars->do_full);
+            ptx::mbar_arrive_expect_tx(df, Cfg::kQTile);
+#pragma unroll
+            for (int a = 0; a < HD / 64; ++a)
+              ptx::tma_load_3d(ptx::smem_u32(sDO + a * Cfg::kAtom), &tm_do, item.h * HD + 64 * a, item.qt * 128,
+                               item.b, df);
+            do_loaded = true;
+          }
+          if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag,
+                                             kWaitLimitNs)))
+            break;
+          const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
+          ptx::mbar_arrive_expect_tx(vf, Cfg::kKTile);
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kKTile + a * Cfg::kAtom), &tm_v,
+                             g.C + g.NKV * HD + kh * HD + 64 * a, n * 128, item.b, vf);
+          v_issued = gi + 1;
+        }
+        gs += n_steps;
       }
       if (!ok) fail();
       if (*abort_flag) {
-        ptx::mbar_wait(qf, 0, nullptr, kWaitLimitNs);
+        // Let every copy already in flight land before shared memory is released.
+        if (q_issued > 0) {
+          ptx::mbar_wait(ptx::smem_u32(&bars->q_full), (q_issued - 1) & 1, nullptr, kWaitLimitNs);
+          ptx::mbar_wait(ptx::smem_u32(&bars->do_full), (q_issued - 1) & 1, nullptr, kWaitLimitNs);
+        }
         for (int st = 0; st < NKS && st < k_issued; ++st)
           ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
         for (int st = 0; st < NKS && st < v_issued; ++st)
@@ -602,51 +679,78 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
       const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), 16, 1024);
       const uint64_t dKm = ptx::sw128_desc(ptx::smem_u32(sK), Cfg::kAtom, 1024);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
-      // dQ += dS K of step m once both groups wrote dS(m); frees K_m.
-      auto issue_dq = [&](int m) -> bool {
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), m & 1, abort_flag, kWaitLimitNs)) return false;
+      bool ok = true;
+      // The pending dQ MMA group: global step index, its item, and whether it
+      // is that item's first / last step.
+      int p_g = -1, p_it = 0;
+      bool p_first = false, p_last = false;
+      auto issue_dq = [&]() -> bool {
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), p_g & 1, abort_flag, kWaitLimitNs)) return false;
+        const int db = p_it & 1;
+        // The item's first dQ MMA overwrites accumulator db: the epilogue of
+        // the item two before must have read it.
+        if (p_first && p_it >= 2 &&
+            !ptx::mbar_wait(ptx::smem_u32(&bars->dq_free[db]), ((p_it >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
+          return false;
         ptx::tc_fence_after();
-        const int ms = m % NKS;
+        const int ms = p_g % NKS;
         const uint64_t bk = ptx::desc_advance(dKm, ms * Cfg::kKTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kKeys / 16; ++kk)
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDQ, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(bk, kk * 2048),
-                           idesc_g, (m > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + Cfg::kTmemDQ + 128 * db, tmem + Cfg::kTmemDP + pair_col(kk),
+                           ptx::desc_advance(bk, kk * 2048), idesc_g, (!p_first || kk > 0) ? 1u : 0u);
         ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ms]));
+        if (p_last) ptx::mma_commit(ptx::smem_u32(&bars->acc_done[db]));
         return true;
       };
-      for (int n = 0; n < n_steps && ok; ++n) {
-        const int ks = n % NKS, u = n / NKS;
-        // K_n landed; the groups have read S(n-1) out of TMEM.
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), u & 1, abort_flag, kWaitLimitNs);
-        if (ok && n > 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free), (n - 1) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, ks * Cfg::kKTile);
+      int gs = 0;
+      for (int it = 0; ok; ++it) {
+        const int w = next_item(it, &ok);
+        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[it % NIS]));
+        if (!ok || w < 0) break;
+        const DqItem item = dq_item(w, g);
+        const int n_steps = item.qt + 1;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs);
+        for (int n = 0; n < n_steps && ok; ++n) {
+          const int gi = gs + n, ks = gi % NKS, u = gi / NKS;
+          // K landed; the groups have read the previous S out of TMEM.
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), u & 1, abort_flag, kWaitLimitNs);
+          if (ok && gi > 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free), (gi - 1) & 1, abort_flag, kWaitLimitNs);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, ks * Cfg::kKTile);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemS, ptx::desc_advance(dQ, off), ptx::desc_advance(bk, off), idesc_s,
-                           kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
-        // dQ(n-1) reads dS(n-1) in the dP columns: issued before dP(n)
-        // overwrites them (MMAs from one thread run in order).
-        if (n > 0 && !(ok = issue_dq(n - 1))) break;
-        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[ks]), u & 1, abort_flag, kWaitLimitNs))) break;
-        ptx::tc_fence_after();
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
+            ptx::mma_bf16_ss(tmem + Cfg::kTmemS, ptx::desc_advance(dQ, off), ptx::desc_advance(bk, off), idesc_s,
+                             kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+          if (n == n_steps - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+          // The previous step's dQ reads its dS in the dP columns: issued
+          // before dP overwrites them (MMAs from one thread run in order).
+          if (p_g >= 0 && !(ok = issue_dq())) break;
+          if (n == 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->do_full), it & 1, abort_flag, kWaitLimitNs)))
+            break;
+          if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[ks]), u & 1, abort_flag, kWaitLimitNs))) break;
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDP, ptx::desc_advance(dDO, off), ptx::desc_advance(bv, off), idesc_s,
-                           kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
+            ptx::mma_bf16_ss(tmem + Cfg::kTmemDP, ptx::desc_advance(dDO, off), ptx::desc_advance(bv, off), idesc_s,
+                             kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[ks]));
+          if (n == n_steps - 1) ptx::mma_commit(ptx::smem_u32(&bars->do_empty));
+          p_g = gi;
+          p_it = it;
+          p_first = n == 0;
+          p_last = n == n_steps - 1;
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[ks]));
+        gs += n_steps;
       }
-      if (ok && n_steps > 0) ok = issue_dq(n_steps - 1);
-      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (ok && p_g >= 0) ok = issue_dq();
       if (!ok) fail();
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
       ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
@@ -658,94 +762,118 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;           // query row within the tile
-    const int tq = qt * 128 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t t_s = t_lane + Cfg::kTmemS + 64 * wg, t_dp = t_lane + Cfg::kTmemDP + 64 * wg;
     const float sl2 = g.scale * kLog2e;
-    // This row's table entries -lse * log2(e) and -D; padding rows have zero
-    // Q and dO, hence dP = 0 and dS = 0.
-    const int Tp = row_table_rows(g.T);
-    const float2 ldr = (tq < g.T) ? make_float2(LD[(size_t)(2 * (b * g.NH + h)) * Tp + tq],
-                                                LD[(size_t)(2 * (b * g.NH + h) + 1) * Tp + tq])
-                                  : make_float2(0.f, 0.f);
-    const float2 nl2 = make_float2(ldr.x, ldr.x), nd2 = make_float2(ldr.y, ldr.y);
     const float2 sl2x2 = make_float2(sl2, sl2);
+    const int Tp = row_table_rows(g.T);
+    const int k0 = 64 * wg;                        // first key (within a tile) of this group
     bool ok = true;
-    for (int n = 0; n < n_steps; ++n) {
-      const bool diag = n == qt;                   // key tile == query tile: key k is after row iff k > row
-      const int k0 = 64 * wg;                      // first key (within the tile) of this group
-      // ---- P = exp2(S * scale * log2(e) - lse * log2(e)), while dP is computed.
-      float p[64];
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, abort_flag, kWaitLimitNs));
-      if (!ok) break;
-      ptx::tc_fence_after();
+    int gs = 0;
+    for (int it = 0; ok; ++it) {
+      const int w = __shfl_sync(0xffffffffu, lane == 0 ? next_item(it, &ok) : 0, 0);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[it % NIS]));
+      if (!ok || w < 0) break;
+      const DqItem item = dq_item(w, g);
+      const int n_steps = item.qt + 1;
+      const int tq = item.qt * 128 + row;
+      // This row's table entries -lse * log2(e) and -D; padding rows have
+      // zero Q and dO, hence dP = 0 and dS = 0.
+      const size_t tab = (size_t)(2 * (item.b * g.NH + item.h)) * Tp + tq;
+      const float2 ldr = (tq < g.T) ? make_float2(LD[tab], LD[tab + Tp]) : make_float2(0.f, 0.f);
+      const float2 nl2 = make_float2(ldr.x, ldr.x), nd2 = make_float2(ldr.y, ldr.y);
+      for (int n = 0; n < n_steps; ++n) {
+        const int gi = gs + n;
+        const bool diag = n == item.qt;            // key tile == query tile: key k is after row iff k > row
+        // ---- P = exp2(S * scale * log2(e) - lse * log2(e)), while dP is computed.
+        float p[64];
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), gi & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+        ptx::tc_fence_after();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32];
-        ptx::tmem_ld32(t_s + 32 * half, sr);
-        ptx::tmem_wait_ld();
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sr[32];
+          ptx::tmem_ld32(t_s + 32 * half, sr);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl2);
-          float e0 = ptx::ex2_approx(x.x), e1 = ptx::ex2_approx(x.y);
-          if (diag) {
-            if (k0 + 32 * half + c > row) e0 = 0.f;
-            if (k0 + 32 * half + c + 1 > row) e1 = 0.f;
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl2);
+            float e0 = ptx::ex2_approx(x.x), e1 = ptx::ex2_approx(x.y);
+            if (diag) {
+              if (k0 + 32 * half + c > row) e0 = 0.f;
+              if (k0 + 32 * half + c + 1 > row) e1 = 0.f;
+            }
+            p[32 * half + c] = e0;
+            p[32 * half + c + 1] = e1;
           }
-          p[32 * half + c] = e0;
-          p[32 * half + c + 1] = e1;
         }
+        // S is in registers: the next score MMA may overwrite it.
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free));
+        // ---- dS = P * (dP - D), while the previous dQ is accumulated.
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), gi & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t dr[32], dw[16];
+          ptx::tmem_ld32(t_dp + 32 * half, dr);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 ds = __fmul2_rn(make_float2(p[32 * half + c], p[32 * half + c + 1]),
+                                         __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                                                    nd2));
+            dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
+          }
+          ptx::tmem_st16(t_dp + 16 * half, dw);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
       }
-      // S is in registers: the next score MMA may overwrite it.
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->s_free));
-      // ---- dS = P * (dP - D), while dQ(n-1) is accumulated.
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), n & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      gs += n_steps;
+      // ---- Epilogue: dQ of this item, staged and written with TMA stores
+      // (rows past T are clipped) while the next item's MMAs start.
+      const int db = it & 1;
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(ptx::smem_u32(&bars->acc_done[db]), (it >> 1) & 1, abort_flag, kWaitLimitNs));
+      // The staging tile is free once the previous item's stores have read it.
+      if (ok && it > 0)
+        ok = __all_sync(0xffffffffu,
+                        ptx::mbar_wait(ptx::smem_u32(&bars->stage_free), (it - 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t dr[32], dw[16];
-        ptx::tmem_ld32(t_dp + 32 * half, dr);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 ds = __fmul2_rn(make_float2(p[32 * half + c], p[32 * half + c + 1]),
-                                       __fadd2_rn(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), nd2));
-          dw[c >> 1] = pack_bf16x2(ds.x, ds.y);
-        }
-        ptx::tmem_st16(t_dp + 16 * half, dw);
-      }
-      ptx::tmem_wait_st();
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ + 128 * db, g.scale, ROPE, tq, g, sSt, row, wg, 2);
+      ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->acc_done), 0, abort_flag, kWaitLimitNs));
-    // Every MMA has completed: the Q buffer is free and stages the dQ tile;
-    // rows past T are clipped by the TMA store.
-    if (ok) {
-      ptx::tc_fence_after();
-      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ, g.scale, ROPE, tq, g, sQ, row, wg, 2);
-    } else {
-      fail();
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->staged));
-    if (warp == 2 && lane == 0) {
-      if (ptx::mbar_wait(ptx::smem_u32(&bars->staged), 0, abort_flag, kWaitLimitNs) && !*abort_flag) {
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(sQ + a * Cfg::kAtom), h * HD + 64 * a, qt * 128, b);
-        ptx::bulk_commit();
-        ptx::bulk_wait();
-      } else {
-        fail();
+      if (lane == 0) {
+        ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free[db]));
+        ptx::mbar_arrive(ptx::smem_u32(&bars->staged));
       }
+      if (warp == 2 && lane == 0) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->staged), it & 1, abort_flag, kWaitLimitNs);
+        if (ok) {
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(sSt + a * Cfg::kAtom), item.h * HD + 64 * a, item.qt * 128,
+                              item.b);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read();
+          ptx::mbar_arrive(ptx::smem_u32(&bars->stage_free));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
+    if (!ok) fail();
+    // Every tile store has landed in global memory before the CTA exits.
+    if (warp == 2 && lane == 0) ptx::bulk_wait();
   }
 
   // Finish only after the dK/dV kernel this grid overlapped has completed, so
@@ -776,10 +904,11 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
                  a.tm_qk[1], a.tm_do[1], a.tm_dqkv, a.LD, a.status, g);
   prof_end(kKernelBwdDkdvTc05, stream);
   if (e != cudaSuccess) return e;
-  const unsigned grid2 = (unsigned)(((g.T + 127) / 128) * g.B * g.NH);
+  const int n_items = ((g.T + 127) / 128) * g.B * g.NH;
+  const unsigned grid2 = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelBwdDqTc05, stream);
   e = launch_pdl(k2, dim3(grid2), dim3(kThreadsDq), DqCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_do[1],
-                 a.tm_qk[1], a.tm_v[1], a.tm_dqkv, a.LD, a.status, g);
+                 a.tm_qk[1], a.tm_v[1], a.tm_dqkv, a.LD, a.item_counter, n_items, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
   return e;
 }

@@ -59,9 +59,10 @@ __host__ __device__ inline int row_table_rows(int T) { return (T + 127) / 128 * 
 // bf16 (hd a multiple of 16): the row tables, two float arrays of Tp rows per
 // (b, h): LD[(2*(b*NH + h))*Tp + t] = -lse * log2(e) and
 // LD[(2*(b*NH + h) + 1)*Tp + t] = -D with D = dO . O (zeros for t >= T); and,
-// when `rot` is not NULL, the RoPE-rotated Q/K copy; in one launch.
-cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, const void* dout, const float* lse,
-                                     const void* qkv, const Geometry& g, cudaStream_t stream);
+// when `rot` is not NULL, the RoPE-rotated Q/K copy; it also clears
+// *item_counter; in one launch.
+cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, const void* out, const void* dout,
+                                     const float* lse, const void* qkv, const Geometry& g, cudaStream_t stream);
 
 // ------------------------------------------------------------ tcgen05 bf16 path
 struct Tc05FwdArgs {
@@ -93,6 +94,7 @@ struct Tc05BwdArgs {
   CUtensorMap tm_dqkv;   // over dqkv, 128-row boxes (tile stores of the gradients)
   void* dqkv;            // [B,T,W] bf16
   const float* LD;       // row tables: -lse * log2(e) and -D per (b, h), see launch_bwd_prologue_bf16
+  int* item_counter;     // dQ work-item counter (workspace), cleared by the prologue
   int* status;
   int num_sms;           // persistent grid size
 };

@@ -146,12 +146,14 @@ __global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float* __rest
                                                                  const uint4* __restrict__ dout,
                                                                  const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
+                                                                 int* __restrict__ item_counter,
                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
                                                                  int vph_log2, int rope) {
   // out is written by the forward that may still be finishing (programmatic
   // launch): wait for it, then let the dK/dV kernel get resident.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *item_counter = 0;
   constexpr int R = 2;                            // token rows per iteration
   const int vph = 1 << vph_log2;                  // 16-byte chunks per head (hd / 8)
   const int dot_units = g.C >> 3;                 // chunks per token row
@@ -237,8 +239,8 @@ __global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float* __rest
 
 }  // namespace
 
-cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, const void* dout, const float* lse,
-                                     const void* qkv, const Geometry& g, cudaStream_t stream) {
+cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, const void* out, const void* dout,
+                                     const float* lse, const void* qkv, const Geometry& g, cudaStream_t stream) {
   const int vph = g.hd / 8;  // 8 or 16
   int vph_log2 = 0;
   while ((1 << vph_log2) < vph) ++vph_log2;
@@ -246,7 +248,7 @@ cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, const void* out, cons
   const int blocks = groups < 152 * 4 ? groups : 152 * 4;  // 4 resident 256-thread blocks per SM
   prof_begin(kKernelBwdPrologue, stream);
   cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
-                             (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot,
+                             (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter,
                              (const __nv_bfloat16*)qkv, g, vph_log2, rot != nullptr ? 1 : 0);
   prof_end(kKernelBwdPrologue, stream);
   return e;

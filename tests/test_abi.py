@@ -54,9 +54,10 @@ def test_workspace_size(cdll):
     # the rotated Q/K copy; each part rounded up to 256 bytes.
     row_bytes = B * NH * T * 8
     rot_bytes = B * T * (NH + NKV) * (C // NH) * 2
-    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == row_bytes + rot_bytes
+    cnt_bytes = 256   # the dQ kernel's work-item counter
+    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == row_bytes + rot_bytes + cnt_bytes
     ragged = binding.attn_bwd_workspace_bytes(1, 100, 256, 2, 1, binding.DTYPE_BF16)
-    assert ragged == 2 * 128 * 8 + 100 * 3 * 128 * 2 + (256 - (100 * 3 * 128 * 2) % 256) % 256
+    assert ragged == 2 * 128 * 8 + 100 * 3 * 128 * 2 + (256 - (100 * 3 * 128 * 2) % 256) % 256 + 256
     assert binding.attn_bwd_workspace_bytes(1, 16, 16, 4, 4, binding.DTYPE_F32) == 256
     assert binding.attn_bwd_workspace_bytes(1, 16, 16, 3, 4, binding.DTYPE_F32) == 0
 
