@@ -631,6 +631,7 @@ cudaError_t launch_fwd(const Tc05FwdArgs& a, cudaStream_t stream) {
 
 cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream) {
   const bool rope = a.g.rope_theta > 0.f && !a.pre_rotated;
+  if (!rope && tc05_fwd2_supported(a.g)) return tc05_fwd2_launch(a, stream);
   if (a.g.hd == 128) return rope ? launch_fwd<128, true>(a, stream) : launch_fwd<128, false>(a, stream);
   if (a.g.hd == 64) return rope ? launch_fwd<64, true>(a, stream) : launch_fwd<64, false>(a, stream);
   return cudaErrorInvalidValue;

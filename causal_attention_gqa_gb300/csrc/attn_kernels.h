@@ -81,6 +81,11 @@ struct Tc05FwdArgs {
   int num_sms;        // persistent grid size
 };
 cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream);
+// Paired-head forward (two query heads of one kv group per work item): head
+// size 128, an even number of query heads per kv head, Q/K not rotated in
+// the kernel.
+bool tc05_fwd2_supported(const Geometry& g);
+cudaError_t tc05_fwd2_launch(const Tc05FwdArgs& a, cudaStream_t stream);
 
 struct Tc05BwdArgs {
   Geometry g;

@@ -66,8 +66,18 @@ def test_bf16_forward_shapes(lib, B, T, C, NH, NKV, theta):
 
 
 @pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    # head size 128 with an even number of query heads per kv head: the
+    # paired-head forward kernel (ragged T, T = 1, one tile, several items)
+    (2, 385, 1024, 8, 2, 0.0), (1, 1, 256, 2, 1, 0.0), (1, 128, 256, 2, 1, 0.0), (3, 200, 1024, 8, 4, 0.0),
+    (1, 700, 2048, 16, 2, 0.0),
+])
+def test_bf16_forward_paired_heads(lib, B, T, C, NH, NKV, theta):
+    check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 13), "bf16", backward=False)
+
+
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
     (1, 1, 128, 1, 1, 1e6), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6), (1, 256, 256, 4, 1, 1e4),
-    (1, 1000, 512, 4, 1, 1e6), (1, 77, 512, 4, 4, 0.0),
+    (1, 1000, 512, 4, 1, 1e6), (1, 77, 512, 4, 4, 0.0), (3, 200, 1024, 8, 4, 1e6),
 ])
 def test_bf16_forward_workspace_shapes(lib, B, T, C, NH, NKV, theta):
     """attn_fwd_ws (Q/K rotated once into the workspace, then attention) and
