@@ -37,7 +37,7 @@ METRIC = "causal attn fwd+bwd TFLOP/s on 1 GB300; % of BF16 tensor peak"
 FLUSH_BYTES = 256 << 20          # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
-    "fwd_tc05": "attn_fwd_sm103.cu", "bwd_dkdv_tc05": "attn_bwd_sm103.cu", "bwd_dq_tc05": "attn_bwd_sm103.cu",
+    "fwd_tc05": "attn_fwd2_sm103.cu", "bwd_dkdv_tc05": "attn_bwd_sm103.cu", "bwd_dq_tc05": "attn_bwd_sm103.cu",
     "bwd_row_dot": "attn_prep.cu", "rope_qk": "attn_prep.cu", "bwd_prologue": "attn_prep.cu",
 }
 
