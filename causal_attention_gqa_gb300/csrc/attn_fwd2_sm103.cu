@@ -140,8 +140,12 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // A following backward prologue may get resident now; it waits for this
-  // grid to complete before reading out.
+  // Launched as a programmatic dependent of the preceding kernel (the Q/K
+  // rotation pass of attn_fwd_ws): the set-up above overlapped its tail;
+  // wait for it to complete before reading or writing global memory.  A
+  // following backward prologue may get resident now; it waits for this grid
+  // to complete before reading out.
+  ptx::grid_dep_wait();
   ptx::grid_dep_launch();
 
   auto fail = [&]() {
@@ -445,10 +449,10 @@ cudaError_t tc05_fwd2_launch(const Tc05FwdArgs& a, cudaStream_t stream) {
   const int n_items = n_qt * a.g.B * (a.g.NH / 2);
   const unsigned grid = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelFwdTc05, stream);
-  fwd2_kernel<<<grid, kThreads, Fwd2Cfg::kSmemBytes, stream>>>(a.tm_qk, a.tm_v, a.tm_out, a.lse, a.status, a.g,
-                                                                n_items);
+  e = launch_pdl(fwd2_kernel, dim3(grid), dim3(kThreads), Fwd2Cfg::kSmemBytes, stream, a.tm_qk, a.tm_v, a.tm_out,
+                 a.lse, a.status, a.g, n_items);
   prof_end(kKernelFwdTc05, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace attn

@@ -74,6 +74,9 @@ __global__ void __launch_bounds__(256) row_dot_bf16_vec_kernel(float* __restrict
 __global__ void __launch_bounds__(512) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
                                                             const __nv_bfloat16* __restrict__ qkv, Geometry g,
                                                             int gph_log2) {
+  // The forward kernel that follows may get resident as blocks of this grid
+  // retire (it waits for this grid before touching memory).
+  ptx::grid_dep_launch();
   constexpr int R = 4;
   const int half = g.hd >> 1;
   const int heads = g.NH + g.NKV;

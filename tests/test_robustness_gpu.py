@@ -25,6 +25,58 @@ def test_backward_is_deterministic(lib, dtype, theta):
     assert torch.equal(d1, d2)
 
 
+@pytest.mark.parametrize("theta", [1e6, 0.0])
+def test_benchmark_path_is_deterministic(lib, theta):
+    """Head size 128, four query heads per kv head: the paired-head forward
+    (attn_fwd_ws), and attn_bwd_rot whose dQ kernel hands out work items
+    dynamically; every output element still has one writer and one summation
+    order, so repeated calls are bit-identical."""
+    import torch
+    w = shape_workload(2, 333, 1024, 8, 2, theta, seed=23)
+    qkv_np, dout_np = make_inputs(w, "bf16")
+    qkv, dout = to_device(qkv_np, "bf16"), to_device(dout_np, "bf16")
+    out, lse, fws = lib.forward_ws(qkv, w.NH, w.NKV, theta)
+    out2, lse2, fws2 = lib.forward_ws(qkv, w.NH, w.NKV, theta)
+    d1 = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, theta, qk_rot=fws)
+    d2 = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, theta, qk_rot=fws2)
+    d3 = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, theta)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert torch.equal(d1, d2) and torch.equal(d1, d3)
+
+
+def test_guard_bands_untouched_benchmark_path(lib):
+    """The tile stores of the paired-head forward and of the gradient
+    epilogues clip rows past T: nothing outside the outputs changes."""
+    import torch
+    w = shape_workload(1, 200, 1024, 8, 2, 1e6, seed=24)
+    qkv_np, dout_np = make_inputs(w, "bf16")
+    qkv, dout = to_device(qkv_np, "bf16"), to_device(dout_np, "bf16")
+    pad = 4096
+    canary = -12288.0
+
+    def guarded(n, dt):
+        buf = torch.full((pad + n + pad,), canary, dtype=dt, device="cuda")
+        return buf, buf[pad:pad + n]
+
+    B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
+    out_buf, out = guarded(B * T * C, torch.bfloat16)
+    lse_buf, lse = guarded(B * NH * T, torch.float32)
+    dq_buf, dqkv = guarded(B * T * w.qkv_width, torch.bfloat16)
+    code = lib.DTYPE_BF16
+    fb = lib.attn_fwd_workspace_bytes(B, T, C, NH, NKV, code)
+    fws = torch.empty(fb, dtype=torch.uint8, device="cuda")
+    lib.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, fws, fb)
+    nbytes = lib.attn_bwd_workspace_bytes(B, T, C, NH, NKV, code)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    lib.attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, w.rope_theta, code, fws, ws, nbytes)
+    torch.cuda.synchronize()
+    for buf in (out_buf, lse_buf, dq_buf):
+        host = buf.float().cpu().numpy()
+        assert np.all(host[:pad] == canary) and np.all(host[-pad:] == canary)
+    assert torch.isfinite(out).all() and torch.isfinite(dqkv).all()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_guard_bands_untouched(lib, dtype):
     """Outputs live inside larger buffers filled with a canary; nothing outside
