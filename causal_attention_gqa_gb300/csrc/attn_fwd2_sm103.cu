@@ -258,8 +258,11 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
             // PV_x(j) once group x wrote P_x(j) and V_j landed; the item's
             // first PV overwrites O_x, which the previous item's epilogue
             // must have read.
+            // (V_j is checked once per key tile: every barrier check stalls
+            // this thread, and the tensor pipe with it.)
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full[x]), gk & 1, abort_flag, kWaitLimitNs) &&
-                 ptx::mbar_wait(ptx::smem_u32(&bars->v_full[gk % 2]), (gk >> 1) & 1, abort_flag, kWaitLimitNs);
+                 (x == 1 ||
+                  ptx::mbar_wait(ptx::smem_u32(&bars->v_full[gk % 2]), (gk >> 1) & 1, abort_flag, kWaitLimitNs));
             if (ok && j == 0 && it >= 1)
               ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_free[x]), (it - 1) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
