@@ -10,8 +10,8 @@
 // PV_B(j-1) and S_B(j), and the other way round, so neither the tensor core
 // nor the softmax waits for the other as long as one tile's softmax takes
 // less than two tiles' MMAs.  Warp roles:
-//   warp 0      TMA producer: both Q tiles of an item, then K_j and V_j into
-//               two-stage rings.
+//   warp 0      TMA producer: both Q tiles of an item, then K_j and V_j
+//               together into a two-stage ring (one barrier per key tile).
 //   warp 1      TMEM owner and the single MMA issuer, in the order
 //               S_A(0), S_B(0), then per key tile PV_A(j), S_A(j+1), PV_B(j),
 //               S_B(j+1).
@@ -64,7 +64,7 @@ __device__ __forceinline__ uint32_t tmem_o(int x) { return 256u + 128u * (uint32
 
 struct Fwd2Barriers {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t kv_full[2], kv_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t staged[2], stage_free, drain;
   uint32_t tmem_base;
@@ -117,10 +117,8 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->v_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 4);
       ptx::mbar_init(ptx::smem_u32(&bars->o_done[i]), 1);
@@ -158,7 +156,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
     if (lane == 0) {
       ptx::tma_prefetch_desc(&tm_qk);
       ptx::tma_prefetch_desc(&tm_v);
-      int k_issued = 0, v_issued = 0, q_issued = 0;   // global sequence counters
+      int kv_issued = 0, q_issued = 0;   // global sequence counters
       bool ok = true;
       for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake(it, w0, dw)) {
         const Fwd2Item item = fwd2_item(w, g);
@@ -175,39 +173,31 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
             ptx::tma_load_3d(ptx::smem_u32(sQ + x * Cfg::kTileBytes + a * Cfg::kAtom), &tm_qk,
                              (item.h0 + x) * kHD + 64 * a, item.qt * 128, item.b, qf);
         q_issued = it + 1;
+        // K_j and V_j into one ring stage with one barrier (each barrier the
+        // MMA issuer checks stalls the tensor pipe).
         for (int j = 0; j < n_kv && ok; ++j) {
-          const int gk = k_issued, sk = gk % 2;
-          if (gk >= 2 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[sk]), ((gk >> 1) - 1) & 1, abort_flag,
+          const int gk = kv_issued, st = gk % 2;
+          if (gk >= 2 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[st]), ((gk >> 1) - 1) & 1, abort_flag,
                                                kWaitLimitNs)))
             break;
-          const uint32_t kf = ptx::smem_u32(&bars->k_full[sk]);
-          ptx::mbar_arrive_expect_tx(kf, Cfg::kTileBytes);
+          const uint32_t kvf = ptx::smem_u32(&bars->kv_full[st]);
+          ptx::mbar_arrive_expect_tx(kvf, 2 * Cfg::kTileBytes);
 #pragma unroll
-          for (int a = 0; a < kHD / 64; ++a)
-            ptx::tma_load_3d(ptx::smem_u32(sK + sk * Cfg::kTileBytes + a * Cfg::kAtom), &tm_qk, k_col + 64 * a,
-                             j * 128, item.b, kf);
-          k_issued = gk + 1;
-          const int gv = v_issued, sv = gv % 2;
-          if (gv >= 2 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[sv]), ((gv >> 1) - 1) & 1, abort_flag,
-                                               kWaitLimitNs)))
-            break;
-          const uint32_t vf = ptx::smem_u32(&bars->v_full[sv]);
-          ptx::mbar_arrive_expect_tx(vf, Cfg::kTileBytes);
-#pragma unroll
-          for (int a = 0; a < kHD / 64; ++a)
-            ptx::tma_load_3d(ptx::smem_u32(sV + sv * Cfg::kTileBytes + a * Cfg::kAtom), &tm_v, v_col + 64 * a,
-                             j * 128, item.b, vf);
-          v_issued = gv + 1;
+          for (int a = 0; a < kHD / 64; ++a) {
+            ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtom), &tm_qk, k_col + 64 * a,
+                             j * 128, item.b, kvf);
+            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtom), &tm_v, v_col + 64 * a,
+                             j * 128, item.b, kvf);
+          }
+          kv_issued = gk + 1;
         }
       }
       if (!ok) fail();
       if (*abort_flag) {
         // Let every copy already in flight land before shared memory is released.
         if (q_issued > 0) ptx::mbar_wait(ptx::smem_u32(&bars->q_full), (q_issued - 1) & 1, nullptr, kWaitLimitNs);
-        for (int st = 0; st < 2 && st < k_issued; ++st)
-          ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
-        for (int st = 0; st < 2 && st < v_issued; ++st)
-          ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
+        for (int st = 0; st < 2 && st < kv_issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((kv_issued - 1 - st) >> 1) & 1, nullptr, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -244,12 +234,11 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
         const Fwd2Item item = fwd2_item(w, g);
         const int n_kv = item.qt + 1;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs) &&
-             ptx::mbar_wait(ptx::smem_u32(&bars->k_full[g0 % 2]), (g0 >> 1) & 1, abort_flag, kWaitLimitNs);
+             ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[g0 % 2]), (g0 >> 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_s(0, g0);
         issue_s(1, g0);
-        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[g0 % 2]));
         if (n_kv == 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
         for (int j = 0; j < n_kv && ok; ++j) {
           const int gk = g0 + j;
@@ -258,30 +247,24 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
             // PV_x(j) once group x wrote P_x(j) and V_j landed; the item's
             // first PV overwrites O_x, which the previous item's epilogue
             // must have read.
-            // (V_j is checked once per key tile: every barrier check stalls
-            // this thread, and the tensor pipe with it.)
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full[x]), gk & 1, abort_flag, kWaitLimitNs) &&
-                 (x == 1 ||
-                  ptx::mbar_wait(ptx::smem_u32(&bars->v_full[gk % 2]), (gk >> 1) & 1, abort_flag, kWaitLimitNs));
+            // (V_j landed with K_j, checked before the score MMAs.)
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full[x]), gk & 1, abort_flag, kWaitLimitNs);
             if (ok && j == 0 && it >= 1)
               ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_free[x]), (it - 1) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv(x, gk, j == 0);
-            if (x == 1) ptx::mma_commit(ptx::smem_u32(&bars->v_empty[gk % 2]));
+            if (x == 1) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[gk % 2]));   // last reader of K_j, V_j
             if (j == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->o_done[x]));
             // S_x(j+1) after PV_x(j): it overwrites P_x(j).
             if (j + 1 < n_kv) {
               if (x == 0 &&
-                  !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[(gk + 1) % 2]), ((gk + 1) >> 1) & 1, abort_flag,
-                                        kWaitLimitNs)))
+                  !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[(gk + 1) % 2]), ((gk + 1) >> 1) & 1,
+                                        abort_flag, kWaitLimitNs)))
                 break;
               ptx::tc_fence_after();
               issue_s(x, gk + 1);
-              if (x == 1) {
-                ptx::mma_commit(ptx::smem_u32(&bars->k_empty[(gk + 1) % 2]));
-                if (j + 1 == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
-              }
+              if (x == 1 && j + 1 == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
             }
           }
         }
