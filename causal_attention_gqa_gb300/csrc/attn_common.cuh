@@ -61,15 +61,18 @@ __device__ __forceinline__ float rope_angle(int t, float f_hi, float f_lo) {
   return r + lo;
 }
 
+// The rounding steps are spelled out (one product, then one fused
+// multiply-add) so that every kernel that rotates a row gets the same bits,
+// whatever the compiler would contract.
 __device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0, float& y1) {
-  y0 = x0 * c - x1 * s;
-  y1 = x1 * c + x0 * s;
+  y0 = __fmaf_rn(x0, c, __fmul_rn(-x1, s));
+  y1 = __fmaf_rn(x1, c, __fmul_rn(x0, s));
 }
 
 // Adjoint (inverse) rotation: R^T applied to a gradient pair.
 __device__ __forceinline__ void rope_pair_transpose(float g0, float g1, float c, float s, float& y0, float& y1) {
-  y0 = g0 * c + g1 * s;
-  y1 = g1 * c - g0 * s;
+  y0 = __fmaf_rn(g0, c, __fmul_rn(g1, s));
+  y1 = __fmaf_rn(g1, c, __fmul_rn(-g0, s));
 }
 
 // ---------------------------------------------------------------------------

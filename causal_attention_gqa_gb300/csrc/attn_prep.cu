@@ -64,106 +64,101 @@ __global__ void __launch_bounds__(256) row_dot_bf16_vec_kernel(float* __restrict
   }
 }
 
-// Rotated Q/K copy.  Thread u of a block owns unit u of a token row: 8
-// consecutive NEOX pairs of one head (heads 0..NH-1 are query heads,
-// NH..NH+NKV-1 kv heads; K heads follow Q heads at column C in qkv, so head
-// `head` sits at column head*hd in both arrays).  The block walks groups of
-// R consecutive token rows with a block stride; all 2R loads of a group are
-// issued before the first is used (the kernel is HBM-bound).
+// Rotated Q/K copy.  One thread per unit (token row, chunk of up to 4 heads,
+// group of 8 consecutive NEOX pairs): it forms the 8 angles of its pairs at
+// its row once and applies them to each head of its chunk (heads 0..NH-1 are
+// query heads, NH..NH+NKV-1 kv heads; K heads follow Q heads at column C in
+// qkv, so head `head` sits at column head*hd in both arrays).  All loads of
+// a unit are issued before the first is used (the kernel is HBM-bound); the
+// units of one token row are adjacent threads.
 // dst[b,t,head*hd + ...] = rotated qkv[b,t,head*hd + ...].
-__global__ void __launch_bounds__(512) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
-                                                            const __nv_bfloat16* __restrict__ qkv, Geometry g,
-                                                            int gph_log2) {
+constexpr int kRopeHeadsPerThread = 4;
+__global__ void __launch_bounds__(256, 3) rope_qk_bf16_kernel(__nv_bfloat16* __restrict__ dst,
+                                                               const __nv_bfloat16* __restrict__ qkv, Geometry g,
+                                                               int gph_log2, int n_units) {
   // The forward kernel that follows may get resident as blocks of this grid
   // retire (it waits for this grid before touching memory).
   ptx::grid_dep_launch();
-  constexpr int R = 4;
+  constexpr int HC = kRopeHeadsPerThread;
   const int half = g.hd >> 1;
   const int heads = g.NH + g.NKV;
-  const int upr = heads << gph_log2;               // units per token row
-  const int rows = g.B * g.T, dst_w = heads * g.hd;
-  const int n_groups = (rows + R - 1) / R;
-  for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
-    const int row0 = grp * R;
-    const int nr = min(R, rows - row0);
-    for (int u = threadIdx.x; u < upr; u += blockDim.x) {
-      const int head = u >> gph_log2, gi = u & ((1 << gph_log2) - 1);
-      const int col = head * g.hd + gi * 8;
-      uint4 x0[R], x1[R];
+  const int n_chunks = (heads + HC - 1) / HC;
+  const int dst_w = heads * g.hd;
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
+    const int gi = u & ((1 << gph_log2) - 1);
+    const int rc = u >> gph_log2;
+    const int row = rc / n_chunks, h0 = (rc - row * n_chunks) * HC;
+    const int nh = min(HC, heads - h0);
+    const int t = row % g.T;
+    const __nv_bfloat16* src = qkv + (size_t)row * g.W + h0 * g.hd + gi * 8;
+    uint4 x0[HC], x1[HC];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (r < nr) {
-          const __nv_bfloat16* src = qkv + (size_t)(row0 + r) * g.W + col;
-          x0[r] = *reinterpret_cast<const uint4*>(src);
-          x1[r] = *reinterpret_cast<const uint4*>(src + half);
-        }
+    for (int k = 0; k < HC; ++k) {
+      if (k < nh) {
+        x0[k] = *reinterpret_cast<const uint4*>(src + k * g.hd);
+        x1[k] = *reinterpret_cast<const uint4*>(src + k * g.hd + half);
       }
-      float f_hi[8], f_lo[8];
+    }
+    float cs[8], sn[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        f_hi[e] = g.rope_f_hi[gi * 8 + e];
-        f_lo[e] = g.rope_f_lo[gi * 8 + e];
+    for (int e = 0; e < 8; ++e) __sincosf(rope_angle(t, g.rope_f_hi[gi * 8 + e], g.rope_f_lo[gi * 8 + e]), &sn[e], &cs[e]);
+    __nv_bfloat16* out = dst + (size_t)row * dst_w + h0 * g.hd + gi * 8;
+#pragma unroll
+    for (int k = 0; k < HC; ++k) {
+      if (k >= nh) break;
+      const uint32_t a[4] = {x0[k].x, x0[k].y, x0[k].z, x0[k].w}, c[4] = {x1[k].x, x1[k].y, x1[k].z, x1[k].w};
+      uint32_t ya[4], yc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float y00, y01, y10, y11;
+        rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), cs[2 * q], sn[2 * q], y00, y10);
+        rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), cs[2 * q + 1], sn[2 * q + 1], y01, y11);
+        ya[q] = pack_bf16x2(y00, y01);
+        yc[q] = pack_bf16x2(y10, y11);
       }
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (r >= nr) break;
-        const int row = row0 + r;
-        const int t = row % g.T;
-        const uint32_t a[4] = {x0[r].x, x0[r].y, x0[r].z, x0[r].w}, c[4] = {x1[r].x, x1[r].y, x1[r].z, x1[r].w};
-        uint32_t ya[4], yc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float s0, c0, s1, c1, y00, y01, y10, y11;
-          __sincosf(rope_angle(t, f_hi[2 * q], f_lo[2 * q]), &s0, &c0);
-          __sincosf(rope_angle(t, f_hi[2 * q + 1], f_lo[2 * q + 1]), &s1, &c1);
-          rope_pair(bf16_lo(a[q]), bf16_lo(c[q]), c0, s0, y00, y10);
-          rope_pair(bf16_hi(a[q]), bf16_hi(c[q]), c1, s1, y01, y11);
-          ya[q] = pack_bf16x2(y00, y01);
-          yc[q] = pack_bf16x2(y10, y11);
-        }
-        __nv_bfloat16* out = dst + (size_t)row * dst_w + col;
-        *reinterpret_cast<uint4*>(out) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-        *reinterpret_cast<uint4*>(out + half) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
-      }
+      *reinterpret_cast<uint4*>(out + k * g.hd) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+      *reinterpret_cast<uint4*>(out + k * g.hd + half) = make_uint4(yc[0], yc[1], yc[2], yc[3]);
     }
   }
 }
 
-// bf16 backward prologue, one launch.  Block-stride over pairs of token rows
-// (b, t), (b, t+1) of the flattened B*T rows; for each pair:
-//  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout of both
-//    rows; the hd/8 lanes of a head sum their partials with shuffles and one
-//    of them writes the row-table entries -lse[b,h,t] * log2(e) and -D[b,h,t]
-//    with D = dO . O (two tables per (b, h)): the two per-row values the
-//    backward's elementwise steps use, already in the form they enter the
-//    exponent and the dS difference;
+// bf16 backward prologue, one launch.  Block-stride over groups of four
+// token rows of the flattened B*T rows; for each group:
+//  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout of the
+//    four rows; the hd/8 lanes of a head sum their partials with shuffles and
+//    one of them writes -D[b,h,t] with D = dO . O into the second row table
+//    of (b, h);
 //  * (RoPE only) threads 0..(NH+NKV)*hd/16-1 each rotate 8 NEOX pairs of one
-//    Q or K head of both rows into the workspace copy.
-// Every load of a pair of rows is issued before the first of them is used,
-// so that each thread keeps several 16-byte loads in flight (the kernel is
-// bound by HBM latency and bandwidth, not arithmetic).
-// Afterwards the table rows T..Tp-1 of every (b, h) are cleared, so that whole
-// 64-row tiles of the table can be copied.  All index arithmetic is 32-bit
+//    Q or K head of the four rows into the workspace copy.
+// Every load of a group is issued before the first of them is used, so that
+// each thread keeps several 16-byte loads in flight (the kernel is bound by
+// HBM latency and bandwidth, not arithmetic).
+// Afterwards the first row table, -lse[b,h,t] * log2(e), is written from lse
+// along t, and the rows T..Tp-1 of both tables are cleared, so that whole
+// 64-row tiles of the tables can be copied.  The two tables hold the per-row
+// values the backward's elementwise steps use, already in the form they
+// enter the exponent and the dS difference.  All index arithmetic is 32-bit
 // with shifts: hd/8 and hd/16 are powers of two.
-__global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float* __restrict__ LD, const uint4* __restrict__ out,
+template <bool ROPE>
+__global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(float* __restrict__ LD, const uint4* __restrict__ out,
                                                                  const uint4* __restrict__ dout,
                                                                  const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
                                                                  int* __restrict__ item_counter,
                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
-                                                                 int vph_log2, int rope) {
+                                                                 int vph_log2) {
   // out is written by the forward that may still be finishing (programmatic
   // launch): wait for it, then let the dK/dV kernel get resident.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   if (blockIdx.x == 0 && threadIdx.x == 0) *item_counter = 0;
-  constexpr int R = 2;                            // token rows per iteration
+  constexpr int R = 4;                            // token rows per iteration
   const int vph = 1 << vph_log2;                  // 16-byte chunks per head (hd / 8)
   const int dot_units = g.C >> 3;                 // chunks per token row
   const int dot_threads = (dot_units + 31) & ~31;  // whole warps take part in the shuffles
   const int gph_log2 = vph_log2 - 1;              // 8-pair groups per head (hd / 16), log2
   const int heads = g.NH + g.NKV, half = g.hd >> 1;
-  const int rope_units = rope ? heads << gph_log2 : 0;
+  const int rope_units = ROPE ? heads << gph_log2 : 0;
   const int rows = g.B * g.T, Tp = row_table_rows(g.T);
   const int rot_w = heads * g.hd;
   const int n_groups = (rows + R - 1) / R;
@@ -192,7 +187,6 @@ __global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float* __rest
           const int row = row0 + r;
           const int b = row / g.T, t = row - b * g.T;
           const int bh = b * g.NH + (c >> vph_log2);
-          LD[(size_t)(2 * bh) * Tp + t] = -lse[(size_t)bh * g.T + t] * 1.4426950408889634f;
           LD[(size_t)(2 * bh + 1) * Tp + t] = -acc;
         }
       }
@@ -232,11 +226,17 @@ __global__ void __launch_bounds__(256, 4) bwd_prologue_bf16_kernel(float* __rest
       }
     }
   }
-  // Table padding rows T..Tp-1 of both tables of every (b, h).
-  const int pad = Tp - g.T, n_pad = 2 * g.B * g.NH * pad;
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n_pad; k += gridDim.x * blockDim.x) {
-    const int tab = k / pad;
-    LD[(size_t)tab * Tp + g.T + (k - tab * pad)] = 0.f;
+  // The -lse * log2(e) table of every (b, h), read and written along t
+  // (coalesced on both sides), and the padding rows T..Tp-1 of both tables.
+  const int n_tab = g.B * g.NH * Tp;
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n_tab; k += gridDim.x * blockDim.x) {
+    const int bh = k / Tp, t = k - bh * Tp;
+    if (t < g.T) {
+      LD[(size_t)(2 * bh) * Tp + t] = -lse[(size_t)bh * g.T + t] * 1.4426950408889634f;
+    } else {
+      LD[(size_t)(2 * bh) * Tp + t] = 0.f;
+      LD[(size_t)(2 * bh + 1) * Tp + t] = 0.f;
+    }
   }
 }
 
@@ -247,12 +247,17 @@ cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, co
   const int vph = g.hd / 8;  // 8 or 16
   int vph_log2 = 0;
   while ((1 << vph_log2) < vph) ++vph_log2;
-  const int groups = (g.B * g.T + 1) / 2;           // pairs of token rows
-  const int blocks = groups < 152 * 4 ? groups : 152 * 4;  // 4 resident 256-thread blocks per SM
+  const int groups = (g.B * g.T + 3) / 4;           // groups of four token rows
+  const int per_sm = rot != nullptr ? 3 : 4;         // resident 256-thread blocks per SM
+  const int blocks = groups < 152 * per_sm ? groups : 152 * per_sm;
   prof_begin(kKernelBwdPrologue, stream);
-  cudaError_t e = launch_pdl(bwd_prologue_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
-                             (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter,
-                             (const __nv_bfloat16*)qkv, g, vph_log2, rot != nullptr ? 1 : 0);
+  cudaError_t e = rot != nullptr
+                      ? launch_pdl(bwd_prologue_bf16_kernel<true>, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
+                                   (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter,
+                                   (const __nv_bfloat16*)qkv, g, vph_log2)
+                      : launch_pdl(bwd_prologue_bf16_kernel<false>, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
+                                   (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter,
+                                   (const __nv_bfloat16*)qkv, g, vph_log2);
   prof_end(kKernelBwdPrologue, stream);
   return e;
 }
@@ -277,14 +282,15 @@ cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Ge
 cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, cudaStream_t stream) {
   int gph_log2 = 0;                                   // log2(hd / 16)
   while ((16 << gph_log2) < g.hd) ++gph_log2;
-  const int upr = (g.NH + g.NKV) << gph_log2;
-  const int threads = upr >= 512 ? 512 : (upr + 31) / 32 * 32;
-  const int groups = (g.B * g.T + 3) / 4;
-  const int per_sm = 2048 / threads;                  // resident blocks per SM by thread count
-  const int cap = 152 * (per_sm > 0 ? per_sm : 1);
-  const int blocks = groups < cap ? groups : cap;
+  const int heads = g.NH + g.NKV;
+  const long long units = (long long)g.B * g.T * ((heads + kRopeHeadsPerThread - 1) / kRopeHeadsPerThread)
+                          << gph_log2;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long need = (units + 255) / 256;
+  const int blocks = (int)(need < 152 * 3 ? need : 152 * 3);   // 3 resident 256-thread blocks per SM
   prof_begin(kKernelRopeQK, stream);
-  rope_qk_bf16_kernel<<<blocks, threads, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g, gph_log2);
+  rope_qk_bf16_kernel<<<blocks, 256, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g, gph_log2,
+                                                  (int)units);
   prof_end(kKernelRopeQK, stream);
   return cudaGetLastError();
 }
