@@ -101,14 +101,13 @@ int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtyp
     return ATTN_ERR_BAD_SHAPE;
   switch (dtype) {
     case ATTN_DTYPE_F32:
+    case ATTN_DTYPE_TF32:   // float32 storage and the 1e-4 bar: the exact float32 kernels
       if (hd > 128) return ATTN_ERR_UNSUPPORTED;
       break;
     case ATTN_DTYPE_BF16:
       if (hd != 64 && hd != 128) return ATTN_ERR_UNSUPPORTED;
       if ((long long)((T + 127) / 128) * B * NH > INT_MAX) return ATTN_ERR_BAD_SHAPE;
       break;
-    case ATTN_DTYPE_TF32:
-      return ATTN_ERR_UNSUPPORTED;
     default:
       return ATTN_ERR_BAD_ARGUMENT;
   }
@@ -202,7 +201,7 @@ int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH
   if (st != ATTN_OK) return st;
   if (!out || !lse || !qkv) return ATTN_ERR_NULL_POINTER;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == ATTN_DTYPE_F32) {
+  if (dtype == ATTN_DTYPE_F32 || dtype == ATTN_DTYPE_TF32) {
     if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(qkv)) & 3u)
       return ATTN_ERR_MISALIGNED;
     SimtArgs a{};
@@ -283,7 +282,7 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* Drow = static_cast<float*>(workspace);
-  if (dtype == ATTN_DTYPE_F32) {
+  if (dtype == ATTN_DTYPE_F32 || dtype == ATTN_DTYPE_TF32) {
     if ((reinterpret_cast<uintptr_t>(dqkv) | reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(out) |
          reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(lse)) & 3u)
       return ATTN_ERR_MISALIGNED;

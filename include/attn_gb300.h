@@ -64,7 +64,9 @@ extern "C" {
 typedef enum {
   /* float32 tensors, exact float32 arithmetic on CUDA cores. */
   ATTN_DTYPE_F32 = 0,
-  /* float32 tensors on tensor cores; reserved, currently ATTN_ERR_UNSUPPORTED. */
+  /* float32 tensors held to the same 1e-4 bar as ATTN_DTYPE_F32; the library
+     runs it on the exact float32 kernels (no reduced-precision tensor-core
+     variant is built), so results equal those of ATTN_DTYPE_F32. */
   ATTN_DTYPE_TF32 = 1,
   /* bf16 tensors, tcgen05 tensor-core MMAs with float32 accumulation. */
   ATTN_DTYPE_BF16 = 2

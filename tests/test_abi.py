@@ -70,7 +70,8 @@ def test_workspace_size(cdll):
     ((1, 16, 12, 4, 4, 1e4, 0), -2),     # odd head size with RoPE
     ((1, 16, 1024, 4, 4, 0.0, 0), -3),   # hd 256 unsupported
     ((1, 16, 128, 4, 4, 0.0, 2), -3),    # bf16 needs hd 64 or 128 (hd 32 here)
-    ((1, 16, 512, 4, 4, 0.0, 1), -3),    # TF32 reserved
+    ((1, 16, 1024, 4, 4, 0.0, 1), -3),   # TF32 (float32 kernels): hd 256 unsupported
+    ((1, 16, 512, 4, 4, 0.0, 1), -1),    # TF32 accepted: fails only on the null pointers
     ((1, 16, 512, 4, 4, 0.0, 7), -8),    # unknown dtype
     ((1, 16, 512, 4, 4, float("nan"), 2), -8),
 ])

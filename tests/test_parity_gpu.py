@@ -56,6 +56,29 @@ def test_f32_shapes(lib, B, T, C, NH, NKV, theta):
     check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T), "f32")
 
 
+def test_tf32_dtype_runs_the_float32_kernels(lib):
+    """ATTN_DTYPE_TF32 (float32 tensors, 1e-4 bar) is computed by the exact
+    float32 kernels: bit-identical to ATTN_DTYPE_F32, and within the bar."""
+    import torch
+    from helpers import to_device, to_numpy
+    w = shape_workload(2, 70, 128, 2, 1, 1e6, seed=31)
+    qkv_np, dout_np = make_inputs(w, "f32")
+    qkv, dout = to_device(qkv_np, "f32"), to_device(dout_np, "f32")
+    res = {}
+    for code in (lib.DTYPE_F32, lib.DTYPE_TF32):
+        out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta, dtype=code)
+        dqkv = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta, dtype=code)
+        torch.cuda.synchronize()
+        res[code] = (out, lse, dqkv)
+    for a, b in zip(res[lib.DTYPE_F32], res[lib.DTYPE_TF32]):
+        assert torch.equal(a, b)
+    out, lse, dqkv = res[lib.DTYPE_TF32]
+    ref_dqkv, aux = oracle.attention_backward(qkv_np, dout_np, w.C, w.NH, w.NKV, w.rope_theta, return_aux=True)
+    errs = {"out": rel_err(to_numpy(out), aux["out"]), "lse": rel_err(to_numpy(lse), aux["lse"]),
+            "dqkv": rel_err(to_numpy(dqkv), ref_dqkv)}
+    assert all(v <= TOL["f32"] for v in errs.values()), errs
+
+
 # ------------------------------------------------------------------ bf16 forward
 @pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
     (1, 1, 128, 1, 1, 0.0), (1, 128, 128, 1, 1, 0.0), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6),

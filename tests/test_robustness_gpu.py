@@ -127,8 +127,8 @@ def test_invalid_arguments_launch_nothing(lib):
     with pytest.raises(AttnError) as ei:   # misaligned bf16 pointer
         lib.attn_fwd(out.data_ptr() + 2, lse, qkv, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_BF16)
     assert ei.value.status == -4
-    with pytest.raises(AttnError) as ei:   # TF32 reserved
-        lib.attn_fwd(out, lse, qkv, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_TF32)
+    with pytest.raises(AttnError) as ei:   # TF32 runs the float32 kernels: hd 256 unsupported
+        lib.attn_fwd(out, lse, qkv, 1, 128, 256, 1, 1, 0.0, lib.DTYPE_TF32)
     assert ei.value.status == -3
     with pytest.raises(AttnError) as ei:   # workspace too small
         lib.attn_bwd(qkv, qkv, out, out, lse, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_BF16, qkv, 16)
