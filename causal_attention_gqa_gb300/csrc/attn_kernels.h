@@ -43,6 +43,9 @@ struct SimtArgs {
   const float* Drow;  // bwd: [B,NH,T] row dots
 };
 cudaError_t simt_launch(const SimtArgs& a, cudaStream_t stream);
+// Register-tiled float32 kernels (head size 64, 16-byte aligned tensors).
+bool simt_tiled_supported(const SimtArgs& a);
+cudaError_t simt_tiled_launch(const SimtArgs& a, cudaStream_t stream);
 size_t simt_max_smem_bytes(int hd);
 
 // ------------------------------------------------------------ backward prologue

@@ -398,6 +398,7 @@ cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t simt_launch(const SimtArgs& a, cudaStream_t stream) {
+  if (simt_tiled_supported(a)) return simt_tiled_launch(a, stream);
   if (a.g.hd <= 32) return launch_simt<1>(a, stream);
   if (a.g.hd <= 64) return launch_simt<2>(a, stream);
   return launch_simt<4>(a, stream);

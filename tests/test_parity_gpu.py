@@ -56,6 +56,44 @@ def test_f32_shapes(lib, B, T, C, NH, NKV, theta):
     check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T), "f32")
 
 
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    # head size 64: the register-tiled float32 kernels (64 x 64 tiles):
+    # T = 1, one exact tile, ragged tails, GQA groups of 2 and 3
+    (1, 1, 64, 1, 1, 1e6), (1, 64, 64, 1, 1, 0.0), (2, 130, 256, 4, 2, 1e6), (3, 200, 384, 6, 2, 1e4),
+])
+def test_f32_head64_tiled(lib, B, T, C, NH, NKV, theta):
+    check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 17), "f32")
+
+
+def test_f32_head64_unaligned_tensors(lib):
+    """Float32 tensors only 4-byte aligned go to the row-per-warp kernels
+    (the tiled ones move 16-byte pieces); both meet the bar."""
+    import torch
+    from helpers import to_numpy
+    w = shape_workload(1, 100, 128, 2, 1, 1e6, seed=41)
+    qkv_np, dout_np = make_inputs(w, "f32")
+
+    def shifted(a):
+        flat = torch.zeros(a.size + 1, dtype=torch.float32, device="cuda")
+        v = flat[1:].view(a.shape)
+        v.copy_(torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)))
+        return v
+
+    qkv, dout = shifted(qkv_np), shifted(dout_np)
+    out = shifted(np.zeros((w.B, w.T, w.C)))
+    lse = torch.empty((w.B, w.NH, w.T), dtype=torch.float32, device="cuda")
+    dqkv = shifted(np.zeros(qkv_np.shape))
+    lib.attn_fwd(out, lse, qkv, w.B, w.T, w.C, w.NH, w.NKV, w.rope_theta, lib.DTYPE_F32)
+    nb = lib.attn_bwd_workspace_bytes(w.B, w.T, w.C, w.NH, w.NKV, lib.DTYPE_F32)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    lib.attn_bwd(dqkv, qkv, out, dout, lse, w.B, w.T, w.C, w.NH, w.NKV, w.rope_theta, lib.DTYPE_F32, ws, nb)
+    torch.cuda.synchronize()
+    ref_dqkv, aux = oracle.attention_backward(qkv_np, dout_np, w.C, w.NH, w.NKV, w.rope_theta, return_aux=True)
+    errs = {"out": rel_err(to_numpy(out), aux["out"]), "lse": rel_err(to_numpy(lse), aux["lse"]),
+            "dqkv": rel_err(to_numpy(dqkv), ref_dqkv)}
+    assert all(v <= TOL["f32"] for v in errs.values()), errs
+
+
 def test_tf32_dtype_runs_the_float32_kernels(lib):
     """ATTN_DTYPE_TF32 (float32 tensors, 1e-4 bar) is computed by the exact
     float32 kernels: bit-identical to ATTN_DTYPE_F32, and within the bar."""
