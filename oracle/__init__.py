@@ -13,4 +13,5 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_backward,
     attention_sampled,
+    attention_decode,
 )

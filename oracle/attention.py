@@ -288,3 +288,45 @@ def attention_sampled(qkv, dout, C: int, NH: int, NKV: int, rope_theta: float,
         dv_rows[(b, kh)] = dv_acc
     return {"out_rows": out_rows, "lse_rows": lse_rows, "dq_rows": dq_rows,
             "dk_rows": dk_rows, "dv_rows": dv_rows}
+
+
+# --------------------------------------------------------------------------
+# Single-query (decode) attention over a KV cache
+# --------------------------------------------------------------------------
+def attention_decode(q, k_cache, v_cache, seq_lens):
+    """One new query per batch row against the cached keys and values.
+
+    The per-position form of the forward ("CUDA C microgpt",
+    attention_forward_kernel: one query at position pos_id against the keys
+    0 .. pos_id), with the grouped heads of "nanoeuler -- CUDA kernels"
+    (query head h reads kv head h / (NH/NKV)).
+
+    q [B, NH, hd]: the new token's queries, already rotated at its position
+    when RoPE is in use.  k_cache, v_cache [B, Lmax, NKV, hd]: keys (already
+    rotated at their positions) and values of positions 0 .. Lmax-1.
+    seq_lens [B], 1 <= len <= Lmax: the query attends to cache rows
+    0 .. len-1 (its own key and value included).
+
+    Returns out [B, NH, hd] and lse [B, NH] (natural log of the sum of the
+    exponentials of the scaled scores), float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_cache = np.asarray(k_cache, dtype=np.float64)
+    v_cache = np.asarray(v_cache, dtype=np.float64)
+    B, NH, hd = q.shape
+    NKV = k_cache.shape[2]
+    grp = NH // NKV
+    scale = 1.0 / np.sqrt(hd)
+    out = np.zeros((B, NH, hd))
+    lse = np.zeros((B, NH))
+    for b in range(B):
+        n = int(seq_lens[b])
+        for h in range(NH):
+            kh = h // grp
+            s = scale * (k_cache[b, :n, kh] @ q[b, h])     # scores of the n visible keys
+            m = s.max()
+            e = np.exp(s - m)
+            l = e.sum()
+            out[b, h] = (e / l) @ v_cache[b, :n, kh]
+            lse[b, h] = m + np.log(l)
+    return out, lse
