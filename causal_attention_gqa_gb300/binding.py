@@ -83,6 +83,10 @@ def load() -> ctypes.CDLL:
     lib.attn_abi_version.argtypes = []
     lib.attn_abi_version.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.attn_decode_workspace_bytes.restype = sz
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+    lib.attn_decode.restype = i
     lib.attn_bwd_noalloc.restype = i
     lib.attn_profile_start.argtypes = []
     lib.attn_profile_start.restype = i
@@ -164,6 +168,34 @@ def attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
     _check(st, "attn_bwd_rot")
 
 
+def attn_decode_workspace_bytes(B, NH, NKV, hd, max_len, dtype) -> int:
+    return int(load().attn_decode_workspace_bytes(B, NH, NKV, hd, max_len, int(dtype)))
+
+
+def attn_decode(out, lse, q, k_cache, v_cache, seq_lens, B, NH, NKV, hd, max_len, dtype, workspace,
+                workspace_bytes, stream=None) -> None:
+    st = load().attn_decode(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, NH,
+                            NKV, hd, max_len, int(dtype), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "attn_decode")
+
+
+def decode(q, k_cache, v_cache, seq_lens, dtype=None, stream=None, workspace=None):
+    """Single-query attention over a KV cache: q [B,NH,hd], k_cache/v_cache
+    [B,max_len,NKV,hd], seq_lens int32 [B] on the device.  Returns (out, lse)."""
+    import torch
+    B, NH, hd = q.shape
+    max_len, NKV = k_cache.shape[1], k_cache.shape[2]
+    code = dtype_code(q) if dtype is None else dtype
+    if workspace is None:
+        nbytes = attn_decode_workspace_bytes(B, NH, NKV, hd, max_len, code)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, NH), dtype=torch.float32, device=q.device)
+    attn_decode(out, lse, q, k_cache, v_cache, seq_lens, B, NH, NKV, hd, max_len, code, workspace,
+                workspace.numel(), stream)
+    return out, lse
+
+
 def attn_bwd_noalloc(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, stream=None) -> None:
     """attn_bwd without a workspace argument, for callers that cannot allocate
     device memory; uses the library's built-in scratch buffer (see the header
@@ -185,7 +217,7 @@ def attn_selftest_wait_timeout(limit_ns: int) -> int:
     return v.value
 
 
-N_KERNEL_IDS = 9
+N_KERNEL_IDS = 10
 
 
 def attn_profile_start() -> None:

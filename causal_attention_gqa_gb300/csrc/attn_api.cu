@@ -347,6 +347,55 @@ extern "C" int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const 
                   stream);
 }
 
+// ---------------------------------------------------------------- decode
+namespace {
+int decode_check(int B, int NH, int NKV, int hd, int max_len, int dtype) {
+  if (B < 1 || NH < 1 || NKV < 1 || max_len < 1 || hd < 1) return ATTN_ERR_BAD_SHAPE;
+  if (NH % NKV != 0) return ATTN_ERR_BAD_SHAPE;
+  if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_TF32 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_BAD_ARGUMENT;
+  if (hd != 64 && hd != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long hgroups = (NH / NKV + 3) / 4;
+  if (B > 65535 || (long long)NKV * hgroups > 65535 || (long long)max_len * NKV * hd > (1LL << 40))
+    return ATTN_ERR_BAD_SHAPE;
+  return ATTN_OK;
+}
+}  // namespace
+
+extern "C" size_t attn_decode_workspace_bytes(int B, int NH, int NKV, int hd, int max_len, int dtype) {
+  if (decode_check(B, NH, NKV, hd, max_len, dtype) != ATTN_OK) return 0;
+  return align256(decode_workspace_floats(B, NH, NKV, hd, max_len) * sizeof(float));
+}
+
+extern "C" int attn_decode(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+                           const int* seq_lens, int B, int NH, int NKV, int hd, int max_len, int dtype,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  int st = decode_check(B, NH, NKV, hd, max_len, dtype);
+  if (st != ATTN_OK) return st;
+  if (!out || !lse || !q || !k_cache || !v_cache || !seq_lens) return ATTN_ERR_NULL_POINTER;
+  if (!workspace || ws_bytes < attn_decode_workspace_bytes(B, NH, NKV, hd, max_len, dtype)) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(workspace)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(seq_lens)) & 3u) return ATTN_ERR_MISALIGNED;
+  DecodeArgs a{};
+  a.B = B;
+  a.NH = NH;
+  a.NKV = NKV;
+  a.hd = hd;
+  a.max_len = max_len;
+  a.bf16 = dtype == ATTN_DTYPE_BF16;
+  a.out = out;
+  a.lse = lse;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.lens = seq_lens;
+  a.part = static_cast<float*>(workspace);
+  a.status = status_word();
+  if (!a.status) return ATTN_ERR_CUDA;
+  return from_cuda(decode_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int attn_device_status(int* status, int reset) {
   if (!status) return ATTN_ERR_NULL_POINTER;
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;

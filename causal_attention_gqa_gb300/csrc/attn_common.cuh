@@ -11,6 +11,7 @@ namespace attn {
 // Status codes (mirror attn_status_t of the public header).
 constexpr int kOk = 0;
 constexpr int kErrDeviceTimeout = -7;
+constexpr int kErrBadArgument = -8;
 
 // Geometry of one call.  Packed qkv rows hold Q | K | V column blocks:
 // query head h at h*hd, kv head kh at C + kh*hd (K) and C + NKV*hd + kh*hd

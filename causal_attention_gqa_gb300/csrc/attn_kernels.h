@@ -48,6 +48,24 @@ bool simt_tiled_supported(const SimtArgs& a);
 cudaError_t simt_tiled_launch(const SimtArgs& a, cudaStream_t stream);
 size_t simt_max_smem_bytes(int hd);
 
+// ------------------------------------------------------------ decode
+// Single-query attention over a KV cache (attn_decode).
+struct DecodeArgs {
+  int B, NH, NKV, hd, max_len;
+  bool bf16;
+  void* out;             // [B,NH,hd]
+  float* lse;            // [B,NH]
+  const void* q;         // [B,NH,hd]
+  const void* k_cache;   // [B,max_len,NKV,hd]
+  const void* v_cache;   // [B,max_len,NKV,hd]
+  const int* lens;       // [B], device
+  float* part;           // workspace: per (b, h, chunk) m, l, o[hd]
+  int* status;
+};
+int decode_chunk_rows(int B, int NH, int NKV, int max_len);
+size_t decode_workspace_floats(int B, int NH, int NKV, int hd, int max_len);
+cudaError_t decode_launch(const DecodeArgs& a, cudaStream_t stream);
+
 // ------------------------------------------------------------ backward prologue
 // D[b,h,t] = sum_d dout[b,t,h,d] * out[b,t,h,d] (float32 accumulation).
 cudaError_t launch_row_dot(float* D, const void* out, const void* dout, const Geometry& g, bool bf16,

@@ -17,7 +17,8 @@ enum KernelId {
   kKernelBwdDkdvSimt = 6,
   kKernelBwdDqSimt = 7,
   kKernelBwdPrologue = 8,
-  kKernelCount = 9
+  kKernelDecode = 9,
+  kKernelCount = 10
 };
 
 // Record the start / end of a launch of kernel `id` on `stream` (no-ops while

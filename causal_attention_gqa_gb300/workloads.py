@@ -111,6 +111,20 @@ def make_inputs(w: Workload, dtype: str = "f32"):
     return qkv, dout
 
 
+def make_decode_inputs(B, NH, NKV, hd, max_len, dtype="bf16", seed=11, std=1.0):
+    """Seeded single-query (decode) inputs: q [B,NH,hd], k_cache and v_cache
+    [B,max_len,NKV,hd], float32 arrays already rounded to ``dtype``; N(0, std)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.standard_normal((B, NH, hd), dtype=np.float32) * np.float32(std)
+    k = rng.standard_normal((B, max_len, NKV, hd), dtype=np.float32) * np.float32(std)
+    v = rng.standard_normal((B, max_len, NKV, hd), dtype=np.float32) * np.float32(std)
+    if dtype == "bf16":
+        q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+    elif dtype != "f32":
+        raise ValueError(f"unknown dtype {dtype!r}")
+    return q, k, v
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); returns float32."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)

@@ -202,6 +202,47 @@ ATTN_API int attn_bwd_noalloc(void* dqkv, const void* qkv, const void* out, cons
                               const float* lse, int B, int T, int C, int NH, int NKV,
                               float rope_theta, int dtype, void* stream);
 
+/*
+ * attn_decode -- single-query (decode) attention over a KV cache: one new
+ * token per batch row attends to the cached keys and values of its sequence.
+ * It is the per-position form of the forward ("CUDA C microgpt",
+ * attention_forward_kernel: one query at position pos_id against keys
+ * 0 .. pos_id) with grouped heads ("nanoeuler -- CUDA kernels": query head h
+ * reads kv head h / (NH/NKV)).  For every batch row b and query head h:
+ *   s_j = q[b,h,:] . k_cache[b,j,kh,:] / sqrt(hd)  for j < seq_lens[b],
+ *   out[b,h,:] = sum_j softmax(s)_j v_cache[b,j,kh,:],
+ *   lse[b,h]  = ln sum_j exp(s_j).
+ *
+ * Layouts (dense, row-major, device pointers; element type float for
+ * ATTN_DTYPE_F32 / ATTN_DTYPE_TF32, bf16 for ATTN_DTYPE_BF16; arithmetic in
+ * float32 throughout):
+ *   q        [B, NH, hd]          the new token's queries;
+ *   k_cache  [B, max_len, NKV, hd] keys of positions 0 .. max_len-1;
+ *   v_cache  [B, max_len, NKV, hd] values;
+ *   seq_lens [B] int32, device     visible cache rows per batch row, the new
+ *                                  token's own row included (1 .. max_len);
+ *   out      [B, NH, hd]          written;
+ *   lse      [B, NH] float32       written.
+ * RoPE is the caller's: q is expected rotated at the new token's position and
+ * the cached keys at theirs (a cache holds rotated keys; rotating every cached
+ * key on each step would cost far more than reading it).
+ *
+ * hd must be 64 or 128 (else ATTN_ERR_UNSUPPORTED); NH % NKV == 0.  q, k_cache,
+ * v_cache, out and the workspace must be 16-byte aligned, lse and seq_lens
+ * 4-byte aligned (ATTN_ERR_MISALIGNED).  The workspace (attn_decode_workspace_
+ * bytes(), owned by the caller, contents irrelevant) holds one partial result
+ * per (b, h, chunk of cache rows; the chunk length depends only on the
+ * arguments).  A seq_lens entry outside
+ * [1, max_len] is clamped into it and ATTN_ERR_BAD_ARGUMENT is recorded in
+ * the device status word (attn_device_status).  Asynchronous on `stream`;
+ * deterministic (the chunks of a head are merged in a fixed order).
+ */
+ATTN_API size_t attn_decode_workspace_bytes(int B, int NH, int NKV, int hd, int max_len, int dtype);
+ATTN_API int attn_decode(void* out, float* lse, const void* q, const void* k_cache,
+                         const void* v_cache, const int* seq_lens, int B, int NH, int NKV,
+                         int hd, int max_len, int dtype, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* attn_strerror -- static description of a status code; never NULL. */
 ATTN_API const char* attn_strerror(int status);
 
@@ -232,8 +273,8 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
  *   and the launch count in launches[id] (either array may be NULL).
  * attn_kernel_name -- short name of kernel id (see attn_profile.h ids:
  *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 rope_qk,
- *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt, 8 bwd_prologue); "unknown"
- *   otherwise.
+ *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt, 8 bwd_prologue, 9 decode (both
+ *   of its kernels)); "unknown" otherwise.
  */
 ATTN_API int attn_profile_start(void);
 ATTN_API int attn_profile_stop(double* total_ms, int* launches, int n);
