@@ -17,6 +17,11 @@ the work of all ranks divided by the slowest rank's time.
 
 `--impl reference` times the float64 CPU oracle instead (rank 0 only), on a
 bounded sample of the same workload: one kv group of one batch row per step.
+
+`--decode B,L,NH,NKV,hd` times attn_decode (one new token per batch row
+against a bf16 KV cache of L rows) instead and prints one JSON line with its
+HBM throughput (cache bytes read per call / device time; L2 flushed between
+calls) against the measured copy bandwidth.
 """
 from __future__ import annotations
 
@@ -50,6 +55,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_block")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", default=None, metavar="B,L,NH,NKV,hd")
     return ap.parse_args()
 
 
@@ -370,8 +376,68 @@ def run_ours(args, w):
     return 0
 
 
+def run_decode(args):
+    """attn_decode on a seeded bf16 cache (all rows visible); HBM GB/s."""
+    import torch
+    from causal_attention_gqa_gb300 import binding
+    from causal_attention_gqa_gb300.workloads import make_decode_inputs
+    B, L, NH, NKV, hd = (int(x) for x in args.decode.split(","))
+    torch.cuda.set_device(0)
+    binding.load()
+    q_np, k_np, v_np = make_decode_inputs(B, NH, NKV, hd, L, "bf16", seed=2024)
+    q = torch.from_numpy(q_np).to("cuda", torch.bfloat16)
+    k = torch.from_numpy(k_np).to("cuda", torch.bfloat16)
+    v = torch.from_numpy(v_np).to("cuda", torch.bfloat16)
+    del q_np, k_np, v_np
+    lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    nbytes = binding.attn_decode_workspace_bytes(B, NH, NKV, hd, L, binding.DTYPE_BF16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((B, NH), dtype=torch.float32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def call():
+        binding.attn_decode(out, lse, q, k, v, lens, B, NH, NKV, hd, L, binding.DTYPE_BF16, ws, nbytes)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    steps = min(args.steps, 200)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(0)
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    cache_bytes = 2 * B * L * NKV * hd * 2
+    io_bytes = cache_bytes + 2 * B * NH * hd * 2 + B * NH * 4
+    peaks, src = load_peaks()
+    gbs = io_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "decode attention HBM GB/s on 1 GB300", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode", "B": B, "L": L, "NH": NH, "NKV": NKV, "hd": hd,
+                   "l2": "flushed between calls (256 MiB write outside the timed events)",
+                   "timing": "median of per-call CUDA events"},
+        "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{src} hbm_gbs (copy)", "algorithmic_bytes_per_launch": io_bytes},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.decode:
+        return run_decode(args)
     from causal_attention_gqa_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -10,8 +10,8 @@
 // bf16 cache at four query heads per kv head).
 //
 // Split over the cache length (flash-decoding): a CTA takes a chunk of cache
-// rows (a multiple of 32, sized so that the grid is about one wave of three
-// CTAs per SM) of one kv head and up to kHeads of its query heads, keeps
+// rows (a multiple of 32, sized by a small wave-count cost model) of one kv
+// head and up to kHeads of its query heads, keeps
 // an online softmax per head, and writes a partial (max m, sum l, unnormalised
 // output o) to the workspace; a second kernel merges the chunks of each
 // (batch row, head) in chunk order, so the result is deterministic.
@@ -134,23 +134,20 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
   for (int rb = r0 + 8 * warp; rb < r1; rb += 8 * kWarpsD) {
     Raw kn[8], vn[8];
     if (rb + 8 * kWarpsD < r1) fetch(rb + 8 * kWarpsD, kn, vn);
-    float kv[8][EPL], vv[8][EPL];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      Vec<T, EPL>::widen(kr[r], kv[r]);
-      Vec<T, EPL>::widen(vr[r], vv[r]);
-    }
-    // Partial dot products, value index 4 r + h.
+    // Partial dot products, value index 4 r + h (rows widened one at a time).
     float v[32];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < 8; ++r) {
+      float kv[EPL];
+      Vec<T, EPL>::widen(kr[r], kv);
 #pragma unroll
       for (int h = 0; h < kHeads; ++h) {
         float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc = fmaf(qv[h][e], kv[r][e], acc);
+        for (int e = 0; e < EPL; ++e) acc = fmaf(qv[h][e], kv[e], acc);
         v[4 * r + h] = acc;
       }
+    }
     // Butterfly: after the stage with offset o, a lane keeps the half of its
     // values selected by its bit o and adds the partner's copy of that half.
 #pragma unroll
@@ -192,10 +189,12 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
     for (int r = 0; r < 8; ++r) {
       const float4 pr = *reinterpret_cast<const float4*>(&p_sh[warp][0][4 * r]);
       const float pv[4] = {pr.x, pr.y, pr.z, pr.w};
+      float vrow[EPL];
+      Vec<T, EPL>::widen(vr[r], vrow);
 #pragma unroll
       for (int h = 0; h < kHeads; ++h)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pv[h], vv[r][e], o[h][e]);
+        for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pv[h], vrow[e], o[h][e]);
     }
     __syncwarp();
 #pragma unroll
@@ -311,16 +310,28 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-// Cache rows per chunk: a multiple of 32 (four warps x 8-row blocks), at
-// least 64, chosen so that the split grid is about one wave.
+// Cache rows per chunk: a multiple of 32 (four warps x 8-row blocks), from a
+// small cost model: the split grid runs in waves of kTargetCtas CTAs, a CTA
+// costs its rows plus a fixed ~96 rows' worth (queries, merge of its warps,
+// partial store), and the merge kernel ~2 rows' worth per chunk.  Too few
+// chunks leave SMs idle (a grid of slightly more than one wave waits on its
+// tail); too many make CTAs mostly overhead.
 int decode_chunk_rows(int B, int NH, int NKV, int max_len) {
   const long long hgroups = (NH / NKV + kHeads - 1) / kHeads;
   const long long units = (long long)B * NKV * hgroups;             // CTAs per chunk index
-  long long chunk = ((long long)max_len * units + kTargetCtas - 1) / kTargetCtas;
-  chunk = (chunk + 31) / 32 * 32;
-  if (chunk < 64) chunk = 64;
-  if (chunk > (long long)max_len) chunk = ((long long)max_len + 31) / 32 * 32;
-  return (int)chunk;
+  long long best_chunk = ((long long)max_len + 31) / 32 * 32, best_cost = -1;
+  // Candidate split counts 1, 2, 3, ... growing by about 1/8 each step.
+  for (long long want = 1; want <= ((long long)max_len + 31) / 32; want += (want + 7) / 8) {
+    const long long chunk = (((long long)max_len + want - 1) / want + 31) / 32 * 32;
+    const long long n_split = ((long long)max_len + chunk - 1) / chunk;
+    const long long waves = (units * n_split + kTargetCtas - 1) / kTargetCtas;
+    const long long cost = waves * (chunk + 96) + 2 * n_split;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_chunk = chunk;
+    }
+  }
+  return (int)best_chunk;
 }
 
 size_t decode_workspace_floats(int B, int NH, int NKV, int hd, int max_len) {
