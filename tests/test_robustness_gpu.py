@@ -147,3 +147,49 @@ def test_bounded_wait_expires_and_device_stays_usable(lib):
 
 def test_no_device_errors_recorded(lib):
     assert lib.attn_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("dtype,theta,fwd_ws", [("bf16", 1e6, True), ("bf16", 0.0, False), ("f32", 1e6, False)])
+def test_cuda_graph_capture_replays_identically(lib, dtype, theta, fwd_ws):
+    """A forward + backward captured into a CUDA graph (the launch-overhead
+    remedy for small problems) replays bit-identically to eager calls: no
+    entry point synchronises, allocates or reads host state on the stream."""
+    import torch
+    w = shape_workload(2, 200, 1024 if dtype == "bf16" else 128, 8, 2, theta, seed=51)
+    qkv_np, dout_np = make_inputs(w, dtype)
+    qkv, dout = to_device(qkv_np, dtype), to_device(dout_np, dtype)
+    code = lib.DTYPE_BF16 if dtype == "bf16" else lib.DTYPE_F32
+    B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
+    out = torch.empty((B, T, C), dtype=qkv.dtype, device="cuda")
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device="cuda")
+    dqkv = torch.empty_like(qkv)
+    wsb = lib.attn_bwd_workspace_bytes(B, T, C, NH, NKV, code)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    fwsb = lib.attn_fwd_workspace_bytes(B, T, C, NH, NKV, code)
+    fws = torch.empty(max(fwsb, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        s = stream.cuda_stream
+        if fwd_ws:
+            lib.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, theta, code, fws, fwsb, s)
+            lib.attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, theta, code, fws, ws, wsb, s)
+        else:
+            lib.attn_fwd(out, lse, qkv, B, T, C, NH, NKV, theta, code, s)
+            lib.attn_bwd(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, theta, code, ws, wsb, s)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    ref = [out.clone(), lse.clone(), dqkv.clone()]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for t in (out, lse, dqkv):
+        t.zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1]) and torch.equal(dqkv, ref[2])
+    assert lib.attn_device_status() == 0
