@@ -34,7 +34,15 @@ MUTATIONS = {
     "dv_not_summed_over_group": ("dv[b, :, kh] += P.T @ dO", "dv[b, :, kh] = P.T @ dO"),
     "v_column_offset": ("V = x[:, :, C + NKV * hd:]", "V = x[:, :, C:C + NKV * hd]"),
     "dk_not_unrotated": ("        dk = rope_rotate_transpose(dk, rope_theta)\n", ""),
+    # single-query (decode) attention, pinned by test_oracle_decode_pins.py
+    "decode_gqa_head_mapping_modulo": ("            kh = h // grp\n            s = scale",
+                                       "            kh = h % NKV\n            s = scale"),
+    "decode_length_off_by_one": ("n = int(seq_lens[b])", "n = int(seq_lens[b]) - 1"),
+    "decode_missing_score_scale": ("s = scale * (k_cache[b, :n, kh] @ q[b, h])", "s = (k_cache[b, :n, kh] @ q[b, h])"),
+    "decode_lse_drops_max": ("lse[b, h] = m + np.log(l)", "lse[b, h] = np.log(l)"),
+    "decode_reads_past_length": ("(e / l) @ v_cache[b, :n, kh]", "(e / l) @ v_cache[b, -n:, kh]"),
 }
+PIN_FILE = {name: "test_oracle_decode_pins.py" for name in MUTATIONS if name.startswith("decode_")}
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
@@ -54,7 +62,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env["PYTHONPATH"] = os.pathsep.join([str(tmp_path), ROOT, env.get("PYTHONPATH", "")])
     res = subprocess.run(
         [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-         "--rootdir", str(tmp_path), os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+         "--rootdir", str(tmp_path), os.path.join(ROOT, "tests", PIN_FILE.get(name, "test_oracle_pins.py"))],
         cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=600)
     assert mark.exists(), "the pin suite did not import the mutant oracle"
     assert res.returncode != 0, f"pins did not catch mutation {name}:\n{res.stdout[-2000:]}"
