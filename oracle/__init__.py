@@ -10,6 +10,8 @@ from .attention import (  # noqa: F401
     rope_cos_sin,
     rope_rotate,
     rope_rotate_transpose,
+    rope_rotate_interleaved,
+    rope_rotate_interleaved_transpose,
     attention_forward,
     attention_backward,
     attention_sampled,

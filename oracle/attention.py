@@ -140,9 +140,54 @@ def rope_rotate_transpose(g: np.ndarray, theta: float, positions=None) -> np.nda
     return g * cos + (g * sin) @ rot.T
 
 
-def _rotated_qk(Q, K, rope_theta):
+def rope_rotate_interleaved(x: np.ndarray, theta: float, positions=None) -> np.ndarray:
+    """The interleaved (GPT-J) form of "nanoeuler -- CUDA kernels",
+    rope_kernel: pair (2i, 2i+1) of each head turns by angle t * freq_i with
+    freq_i = theta^(-2i/hd):
+        y[2i]   = x[2i] cos - x[2i+1] sin,
+        y[2i+1] = x[2i] sin + x[2i+1] cos.
+    Axis -3 is the position (or indexes ``positions``), the last axis hd."""
+    x = np.asarray(x, dtype=np.float64)
+    T, hd = x.shape[-3], x.shape[-1]
+    pos = np.arange(T) if positions is None else np.asarray(positions)
+    i = np.arange(hd // 2, dtype=np.float64)
+    freq = float(theta) ** (-2.0 * i / hd)
+    ang = pos.astype(np.float64)[:, None] * freq[None, :]          # [T, hd/2]
+    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x0 * cos - x1 * sin
+    y[..., 1::2] = x0 * sin + x1 * cos
+    return y
+
+
+def rope_rotate_interleaved_transpose(g: np.ndarray, theta: float, positions=None) -> np.ndarray:
+    """Inverse (transposed) interleaved rotation, rope_kernel's inverse=1:
+        y[2i] = g[2i] cos + g[2i+1] sin,  y[2i+1] = -g[2i] sin + g[2i+1] cos."""
+    g = np.asarray(g, dtype=np.float64)
+    T, hd = g.shape[-3], g.shape[-1]
+    pos = np.arange(T) if positions is None else np.asarray(positions)
+    i = np.arange(hd // 2, dtype=np.float64)
+    freq = float(theta) ** (-2.0 * i / hd)
+    ang = pos.astype(np.float64)[:, None] * freq[None, :]
+    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    g0, g1 = g[..., 0::2], g[..., 1::2]
+    y = np.empty_like(g)
+    y[..., 0::2] = g0 * cos + g1 * sin
+    y[..., 1::2] = -g0 * sin + g1 * cos
+    return y
+
+
+def _rope_fns(interleaved: bool):
+    if interleaved:
+        return rope_rotate_interleaved, rope_rotate_interleaved_transpose
+    return rope_rotate, rope_rotate_transpose
+
+
+def _rotated_qk(Q, K, rope_theta, interleaved=False):
     if rope_theta and rope_theta > 0:
-        return rope_rotate(Q, rope_theta), rope_rotate(K, rope_theta)
+        rot, _ = _rope_fns(interleaved)
+        return rot(Q, rope_theta), rot(K, rope_theta)
     return Q, K
 
 
@@ -166,11 +211,12 @@ def _head_probs(q, k, scale, rows=None):
     return E / l[:, None], m + np.log(l)
 
 
-def attention_forward(qkv, C: int, NH: int, NKV: int, rope_theta: float = 0.0):
-    """out [B,T,C] and lse [B,NH,T] (natural log of the scaled scores), float64."""
+def attention_forward(qkv, C: int, NH: int, NKV: int, rope_theta: float = 0.0, rope_interleaved: bool = False):
+    """out [B,T,C] and lse [B,NH,T] (natural log of the scaled scores), float64.
+    rope_interleaved selects the interleaved (GPT-J) pairing instead of NEOX."""
     hd, grp, _ = _dims(C, NH, NKV)
     Q, K, V = split_qkv(qkv, C, NH, NKV)
-    Qr, Kr = _rotated_qk(Q, K, rope_theta)
+    Qr, Kr = _rotated_qk(Q, K, rope_theta, rope_interleaved)
     B, T = Q.shape[:2]
     scale = 1.0 / np.sqrt(hd)
     out = np.zeros((B, T, C))
@@ -184,7 +230,7 @@ def attention_forward(qkv, C: int, NH: int, NKV: int, rope_theta: float = 0.0):
 
 
 def attention_backward(qkv, dout, C: int, NH: int, NKV: int, rope_theta: float = 0.0,
-                       return_aux: bool = False):
+                       return_aux: bool = False, rope_interleaved: bool = False):
     """Gradient of L = sum(dout * out) with respect to the packed qkv, float64.
 
     Returns dqkv [B, T, (NH + 2*NKV)*hd]; with ``return_aux`` also a dict with
@@ -192,7 +238,7 @@ def attention_backward(qkv, dout, C: int, NH: int, NKV: int, rope_theta: float =
     """
     hd, grp, _ = _dims(C, NH, NKV)
     Q, K, V = split_qkv(qkv, C, NH, NKV)
-    Qr, Kr = _rotated_qk(Q, K, rope_theta)
+    Qr, Kr = _rotated_qk(Q, K, rope_theta, rope_interleaved)
     dO_all = np.asarray(dout, dtype=np.float64)
     B, T = Q.shape[:2]
     scale = 1.0 / np.sqrt(hd)
@@ -217,7 +263,10 @@ def attention_backward(qkv, dout, C: int, NH: int, NKV: int, rope_theta: float =
             dq[b, :, h] = scale * (dS @ k)
             dk[b, :, kh] += scale * (dS.T @ q)
             dv[b, :, kh] += P.T @ dO
-    if rope_theta and rope_theta > 0:
+    if rope_theta and rope_theta > 0 and rope_interleaved:
+        dq = rope_rotate_interleaved_transpose(dq, rope_theta)
+        dk = rope_rotate_interleaved_transpose(dk, rope_theta)
+    elif rope_theta and rope_theta > 0:
         dq = rope_rotate_transpose(dq, rope_theta)
         dk = rope_rotate_transpose(dk, rope_theta)
     dqkv = pack_qkv(dq, dk, dv)

@@ -41,8 +41,15 @@ MUTATIONS = {
     "decode_missing_score_scale": ("s = scale * (k_cache[b, :n, kh] @ q[b, h])", "s = (k_cache[b, :n, kh] @ q[b, h])"),
     "decode_lse_drops_max": ("lse[b, h] = m + np.log(l)", "lse[b, h] = np.log(l)"),
     "decode_reads_past_length": ("(e / l) @ v_cache[b, :n, kh]", "(e / l) @ v_cache[b, -n:, kh]"),
+    # interleaved (GPT-J) RoPE, pinned by test_oracle_rope_interleaved_pins.py
+    "gptj_rotation_sign": ("    y[..., 0::2] = x0 * cos - x1 * sin\n", "    y[..., 0::2] = x0 * cos + x1 * sin\n"),
+    "gptj_frequency_exponent": ("    freq = float(theta) ** (-2.0 * i / hd)\n    ang = pos.astype(np.float64)[:, None] * freq[None, :]          # [T, hd/2]",
+                                "    freq = float(theta) ** (-1.0 * i / hd)\n    ang = pos.astype(np.float64)[:, None] * freq[None, :]          # [T, hd/2]"),
+    "gptj_pairs_swapped": ("    x0, x1 = x[..., 0::2], x[..., 1::2]", "    x1, x0 = x[..., 0::2], x[..., 1::2]"),
+    "gptj_adjoint_sign": ("    y[..., 1::2] = -g0 * sin + g1 * cos", "    y[..., 1::2] = g0 * sin + g1 * cos"),
 }
 PIN_FILE = {name: "test_oracle_decode_pins.py" for name in MUTATIONS if name.startswith("decode_")}
+PIN_FILE.update({name: "test_oracle_rope_interleaved_pins.py" for name in MUTATIONS if name.startswith("gptj_")})
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
