@@ -30,6 +30,7 @@ from .build import LIB_PATH
 DTYPE_F32 = 0
 DTYPE_TF32 = 1
 DTYPE_BF16 = 2
+FLAG_ROPE_INTERLEAVED = 0x100   # OR-ed into dtype: GPT-J (interleaved) RoPE pairing
 
 _STATUS_NAMES = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL_POINTER", -2: "ATTN_ERR_BAD_SHAPE", -3: "ATTN_ERR_UNSUPPORTED",
@@ -244,7 +245,8 @@ def dtype_code(t) -> int:
     raise TypeError(f"unsupported tensor dtype {t.dtype}")
 
 
-def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None, workspace=None):
+def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None, workspace=None,
+            rope_interleaved: bool = False):
     """out, lse = attention forward of packed qkv [B, T, (NH+2*NKV)*hd].
 
     With ``workspace`` (a uint8 tensor, or True to allocate one of
@@ -253,7 +255,7 @@ def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=
     B, T, W = qkv.shape
     hd = W // (NH + 2 * NKV)
     C = NH * hd
-    code = dtype_code(qkv) if dtype is None else dtype
+    code = (dtype_code(qkv) if dtype is None else dtype) | (FLAG_ROPE_INTERLEAVED if rope_interleaved else 0)
     out = torch.empty((B, T, C), dtype=qkv.dtype, device=qkv.device)
     lse = torch.empty((B, NH, T), dtype=torch.float32, device=qkv.device)
     if workspace is None:
@@ -266,28 +268,29 @@ def forward(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=
     return out, lse
 
 
-def forward_ws(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None):
+def forward_ws(qkv, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None,
+               rope_interleaved: bool = False):
     """(out, lse, workspace) through attn_fwd_ws; the workspace holds the
     rotated Q/K that backward(..., qk_rot=workspace) can reuse."""
     import torch
     B, T, W = qkv.shape
     hd = W // (NH + 2 * NKV)
-    code = dtype_code(qkv) if dtype is None else dtype
+    code = (dtype_code(qkv) if dtype is None else dtype) | (FLAG_ROPE_INTERLEAVED if rope_interleaved else 0)
     nbytes = attn_fwd_workspace_bytes(B, T, NH * hd, NH, NKV, code)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
-    out, lse = forward(qkv, NH, NKV, rope_theta, dtype, stream, workspace=ws)
+    out, lse = forward(qkv, NH, NKV, rope_theta, code, stream, workspace=ws)
     return out, lse, ws
 
 
 def backward(qkv, out, dout, lse, NH: int, NKV: int, rope_theta: float = 0.0, dtype=None, stream=None,
-             workspace=None, qk_rot=None):
+             workspace=None, qk_rot=None, rope_interleaved: bool = False):
     """dqkv = attention backward; allocates the workspace unless one is given.
     With ``qk_rot`` (the workspace of the attn_fwd_ws call that made out/lse)
     the call goes through attn_bwd_rot, else attn_bwd."""
     import torch
     B, T, W = qkv.shape
     C = out.shape[2]
-    code = dtype_code(qkv) if dtype is None else dtype
+    code = (dtype_code(qkv) if dtype is None else dtype) | (FLAG_ROPE_INTERLEAVED if rope_interleaved else 0)
     nbytes = attn_bwd_workspace_bytes(B, T, C, NH, NKV, code)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)

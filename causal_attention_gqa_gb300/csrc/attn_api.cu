@@ -88,7 +88,12 @@ bool make_tmap(CUtensorMap* m, const void* base, int width, int T, int B, int ro
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtype, Geometry* g) {
+// `dtype` may carry ATTN_FLAG_ROPE_INTERLEAVED; it is stripped here (the
+// element type stays in `dtype`) and recorded in the geometry.
+int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int& dtype, Geometry* g) {
+  const int flags = dtype & ~0xFF;
+  if (flags & ~ATTN_FLAG_ROPE_INTERLEAVED) return ATTN_ERR_BAD_ARGUMENT;
+  dtype &= 0xFF;
   if (B < 1 || T < 1 || C < 1 || NH < 1 || NKV < 1) return ATTN_ERR_BAD_SHAPE;
   if (C % NH != 0 || NH % NKV != 0) return ATTN_ERR_BAD_SHAPE;
   if (!std::isfinite(rope_theta)) return ATTN_ERR_BAD_ARGUMENT;
@@ -121,6 +126,7 @@ int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int dtyp
   g->W = (int)W;
   g->scale = (float)(1.0 / std::sqrt((double)hd));
   g->rope_theta = rope ? rope_theta : 0.f;
+  g->rope_interleaved = (rope && (flags & ATTN_FLAG_ROPE_INTERLEAVED)) ? 1 : 0;
   for (int i = 0; i < 64; ++i) {
     double f = 0.0;
     if (rope && i < hd / 2) f = std::exp(-2.0 * i * std::log((double)rope_theta) / hd);
@@ -214,6 +220,9 @@ int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH
   }
   if (!aligned16(out) || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
   const bool pre_rotate = workspace != nullptr && g.rope_theta > 0.f;
+  // The attention kernel's own rotation (attn_fwd, bf16) pairs NEOX columns
+  // only; the interleaved pairing goes through the rotation pass of attn_fwd_ws.
+  if (g.rope_interleaved && !pre_rotate) return ATTN_ERR_UNSUPPORTED;
   if (pre_rotate && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
   Tc05FwdArgs a{};
   a.g = g;
@@ -252,9 +261,10 @@ extern "C" size_t attn_fwd_workspace_bytes(int B, int T, int C, int NH, int NKV,
 extern "C" int attn_fwd_ws(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV,
                            float rope_theta, int dtype, void* workspace, size_t ws_bytes, void* stream) {
   Geometry g;
-  int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
+  int type = dtype;   // dtype keeps its flags for fwd_impl
+  int st = check_shape(B, T, C, NH, NKV, rope_theta, type, &g);
   if (st != ATTN_OK) return st;
-  const size_t need = attn_fwd_workspace_bytes(B, T, C, NH, NKV, dtype);
+  const size_t need = attn_fwd_workspace_bytes(B, T, C, NH, NKV, type);
   if (need > 0 && (!workspace || ws_bytes < need)) return ATTN_ERR_WORKSPACE;
   return fwd_impl(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, need > 0 ? workspace : nullptr, ws_bytes,
                   stream);

@@ -92,10 +92,20 @@ __device__ __forceinline__ void stage_grad_row(uint32_t acc, float s, bool rope,
       lo[e] = __float_as_uint(y0);
       hi[e] = __float_as_uint(y1);
     }
+    if (!g.rope_interleaved) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      *reinterpret_cast<uint4*>(stile + sw128_chunk(row, c0 + 8 * q)) = pack8(&lo[8 * q], 1.f);
-      *reinterpret_cast<uint4*>(stile + sw128_chunk(row, HALF + c0 + 8 * q)) = pack8(&hi[8 * q], 1.f);
+      for (int q = 0; q < 4; ++q) {
+        *reinterpret_cast<uint4*>(stile + sw128_chunk(row, c0 + 8 * q)) = pack8(&lo[8 * q], 1.f);
+        *reinterpret_cast<uint4*>(stile + sw128_chunk(row, HALF + c0 + 8 * q)) = pack8(&hi[8 * q], 1.f);
+      }
+    } else {
+      // Interleaved pairing: pair i goes back to columns 2i and 2i + 1.
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t w[8] = {lo[4 * q], hi[4 * q], lo[4 * q + 1], hi[4 * q + 1],
+                               lo[4 * q + 2], hi[4 * q + 2], lo[4 * q + 3], hi[4 * q + 3]};
+        *reinterpret_cast<uint4*>(stile + sw128_chunk(row, 2 * c0 + 8 * q)) = pack8(w, 1.f);
+      }
     }
   }
 }

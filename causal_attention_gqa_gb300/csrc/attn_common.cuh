@@ -23,6 +23,12 @@ struct Geometry {
   int W;         // packed row width (NH + 2*NKV) * hd
   float scale;   // 1 / sqrt(hd)
   float rope_theta;  // <= 0: no RoPE
+  // 0: NEOX pairs (i, i + hd/2); 1: interleaved (GPT-J) pairs (2i, 2i+1).  The
+  // kernels work on NEOX-ordered rotated rows either way: an interleaved head
+  // row is read with its even elements first (pair i moves to slots i and
+  // i + hd/2), and gradients are written back through the same permutation.
+  // Scores q . k are unchanged by a permutation shared by Q and K.
+  int rope_interleaved;
   // RoPE inverse frequencies theta^(-2i/hd), i < hd/2, as float head + tail
   // (computed once on the host in double precision).
   float rope_f_hi[64];
@@ -85,6 +91,25 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The eight pairs 8 gi .. 8 gi + 7 of one bf16 head row as two 16-byte words:
+// x0 holds the first elements of the pairs, x1 the second ones.  NEOX pairs
+// (i, i + hd/2) are two contiguous runs; interleaved pairs (2i, 2i+1) are the
+// sixteen elements 16 gi .. 16 gi + 15, split into even and odd ones.
+__device__ __forceinline__ void load_rope_pairs(const __nv_bfloat16* head_row, int gi, int half, bool interleaved,
+                                                uint4& x0, uint4& x1) {
+  if (!interleaved) {
+    x0 = *reinterpret_cast<const uint4*>(head_row + gi * 8);
+    x1 = *reinterpret_cast<const uint4*>(head_row + half + gi * 8);
+    return;
+  }
+  const uint4 u = *reinterpret_cast<const uint4*>(head_row + gi * 16);
+  const uint4 v = *reinterpret_cast<const uint4*>(head_row + gi * 16 + 8);
+  auto even = [](uint32_t a, uint32_t b) { return (a & 0xFFFFu) | (b << 16); };
+  auto odd = [](uint32_t a, uint32_t b) { return (a >> 16) | (b & 0xFFFF0000u); };
+  x0 = make_uint4(even(u.x, u.y), even(u.z, u.w), even(v.x, v.y), even(v.z, v.w));
+  x1 = make_uint4(odd(u.x, u.y), odd(u.z, u.w), odd(v.x, v.y), odd(v.z, v.w));
 }
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);

@@ -90,15 +90,11 @@ __global__ void __launch_bounds__(256, 3) rope_qk_bf16_kernel(__nv_bfloat16* __r
     const int row = rc / n_chunks, h0 = (rc - row * n_chunks) * HC;
     const int nh = min(HC, heads - h0);
     const int t = row % g.T;
-    const __nv_bfloat16* src = qkv + (size_t)row * g.W + h0 * g.hd + gi * 8;
+    const __nv_bfloat16* src = qkv + (size_t)row * g.W + h0 * g.hd;
     uint4 x0[HC], x1[HC];
 #pragma unroll
-    for (int k = 0; k < HC; ++k) {
-      if (k < nh) {
-        x0[k] = *reinterpret_cast<const uint4*>(src + k * g.hd);
-        x1[k] = *reinterpret_cast<const uint4*>(src + k * g.hd + half);
-      }
-    }
+    for (int k = 0; k < HC; ++k)
+      if (k < nh) load_rope_pairs(src + k * g.hd, gi, half, g.rope_interleaved != 0, x0[k], x1[k]);
     float cs[8], sn[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) __sincosf(rope_angle(t, g.rope_f_hi[gi * 8 + e], g.rope_f_lo[gi * 8 + e]), &sn[e], &cs[e]);
@@ -198,8 +194,7 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
       for (int r = 0; r < R; ++r) {
         if (r < nr) {
           const __nv_bfloat16* src = qkv + (size_t)(row0 + r) * g.W + head * g.hd;  // K heads follow Q heads
-          x0[r] = *reinterpret_cast<const uint4*>(src + gi * 8);
-          x1[r] = *reinterpret_cast<const uint4*>(src + half + gi * 8);
+          load_rope_pairs(src, gi, half, g.rope_interleaved != 0, x0[r], x1[r]);
         }
       }
 #pragma unroll

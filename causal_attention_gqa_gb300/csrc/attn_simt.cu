@@ -53,7 +53,9 @@ __device__ void load_head_tile(float* dst, const float* src, const Geometry& g, 
       const float* row = src + ((size_t)b * g.T + t) * g.W + col0;
       float s, c;
       sincosf(rope_angle(t, f_hi[i], f_lo[i]), &s, &c);
-      rope_pair(row[i], row[i + half], c, s, y0, y1);
+      // Interleaved pair i is (2i, 2i+1); it lands in NEOX slots i, i + hd/2.
+      const int i0 = g.rope_interleaved ? 2 * i : i, i1 = g.rope_interleaved ? 2 * i + 1 : i + half;
+      rope_pair(row[i0], row[i1], c, s, y0, y1);
     }
     dst[r * pitch + i] = y0;
     dst[r * pitch + i + half] = y1;
@@ -87,8 +89,8 @@ __device__ void store_grad_tile(float* dqkv, const float* tile, const Geometry& 
     sincosf(rope_angle(t, f_hi[i], f_lo[i]), &s, &c);
     rope_pair_transpose(tile[r * pitch + i], tile[r * pitch + i + half], c, s, y0, y1);
     float* row = dqkv + ((size_t)b * g.T + t) * g.W + col0;
-    row[i] = y0;
-    row[i + half] = y1;
+    row[g.rope_interleaved ? 2 * i : i] = y0;
+    row[g.rope_interleaved ? 2 * i + 1 : i + half] = y1;
   }
 }
 

@@ -65,8 +65,16 @@ __device__ void stage_rows(float* dst, const float* src, int width, const Geomet
     float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
     if (t < g.T) {
       const float* row = src + ((size_t)b * g.T + t) * width + col0;
-      const float4 a = *reinterpret_cast<const float4*>(row + 4 * c);
-      const float4 e = *reinterpret_cast<const float4*>(row + half + 4 * c);
+      float4 a, e;
+      if (!g.rope_interleaved) {
+        a = *reinterpret_cast<const float4*>(row + 4 * c);
+        e = *reinterpret_cast<const float4*>(row + half + 4 * c);
+      } else {            // pairs (2i, 2i+1), i = 4c .. 4c+3: elements 8c .. 8c+7
+        const float4 u = *reinterpret_cast<const float4*>(row + 8 * c);
+        const float4 w = *reinterpret_cast<const float4*>(row + 8 * c + 4);
+        a = make_float4(u.x, u.z, w.x, w.z);
+        e = make_float4(u.y, u.w, w.y, w.w);
+      }
       const float x0[4] = {a.x, a.y, a.z, a.w}, x1[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -239,8 +247,13 @@ __device__ void store_rows(float* dqkv, const float* tile, const Geometry& g, in
       rope_pair_transpose(g0[k], g1[k], co, sn, y0[k], y1[k]);
     }
     float* row = dqkv + ((size_t)b * g.T + t) * g.W + col0;
-    *reinterpret_cast<float4*>(row + 4 * c) = make_float4(y0[0], y0[1], y0[2], y0[3]);
-    *reinterpret_cast<float4*>(row + half + 4 * c) = make_float4(y1[0], y1[1], y1[2], y1[3]);
+    if (!g.rope_interleaved) {
+      *reinterpret_cast<float4*>(row + 4 * c) = make_float4(y0[0], y0[1], y0[2], y0[3]);
+      *reinterpret_cast<float4*>(row + half + 4 * c) = make_float4(y1[0], y1[1], y1[2], y1[3]);
+    } else {
+      *reinterpret_cast<float4*>(row + 8 * c) = make_float4(y0[0], y1[0], y0[1], y1[1]);
+      *reinterpret_cast<float4*>(row + 8 * c + 4) = make_float4(y0[2], y1[2], y0[3], y1[3]);
+    }
   }
 }
 

@@ -72,6 +72,20 @@ typedef enum {
   ATTN_DTYPE_BF16 = 2
 } attn_dtype_t;
 
+/*
+ * ATTN_FLAG_ROPE_INTERLEAVED -- OR-ed into the dtype argument of attn_fwd_ws,
+ * attn_bwd, attn_bwd_rot, attn_bwd_noalloc (and, for the float32 dtypes,
+ * attn_fwd) to use the interleaved (GPT-J) RoPE pairing of "nanoeuler -- CUDA
+ * kernels", rope_kernel -- pair (2i, 2i+1) of each head turns by t*theta^(-2i/hd):
+ *   y[2i] = x[2i] cos - x[2i+1] sin,   y[2i+1] = x[2i] sin + x[2i+1] cos
+ * -- instead of the NEOX pairing (i, i + hd/2).  Ignored when rope_theta <= 0.
+ * attn_fwd with ATTN_DTYPE_BF16 rotates inside its attention kernel, which
+ * pairs NEOX columns only, and returns ATTN_ERR_UNSUPPORTED with this flag
+ * (use attn_fwd_ws).  The *_workspace_bytes() functions accept and ignore it.
+ * A forward and its backward must use the same pairing.
+ */
+#define ATTN_FLAG_ROPE_INTERLEAVED 0x100
+
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_NULL_POINTER = -1,    /* a required pointer is NULL */

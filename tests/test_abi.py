@@ -73,6 +73,8 @@ def test_workspace_size(cdll):
     ((1, 16, 1024, 4, 4, 0.0, 1), -3),   # TF32 (float32 kernels): hd 256 unsupported
     ((1, 16, 512, 4, 4, 0.0, 1), -1),    # TF32 accepted: fails only on the null pointers
     ((1, 16, 512, 4, 4, 0.0, 7), -8),    # unknown dtype
+    ((1, 16, 512, 4, 4, 0.0, 2 | 0x200), -8),   # unknown flag bit
+    ((1, 16, 512, 4, 4, 1e4, 2 | 0x100), -1),   # interleaved RoPE flag accepted (null pointers)
     ((1, 16, 512, 4, 4, float("nan"), 2), -8),
 ])
 def test_forward_rejects_invalid_shapes(cdll, args, code):
