@@ -16,4 +16,5 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_sampled,
     attention_decode,
+    qkv_projection,
 )

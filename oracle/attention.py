@@ -379,3 +379,30 @@ def attention_decode(q, k_cache, v_cache, seq_lens):
             out[b, h] = (e / l) @ v_cache[b, :n, kh]
             lse[b, h] = m + np.log(l)
     return out, lse
+
+
+# --------------------------------------------------------------------------
+# QKV projection feeding the attention (for the fused projection epilogue)
+# --------------------------------------------------------------------------
+def qkv_projection(x, w, T: int, NH: int, NKV: int, rope_theta: float = 0.0, rope_interleaved: bool = False):
+    """The packed QKV projection of the trainers on the pages ("nanoeuler --
+    CUDA kernels": qkv = x W_qkv, row width C + 2 NKV hs, followed by the RoPE
+    passes over the Q and K column blocks).
+
+    x [M, Cm] (M = B*T rows, row m at position m % T), w [N, Cm] with
+    N = (NH + 2*NKV)*hd (output column n of the packed Q | K | V layout reads
+    row n of w).  Returns (qkv [M, N], qk_rot [M, (NH+NKV)*hd]): the
+    unrotated projection, and its Q and K heads rotated at their positions
+    (columns in the natural order of each head), float64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    M = x.shape[0]
+    N = w.shape[0]
+    hd = N // (NH + 2 * NKV)
+    qkv = x @ w.T
+    qk = qkv[:, :(NH + NKV) * hd].reshape(M // T, T, NH + NKV, hd)
+    if rope_theta and rope_theta > 0:
+        rot, _ = _rope_fns(rope_interleaved)
+        qk = rot(qk, rope_theta)
+    return qkv, qk.reshape(M, (NH + NKV) * hd)
