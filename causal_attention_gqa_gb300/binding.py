@@ -85,6 +85,10 @@ def load() -> ctypes.CDLL:
     lib.attn_abi_version.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.attn_qkv_proj.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.attn_qkv_proj.restype = i
+    lib.attn_fwd_rot.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.attn_fwd_rot.restype = i
     lib.attn_decode_workspace_bytes.restype = sz
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
     lib.attn_decode.restype = i
@@ -169,6 +173,35 @@ def attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
     _check(st, "attn_bwd_rot")
 
 
+def attn_qkv_proj(qkv, qk_rot, x, w, B, T, Cm, NH, NKV, hd, rope_theta, flags=0, stream=None) -> None:
+    st = load().attn_qkv_proj(_ptr(qkv), _ptr(qk_rot), _ptr(x), _ptr(w), B, T, Cm, NH, NKV, hd, float(rope_theta),
+                              int(flags), _stream(stream))
+    _check(st, "attn_qkv_proj")
+
+
+def attn_fwd_rot(out, lse, qkv, qk_rot, B, T, C, NH, NKV, rope_theta, dtype, stream=None) -> None:
+    st = load().attn_fwd_rot(_ptr(out), _ptr(lse), _ptr(qkv), _ptr(qk_rot), B, T, C, NH, NKV, float(rope_theta),
+                             int(dtype), _stream(stream))
+    _check(st, "attn_fwd_rot")
+
+
+def qkv_proj(x, w, T: int, NH: int, NKV: int, rope_theta: float = 0.0, rope_interleaved: bool = False,
+             stream=None):
+    """(qkv, qk_rot) = the QKV projection of x [B*T, Cm] by w [(NH+2NKV)*hd, Cm]
+    (bf16) and the rotated Q/K copy (None when rope_theta <= 0)."""
+    import torch
+    M, Cm = x.shape
+    N = w.shape[0]
+    hd = N // (NH + 2 * NKV)
+    qkv = torch.empty((M // T, T, N), dtype=torch.bfloat16, device=x.device)
+    rot = None
+    if rope_theta > 0:
+        rot = torch.empty(((M * (NH + NKV) * hd * 2 + 255) // 256 * 256,), dtype=torch.uint8, device=x.device)
+    attn_qkv_proj(qkv, rot, x, w, M // T, T, Cm, NH, NKV, hd, rope_theta,
+                  FLAG_ROPE_INTERLEAVED if rope_interleaved else 0, stream)
+    return qkv, rot
+
+
 def attn_decode_workspace_bytes(B, NH, NKV, hd, max_len, dtype) -> int:
     return int(load().attn_decode_workspace_bytes(B, NH, NKV, hd, max_len, int(dtype)))
 
@@ -218,7 +251,7 @@ def attn_selftest_wait_timeout(limit_ns: int) -> int:
     return v.value
 
 
-N_KERNEL_IDS = 10
+N_KERNEL_IDS = 11
 
 
 def attn_profile_start() -> None:

@@ -201,7 +201,7 @@ namespace {
 // the rotated Q/K copy into the workspace, and the attention kernel reads Q
 // and K from there).
 int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV, float rope_theta,
-             int dtype, void* workspace, size_t ws_bytes, void* stream) {
+             int dtype, void* workspace, size_t ws_bytes, void* stream, bool rotated_given = false) {
   Geometry g;
   int st = check_shape(B, T, C, NH, NKV, rope_theta, dtype, &g);
   if (st != ATTN_OK) return st;
@@ -237,7 +237,7 @@ int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH
   if (!make_tmap(&a.tm_qk, qk_src, qk_width, g.T, g.B) || !make_tmap(&a.tm_v, qkv, g.W, g.T, g.B) ||
       !make_tmap(&a.tm_out, out, g.C, g.T, g.B))
     return ATTN_ERR_CUDA;
-  if (pre_rotate) {
+  if (pre_rotate && !rotated_given) {
     cudaError_t e = launch_rope_qk_bf16(workspace, qkv, g, s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
   }
@@ -355,6 +355,55 @@ extern "C" int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const 
                             void* workspace, size_t ws_bytes, void* stream) {
   return bwd_impl(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, qk_rot, workspace, ws_bytes,
                   stream);
+}
+
+// ---------------------------------------------------------------- QKV projection
+extern "C" int attn_qkv_proj(void* qkv, void* qk_rot, const void* x, const void* w, int B, int T, int Cm, int NH,
+                             int NKV, int hd, float rope_theta, int flags, void* stream) {
+  if (B < 1 || T < 1 || Cm < 1 || NH < 1 || NKV < 1 || hd < 1 || NH % NKV != 0) return ATTN_ERR_BAD_SHAPE;
+  if (flags & ~ATTN_FLAG_ROPE_INTERLEAVED) return ATTN_ERR_BAD_ARGUMENT;
+  if (!std::isfinite(rope_theta)) return ATTN_ERR_BAD_ARGUMENT;
+  if (hd != 64 && hd != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Cm % 8 != 0) return ATTN_ERR_BAD_SHAPE;           // 16-byte rows for the tensor maps
+  const long long M = (long long)B * T, N = (long long)(NH + 2 * NKV) * hd;
+  if (M > INT_MAX / 2 || N > 65535 * 8 || (long long)T > (1LL << 24)) return ATTN_ERR_BAD_SHAPE;
+  if (!qkv || !x || !w) return ATTN_ERR_NULL_POINTER;
+  if (!aligned16(qkv) || !aligned16(x) || !aligned16(w) || (qk_rot && !aligned16(qk_rot))) return ATTN_ERR_MISALIGNED;
+  ProjArgs a{};
+  ProjGeometry& pg = a.pg;
+  pg.M = (int)M;
+  pg.N = (int)N;
+  pg.Cm = Cm;
+  pg.T = T;
+  pg.NQK = (NH + NKV) * hd;
+  pg.hd = hd;
+  pg.rope = rope_theta > 0.f ? 1 : 0;
+  pg.interleaved = (flags & ATTN_FLAG_ROPE_INTERLEAVED) ? 1 : 0;
+  for (int i = 0; i < 64; ++i) {
+    double f = 0.0;
+    if (pg.rope && i < hd / 2) f = std::exp(-2.0 * i * std::log((double)rope_theta) / hd);
+    pg.rope_f_hi[i] = (float)f;
+    pg.rope_f_lo[i] = (float)(f - (double)pg.rope_f_hi[i]);
+  }
+  a.qkv = qkv;
+  a.rot = (pg.rope && qk_rot) ? qk_rot : nullptr;
+  a.status = status_word();
+  a.num_sms = num_sms();
+  if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
+  if (!make_tmap(&a.tm_x, x, Cm, (int)M, 1, 128) || !make_tmap(&a.tm_w, w, Cm, (int)N, 1, 256)) return ATTN_ERR_CUDA;
+  return from_cuda(proj_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int attn_fwd_rot(void* out, float* lse, const void* qkv, const void* qk_rot, int B, int T, int C, int NH,
+                            int NKV, float rope_theta, int dtype, void* stream) {
+  Geometry g;
+  int type = dtype;
+  int st = check_shape(B, T, C, NH, NKV, rope_theta, type, &g);
+  if (st != ATTN_OK) return st;
+  if (type != ATTN_DTYPE_BF16 || g.rope_theta <= 0.f)   // the copy only matters on the bf16 RoPE path
+    return fwd_impl(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, nullptr, 0, stream);
+  if (!qk_rot) return ATTN_ERR_NULL_POINTER;
+  return fwd_impl(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, const_cast<void*>(qk_rot), 0, stream, true);
 }
 
 // ---------------------------------------------------------------- decode

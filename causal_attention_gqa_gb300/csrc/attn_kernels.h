@@ -48,6 +48,27 @@ bool simt_tiled_supported(const SimtArgs& a);
 cudaError_t simt_tiled_launch(const SimtArgs& a, cudaStream_t stream);
 size_t simt_max_smem_bytes(int hd);
 
+// ------------------------------------------------------------ QKV projection
+// qkv = x w^T with the rotated Q/K copy written from the same accumulators.
+struct ProjGeometry {
+  int M, N, Cm, T;   // rows B*T, packed width (NH+2NKV)*hd, input width, sequence length
+  int NQK;           // (NH+NKV)*hd: the Q and K columns (rotated copy width)
+  int hd;
+  int rope;          // rotate (and write the copy) at all
+  int interleaved;   // pairing of the rotation (see Geometry::rope_interleaved)
+  float rope_f_hi[64];
+  float rope_f_lo[64];
+};
+struct ProjArgs {
+  CUtensorMap tm_x, tm_w;
+  void* qkv;
+  void* rot;         // may be null
+  ProjGeometry pg;
+  int* status;
+  int num_sms;
+};
+cudaError_t proj_launch(const ProjArgs& a, cudaStream_t stream);
+
 // ------------------------------------------------------------ decode
 // Single-query attention over a KV cache (attn_decode).
 struct DecodeArgs {

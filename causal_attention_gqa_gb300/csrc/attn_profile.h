@@ -18,7 +18,8 @@ enum KernelId {
   kKernelBwdDqSimt = 7,
   kKernelBwdPrologue = 8,
   kKernelDecode = 9,
-  kKernelCount = 10
+  kKernelProj = 10,
+  kKernelCount = 11
 };
 
 // Record the start / end of a launch of kernel `id` on `stream` (no-ops while

@@ -125,6 +125,15 @@ def make_decode_inputs(B, NH, NKV, hd, max_len, dtype="bf16", seed=11, std=1.0):
     return q, k, v
 
 
+def make_proj_inputs(M, Cm, N, seed=13):
+    """Seeded QKV-projection inputs, bf16-rounded float32 arrays: x [M, Cm]
+    ~ N(0, 1) and w [N, Cm] ~ N(0, 1/Cm) (so the projection is ~ N(0, 1))."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal((M, Cm), dtype=np.float32)
+    w = rng.standard_normal((N, Cm), dtype=np.float32) * np.float32(1.0 / np.sqrt(Cm))
+    return round_to_bf16(x), round_to_bf16(w)
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); returns float32."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)

@@ -257,6 +257,39 @@ ATTN_API int attn_decode(void* out, float* lse, const void* q, const void* k_cac
                          int hd, int max_len, int dtype, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/*
+ * attn_qkv_proj -- the QKV projection that feeds the attention, with the RoPE
+ * rotation fused into its epilogue.  The trainers on the pages project the
+ * layer input into the packed Q | K | V activation with a GEMM and then run
+ * separate RoPE passes over the Q and K column blocks ("nanoeuler -- CUDA
+ * kernels": the qkv matmul, then rope_kernel over the query and kv heads);
+ * here both come out of one kernel:
+ *   qkv[m, n] = sum_k x[m, k] * w[n, k]     m < B*T, n < (NH + 2*NKV)*hd, k < Cm
+ * (bf16 in and out, float32 accumulation; row m is position m % T of
+ * sequence m / T), and, when rope_theta > 0 and qk_rot != NULL, the rotated
+ * copy of its Q and K heads [B*T, (NH+NKV)*hd] bf16, rotated from the float32
+ * accumulators, in the layout attn_fwd_rot / attn_bwd_rot read (the copy the
+ * rotation pass of attn_fwd_ws makes).  `flags` may be
+ * ATTN_FLAG_ROPE_INTERLEAVED (then pass it to the attention calls as well).
+ *   x   [B*T, Cm] bf16, row-major (Cm a multiple of 8);
+ *   w   [(NH+2*NKV)*hd, Cm] bf16, row-major (row n produces output column n);
+ *   qkv [B*T, (NH+2*NKV)*hd] bf16, written.
+ * hd must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).  All pointers
+ * 16-byte aligned; a copy handed to attn_fwd_rot / attn_bwd_rot must be
+ * 256-byte aligned.  Asynchronous on `stream`; deterministic.
+ *
+ * attn_fwd_rot -- attn_fwd (bf16 with RoPE) reading the rotated Q/K from
+ * qk_rot (made by attn_qkv_proj or attn_fwd_ws on the same qkv) instead of
+ * rotating them: no rotation pass.  Other dtypes, or rope_theta <= 0, behave
+ * as attn_fwd and ignore qk_rot.  The library cannot check that qk_rot holds
+ * the rotation of this qkv.
+ */
+ATTN_API int attn_qkv_proj(void* qkv, void* qk_rot, const void* x, const void* w, int B, int T,
+                           int Cm, int NH, int NKV, int hd, float rope_theta, int flags,
+                           void* stream);
+ATTN_API int attn_fwd_rot(void* out, float* lse, const void* qkv, const void* qk_rot, int B,
+                          int T, int C, int NH, int NKV, float rope_theta, int dtype, void* stream);
+
 /* attn_strerror -- static description of a status code; never NULL. */
 ATTN_API const char* attn_strerror(int status);
 
@@ -288,7 +321,7 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
  * attn_kernel_name -- short name of kernel id (see attn_profile.h ids:
  *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 rope_qk,
  *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt, 8 bwd_prologue, 9 decode (both
- *   of its kernels)); "unknown" otherwise.
+ *   of its kernels), 10 qkv_proj); "unknown" otherwise.
  */
 ATTN_API int attn_profile_start(void);
 ATTN_API int attn_profile_stop(double* total_ms, int* launches, int n);
