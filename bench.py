@@ -18,6 +18,10 @@ the work of all ranks divided by the slowest rank's time.
 `--impl reference` times the float64 CPU oracle instead (rank 0 only), on a
 bounded sample of the same workload: one kv group of one batch row per step.
 
+`--proj B,T,Cm,NH,NKV,hd` times attn_qkv_proj (the QKV projection GEMM with
+the rotated Q/K copy in its epilogue, and without the copy), with cuBLAS
+(torch.matmul) on the same GEMM for context, and prints one JSON line.
+
 `--decode B,L,NH,NKV,hd` times attn_decode (one new token per batch row
 against a bf16 KV cache of L rows) instead and prints one JSON line with its
 HBM throughput (cache bytes read per call / device time; L2 flushed between
@@ -56,6 +60,7 @@ def parse_args():
     ap.add_argument("--workload", default="gqa_block")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", default=None, metavar="B,L,NH,NKV,hd")
+    ap.add_argument("--proj", default=None, metavar="B,T,Cm,NH,NKV,hd")
     return ap.parse_args()
 
 
@@ -434,10 +439,64 @@ def run_decode(args):
     return 0
 
 
+def run_proj(args):
+    """attn_qkv_proj on seeded bf16 inputs; TFLOP/s of the GEMM."""
+    import torch
+    from causal_attention_gqa_gb300 import binding
+    from causal_attention_gqa_gb300.workloads import make_proj_inputs
+    B, T, Cm, NH, NKV, hd = (int(v) for v in args.proj.split(","))
+    torch.cuda.set_device(0)
+    binding.load()
+    M, N = B * T, (NH + 2 * NKV) * hd
+    x_np, w_np = make_proj_inputs(M, Cm, N, seed=2025)
+    x = torch.from_numpy(x_np).to("cuda", torch.bfloat16)
+    w = torch.from_numpy(w_np).to("cuda", torch.bfloat16)
+    qkv = torch.empty((B, T, N), dtype=torch.bfloat16, device="cuda")
+    rot = torch.empty((M * (NH + NKV) * hd * 2 + 256,), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    calls = {
+        "fused_rope_copy": lambda: binding.attn_qkv_proj(qkv, rot, x, w, B, T, Cm, NH, NKV, hd, 1e6, 0),
+        "gemm_only": lambda: binding.attn_qkv_proj(qkv, None, x, w, B, T, Cm, NH, NKV, hd, 0.0, 0),
+        "cublas_context": lambda: torch.matmul(x, w.t(), out=qkv.view(M, N)),
+    }
+    steps = min(args.steps, 100)
+    res = {}
+    for name, fn in calls.items():
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        res[name] = {"ms": ms, "tflops": 2.0 * M * N * Cm / (ms * 1e-3) / 1e12}
+    peaks, src = load_peaks()
+    v = res["fused_rope_copy"]["tflops"]
+    line = {
+        "metric": "QKV projection (+ rotated Q/K copy) TFLOP/s on 1 GB300", "value": v, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": res["fused_rope_copy"]["ms"],
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "qkv_projection", "B": B, "T": T, "Cm": Cm, "NH": NH, "NKV": NKV, "hd": hd,
+                   "l2": "flushed between calls (256 MiB write outside the timed events)"},
+        "variants": res,
+        "roofline": {"bound": "tensor", "achieved": v, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": v / peaks["bf16_tflops"], "traffic": None, "peak_source": f"{src} bf16_tflops (burst)"},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.decode:
         return run_decode(args)
+    if args.proj:
+        return run_proj(args)
     from causal_attention_gqa_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -30,9 +30,17 @@ namespace attn {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kATile = kBM * kBK * 2;               // 16 KB
-constexpr int kBTile = kBN * kBK * 2;               // 32 KB
+#ifndef PROJ_BK
+#define PROJ_BK 64
+#endif
+#ifndef PROJ_STAGES
+#define PROJ_STAGES 4
+#endif
+constexpr int kBM = 128, kBN = 256, kBK = PROJ_BK, kStages = PROJ_STAGES;
+constexpr int kAtoms = kBK / 64;                    // 64-column swizzle atoms per k-block
+constexpr int kAAtom = kBM * 128, kBAtom = kBN * 128;
+constexpr int kATile = kBM * kBK * 2;
+constexpr int kBTile = kBN * kBK * 2;
 constexpr int kStageBytes = kATile + kBTile;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;    // + barriers + alignment slack
@@ -103,8 +111,11 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           const uint32_t fb = ptx::smem_u32(&bars->full[st]);
           ptx::mbar_arrive_expect_tx(fb, kStageBytes);
           uint8_t* sa = smem + st * kStageBytes;
-          ptx::tma_load_3d(ptx::smem_u32(sa), &tm_x, kb * kBK, m0, 0, fb);
-          ptx::tma_load_3d(ptx::smem_u32(sa + kATile), &tm_w, kb * kBK, n0, 0, fb);
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a) {
+            ptx::tma_load_3d(ptx::smem_u32(sa + a * kAAtom), &tm_x, kb * kBK + 64 * a, m0, 0, fb);
+            ptx::tma_load_3d(ptx::smem_u32(sa + kATile + a * kBAtom), &tm_w, kb * kBK + 64 * a, n0, 0, fb);
+          }
         }
       }
       if (!ok) fail();
@@ -143,7 +154,8 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
           const uint64_t db = ptx::desc_advance(d0, st * kStageBytes + kATile);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            ptx::mma_bf16_ss(tmem + buf * kBN, ptx::desc_advance(da, kk * 32), ptx::desc_advance(db, kk * 32), idesc,
+            ptx::mma_bf16_ss(tmem + buf * kBN, ptx::desc_advance(da, (kk >> 2) * kAAtom + (kk & 3) * 32),
+                             ptx::desc_advance(db, (kk >> 2) * kBAtom + (kk & 3) * 32), idesc,
                              (kb > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_commit(ptx::smem_u32(&bars->empty[st]));
         }
