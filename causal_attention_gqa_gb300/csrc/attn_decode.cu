@@ -71,8 +71,10 @@ __device__ __forceinline__ int clamp_len(const int* lens, int b, int max_len, in
   return n;
 }
 
-// Partial of one (batch row, head, chunk): m, l, then o[HD].
-template <typename T, int HD>
+// Partial of one (batch row, head, chunk): m, l, then o[HD].  KH query heads
+// per CTA: 4, or 1 when a kv head serves a single query head (each lane then
+// reduces 8 partial sums instead of 32).
+template <typename T, int HD, int KH>
 __global__ void __launch_bounds__(kThreadsD, sizeof(T) == 2 ? 3 : 2)
 decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* __restrict__ kc,
                     const T* __restrict__ vc, const int* __restrict__ lens, int NH, int NKV, int max_len,
@@ -83,19 +85,19 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
   constexpr int EPL = HD / 32;
   // Per warp: the probabilities of a block of rows, then the heads' corrections.
   __shared__ __align__(16) float p_sh[kWarpsD][2][32];
-  __shared__ float m_sh[kWarpsD][kHeads], l_sh[kWarpsD][kHeads];
-  __shared__ float o_sh[kWarpsD][kHeads][HD];
-  const int grp = NH / NKV, hgroups = (grp + kHeads - 1) / kHeads;
+  __shared__ float m_sh[kWarpsD][KH], l_sh[kWarpsD][KH];
+  __shared__ float o_sh[kWarpsD][KH][HD];
+  const int grp = NH / NKV, hgroups = (grp + KH - 1) / KH;
   const int s = blockIdx.x, kh = blockIdx.y / hgroups, hg = blockIdx.y % hgroups, b = blockIdx.z;
-  const int h0 = kh * grp + hg * kHeads, gcnt = min(kHeads, grp - hg * kHeads);
+  const int h0 = kh * grp + hg * KH, gcnt = min(KH, grp - hg * KH);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int len = clamp_len(lens, b, max_len, status);
   const int r0 = s * chunk, r1 = min(r0 + chunk, len);
 
   // This lane's elements of the queries (heads past gcnt: zero).
-  float qv[kHeads][EPL];
+  float qv[KH][EPL];
 #pragma unroll
-  for (int h = 0; h < kHeads; ++h) {
+  for (int h = 0; h < KH; ++h) {
     if (h < gcnt) {
       Vec<T, EPL>::widen(Vec<T, EPL>::load(q + ((size_t)b * NH + h0 + h) * HD + lane * EPL), qv[h]);
     } else {
@@ -103,11 +105,12 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
       for (int e = 0; e < EPL; ++e) qv[h][e] = 0.f;
     }
   }
-  // Running state: m, l of head (lane % 4) (replicated over its 8 lanes), and
+  // Running state: m, l of head (lane % 4) (replicated over its 8 lanes; KH = 1:
+  // all lanes hold head 0), and
   // this lane's elements of every head's unnormalised output.
-  float m = -INFINITY, l = 0.f, o[kHeads][EPL];
+  float m = -INFINITY, l = 0.f, o[KH][EPL];
 #pragma unroll
-  for (int h = 0; h < kHeads; ++h)
+  for (int h = 0; h < KH; ++h)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[h][e] = 0.f;
 
@@ -134,33 +137,42 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
   for (int rb = r0 + 8 * warp; rb < r1; rb += 8 * kWarpsD) {
     Raw kn[8], vn[8];
     if (rb + 8 * kWarpsD < r1) fetch(rb + 8 * kWarpsD, kn, vn);
-    // Partial dot products, value index 4 r + h (rows widened one at a time).
-    float v[32];
+    // Partial dot products, value index KH r + h (rows widened one at a time).
+    constexpr int NV = 8 * KH;
+    float v[NV];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       float kv[EPL];
       Vec<T, EPL>::widen(kr[r], kv);
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) {
+      for (int h = 0; h < KH; ++h) {
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc = fmaf(qv[h][e], kv[e], acc);
-        v[4 * r + h] = acc;
+        v[KH * r + h] = acc;
       }
     }
-    // Butterfly: after the stage with offset o, a lane keeps the half of its
-    // values selected by its bit o and adds the partner's copy of that half.
+    // Butterfly: while a lane holds several values, the stage with offset o
+    // keeps the half selected by its lane bit o and adds the partner's copy of
+    // that half; once one value is left the stages just add.  Lane l ends
+    // with value index l >> (5 - log2(NV)), i.e. row l / 4 and head l % 4
+    // (KH = 4) or row l / 4 (KH = 1).
 #pragma unroll
-    for (int o2 = 16, n = 32; o2 >= 1; o2 >>= 1, n >>= 1) {
-      const bool upper = (lane & o2) != 0;
+    for (int stage = 0; stage < 5; ++stage) {
+      const int o2 = 16 >> stage, n = NV >> stage;   // compile-time once unrolled
+      if (n > 1) {
+        const bool upper = (lane & o2) != 0;
 #pragma unroll
-      for (int i = 0; i < n / 2; ++i) {
-        const float send = upper ? v[i] : v[i + n / 2];
-        const float keep = upper ? v[i + n / 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
+        for (int i = 0; i < n / 2; ++i) {
+          const float send = upper ? v[i] : v[i + n / 2];
+          const float keep = upper ? v[i + n / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
+        }
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o2);
       }
     }
-    // Lane 4 r + h: score of row rb + r for head h.
+    // Lane 4 r + h: score of row rb + r for head h (KH = 1: head 0 on all four).
     const int row = rb + lane / 4;
     const float sc = (row < r1) ? v[0] * scale : -INFINITY;
     float bm = sc;
@@ -180,7 +192,7 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
     p_sh[warp][1][lane] = corr;
     __syncwarp();
 #pragma unroll
-    for (int h = 0; h < kHeads; ++h) {
+    for (int h = 0; h < KH; ++h) {
       const float c = p_sh[warp][1][h];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) o[h][e] *= c;
@@ -188,11 +200,11 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const float4 pr = *reinterpret_cast<const float4*>(&p_sh[warp][0][4 * r]);
-      const float pv[4] = {pr.x, pr.y, pr.z, pr.w};
+      const float pv[4] = {pr.x, pr.y, pr.z, pr.w};   // heads 0..3 (KH = 1: head 0 in pv[0])
       float vrow[EPL];
       Vec<T, EPL>::widen(vr[r], vrow);
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h)
+      for (int h = 0; h < KH; ++h)
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pv[h], vrow[e], o[h][e]);
     }
@@ -204,12 +216,12 @@ decode_split_kernel(float* __restrict__ part, const T* __restrict__ q, const T* 
     }
   }
   // Merge the warps: lanes 0..3 hold m, l of heads 0..3.
-  if (lane < kHeads) {
+  if (lane < KH) {
     m_sh[warp][lane] = m;
     l_sh[warp][lane] = l;
   }
 #pragma unroll
-  for (int h = 0; h < kHeads; ++h)
+  for (int h = 0; h < KH; ++h)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o_sh[warp][h][lane * EPL + e] = o[h][e];
   __syncthreads();
@@ -292,14 +304,20 @@ decode_merge_kernel(T* __restrict__ out, float* __restrict__ lse, const float* _
 
 template <typename T, int HD>
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  const int grp = a.NH / a.NKV, hgroups = (grp + kHeads - 1) / kHeads;
+  const int grp = a.NH / a.NKV, hgroups = (grp + kHeads - 1) / kHeads;   // grp 1: one group either way
   const int chunk = decode_chunk_rows(a.B, a.NH, a.NKV, a.max_len);
   const int n_split = (a.max_len + chunk - 1) / chunk;
   const float scale = (float)(1.0 / sqrt((double)HD));
   prof_begin(kKernelDecode, stream);
-  decode_split_kernel<T, HD><<<dim3(n_split, a.NKV * hgroups, a.B), kThreadsD, 0, stream>>>(
-      a.part, (const T*)a.q, (const T*)a.k_cache, (const T*)a.v_cache, a.lens, a.NH, a.NKV, a.max_len, chunk,
-      n_split, scale, a.status);
+  const dim3 grid(n_split, a.NKV * hgroups, a.B);
+  if (grp == 1)
+    decode_split_kernel<T, HD, 1><<<grid, kThreadsD, 0, stream>>>(
+        a.part, (const T*)a.q, (const T*)a.k_cache, (const T*)a.v_cache, a.lens, a.NH, a.NKV, a.max_len, chunk,
+        n_split, scale, a.status);
+  else
+    decode_split_kernel<T, HD, kHeads><<<grid, kThreadsD, 0, stream>>>(
+        a.part, (const T*)a.q, (const T*)a.k_cache, (const T*)a.v_cache, a.lens, a.NH, a.NKV, a.max_len, chunk,
+        n_split, scale, a.status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
     e = launch_pdl(decode_merge_kernel<T, HD>, dim3(a.NH, a.B), dim3(kMergeGroups * HD), 0, stream, (T*)a.out, a.lse,
