@@ -86,6 +86,10 @@ def load() -> ctypes.CDLL:
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.attn_qkv_proj.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.attn_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.attn_fwd_fp8_workspace_bytes.restype = sz
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.attn_fwd_fp8.restype = i
     lib.attn_qkv_proj.restype = i
     lib.attn_fwd_rot.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.attn_fwd_rot.restype = i
@@ -173,6 +177,31 @@ def attn_bwd_rot(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype,
     _check(st, "attn_bwd_rot")
 
 
+def attn_fwd_fp8_workspace_bytes(B, T, C, NH, NKV, dtype) -> int:
+    return int(load().attn_fwd_fp8_workspace_bytes(B, T, C, NH, NKV, int(dtype)))
+
+
+def attn_fwd_fp8(out, lse, qkv, B, T, C, NH, NKV, rope_theta, dtype, workspace, workspace_bytes, stream=None) -> None:
+    st = load().attn_fwd_fp8(_ptr(out), _ptr(lse), _ptr(qkv), B, T, C, NH, NKV, float(rope_theta), int(dtype),
+                             _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "attn_fwd_fp8")
+
+
+def forward_fp8(qkv, NH: int, NKV: int, rope_theta: float = 0.0, rope_interleaved: bool = False, stream=None):
+    """(out, lse) of the e4m3 forward (attn_fwd_fp8) on a bf16 qkv."""
+    import torch
+    B, T, W = qkv.shape
+    hd = W // (NH + 2 * NKV)
+    C = NH * hd
+    code = DTYPE_BF16 | (FLAG_ROPE_INTERLEAVED if rope_interleaved else 0)
+    nbytes = attn_fwd_fp8_workspace_bytes(B, T, C, NH, NKV, code)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
+    out = torch.empty((B, T, C), dtype=qkv.dtype, device=qkv.device)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=qkv.device)
+    attn_fwd_fp8(out, lse, qkv, B, T, C, NH, NKV, rope_theta, code, ws, ws.numel(), stream)
+    return out, lse
+
+
 def attn_qkv_proj(qkv, qk_rot, x, w, B, T, Cm, NH, NKV, hd, rope_theta, flags=0, stream=None) -> None:
     st = load().attn_qkv_proj(_ptr(qkv), _ptr(qk_rot), _ptr(x), _ptr(w), B, T, Cm, NH, NKV, hd, float(rope_theta),
                               int(flags), _stream(stream))
@@ -251,7 +280,7 @@ def attn_selftest_wait_timeout(limit_ns: int) -> int:
     return v.value
 
 
-N_KERNEL_IDS = 11
+N_KERNEL_IDS = 13
 
 
 def attn_profile_start() -> None:

@@ -88,6 +88,19 @@ bool make_tmap(CUtensorMap* m, const void* base, int width, int T, int B, int ro
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Byte (e4m3) tensor of d0 x d1 x d2 elements, rows of d0 bytes, 128 x 128 boxes.
+bool make_tmap_u8(CUtensorMap* m, const void* base, int d0, int d1, int d2) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)d0, (cuuint64_t)d0 * (cuuint64_t)d1};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // `dtype` may carry ATTN_FLAG_ROPE_INTERLEAVED; it is stripped here (the
 // element type stays in `dtype`) and recorded in the geometry.
 int check_shape(int B, int T, int C, int NH, int NKV, float rope_theta, int& dtype, Geometry* g) {
@@ -355,6 +368,64 @@ extern "C" int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const 
                             void* workspace, size_t ws_bytes, void* stream) {
   return bwd_impl(dqkv, qkv, out, dout, lse, B, T, C, NH, NKV, rope_theta, dtype, qk_rot, workspace, ws_bytes,
                   stream);
+}
+
+// ---------------------------------------------------------------- FP8 forward
+namespace {
+struct Fp8Layout {
+  size_t qk8, vt8, deq_qk, deq_v, total;
+  int Tp;
+};
+Fp8Layout fp8_layout(const Geometry& g) {
+  Fp8Layout L;
+  const int n_qt = (g.T + 127) / 128;
+  L.Tp = n_qt * 128;
+  const size_t heads = (size_t)(g.NH + g.NKV);
+  L.qk8 = 0;
+  L.vt8 = L.qk8 + align256((size_t)g.B * g.T * heads * g.hd);
+  L.deq_qk = L.vt8 + align256((size_t)g.B * g.NKV * g.hd * L.Tp);
+  L.deq_v = L.deq_qk + align256((size_t)g.B * heads * n_qt * sizeof(float));
+  L.total = L.deq_v + align256((size_t)g.B * g.NKV * sizeof(float));
+  return L;
+}
+}  // namespace
+
+extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype) {
+  Geometry g;
+  if (check_shape(B, T, C, NH, NKV, 0.f, dtype, &g) != ATTN_OK || dtype != ATTN_DTYPE_BF16) return 0;
+  if (!fp8_fwd_supported(g)) return 0;
+  return fp8_layout(g).total;
+}
+
+extern "C" int attn_fwd_fp8(void* out, float* lse, const void* qkv, int B, int T, int C, int NH, int NKV,
+                            float rope_theta, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  Geometry g;
+  int type = dtype;
+  int st = check_shape(B, T, C, NH, NKV, rope_theta, type, &g);
+  if (st != ATTN_OK) return st;
+  if (type != ATTN_DTYPE_BF16 || !fp8_fwd_supported(g)) return ATTN_ERR_UNSUPPORTED;
+  if (!out || !lse || !qkv) return ATTN_ERR_NULL_POINTER;
+  if (!aligned16(out) || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
+  const Fp8Layout L = fp8_layout(g);
+  if (!workspace || ws_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Fp8FwdArgs a{};
+  a.g = g;
+  a.qkv = qkv;
+  a.qk8 = ws + L.qk8;
+  a.vt8 = ws + L.vt8;
+  a.deq_qk = reinterpret_cast<float*>(ws + L.deq_qk);
+  a.deq_v = reinterpret_cast<float*>(ws + L.deq_v);
+  a.Tp = L.Tp;
+  a.lse = lse;
+  a.status = status_word();
+  a.num_sms = num_sms();
+  if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
+  if (!make_tmap_u8(&a.tm_qk8, a.qk8, (g.NH + g.NKV) * g.hd, g.T, g.B) ||
+      !make_tmap_u8(&a.tm_vt, a.vt8, L.Tp, g.hd, g.B * g.NKV) || !make_tmap(&a.tm_out, out, g.C, g.T, g.B))
+    return ATTN_ERR_CUDA;
+  return from_cuda(fp8_fwd_launch(a, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- QKV projection

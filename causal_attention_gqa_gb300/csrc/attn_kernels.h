@@ -48,6 +48,25 @@ bool simt_tiled_supported(const SimtArgs& a);
 cudaError_t simt_tiled_launch(const SimtArgs& a, cudaStream_t stream);
 size_t simt_max_smem_bytes(int hd);
 
+// ------------------------------------------------------------ FP8 forward
+// e4m3 operands with per-tile (Q, K) and per-head (V) scales; head size 128,
+// an even number of query heads per kv head.
+struct Fp8FwdArgs {
+  Geometry g;
+  CUtensorMap tm_qk8, tm_vt, tm_out;
+  const void* qkv;
+  uint8_t* qk8;      // [B*T, (NH+NKV)*hd] e4m3, rotated Q | K
+  uint8_t* vt8;      // [B, NKV, hd, Tp] e4m3, V transposed
+  float* deq_qk;     // [B, NH+NKV, T/128] dequantization factors
+  float* deq_v;      // [B, NKV]
+  int Tp;            // T rounded up to 128
+  float* lse;
+  int* status;
+  int num_sms;
+};
+bool fp8_fwd_supported(const Geometry& g);
+cudaError_t fp8_fwd_launch(const Fp8FwdArgs& a, cudaStream_t stream);
+
 // ------------------------------------------------------------ QKV projection
 // qkv = x w^T with the rotated Q/K copy written from the same accumulators.
 struct ProjGeometry {

@@ -19,7 +19,9 @@ enum KernelId {
   kKernelBwdPrologue = 8,
   kKernelDecode = 9,
   kKernelProj = 10,
-  kKernelCount = 11
+  kKernelFp8Prep = 11,
+  kKernelFwdFp8 = 12,
+  kKernelCount = 13
 };
 
 // Record the start / end of a launch of kernel `id` on `stream` (no-ops while

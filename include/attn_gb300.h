@@ -290,6 +290,25 @@ ATTN_API int attn_qkv_proj(void* qkv, void* qk_rot, const void* x, const void* w
 ATTN_API int attn_fwd_rot(void* out, float* lse, const void* qkv, const void* qk_rot, int B,
                           int T, int C, int NH, int NKV, float rope_theta, int dtype, void* stream);
 
+/*
+ * attn_fwd_fp8 -- the forward with e4m3 (FP8) tensor-core operands (an
+ * adjacent GB300 capability, not on the source pages): same inputs, outputs
+ * and RoPE handling as attn_fwd_ws with ATTN_DTYPE_BF16, but Q and K are
+ * rotated and rounded to e4m3 with one scale per (batch row, head, 128-row
+ * tile) (x8 = rn(x * 448 / amax)), V to e4m3 with one scale per (batch row, kv
+ * head), and P = exp(s - m) to e4m3 (as 448 P) before the P V product; scores,
+ * sums, O, out (bf16) and lse (float32) are accumulated in float32.  Expect
+ * errors of a few 1e-2 of max|out| (3 mantissa bits), not the bf16 path's
+ * 2e-2.  Head size 128 and an even number of query heads per kv head only
+ * (ATTN_ERR_UNSUPPORTED otherwise).  The workspace (attn_fwd_fp8_workspace_
+ * bytes(), 256-byte aligned) holds the e4m3 copies and their scales.  There
+ * is no FP8 backward.
+ */
+ATTN_API size_t attn_fwd_fp8_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype);
+ATTN_API int attn_fwd_fp8(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
+                          int NKV, float rope_theta, int dtype, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* attn_strerror -- static description of a status code; never NULL. */
 ATTN_API const char* attn_strerror(int status);
 
@@ -321,7 +340,7 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_ns, int* status);
  * attn_kernel_name -- short name of kernel id (see attn_profile.h ids:
  *   0 fwd_tc05, 1 bwd_dkdv_tc05, 2 bwd_dq_tc05, 3 bwd_row_dot, 4 rope_qk,
  *   5 fwd_simt, 6 bwd_dkdv_simt, 7 bwd_dq_simt, 8 bwd_prologue, 9 decode (both
- *   of its kernels), 10 qkv_proj); "unknown" otherwise.
+ *   of its kernels), 10 qkv_proj, 11 fp8_prep, 12 fwd_fp8); "unknown" otherwise.
  */
 ATTN_API int attn_profile_start(void);
 ATTN_API int attn_profile_stop(double* total_ms, int* launches, int n);
