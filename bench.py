@@ -22,6 +22,11 @@ bounded sample of the same workload: one kv group of one batch row per step.
 the rotated Q/K copy in its epilogue, and without the copy), with cuBLAS
 (torch.matmul) on the same GEMM for context, and prints one JSON line.
 
+`--fp8` times attn_fwd_fp8 (the e4m3 forward, its quantization pass
+included) next to attn_fwd_ws on the workload and prints one JSON line
+(forward TFLOP/s against the FP8 peak = 2 x the measured bf16 peak, the
+nominal dense fp8/bf16 ratio).
+
 `--decode B,L,NH,NKV,hd` times attn_decode (one new token per batch row
 against a bf16 KV cache of L rows) instead and prints one JSON line with its
 HBM throughput (cache bytes read per call / device time; L2 flushed between
@@ -61,6 +66,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", default=None, metavar="B,L,NH,NKV,hd")
     ap.add_argument("--proj", default=None, metavar="B,T,Cm,NH,NKV,hd")
+    ap.add_argument("--fp8", action="store_true")
     return ap.parse_args()
 
 
@@ -491,8 +497,77 @@ def run_proj(args):
     return 0
 
 
+def run_fp8(args, w):
+    """attn_fwd_fp8 vs attn_fwd_ws on the workload; forward TFLOP/s."""
+    import torch
+    from causal_attention_gqa_gb300 import binding
+    from causal_attention_gqa_gb300.workloads import make_inputs
+    torch.cuda.set_device(0)
+    binding.load()
+    B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
+    qkv_np, _ = make_inputs(w, "bf16")
+    qkv = torch.from_numpy(qkv_np).to("cuda", torch.bfloat16)
+    del qkv_np
+    out = torch.empty((B, T, C), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device="cuda")
+    code = binding.DTYPE_BF16
+    nb8 = binding.attn_fwd_fp8_workspace_bytes(B, T, C, NH, NKV, code)
+    ws8 = torch.empty(nb8, dtype=torch.uint8, device="cuda")
+    nbw = binding.attn_fwd_workspace_bytes(B, T, C, NH, NKV, code)
+    wsw = torch.empty(nbw, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    calls = {
+        "fp8": lambda: binding.attn_fwd_fp8(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, ws8, nb8),
+        "bf16_ws": lambda: binding.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, wsw, nbw),
+    }
+    steps = min(args.steps, 200)
+    res = {}
+    for name, fn in calls.items():
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        res[name] = {"ms": ms, "tflops": w.flops_fwd() / (ms * 1e-3) / 1e12}
+    binding.attn_profile_start()
+    for _ in range(20):
+        flush.zero_()
+        calls["fp8"]()
+    torch.cuda.synchronize()
+    prof = binding.attn_profile_stop()
+    peaks, src = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    v = res["fp8"]["tflops"]
+    kern = {k: {"launches": n, "avg_ms": t / n} for k, (n, t) in prof.items()}
+    fk = kern.get("fwd_fp8", {}).get("avg_ms")
+    line = {
+        "metric": "causal attn forward TFLOP/s with e4m3 operands on 1 GB300", "value": v, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": res["fp8"]["ms"],
+        "higher_is_better": True, "dtype": "e4m3 (bf16 in/out)", "data": "synthetic",
+        "config": config_of(w, {"l2": "flushed between calls (256 MiB write outside the timed events)",
+                                "timing": "median of per-call CUDA events"}),
+        "variants": res, "kernels": kern,
+        "roofline": {"bound": "tensor", "kernel": "fwd_fp8",
+                     "achieved": (w.flops_fwd() / (fk * 1e-3) / 1e12) if fk else None, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": (w.flops_fwd() / (fk * 1e-3) / 1e12 / fp8_peak) if fk else None,
+                     "traffic": None, "peak_source": f"2 x {src} bf16_tflops (burst), the nominal fp8/bf16 ratio"},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.fp8:
+        from causal_attention_gqa_gb300.workloads import WORKLOADS
+        return run_fp8(args, WORKLOADS[args.workload])
     if args.decode:
         return run_decode(args)
     if args.proj:

@@ -373,7 +373,7 @@ extern "C" int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const 
 // ---------------------------------------------------------------- FP8 forward
 namespace {
 struct Fp8Layout {
-  size_t qk8, vt8, deq_qk, deq_v, total;
+  size_t qk8, vt8, deq_qk, deq_v, vtile_amax, total;
   int Tp;
 };
 Fp8Layout fp8_layout(const Geometry& g) {
@@ -385,7 +385,8 @@ Fp8Layout fp8_layout(const Geometry& g) {
   L.vt8 = L.qk8 + align256((size_t)g.B * g.T * heads * g.hd);
   L.deq_qk = L.vt8 + align256((size_t)g.B * g.NKV * g.hd * L.Tp);
   L.deq_v = L.deq_qk + align256((size_t)g.B * heads * n_qt * sizeof(float));
-  L.total = L.deq_v + align256((size_t)g.B * g.NKV * sizeof(float));
+  L.vtile_amax = L.deq_v + align256((size_t)g.B * g.NKV * sizeof(float));
+  L.total = L.vtile_amax + align256((size_t)g.B * g.NKV * n_qt * sizeof(float));
   return L;
 }
 }  // namespace
@@ -417,6 +418,7 @@ extern "C" int attn_fwd_fp8(void* out, float* lse, const void* qkv, int B, int T
   a.vt8 = ws + L.vt8;
   a.deq_qk = reinterpret_cast<float*>(ws + L.deq_qk);
   a.deq_v = reinterpret_cast<float*>(ws + L.deq_v);
+  a.vtile_amax = reinterpret_cast<float*>(ws + L.vtile_amax);
   a.Tp = L.Tp;
   a.lse = lse;
   a.status = status_word();

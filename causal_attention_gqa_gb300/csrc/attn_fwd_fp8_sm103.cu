@@ -412,14 +412,18 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
 // ---------------------------------------------------------------------------
 // Quantization pass.
 // ---------------------------------------------------------------------------
-// amax of V over all rows of one (batch row, kv head): deq_v = amax / 448.
-__global__ void __launch_bounds__(256) fp8_vamax_kernel(float* __restrict__ deq_v, const __nv_bfloat16* __restrict__ qkv,
-                                                        Geometry g) {
+// amax of V over one 128-row tile of one (batch row, kv head), into
+// vtile_amax[b][kv][tile]; the quantization pass takes the maximum over the
+// tiles of a head (deq_v = amax / 448), so every tile of a head shares one
+// scale and the result does not depend on the order of anything.
+__global__ void __launch_bounds__(256) fp8_vamax_kernel(float* __restrict__ vtile_amax,
+                                                        const __nv_bfloat16* __restrict__ qkv, Geometry g) {
   __shared__ float red[256];
-  const int kh = blockIdx.x, b = blockIdx.y;
+  const int tile = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   float mx = 0.f;
-  for (int u = threadIdx.x; u < g.T * (kHD / 8); u += 256) {
-    const int t = u / (kHD / 8), c = u % (kHD / 8);
+  for (int u = threadIdx.x; u < 128 * (kHD / 8); u += 256) {
+    const int t = tile * 128 + u / (kHD / 8), c = u % (kHD / 8);
+    if (t >= g.T) break;
     const uint4 v = *reinterpret_cast<const uint4*>(qkv + ((size_t)b * g.T + t) * g.W + g.C + g.NKV * kHD + kh * kHD +
                                                     8 * c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -432,31 +436,37 @@ __global__ void __launch_bounds__(256) fp8_vamax_kernel(float* __restrict__ deq_
     if ((int)threadIdx.x < s) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + s]);
     __syncthreads();
   }
-  if (threadIdx.x == 0) deq_v[(size_t)b * g.NKV + kh] = red[0] > 0.f ? red[0] / 448.f : 1.f;
+  if (threadIdx.x == 0) vtile_amax[((size_t)b * g.NKV + kh) * gridDim.x + tile] = red[0];
 }
 
 // One CTA per (128-row tile, head, batch row); heads 0..NH+NKV-1 are the Q
 // and K heads (rotated, one scale per tile, into the e4m3 copy with the
 // layout of the bf16 rotated copy), heads NH+NKV.. the V heads (scale per
-// head from fp8_vamax_kernel, written transposed into V^T [b][kv][d][Tp]).
-// Thread = (row r = tid / 2, half of the head's pairs or columns).
-__global__ void __launch_bounds__(256) fp8_quant_kernel(uint8_t* __restrict__ qk8, uint8_t* __restrict__ vt8,
-                                                        float* __restrict__ deq_qk, const float* __restrict__ deq_v,
-                                                        const __nv_bfloat16* __restrict__ qkv, Geometry g, int Tp) {
-  __shared__ float red[256];
+// head from the tile maxima of fp8_vamax_kernel, written transposed into
+// V^T [b][kv][d][Tp]).  Thread = (row r = tid / 4, quarter of the head's
+// pairs or columns), so a thread holds 32 rotated values.
+constexpr int kQuantThreads = 512;
+
+__global__ void __launch_bounds__(kQuantThreads) fp8_quant_kernel(uint8_t* __restrict__ qk8, uint8_t* __restrict__ vt8,
+                                                                  float* __restrict__ deq_qk,
+                                                                  float* __restrict__ deq_v,
+                                                                  const float* __restrict__ vtile_amax,
+                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
+                                                                  int Tp) {
+  __shared__ float red[kQuantThreads / 32];
   __shared__ __align__(16) uint8_t tile8[kHD][128 + 16];
   const int tile = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
-  const int r = threadIdx.x >> 1, part = threadIdx.x & 1;
+  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int t = tile * 128 + r;
   const bool valid = t < g.T;
   const int heads = g.NH + g.NKV, n_qt = (g.T + 127) / 128;
   if (head < heads) {
     const __nv_bfloat16* src = qkv + ((size_t)b * g.T + (valid ? t : 0)) * g.W + head * kHD;
-    float y0[32], y1[32];
+    float y0[16], y1[16];
     float mx = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int gi = part * 4 + q;                          // 8 pairs 8 gi .. 8 gi + 7
+    for (int q = 0; q < 2; ++q) {
+      const int gi = part * 2 + q;                          // 8 pairs 8 gi .. 8 gi + 7
       uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
       if (valid) load_rope_pairs(src, gi, kHD / 2, g.rope_interleaved != 0, x0, x1);
       const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, c[4] = {x1.x, x1.y, x1.z, x1.w};
@@ -476,56 +486,57 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(uint8_t* __restrict__ qk
         mx = fmaxf(mx, fmaxf(fabsf(v0), fabsf(v1)));
       }
     }
-    red[threadIdx.x] = mx;
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
-    for (int s = 128; s > 0; s >>= 1) {
-      if ((int)threadIdx.x < s) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + s]);
-      __syncthreads();
-    }
-    const float amax = red[0];
+    float amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     const float scale = amax > 0.f ? 448.f / amax : 1.f;
     if (threadIdx.x == 0) deq_qk[((size_t)b * heads + head) * n_qt + tile] = amax > 0.f ? amax / 448.f : 1.f;
     if (valid) {
-      // Pairs 32 part .. 32 part + 31 -> slots i and i + hd/2 of the head.
+      // Pairs 16 part .. 16 part + 15 -> slots i and i + hd/2 of the head.
       uint8_t* dst = qk8 + ((size_t)b * g.T + t) * (size_t)(heads * kHD) + head * kHD;
-      uint32_t w0[8], w1[8];
+      uint32_t w0[4], w1[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 4; ++k) {
         w0[k] = ptx::cvt_e4m3x2(y0[4 * k] * scale, y0[4 * k + 1] * scale) |
                 (ptx::cvt_e4m3x2(y0[4 * k + 2] * scale, y0[4 * k + 3] * scale) << 16);
         w1[k] = ptx::cvt_e4m3x2(y1[4 * k] * scale, y1[4 * k + 1] * scale) |
                 (ptx::cvt_e4m3x2(y1[4 * k + 2] * scale, y1[4 * k + 3] * scale) << 16);
       }
-      *reinterpret_cast<uint4*>(dst + 32 * part) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-      *reinterpret_cast<uint4*>(dst + 32 * part + 16) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-      *reinterpret_cast<uint4*>(dst + kHD / 2 + 32 * part) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-      *reinterpret_cast<uint4*>(dst + kHD / 2 + 32 * part + 16) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+      *reinterpret_cast<uint4*>(dst + 16 * part) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+      *reinterpret_cast<uint4*>(dst + kHD / 2 + 16 * part) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
     }
     return;
   }
-  // V head kv: columns 64 part .. 64 part + 63 of row r, transposed.
+  // V head kv: columns 32 part .. 32 part + 31 of row r, transposed, with the
+  // head's scale (maximum of its tile maxima).
   const int kv = head - heads;
-  const float scale = 1.f / deq_v[(size_t)b * g.NKV + kv];
-  const __nv_bfloat16* src = qkv + ((size_t)b * g.T + (valid ? t : 0)) * g.W + g.C + g.NKV * kHD + kv * kHD + 64 * part;
+  float mx = 0.f;
+  for (int k = 0; k < n_qt; ++k) mx = fmaxf(mx, vtile_amax[((size_t)b * g.NKV + kv) * n_qt + k]);
+  const float scale = mx > 0.f ? 448.f / mx : 1.f;
+  if (tile == 0 && threadIdx.x == 0) deq_v[(size_t)b * g.NKV + kv] = mx > 0.f ? mx / 448.f : 1.f;
+  const __nv_bfloat16* src = qkv + ((size_t)b * g.T + (valid ? t : 0)) * g.W + g.C + g.NKV * kHD + kv * kHD + 32 * part;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     uint4 v = make_uint4(0, 0, 0, 0);
     if (valid) v = *reinterpret_cast<const uint4*>(src + 8 * q);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t e = ptx::cvt_e4m3x2(bf16_lo(w[k]) * scale, bf16_hi(w[k]) * scale);
-      tile8[64 * part + 8 * q + 2 * k][r] = (uint8_t)(e & 0xFF);
-      tile8[64 * part + 8 * q + 2 * k + 1][r] = (uint8_t)(e >> 8);
+      tile8[32 * part + 8 * q + 2 * k][r] = (uint8_t)(e & 0xFF);
+      tile8[32 * part + 8 * q + 2 * k + 1][r] = (uint8_t)(e >> 8);
     }
   }
   __syncthreads();
-  // Row d of V^T: keys tile*128 .. +127, 64 bytes per thread.
-  const int d = threadIdx.x >> 1;
-  uint8_t* dst = vt8 + (((size_t)b * g.NKV + kv) * kHD + d) * (size_t)Tp + tile * 128 + 64 * part;
+  // Row d of V^T: keys tile*128 .. +127, 32 bytes per thread.
+  const int d = threadIdx.x >> 2;
+  uint8_t* dst = vt8 + (((size_t)b * g.NKV + kv) * kHD + d) * (size_t)Tp + tile * 128 + 32 * part;
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(dst + 16 * q) = *reinterpret_cast<const uint4*>(&tile8[d][64 * part + 16 * q]);
+  for (int q = 0; q < 2; ++q)
+    *reinterpret_cast<uint4*>(dst + 16 * q) = *reinterpret_cast<const uint4*>(&tile8[d][32 * part + 16 * q]);
 }
 
 }  // namespace
@@ -536,11 +547,11 @@ cudaError_t fp8_fwd_launch(const Fp8FwdArgs& a, cudaStream_t stream) {
   const Geometry& g = a.g;
   const int n_qt = (g.T + 127) / 128, heads = g.NH + g.NKV;
   prof_begin(kKernelFp8Prep, stream);
-  fp8_vamax_kernel<<<dim3(g.NKV, g.B), 256, 0, stream>>>(a.deq_v, (const __nv_bfloat16*)a.qkv, g);
+  fp8_vamax_kernel<<<dim3(n_qt, g.NKV, g.B), 256, 0, stream>>>(a.vtile_amax, (const __nv_bfloat16*)a.qkv, g);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) {
-    fp8_quant_kernel<<<dim3(n_qt, heads + g.NKV, g.B), 256, 0, stream>>>(
-        a.qk8, a.vt8, a.deq_qk, a.deq_v, (const __nv_bfloat16*)a.qkv, g, a.Tp);
+    fp8_quant_kernel<<<dim3(n_qt, heads + g.NKV, g.B), kQuantThreads, 0, stream>>>(
+        a.qk8, a.vt8, a.deq_qk, a.deq_v, a.vtile_amax, (const __nv_bfloat16*)a.qkv, g, a.Tp);
     e = cudaGetLastError();
   }
   prof_end(kKernelFp8Prep, stream);

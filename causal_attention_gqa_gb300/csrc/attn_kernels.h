@@ -59,6 +59,7 @@ struct Fp8FwdArgs {
   uint8_t* vt8;      // [B, NKV, hd, Tp] e4m3, V transposed
   float* deq_qk;     // [B, NH+NKV, T/128] dequantization factors
   float* deq_v;      // [B, NKV]
+  float* vtile_amax; // [B, NKV, T/128] amax of each V tile
   int Tp;            // T rounded up to 128
   float* lse;
   int* status;

@@ -18,3 +18,4 @@ from .attention import (  # noqa: F401
     attention_decode,
     qkv_projection,
 )
+from .e4m3 import e4m3_round, attention_forward_e4m3  # noqa: F401,E402

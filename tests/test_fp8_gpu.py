@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
-from causal_attention_gqa_gb300.workloads import make_inputs, shape_workload
+from causal_attention_gqa_gb300.workloads import WORKLOADS, make_inputs, sample_rows, shape_workload
 from helpers import rel_err, to_device, to_numpy
 
 pytestmark = pytest.mark.gpu
@@ -48,6 +48,41 @@ def test_fp8_forward_within_bar(lib, B, T, C, NH, NKV, theta, interleaved):
     assert lib.attn_device_status() == 0
 
 
+@pytest.mark.parametrize("B,T,C,NH,NKV", [
+    (2, 300, 1024, 8, 2),
+    (1, 257, 2048, 16, 4),
+    (1, 1000, 512, 4, 1),
+    (1, 128, 256, 2, 1),
+    (1, 1, 256, 2, 1),
+])
+def test_fp8_forward_matches_quantized_oracle(lib, B, T, C, NH, NKV):
+    """Without RoPE both sides quantize the same float32 values with the same
+    float32 scale arithmetic, so every Q/K/V code agrees; what remains is the
+    kernel's e4m3 rounding of the softmax weights (448 p) before PV.  With
+    out = sum_j P8_j Vd_j / l, l >= 1 (the row maximum contributes 1), a
+    weight rounds with relative error <= 2^-4 in the normal range and
+    absolute error <= 2^-10 / 448 below it (448 p < 2^-6), and out is rounded
+    to bf16 (2^-8 relative), so |out - ref| <= max|Vd| (2^-4 + T 2^-10 / 448
+    + 2^-8).  lse uses the unrounded float32 weights: float32 score sums and
+    exp2/log2 approximations give ~1e-6; the bar is 1e-3 max(1, |lse|)."""
+    import torch
+    from oracle.e4m3 import attention_forward_e4m3
+    w = shape_workload(B, T, C, NH, NKV, 0.0, seed=B * 100 + T + 79)
+    qkv_np, _ = make_inputs(w, "bf16")
+    qkv = to_device(qkv_np, "bf16")
+    out, lse = lib.forward_fp8(qkv, NH, NKV, 0.0)
+    torch.cuda.synchronize()
+    ref_out, ref_lse, Vd = attention_forward_e4m3(qkv_np, C, NH, NKV, 0.0)
+    vmax = float(np.abs(Vd).max())
+    out_bar = vmax * (2.0 ** -4 + T * 2.0 ** -10 / 448.0 + 2.0 ** -8)
+    lse_bar = 1e-3 * max(1.0, float(np.abs(ref_lse).max()))
+    e_out = float(np.abs(to_numpy(out) - ref_out).max())
+    e_lse = float(np.abs(to_numpy(lse) - ref_lse).max())
+    assert np.isfinite(to_numpy(out)).all()
+    assert e_out <= out_bar and e_lse <= lse_bar, (e_out, out_bar, e_lse, lse_bar)
+    assert lib.attn_device_status() == 0
+
+
 def test_fp8_forward_rejects_unsupported_shapes(lib):
     import torch
     from causal_attention_gqa_gb300.binding import AttnError
@@ -55,3 +90,30 @@ def test_fp8_forward_rejects_unsupported_shapes(lib):
     with pytest.raises(AttnError) as ei:
         lib.forward_fp8(qkv, 3, 1, 0.0)
     assert ei.value.status == -3
+
+
+@pytest.mark.parametrize("name", ["gqa_block", "long_context_gqa"])
+def test_fp8_forward_full_size_sampled(lib, name):
+    """Full-size call as bench.py --fp8 makes it (caller workspace); the
+    oracle is evaluated on seeded query rows of every head."""
+    import torch
+    from causal_attention_gqa_gb300 import binding
+    w = WORKLOADS[name]
+    qkv_np, dout_np = make_inputs(w, "bf16")
+    qkv = to_device(qkv_np, "bf16")
+    out = torch.empty((w.B, w.T, w.C), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.NH, w.T), dtype=torch.float32, device="cuda")
+    nb = binding.attn_fwd_fp8_workspace_bytes(w.B, w.T, w.C, w.NH, w.NKV, binding.DTYPE_BF16)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    binding.attn_fwd_fp8(out, lse, qkv, w.B, w.T, w.C, w.NH, w.NKV, w.rope_theta, binding.DTYPE_BF16, ws, nb)
+    torch.cuda.synchronize()
+    qr = sample_rows(w.T, 48, w.seed + 11)
+    ref = oracle.attention_sampled(qkv_np, dout_np, w.C, w.NH, w.NKV, w.rope_theta, qr, [], qr)
+    _, _, V = oracle.split_qkv(qkv_np, w.C, w.NH, w.NKV)
+    got_out = to_numpy(out)[:, qr]
+    got_lse = to_numpy(lse)[:, :, qr]
+    assert np.isfinite(got_out).all() and np.isfinite(got_lse).all()
+    e_out = float(np.abs(got_out - ref["out_rows"]).max()) / float(np.abs(V).max())
+    e_lse = float(np.abs(got_lse - ref["lse_rows"]).max()) / max(1.0, float(np.abs(ref["lse_rows"]).max()))
+    assert e_out <= OUT_BAR and e_lse <= LSE_BAR, (e_out, e_lse)
+    assert lib.attn_device_status() == 0

@@ -47,9 +47,20 @@ MUTATIONS = {
                                 "    freq = float(theta) ** (-1.0 * i / hd)\n    ang = pos.astype(np.float64)[:, None] * freq[None, :]          # [T, hd/2]"),
     "gptj_pairs_swapped": ("    x0, x1 = x[..., 0::2], x[..., 1::2]", "    x1, x0 = x[..., 0::2], x[..., 1::2]"),
     "gptj_adjoint_sign": ("    y[..., 1::2] = -g0 * sin + g1 * cos", "    y[..., 1::2] = g0 * sin + g1 * cos"),
+    # e4m3 quantization (oracle/e4m3.py), pinned by test_oracle_e4m3_pins.py
+    "e4m3_ties_away_from_zero": ("q = np.round(a / spacing) * spacing", "q = np.floor(a / spacing + 0.5) * spacing"),
+    "e4m3_no_subnormal_floor": ("e = np.maximum(E - 1, _E4M3_MIN_EXP)", "e = E - 1"),
+    "e4m3_two_mantissa_bits": ("_E4M3_MANT_BITS = 3", "_E4M3_MANT_BITS = 2"),
+    "e4m3_no_saturation": ("    q = np.minimum(q, E4M3_MAX)\n", ""),
+    "e4m3_scale_per_head": ("Qd = quantize_rows_e4m3(Qr, tile)", "Qd = quantize_rows_e4m3(Qr, None)"),
+    "e4m3_v_scale_per_tile": ("Vd = quantize_rows_e4m3(V, None)", "Vd = quantize_rows_e4m3(V, tile)"),
+    "e4m3_gqa_head_mapping_modulo": ("kh = h // grp\n            P, lse[b, h]", "kh = h % NKV\n            P, lse[b, h]"),
+    "e4m3_dequant_uses_scale": ("out[b, t0:t0 + step, h] = codes * d", "out[b, t0:t0 + step, h] = codes / d"),
 }
+MUTATED_FILE = {name: "e4m3.py" for name in MUTATIONS if name.startswith("e4m3_")}
 PIN_FILE = {name: "test_oracle_decode_pins.py" for name in MUTATIONS if name.startswith("decode_")}
 PIN_FILE.update({name: "test_oracle_rope_interleaved_pins.py" for name in MUTATIONS if name.startswith("gptj_")})
+PIN_FILE.update({name: "test_oracle_e4m3_pins.py" for name in MUTATIONS if name.startswith("e4m3_")})
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
@@ -58,7 +69,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     src_dir = os.path.join(ROOT, "oracle")
     dst_dir = tmp_path / "oracle"
     shutil.copytree(src_dir, dst_dir, ignore=shutil.ignore_patterns("__pycache__"))
-    path = dst_dir / "attention.py"
+    path = dst_dir / MUTATED_FILE.get(name, "attention.py")
     text = path.read_text()
     assert text.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     path.write_text(text.replace(old, new))
