@@ -9,11 +9,15 @@
 //     tile): x8 = rn(x * 448 / amax(tile)), dequantized by amax/448;
 //   * V in e4m3 with one scale per (batch row, kv head), stored transposed
 //     (V^T, keys contiguous) so that both operands of the PV MMA are K-major;
-//   * P = 2^(s - m) in [0, 1], stored as rn(448 * P) in e4m3 in TMEM.
+//   * P = 2^(s - m) with m the running row maximum, renewed only when a
+//     tile's maximum exceeds it by more than 2 (so P <= 4), stored as
+//     rn(112 * P) <= 448 in e4m3 in TMEM; the factor 112 is added to the
+//     exponent (2^(s - m + log2 112)), not multiplied in.
 // The scores S = Q8 K8^T come out of kind::f8f6f4 MMAs (32 elements per K
 // step, twice the bf16 rate) and are dequantized in the exponent: s =
-// S * scale * log2(e) * deq_q * deq_k.  O accumulates (448 P) V8 and is
-// scaled by deq_v / 448 with 1/l in the epilogue; l and lse use the float32 P.
+// S * scale * log2(e) * deq_q * deq_k.  O accumulates (112 P) V8 and l the
+// float32 112 P, so the epilogue scales O by deq_v / l; lse = m + log2(l) -
+// log2(112), in natural-log units.
 // The arithmetic is that of "nanoeuler -- CUDA kernels",
 // attention_forward_kernel, with the inputs rounded to e4m3 (3 mantissa bits)
 // and P rounded to e4m3 before the PV product.
@@ -27,9 +31,11 @@ namespace {
 
 constexpr int kHD = 128;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-// P is stored as 448 P in e4m3 (largest finite value 448), so P must stay <= 1:
-// O and l are rescaled whenever the row max grows (no lazy threshold).
-constexpr float kRescaleThreshold = 0.0f;
+// Lazy rescale: the running max m is renewed (and O, l rescaled) only when a
+// tile's maximum exceeds it by more than kRescaleThreshold, so P = 2^(s - m)
+// stays <= 4 and 112 P <= 448, the largest finite e4m3 value.
+constexpr float kRescaleThreshold = 2.0f;
+constexpr float kLog2PScale = 6.807354922057604f;   // log2(112)
 constexpr int kThreads = 320;
 
 struct Fp8Cfg {
@@ -268,7 +274,11 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
       const float dq = deq_qk[((size_t)item.b * heads + item.h0 + x) * n_qt + item.qt];
       const float* dk_row = deq_qk + ((size_t)item.b * heads + g.NH + item.kh) * n_qt;
       float m = -INFINITY, l = 0.f;
+      float dk_next = dk_row[0];
       for (int j = 0; j < n_kv; ++j, ++gk) {
+        // K-tile scale of this step, and the next one's load issued early.
+        const float dk_j = dk_next;
+        if (j + 1 < n_kv) dk_next = dk_row[j + 1];
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[x]), gk & 1, abort_flag,
                                                       kWaitLimitNs));
         if (!ok) break;
@@ -284,24 +294,27 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
           for (int c = 0; c < 128; ++c)
             if (c > row) sr[c] = __float_as_uint(-INFINITY);
         }
-        // Row max with 4 independent partial maxima.
+        // Row max with 4 independent partial maxima, two new scores per
+        // three-input max.
         float mx[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sr[k]);
 #pragma unroll
-        for (int c = 4; c < 128; c += 4)
+        for (int c = 4; c < 128; c += 8)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
-        const float sl2j = sl2 * dq * dk_row[j];        // scale * log2(e) * dequantization
+          for (int k = 0; k < 4; ++k)
+            mx[k] = ptx::fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 4 + k]));
+        const float sl2j = sl2 * dq * dk_j;             // scale * log2(e) * dequantization
         const float m_cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2j;
         const bool grow = m_cand > m + kRescaleThreshold;   // always true on an item's first tile
         const float m_new = grow ? m_cand : m;
         const float corr = grow ? ptx::ex2_approx(m - m_new) : 1.f;
-        // p = 2^(s - m) with s the dequantized scaled score; 448 p in e4m3,
-        // four per column, written over the score columns 8 at a time
+        // 112 p = 2^(s - m + log2 112) with s the dequantized scaled score, in
+        // e4m3, four per column, written over the score columns 8 at a time
         // (columns 8h.. hold keys 32h.., already read); row sum of the
-        // float32 p in 4 partial sums.
-        const float2 sl2x2 = make_float2(sl2j, sl2j), negm2 = make_float2(-m_new, -m_new);
+        // float32 112 p in 4 partial sums.
+        const float2 sl2x2 = make_float2(sl2j, sl2j);
+        const float2 negm2 = make_float2(kLog2PScale - m_new, kLog2PScale - m_new);
         float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -317,7 +330,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
             const float2 p1 = make_float2(ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y));
             acc[0] = __fadd2_rn(acc[0], p0);
             acc[1] = __fadd2_rn(acc[1], p1);
-            pw[c >> 2] = ptx::cvt_e4m3x2(448.f * p0.x, 448.f * p0.y) | (ptx::cvt_e4m3x2(448.f * p1.x, 448.f * p1.y) << 16);
+            pw[c >> 2] = ptx::cvt_e4m3x2(p0.x, p0.y) | (ptx::cvt_e4m3x2(p1.x, p1.y) << 16);
           }
           ptx::tmem_st8(s_addr + 8 * h, pw);
         }
@@ -353,7 +366,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
                         ptx::mbar_wait(ptx::smem_u32(&bars->stage_free), (use - 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
-      const float inv_l = deq_v[(size_t)item.b * g.NKV + item.kh] * (1.f / 448.f) / l;
+      const float inv_l = deq_v[(size_t)item.b * g.NKV + item.kh] / l;
 #pragma unroll 1
       for (int c0 = 0; c0 < kHD; c0 += 32) {
         uint32_t o[32];
@@ -377,7 +390,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
         ptx::mbar_arrive(ptx::smem_u32(&bars->staged[x]));
       }
       const int tq = item.qt * 128 + row;
-      if (tq < g.T) lse[((size_t)item.b * g.NH + item.h0 + x) * g.T + tq] = (m + log2f(l)) * 0.6931471805599453f;
+      if (tq < g.T)
+        lse[((size_t)item.b * g.NH + item.h0 + x) * g.T + tq] = (m + (log2f(l) - kLog2PScale)) * 0.6931471805599453f;
       if (storer) {
         // All four warps staged their rows: store the tile, and release the
         // staging tile once the TMA engine has read it.
