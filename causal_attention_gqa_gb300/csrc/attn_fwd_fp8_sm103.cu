@@ -39,7 +39,6 @@ constexpr float kLog2PScale = 6.807354922057604f;   // log2(112)
 constexpr int kThreads = 320;
 
 struct Fp8Cfg {
-  static constexpr int kAtom = 128 * 128;               // 128 rows x one 128-byte swizzle-atom column
   static constexpr int kTileBytes = 128 * kHD;          // e4m3 Q / K / V^T tile: one atom
   static constexpr int kOutBytes = 128 * kHD * 2;       // bf16 output tile
   static constexpr int kKStages = 2, kVStages = 2;
@@ -434,6 +433,9 @@ __global__ void __launch_bounds__(256) fp8_vamax_kernel(float* __restrict__ vtil
                                                         const __nv_bfloat16* __restrict__ qkv, Geometry g) {
   __shared__ float red[256];
   const int tile = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  // The quantization grid is launched as a programmatic dependent: its Q/K
+  // blocks need nothing from here and may start at once.
+  ptx::grid_dep_launch();
   float mx = 0.f;
   for (int u = threadIdx.x; u < 128 * (kHD / 8); u += 256) {
     const int t = tile * 128 + u / (kHD / 8), c = u % (kHD / 8);
@@ -457,8 +459,8 @@ __global__ void __launch_bounds__(256) fp8_vamax_kernel(float* __restrict__ vtil
 // and K heads (rotated, one scale per tile, into the e4m3 copy with the
 // layout of the bf16 rotated copy), heads NH+NKV.. the V heads (scale per
 // head from the tile maxima of fp8_vamax_kernel, written transposed into
-// V^T [b][kv][d][Tp]).  Thread = (row r = tid / 4, quarter of the head's
-// pairs or columns), so a thread holds 32 rotated values.
+// V^T [b][kv][d][Tp]).  In a Q/K block, thread = (row r = tid / 4, quarter of
+// the head's pairs), so a thread holds 32 rotated values.
 constexpr int kQuantThreads = 512;
 
 __global__ void __launch_bounds__(kQuantThreads) fp8_quant_kernel(uint8_t* __restrict__ qk8, uint8_t* __restrict__ vt8,
@@ -470,11 +472,11 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quant_kernel(uint8_t* __res
   __shared__ float red[kQuantThreads / 32];
   __shared__ __align__(16) uint8_t tile8[kHD][128 + 16];
   const int tile = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
-  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
-  const int t = tile * 128 + r;
-  const bool valid = t < g.T;
   const int heads = g.NH + g.NKV, n_qt = (g.T + 127) / 128;
   if (head < heads) {
+    const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int t = tile * 128 + r;
+    const bool valid = t < g.T;
     const __nv_bfloat16* src = qkv + ((size_t)b * g.T + (valid ? t : 0)) * g.W + head * kHD;
     float y0[16], y1[16];
     float mx = 0.f;
@@ -524,33 +526,47 @@ __global__ void __launch_bounds__(kQuantThreads) fp8_quant_kernel(uint8_t* __res
     }
     return;
   }
-  // V head kv: columns 32 part .. 32 part + 31 of row r, transposed, with the
-  // head's scale (maximum of its tile maxima).
+  // V head kv, transposed, with the head's scale (maximum of its tile
+  // maxima, written by fp8_vamax_kernel, which this grid may overlap: wait
+  // for it here).  Warp cw takes columns 8 cw .. 8 cw + 7, lane rg rows
+  // 4 rg .. 4 rg + 3, and writes each column's four bytes as one word, so
+  // the 32 lanes of a warp store 32 consecutive words.
+  ptx::grid_dep_wait();
   const int kv = head - heads;
   float mx = 0.f;
   for (int k = 0; k < n_qt; ++k) mx = fmaxf(mx, vtile_amax[((size_t)b * g.NKV + kv) * n_qt + k]);
   const float scale = mx > 0.f ? 448.f / mx : 1.f;
   if (tile == 0 && threadIdx.x == 0) deq_v[(size_t)b * g.NKV + kv] = mx > 0.f ? mx / 448.f : 1.f;
-  const __nv_bfloat16* src = qkv + ((size_t)b * g.T + (valid ? t : 0)) * g.W + g.C + g.NKV * kHD + kv * kHD + 32 * part;
+  const int cw = threadIdx.x >> 5, rg = threadIdx.x & 31;
+  uint4 raw[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = *reinterpret_cast<const uint4*>(src + 8 * q);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int i = 0; i < 4; ++i) {
+    const int tv = tile * 128 + 4 * rg + i;
+    raw[i] = make_uint4(0, 0, 0, 0);
+    if (tv < g.T)
+      raw[i] = *reinterpret_cast<const uint4*>(qkv + ((size_t)b * g.T + tv) * g.W + g.C + g.NKV * kHD + kv * kHD +
+                                               8 * cw);
+  }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t e = ptx::cvt_e4m3x2(bf16_lo(w[k]) * scale, bf16_hi(w[k]) * scale);
-      tile8[32 * part + 8 * q + 2 * k][r] = (uint8_t)(e & 0xFF);
-      tile8[32 * part + 8 * q + 2 * k + 1][r] = (uint8_t)(e >> 8);
-    }
+  for (int k = 0; k < 4; ++k) {          // bf16 pair k = columns 2k, 2k+1
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = (&raw[i].x)[k];
+    const uint32_t lo01 = ptx::cvt_e4m3x2(bf16_lo(w[0]) * scale, bf16_lo(w[1]) * scale);
+    const uint32_t lo23 = ptx::cvt_e4m3x2(bf16_lo(w[2]) * scale, bf16_lo(w[3]) * scale);
+    const uint32_t hi01 = ptx::cvt_e4m3x2(bf16_hi(w[0]) * scale, bf16_hi(w[1]) * scale);
+    const uint32_t hi23 = ptx::cvt_e4m3x2(bf16_hi(w[2]) * scale, bf16_hi(w[3]) * scale);
+    *reinterpret_cast<uint32_t*>(&tile8[8 * cw + 2 * k][4 * rg]) = lo01 | (lo23 << 16);
+    *reinterpret_cast<uint32_t*>(&tile8[8 * cw + 2 * k + 1][4 * rg]) = hi01 | (hi23 << 16);
   }
   __syncthreads();
-  // Row d of V^T: keys tile*128 .. +127, 32 bytes per thread.
-  const int d = threadIdx.x >> 2;
-  uint8_t* dst = vt8 + (((size_t)b * g.NKV + kv) * kHD + d) * (size_t)Tp + tile * 128 + 32 * part;
+  // Row d of V^T (keys tile*128 .. +127) in eight 16-byte chunks.
 #pragma unroll
-  for (int q = 0; q < 2; ++q)
-    *reinterpret_cast<uint4*>(dst + 16 * q) = *reinterpret_cast<const uint4*>(&tile8[d][32 * part + 16 * q]);
+  for (int k = 0; k < (kHD * 8) / kQuantThreads; ++k) {
+    const int id = threadIdx.x + k * kQuantThreads, d = id >> 3, q = id & 7;
+    uint8_t* dst = vt8 + (((size_t)b * g.NKV + kv) * kHD + d) * (size_t)Tp + tile * 128 + 16 * q;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile8[d][16 * q]);
+  }
 }
 
 }  // namespace
@@ -564,9 +580,8 @@ cudaError_t fp8_fwd_launch(const Fp8FwdArgs& a, cudaStream_t stream) {
   fp8_vamax_kernel<<<dim3(n_qt, g.NKV, g.B), 256, 0, stream>>>(a.vtile_amax, (const __nv_bfloat16*)a.qkv, g);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) {
-    fp8_quant_kernel<<<dim3(n_qt, heads + g.NKV, g.B), kQuantThreads, 0, stream>>>(
-        a.qk8, a.vt8, a.deq_qk, a.deq_v, a.vtile_amax, (const __nv_bfloat16*)a.qkv, g, a.Tp);
-    e = cudaGetLastError();
+    e = launch_pdl(fp8_quant_kernel, dim3(n_qt, heads + g.NKV, g.B), dim3(kQuantThreads), 0, stream, a.qk8, a.vt8,
+                   a.deq_qk, a.deq_v, (const float*)a.vtile_amax, (const __nv_bfloat16*)a.qkv, g, a.Tp);
   }
   prof_end(kKernelFp8Prep, stream);
   if (e != cudaSuccess) return e;
