@@ -296,8 +296,10 @@ ATTN_API int attn_fwd_rot(void* out, float* lse, const void* qkv, const void* qk
  * and RoPE handling as attn_fwd_ws with ATTN_DTYPE_BF16, but Q and K are
  * rotated and rounded to e4m3 with one scale per (batch row, head, 128-row
  * tile) (x8 = rn(x * 448 / amax)), V to e4m3 with one scale per (batch row, kv
- * head), and P = exp(s - m) to e4m3 (as 448 P) before the P V product; scores,
- * sums, O, out (bf16) and lse (float32) are accumulated in float32.  Expect
+ * head), and the softmax weights P = exp(s - m) to e4m3 (as 112 P, with the
+ * running row maximum m renewed only when exceeded by more than 2 log2 units,
+ * so 112 P <= 448) before the P V product; scores, sums, O, out (bf16) and lse
+ * (float32) are accumulated in float32.  Expect
  * errors of a few 1e-2 of max|out| (3 mantissa bits), not the bf16 path's
  * 2e-2.  Head size 128 and an even number of query heads per kv head only
  * (ATTN_ERR_UNSUPPORTED otherwise).  The workspace (attn_fwd_fp8_workspace_
