@@ -282,7 +282,10 @@ cudaError_t launch_rope_qk_bf16(void* dst, const void* qkv, const Geometry& g, c
                           << gph_log2;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   const long long need = (units + 255) / 256;
-  const int blocks = (int)(need < 152 * 3 ? need : 152 * 3);   // 3 resident 256-thread blocks per SM
+  // One unit per thread: blocks retire and refill the SMs while others wait
+  // on their loads (measured faster than 3 resident blocks per SM walking the
+  // units).
+  const int blocks = (int)need;
   prof_begin(kKernelRopeQK, stream);
   rope_qk_bf16_kernel<<<blocks, 256, 0, stream>>>((__nv_bfloat16*)dst, (const __nv_bfloat16*)qkv, g, gph_log2,
                                                   (int)units);
