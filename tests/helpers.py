@@ -6,7 +6,7 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
 def rel_err(x, ref) -> float:
-    """max |x - ref| / max |ref| (the spec error metric)."""
+    """max |x - ref| / max |ref| (the normalised error metric of the parity bars)."""
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     denom = np.abs(ref).max()
