@@ -90,6 +90,20 @@ def shape_workload(B, T, C, NH, NKV, rope_theta=0.0, qkv_std=1.0, dout_std=1.0,
                     float(rope_theta), ("f32", "bf16"), qkv_std, dout_std, seed)
 
 
+def rank_shard(w: Workload, rank: int, world: int) -> Workload:
+    """Rank ``rank``'s share of a data-parallel job over ``world`` ranks: the
+    batch rows rank*B .. rank*B + B - 1 of a global batch of world*B rows.
+
+    Batch rows are independent problems (no term of the method couples two of
+    them), so each rank draws its own rows from its own seed -- the workload's
+    seed plus 7919 * rank, shard 0 being the workload itself -- and the global
+    batch is the concatenation of the shards in rank order.
+    """
+    if not 0 <= rank < world:
+        raise ValueError("rank must lie in [0, world)")
+    return w if rank == 0 else w.replace(seed=w.seed + 7919 * rank)
+
+
 def make_inputs(w: Workload, dtype: str = "f32"):
     """Return (qkv, dout) as float32 NumPy arrays, already rounded to ``dtype``.
 
