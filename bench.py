@@ -28,6 +28,8 @@ included) next to attn_fwd_ws on the workload and prints one JSON line
 (forward TFLOP/s against the FP8 peak = 2 x the measured bf16 peak, the
 nominal dense fp8/bf16 ratio).
 
+`--rope-interleaved` runs the same step with interleaved (GPT-J) RoPE pairs.
+
 `--decode B,L,NH,NKV,hd` times attn_decode (one new token per batch row
 against a bf16 KV cache of L rows) instead and prints one JSON line with its
 HBM throughput (cache bytes read per call / device time; L2 flushed between
@@ -68,6 +70,7 @@ def parse_args():
     ap.add_argument("--decode", default=None, metavar="B,L,NH,NKV,hd")
     ap.add_argument("--proj", default=None, metavar="B,T,Cm,NH,NKV,hd")
     ap.add_argument("--fp8", action="store_true")
+    ap.add_argument("--rope-interleaved", action="store_true")
     return ap.parse_args()
 
 
@@ -279,7 +282,7 @@ def run_ours(args, w):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
-    code = binding.DTYPE_BF16
+    code = binding.DTYPE_BF16 | (binding.FLAG_ROPE_INTERLEAVED if args.rope_interleaved else 0)
 
     def step(qkv=qkv, dout=dout, dqkv=dqkv):
         binding.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, fws, fws_bytes, sptr)
@@ -402,6 +405,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, {"parallelism": f"batch rows sharded over {world} ranks, no collective"
                                 if world > 1 else "single GPU", "global_batch": world * w.B,
+                                "rope_pairs": "interleaved (GPT-J)" if args.rope_interleaved else "NEOX",
                                 "l2": "flushed between timed steps (256 MiB write outside the timed events)",
                                 "kernel_breakdown": f"separate pass of {n_prof} steps with per-kernel events",
                                 "peak_bf16_frac": value / world / peak_tf,
