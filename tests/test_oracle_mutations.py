@@ -47,6 +47,13 @@ MUTATIONS = {
                                 "    freq = float(theta) ** (-1.0 * i / hd)\n    ang = pos.astype(np.float64)[:, None] * freq[None, :]          # [T, hd/2]"),
     "gptj_pairs_swapped": ("    x0, x1 = x[..., 0::2], x[..., 1::2]", "    x1, x0 = x[..., 0::2], x[..., 1::2]"),
     "gptj_adjoint_sign": ("    y[..., 1::2] = -g0 * sin + g1 * cos", "    y[..., 1::2] = g0 * sin + g1 * cos"),
+    # QKV projection, pinned by test_oracle_projection_pins.py
+    "proj_rotates_v_too": ("    qk = qkv[:, :(NH + NKV) * hd].reshape(M // T, T, NH + NKV, hd)",
+                           "    qk = qkv.reshape(M // T, T, NH + 2 * NKV, hd)"),
+    "proj_positions_run_across_sequences": ("    qk = qkv[:, :(NH + NKV) * hd].reshape(M // T, T, NH + NKV, hd)",
+                                            "    qk = qkv[:, :(NH + NKV) * hd].reshape(1, M, NH + NKV, hd)"),
+    "proj_ignores_interleaved_flag": ("        rot, _ = _rope_fns(rope_interleaved)\n        qk = rot(qk, rope_theta)",
+                                      "        rot, _ = _rope_fns(False)\n        qk = rot(qk, rope_theta)"),
     # e4m3 quantization (oracle/e4m3.py), pinned by test_oracle_e4m3_pins.py
     "e4m3_ties_away_from_zero": ("q = np.round(a / spacing) * spacing", "q = np.floor(a / spacing + 0.5) * spacing"),
     "e4m3_no_subnormal_floor": ("e = np.maximum(E - 1, _E4M3_MIN_EXP)", "e = E - 1"),
@@ -61,6 +68,7 @@ MUTATED_FILE = {name: "e4m3.py" for name in MUTATIONS if name.startswith("e4m3_"
 PIN_FILE = {name: "test_oracle_decode_pins.py" for name in MUTATIONS if name.startswith("decode_")}
 PIN_FILE.update({name: "test_oracle_rope_interleaved_pins.py" for name in MUTATIONS if name.startswith("gptj_")})
 PIN_FILE.update({name: "test_oracle_e4m3_pins.py" for name in MUTATIONS if name.startswith("e4m3_")})
+PIN_FILE.update({name: "test_oracle_projection_pins.py" for name in MUTATIONS if name.startswith("proj_")})
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
