@@ -328,3 +328,28 @@ def test_sampled_mode_equals_full_oracle():
     for (b, kh) in groups:
         np.testing.assert_allclose(s["dk_rows"][(b, kh)], dk[b, kr, kh], rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(s["dv_rows"][(b, kh)], dv[b, kr, kh], rtol=1e-11, atol=1e-13)
+
+
+def test_key_shift_and_value_scale_invariances():
+    """Without RoPE, adding one vector c to every key adds q.c/sqrt(hd) to all
+    scores of a query row: the softmax (so out) is unchanged and lse shifts by
+    q.c/sqrt(hd).  Scaling V by a scales out by a and leaves lse alone."""
+    rng = np.random.default_rng(17)
+    B, T, NH, NKV, hd = 2, 9, 4, 2, 8
+    C = NH * hd
+    qkv = rng.normal(size=(B, T, (NH + 2 * NKV) * hd))
+    out, lse = oracle.attention_forward(qkv, C, NH, NKV, 0.0)
+    c = rng.normal(size=hd)
+    shifted = qkv.copy()
+    for kh in range(NKV):
+        shifted[:, :, C + kh * hd:C + (kh + 1) * hd] += c
+    out_s, lse_s = oracle.attention_forward(shifted, C, NH, NKV, 0.0)
+    np.testing.assert_allclose(out_s, out, rtol=0, atol=1e-12)
+    Q, _, _ = oracle.split_qkv(qkv, C, NH, NKV)
+    want = lse + np.einsum("bthd,d->bht", Q, c) / np.sqrt(hd)
+    np.testing.assert_allclose(lse_s, want, rtol=0, atol=1e-12)
+    scaled = qkv.copy()
+    scaled[:, :, C + NKV * hd:] *= -2.5
+    out_v, lse_v = oracle.attention_forward(scaled, C, NH, NKV, 0.0)
+    np.testing.assert_allclose(out_v, -2.5 * out, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(lse_v, lse)
