@@ -61,8 +61,19 @@ MUTATIONS = {
     "e4m3_no_saturation": ("    q = np.minimum(q, E4M3_MAX)\n", ""),
     "e4m3_scale_per_head": ("Qd = quantize_rows_e4m3(Qr, tile)", "Qd = quantize_rows_e4m3(Qr, None)"),
     "e4m3_v_scale_per_tile": ("Vd = quantize_rows_e4m3(V, None)", "Vd = quantize_rows_e4m3(V, tile)"),
-    "e4m3_gqa_head_mapping_modulo": ("kh = h // grp\n            P, lse[b, h]", "kh = h % NKV\n            P, lse[b, h]"),
+    "e4m3_gqa_head_mapping_modulo": ("kh = h // grp\n                P, lse[b, h]",
+                                     "kh = h % NKV\n                P, lse[b, h]"),
     "e4m3_dequant_uses_scale": ("out[b, t0:t0 + step, h] = codes * d", "out[b, t0:t0 + step, h] = codes / d"),
+    # rounding of the softmax weights in the e4m3 forward (oracle/e4m3.py)
+    "e4m3_weight_scale_448": ("P_SCALE = 112.0 ", "P_SCALE = 448.0 "),
+    "e4m3_renewal_threshold_zero": ("RESCALE_THRESHOLD = 2.0 ", "RESCALE_THRESHOLD = 0.0 "),
+    "e4m3_renew_every_block": ("renew = bool(mb > m + threshold)", "renew = True"),
+    "e4m3_weights_unrounded": ("p8 = e4m3_round(p)", "p8 = p"),
+    "e4m3_l_sums_rounded_weights": ("l += p.sum()", "l += p8.sum()"),
+    "e4m3_no_rescale_on_renewal": ("            o *= c\n            o_abs *= c", "            o_abs *= c"),
+    "e4m3_rounded_path_head_mapping": ("            kh = h // grp\n            for t in rows:",
+                                       "            kh = h % NKV\n            for t in rows:"),
+    "e4m3_midpoint_not_reported": ("dev = np.maximum(hi - p8, p8 - lo)", "dev = np.zeros_like(p8)"),
 }
 MUTATED_FILE = {name: "e4m3.py" for name in MUTATIONS if name.startswith("e4m3_")}
 PIN_FILE = {name: "test_oracle_decode_pins.py" for name in MUTATIONS if name.startswith("decode_")}
