@@ -16,6 +16,15 @@ workload's shapes, its own seeded batch rows: the path shards over batch rows
 and kv groups with no exchange); the value is the work of all ranks divided by
 the slowest rank's time.
 
+The default run also times the long-context GQA workload (`--also`, at most
+`--also-steps` steps) in the same process and reports it under `per_config`,
+so both GQA bf16 configurations are measured by one command.  Fractions are
+priced against the measured burst bf16 peak (a short cuBLAS loop at full
+clocks) unless a timed region lasts at least two seconds, when the sustained
+(power-capped) figure applies; the line names the peak it used.  Next to the
+per-kernel roofline, `bwd_combined` gives the backward's five algorithmic GEMM
+units over the summed time of its two tensor-core kernels.
+
 `--impl reference` times the float64 CPU oracle instead (rank 0 only), on a
 bounded sample of the same workload: one kv group of one batch row per step.
 
@@ -66,6 +75,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_block")
+    ap.add_argument("--also", default="long_context_gqa",
+                    help="second workload timed in the same run and reported under per_config ('' for none)")
+    ap.add_argument("--also-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", default=None, metavar="B,L,NH,NKV,hd")
     ap.add_argument("--proj", default=None, metavar="B,T,Cm,NH,NKV,hd")
@@ -247,28 +259,59 @@ def max_over_ranks(values, device):
     return [float(x) for x in t]
 
 
-def run_ours(args, w):
+SUSTAINED_AFTER_S = 2.0     # a timed region at least this long is priced against the sustained peak
+
+
+def choose_peak(peaks, peak_src, timed_seconds):
+    """The bf16 peak a timed region is priced against: the burst figure (a
+    short cuBLAS loop at full clocks) unless the region lasted long enough
+    for the power cap to pull the clocks down, then the sustained one."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    if timed_seconds >= SUSTAINED_AFTER_S:
+        return sustained, f"{peak_src} bf16_tflops_sustained ({timed_seconds:.2f} s timed region)"
+    return burst, f"{peak_src} bf16_tflops (burst: {timed_seconds:.3f} s timed region < {SUSTAINED_AFTER_S} s)"
+
+
+def roofline_of(prof, w, peak_tf, peak_desc):
+    """Dominant kernel's roofline (algorithmic FLOPs per launch / mean launch
+    time) and the backward's combined figure: the five backward GEMM units
+    over the summed time of the dK/dV and dQ kernels (the per-kernel split
+    credits the S/dP recomputation of the dQ kernel to neither)."""
+    kernel_ms = {k: v[1] for k, v in prof.items()}
+    dom = max(kernel_ms, key=kernel_ms.get)
+    n_launch, tot_ms = prof[dom]
+    kfl = kernel_algorithmic_flops(dom, w)
+    roof = None
+    if kfl is not None:
+        achieved = kfl / (tot_ms / n_launch * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": traffic_for(dom), "peak_source": peak_desc,
+                "avg_launch_ms": tot_ms / n_launch, "algorithmic_flop_per_launch": kfl}
+    bwd = [k for k in ("bwd_dkdv_tc05", "bwd_dq_tc05") if k in prof]
+    combined = None
+    if bwd:
+        t = sum(prof[k][1] / prof[k][0] for k in bwd)
+        achieved = w.flops_bwd() / (t * 1e-3) / 1e12
+        combined = {"kernels": bwd, "algorithmic_flop_per_step": w.flops_bwd(), "ms": t,
+                    "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf}
+    return roof, combined
+
+
+def time_workload(args, w, dev, world, steps, e2e):
+    """Time `steps` fwd+bwd steps of workload `w` (this rank's shard) with
+    inputs resident in HBM; then a per-kernel event pass; then (if `e2e`) the
+    end-to-end loop with host buffers.  Returns raw per-rank numbers."""
     import torch
     import torch.distributed as dist
     from causal_attention_gqa_gb300 import binding
-    from causal_attention_gqa_gb300.workloads import make_inputs, rank_shard
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    w = rank_shard(w, rank, world)     # this rank's batch rows of the global batch
-    if world > 1:
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    binding.load()
+    from causal_attention_gqa_gb300.workloads import make_inputs
 
     B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
     qkv_np, dout_np = make_inputs(w, "bf16")
     qkv_host = torch.from_numpy(qkv_np).to(torch.bfloat16).pin_memory()
     dout_host = torch.from_numpy(dout_np).to(torch.bfloat16).pin_memory()
+    del qkv_np, dout_np
     qkv = qkv_host.to(dev)
     dout = dout_host.to(dev)
     out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
@@ -304,13 +347,13 @@ def run_ours(args, w):
     # ---- device-resident timed region: K steps, L2 flushed between steps.
     # No per-kernel events here: events between the backward's programmatically
     # dependent launches would serialise them.
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     time.sleep(0.15)
     barrier()
     wall0 = time.perf_counter()
-    for k in range(args.steps):
+    for k in range(steps):
         flush.zero_()
         starts[k].record(stream)
         step()
@@ -319,19 +362,23 @@ def run_ours(args, w):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     ms_steps = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
-    ms_per_step = sum(ms_steps) / args.steps
+    ms_per_step = sum(ms_steps) / steps
     if binding.attn_device_status() != 0:
         raise RuntimeError("device-side error recorded during the timed region")
 
     # ---- the same steps again with the library's per-kernel CUDA events on
     # the launching stream: kernel breakdown, dominant kernel, roofline.
-    n_prof = max(1, min(args.steps, 50))
+    n_prof = max(1, min(steps, 50))
     binding.attn_profile_start()
     for _ in range(n_prof):
         flush.zero_()
         step()
     barrier()
     prof = binding.attn_profile_stop()
+    res = {"ms_per_step": ms_per_step, "timed_s": sum(ms_steps) * 1e-3, "wall": wall, "clocks": clocks,
+           "prof": prof, "n_prof": n_prof, "steps": steps}
+    if not e2e:
+        return res
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its qkv and dout from pinned host memory and reads its dqkv back; the
@@ -345,7 +392,7 @@ def run_ours(args, w):
     ev_out = [torch.cuda.Event() for _ in range(2)]
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(2, min(args.steps, 50))
+    e2e_steps = max(2, min(steps, 50))
     barrier()
     e_start.record(stream)
     s_in.wait_event(e_start)
@@ -371,58 +418,104 @@ def run_ours(args, w):
     stream.wait_event(ev_out[1])
     e_end.record(stream)
     barrier()
-    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
+    res.update({"e2e_ms": e_start.elapsed_time(e_end) / e2e_steps, "e2e_steps": e2e_steps,
+                "h2d_bytes": qkv_host.numel() * 2 + dout_host.numel() * 2, "d2h_bytes": dqkv_host.numel() * 2})
+    return res
 
-    ms_per_step, e2e_ms = max_over_ranks([ms_per_step, e2e_ms], dev)
+
+def summarise(w, world, r, peaks, peak_src):
+    """Whole-job throughput, peak fraction, kernel table and roofline of one
+    timed workload (r from time_workload, times already max-reduced)."""
+    prof = r["prof"]
+    fl = flops_per_step(w)
+    value = world * fl / (r["ms_per_step"] * 1e-3) / 1e12
+    peak_tf, peak_desc = choose_peak(peaks, peak_src, r["timed_s"])
+    roof, combined = roofline_of(prof, w, peak_tf, peak_desc)
+    kernel_ms = {k: v[1] for k, v in prof.items()}
+    return {
+        "value": value, "ms_per_step": r["ms_per_step"], "steps": r["steps"],
+        "peak_bf16_frac": value / world / peak_tf, "peak_bf16_tflops": peak_tf, "peak_source": peak_desc,
+        "wall_s_timed_region": r["wall"], "clocks": r["clocks"],
+        "kernels": {k: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / sum(kernel_ms.values())}
+                    for k, v in prof.items()},
+        "gpu_launches": int(round(sum(v[0] for v in prof.values()) / r["n_prof"] * r["steps"])),
+        "roofline": roof, "bwd_combined": combined,
+    }
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from causal_attention_gqa_gb300 import binding
+    from causal_attention_gqa_gb300.workloads import WORKLOADS, rank_shard
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    binding.load()
+
+    # The headline workload, then (default run) the long-context GQA workload
+    # in the same process: the two GQA bf16 configurations.
+    ws = rank_shard(w, rank, world)     # this rank's batch rows of the global batch
+    head = time_workload(args, ws, dev, world, args.steps, e2e=True)
+    extra = {}
+    if args.also and args.also != w.name:
+        wa = WORKLOADS[args.also]
+        extra[wa.name] = (wa, time_workload(args, rank_shard(wa, rank, world), dev, world,
+                                            min(args.steps, args.also_steps), e2e=False))
+    head["ms_per_step"], head["e2e_ms"] = max_over_ranks([head["ms_per_step"], head["e2e_ms"]], dev)
+    for name, (wa, r) in extra.items():
+        (r["ms_per_step"],) = max_over_ranks([r["ms_per_step"]], dev)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
-    fl = flops_per_step(w)
-    value = world * fl / (ms_per_step * 1e-3) / 1e12
-    e2e_value = world * fl / (e2e_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
-    peak_tf = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-
-    # dominant kernel by device time in the timed region
-    kernel_ms = {k: v[1] for k, v in prof.items()}
-    dom = max(kernel_ms, key=kernel_ms.get)
-    n_launch, tot_ms = prof[dom]
-    kfl = kernel_algorithmic_flops(dom, w)
-    roofline = None
-    if kfl is not None:
-        achieved = kfl / (tot_ms / n_launch * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": achieved / peak_tf, "traffic": traffic_for(dom),
-                    "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a step loop)",
-                    "avg_launch_ms": tot_ms / n_launch,
-                    "algorithmic_flop_per_launch": kfl}
+    s = summarise(ws, world, head, peaks, peak_src)
+    fl = flops_per_step(ws)
+    e2e_value = world * fl / (head["e2e_ms"] * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": s["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": s["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, {"parallelism": f"batch rows sharded over {world} ranks, no collective"
-                                if world > 1 else "single GPU", "global_batch": world * w.B,
-                                "rope_pairs": "interleaved (GPT-J)" if args.rope_interleaved else "NEOX",
-                                "l2": "flushed between timed steps (256 MiB write outside the timed events)",
-                                "kernel_breakdown": f"separate pass of {n_prof} steps with per-kernel events",
-                                "peak_bf16_frac": value / world / peak_tf,
-                                "wall_s_timed_region": wall}),
-        "clocks": clocks,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": qkv_host.numel() * 2 + dout_host.numel() * 2,
-                "d2h_bytes_per_step": dqkv_host.numel() * 2, "ms_per_step": e2e_ms, "steps": e2e_steps,
+        "config": config_of(ws, {"parallelism": f"batch rows sharded over {world} ranks, no collective"
+                                 if world > 1 else "single GPU", "global_batch": world * ws.B,
+                                 "rope_pairs": "interleaved (GPT-J)" if args.rope_interleaved else "NEOX",
+                                 "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                                 "kernel_breakdown": f"separate pass of {head['n_prof']} steps with per-kernel "
+                                                     "events",
+                                 "peak_bf16_frac": s["peak_bf16_frac"], "peak_bf16_tflops": s["peak_bf16_tflops"],
+                                 "peak_source": s["peak_source"],
+                                 "measured_peaks": {k: peaks.get(k) for k in
+                                                    ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs")},
+                                 "wall_s_timed_region": s["wall_s_timed_region"]}),
+        "clocks": s["clocks"],
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": head["h2d_bytes"],
+                "d2h_bytes_per_step": head["d2h_bytes"], "ms_per_step": head["e2e_ms"],
+                "steps": head["e2e_steps"],
                 "copies": "pinned host buffers; h2d and d2h on two copy streams overlapping the neighbouring "
                           "steps' kernels (two device buffer sets); L2 not flushed"},
-        "gpu_launches": int(round(sum(v[0] for v in prof.values()) / n_prof * args.steps)),
-        "kernels": {k: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / sum(kernel_ms.values())}
-                    for k, v in prof.items()},
-        "roofline": roofline,
+        "gpu_launches": s["gpu_launches"],
+        "kernels": s["kernels"],
+        "roofline": s["roofline"],
+        "bwd_combined": s["bwd_combined"],
     }
+    if extra:
+        line["per_config"] = {}
+        for name, (wa, r) in extra.items():
+            sa = summarise(rank_shard(wa, rank, world), world, r, peaks, peak_src)
+            sa["config"] = config_of(rank_shard(wa, rank, world))
+            line["per_config"][name] = sa
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = {k: v for k, v in time_oracle(w).items() if k != "seconds"}
+        line["cpu_baseline"] = {k: v for k, v in time_oracle(ws).items() if k != "seconds"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

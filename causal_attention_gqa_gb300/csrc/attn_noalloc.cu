@@ -14,7 +14,10 @@
 // Every GPU on which this library's code for this file is loaded holds it
 // until the process exits.  Host code cannot use the array's name as a
 // device address, so the first call on each device (with that device
-// current) asks the runtime for the array's device address and remembers it.
+// current) asks the runtime for the array's device address and remembers it
+// for the rest of the process.  A cudaDeviceReset() makes that address stale
+// (the array is placed again in the new context); the header tells callers
+// not to use this entry point on a device after resetting it.
 #include <mutex>
 
 #include <cuda_runtime.h>

@@ -31,3 +31,25 @@ def test_kernel_flops_add_up_to_the_step():
     assert k["bwd_dkdv_tc05"] + k["bwd_dq_tc05"] == w.flops_bwd()
     assert sum(k.values()) == bench.flops_per_step(w)
     assert bench.kernel_algorithmic_flops("rope_qk", w) is None     # memory pass: no FLOP roofline
+
+
+def test_peak_choice_follows_the_length_of_the_timed_region():
+    peaks = {"bf16_tflops": 1842.5, "bf16_tflops_sustained": 1679.4}
+    tf, desc = bench.choose_peak(peaks, "measured", 0.0064)
+    assert tf == 1842.5 and "burst" in desc
+    tf, desc = bench.choose_peak(peaks, "measured", 3.0)
+    assert tf == 1679.4 and "sustained" in desc
+
+
+def test_combined_backward_fraction_counts_five_units_over_both_kernels():
+    w = WORKLOADS["gqa_block"]
+    # per-kernel events: (launches, total ms)
+    prof = {"fwd_tc05": (10, 0.665), "bwd_dkdv_tc05": (10, 1.173), "bwd_dq_tc05": (10, 1.128),
+            "rope_qk": (10, 0.192)}
+    roof, comb = bench.roofline_of(prof, w, 1842.5, "burst")
+    assert roof["kernel"] == "bwd_dkdv_tc05"
+    assert abs(roof["achieved"] - 4 * 2.0 * w.B * w.NH * w.hd * w.causal_pairs / 0.1173e-3 / 1e12) < 1e-6
+    assert comb["algorithmic_flop_per_step"] == w.flops_bwd()
+    assert abs(comb["ms"] - 0.2301) < 1e-9
+    assert abs(comb["achieved"] - w.flops_bwd() / 0.2301e-3 / 1e12) < 1e-6
+    assert abs(comb["frac"] - comb["achieved"] / 1842.5) < 1e-12

@@ -6,8 +6,10 @@ fixed memory budget, plugins handed only input/output pointers).  These tests
 call it through the C ABI and compare its dqkv with the regular attn_bwd
 (caller-provided workspace) on the same inputs, twice in a row, because the
 built-in scratch buffer is shared by every call and keeps the previous call's
-contents.  This file is collected last so that a run stopping at the first
-failure has already run every other test.
+contents.  Both entry points run the same deterministic kernels on the same
+workspace layout, so the results must agree bit for bit: a tolerance would hide
+a scratch-layout mistake.  This file is collected last so that a run stopping
+at the first failure has already run every other test.
 """
 import numpy as np
 import pytest
@@ -39,6 +41,7 @@ def test_noalloc_backward_matches_workspace_backward_twice(lib, dtype, shape, th
         got = to_numpy(dqkv)
         assert np.isfinite(got).all()
         assert rel_err(got, to_numpy(ref)) <= TOL[dtype]
+        assert torch.equal(dqkv, ref), "attn_bwd_noalloc differs from attn_bwd on the same inputs"
     assert lib.attn_device_status() == 0
 
 
