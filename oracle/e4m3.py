@@ -112,9 +112,10 @@ def weighted_row_e4m3(s2, vcodes, ds2=None, decisions=None, block: int = KEY_BLO
 
     s2      : float64 scores of the row's visible keys (key 0 first), log2 units.
     vcodes  : [n, hd] e4m3 codes of those keys' V rows.
-    ds2     : optional per-key bound on how far a float32 evaluation of s2 - m
+    ds2     : optional per-key bound on how far a float32 evaluation of s2
               may lie from this one (log2 units); when given, the row also
-              reports what float32 may decide either way.
+              reports what float32 may decide either way (a weight's exponent
+              s - m moves by its own key's reach plus that of m).
     decisions : optional {block index: bool} that replaces the renewal decision
               of those blocks (to follow the other outcome of an open
               decision); the other blocks decide as usual.
@@ -164,7 +165,9 @@ def weighted_row_e4m3(s2, vcodes, ds2=None, decisions=None, block: int = KEY_BLO
         o += p8 @ v[j0:j0 + block]
         o_abs += p8 @ np.abs(v[j0:j0 + block])
         if ds2 is not None:
-            db = ds2[j0:j0 + block]
+            # s - m moves by the reach of s and by that of m (the score of a
+            # key seen so far)
+            db = ds2[j0:j0 + block] + ds2[:j0 + sb.size].max()
             lo = e4m3_round(p * 2.0 ** (-db))
             hi = e4m3_round(p * 2.0 ** db)
             dev = np.maximum(hi - p8, p8 - lo)          # > 0 only next to a midpoint

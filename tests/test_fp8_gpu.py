@@ -1,93 +1,117 @@
-"""GPU check of the e4m3 (FP8) forward (attn_fwd_fp8) against the float64
-oracle on the original inputs.
+"""GPU check of the e4m3 (FP8) forward (attn_fwd_fp8) against the e4m3
+oracle (oracle/e4m3.py), which restates every step the kernel takes: Q/K
+quantized per 128-row tile after RoPE, V per head, and the softmax weights
+rounded to e4m3 as P8 = e4m3(112 * 2^(s - m)) with the lazily renewed row
+maximum, walking the keys in 128-key blocks.
 
-Bars, from the e4m3 rounding model (3 mantissa bits: a value scaled into the
-e4m3 range is rounded with a relative error of at most 2^-4):
-  * out: out = sum_j P_j V_j / l with every P_j and every V element rounded,
-    so |out - ref| <= (2^-4 + 2^-4 + 2^-8) max|V| = 0.129 max|V| from those
-    two roundings (rows that see a single key reach it: out = the rounded
-    V_0), plus the absolute error of weights in the e4m3 subnormal range.
-    The kernel stores 112 p (p = 2^(s - m) <= 4 with a lazily renewed row
-    maximum m), so a weight with 112 p < 2^-6 is off by at most 2^-10 / 112,
-    and l >= 1: at most T 2^-10 / 112 max|V| over a row.
-  * lse: the scores s = q . k / sqrt(hd) inherit the rounding of Q and K;
-    its worst case (all 128 products rounded the same way) is far larger
-    than what random inputs show, so the bar, 0.1 max(1, max|lse|), is an
-    empirical margin over the measured ~0.01 relative error.
+The bar is element-wise and does not grow with T.  It is the sum of:
+  * the bf16 rounding of out (8 significant bits): 2^-8 |out|;
+  * float32 evaluation order (the sum l of up to T weights, the O
+    accumulator's rescales, the final scaling): |out| * (l_rel + 2^-16), with
+    l_rel the oracle's bound on how far l moves when every weight is
+    evaluated in float32 (see weighted_row_e4m3);
+  * the weights that lie within float32 reach of an e4m3 midpoint (they may
+    round either way): the oracle's o_bound, one code step times |V| for
+    each such weight, over l; zero for most rows;
+  * the tensor core's accumulation of the PV products: MMA_REL per added
+    K slice times the sum of |P8 V8|, over l.
+With RoPE the rotated Q/K values differ from the oracle's by the rotation's
+float32 arithmetic and angle error (at most ANGLE_ERROR times the pair's
+norm); the oracle carries that into the score reach, so Q/K codes next to a
+midpoint are covered the same way.  A row whose renewal decision is open
+(its block maximum within reach of m + 2) may follow either branch; the
+oracle evaluates both.
+
+lse: the kernel's l sums unrounded weights, so lse is the log-sum-exp of the
+quantized scores whatever the rounding: |lse - ref| <= ln 2 * (score reach)
++ float32 terms.
 """
 import numpy as np
 import pytest
 
-import oracle
 from causal_attention_gqa_gb300.workloads import WORKLOADS, make_inputs, sample_rows, shape_workload
-from helpers import rel_err, to_device, to_numpy
+from helpers import to_device, to_numpy
 
 pytestmark = pytest.mark.gpu
-P_SUBNORMAL = 2.0 ** -10 / 112.0     # absolute error of one stored weight below the normal range
+ANGLE_ERROR = 2e-6          # rotation error per unit pair norm (angle ~6e-7 rad plus float32 products)
+MMA_REL = 2.0 ** -22        # rounding of one tensor-core accumulation step, relative to what it adds
 
 
-def out_bar(T):   # times max|V|
-    return 2.0 ** -4 + 2.0 ** -4 + 2.0 ** -8 + T * P_SUBNORMAL
-LSE_BAR = 0.1      # times max(1, max|lse|)
+def fp8_reference(qkv_np, w, theta, interleaved=False, rows=None):
+    from oracle.e4m3 import attention_forward_e4m3
+    return attention_forward_e4m3(qkv_np, w.C, w.NH, w.NKV, theta, rope_interleaved=interleaved, rows=rows,
+                                  angle_error=ANGLE_ERROR if theta > 0 else 0.0, mma_rel=MMA_REL)
+
+
+def check_against_e4m3_oracle(got_out, got_lse, ref, rows, hd):
+    """Element-wise comparison with the bar described above; returns the
+    largest error / bar, the bars of every checked element over max|V|, and
+    the number of rows with an open renewal decision."""
+    ref_out, ref_lse, Vd, reach = ref
+    vmax = float(np.abs(Vd).max())
+    B, T, C = ref_out.shape
+    NH = ref_lse.shape[1]
+    worst = 0.0
+    bars = []
+    open_rows = 0
+    for b in range(B):
+        for t in rows:
+            for h in range(NH):
+                cols = slice(h * hd, (h + 1) * hd)
+                g = got_out[b, t, cols]
+                assert np.isfinite(g).all()
+                cand = [(ref_out[b, t, cols], reach["o_bound"][b, t, cols], reach["l_rel"][b, h, t])]
+                cand += reach["open"].get((b, h, int(t)), [])
+                open_rows += len(cand) > 1
+                best = None
+                for o_ref, o_bnd, l_rel in cand:
+                    bar = (2.0 ** -8 * np.abs(o_ref)
+                           + (1 + 2.0 ** -8) * (o_bnd + np.abs(o_ref) * (l_rel + 2.0 ** -16)
+                                                + reach["o_acc"][b, t, cols])
+                           + 2.0 ** -30 * vmax)
+                    r = float((np.abs(g - o_ref) / bar).max())
+                    if best is None or r < best[0]:
+                        best = (r, bar)
+                worst = max(worst, best[0])
+                bars.append(best[1] / vmax)
+                lse_bar = (np.log(2.0) * reach["s_reach"][b, h, t] + 2.0 ** -18
+                           + 2.0 ** -20 * abs(ref_lse[b, h, t]))
+                e_lse = abs(got_lse[b, h, t] - ref_lse[b, h, t])
+                assert e_lse <= lse_bar, (b, h, t, e_lse, lse_bar)
+    assert worst <= 1.0, f"out error reaches {worst:.3f} of the bar"
+    return worst, np.concatenate(bars), open_rows
+
+
+def assert_bar_is_tight(bars):
+    """The bar does not hide a loose comparison: on a typical element it is
+    within two bf16 steps of max|V| (measured medians: 1e-4 without RoPE,
+    2e-3 to 4e-3 with it, where most rows have a Q/K code within the
+    rotation's reach of a midpoint), and nowhere more than the error one
+    rounded weight can make (2^-4 relative)."""
+    assert np.median(bars) <= 2.0 ** -7, np.median(bars)
+    assert bars.max() <= 2.0 ** -4, bars.max()
 
 
 @pytest.mark.parametrize("B,T,C,NH,NKV,theta,interleaved", [
+    (2, 300, 1024, 8, 2, 0.0, False),
+    (1, 257, 2048, 16, 4, 0.0, False),
+    (1, 1000, 512, 4, 1, 0.0, False),
+    (1, 128, 256, 2, 1, 0.0, False),
+    (1, 1, 256, 2, 1, 0.0, False),
     (2, 300, 1024, 8, 2, 1e6, False),
     (1, 257, 2048, 16, 4, 1e4, True),
-    (1, 128, 256, 2, 1, 0.0, False),
     (1, 1, 256, 2, 1, 1e6, False),
 ])
-def test_fp8_forward_within_bar(lib, B, T, C, NH, NKV, theta, interleaved):
+def test_fp8_forward_matches_e4m3_oracle(lib, B, T, C, NH, NKV, theta, interleaved):
     import torch
     w = shape_workload(B, T, C, NH, NKV, theta, seed=B * 100 + T + 71)
     qkv_np, _ = make_inputs(w, "bf16")
     qkv = to_device(qkv_np, "bf16")
     out, lse = lib.forward_fp8(qkv, NH, NKV, theta, rope_interleaved=interleaved)
     torch.cuda.synchronize()
-    ref_out, ref_lse = oracle.attention_forward(qkv_np, C, NH, NKV, theta, rope_interleaved=interleaved)
-    _, _, V = oracle.split_qkv(qkv_np, C, NH, NKV)
-    e_out = float(np.abs(to_numpy(out) - ref_out).max()) / float(np.abs(V).max())
-    e_lse = float(np.abs(to_numpy(lse) - ref_lse).max()) / max(1.0, float(np.abs(ref_lse).max()))
-    assert np.isfinite(to_numpy(out)).all()
-    assert e_out <= out_bar(T) and e_lse <= LSE_BAR, (e_out, e_lse)
-    # and in the normalised metric of the other paths (reported on failure)
-    assert rel_err(to_numpy(out), ref_out) <= 2 * out_bar(T)
-    assert lib.attn_device_status() == 0
-
-
-@pytest.mark.parametrize("B,T,C,NH,NKV", [
-    (2, 300, 1024, 8, 2),
-    (1, 257, 2048, 16, 4),
-    (1, 1000, 512, 4, 1),
-    (1, 128, 256, 2, 1),
-    (1, 1, 256, 2, 1),
-])
-def test_fp8_forward_matches_quantized_oracle(lib, B, T, C, NH, NKV):
-    """Without RoPE both sides quantize the same float32 values with the same
-    float32 scale arithmetic, so every Q/K/V code agrees; what remains is the
-    kernel's e4m3 rounding of the softmax weights (stored as 112 p, p <= 4)
-    before PV.  With out = sum_j P8_j Vd_j / l, l >= 1 (the row maximum
-    contributes at least 1), a weight rounds with relative error <= 2^-4 in
-    the normal range and absolute error <= 2^-10 / 112 below it
-    (112 p < 2^-6), and out is rounded to bf16 (2^-8 relative), so
-    |out - ref| <= max|Vd| (2^-4 + T 2^-10 / 112 + 2^-8).  lse uses the
-    unrounded float32 weights: float32 score sums and exp2/log2
-    approximations give ~1e-6; the bar is 1e-3 max(1, |lse|)."""
-    import torch
-    from oracle.e4m3 import attention_forward_e4m3
-    w = shape_workload(B, T, C, NH, NKV, 0.0, seed=B * 100 + T + 79)
-    qkv_np, _ = make_inputs(w, "bf16")
-    qkv = to_device(qkv_np, "bf16")
-    out, lse = lib.forward_fp8(qkv, NH, NKV, 0.0)
-    torch.cuda.synchronize()
-    ref_out, ref_lse, Vd = attention_forward_e4m3(qkv_np, C, NH, NKV, 0.0)
-    vmax = float(np.abs(Vd).max())
-    bar_out = vmax * (2.0 ** -4 + T * P_SUBNORMAL + 2.0 ** -8)
-    lse_bar = 1e-3 * max(1.0, float(np.abs(ref_lse).max()))
-    e_out = float(np.abs(to_numpy(out) - ref_out).max())
-    e_lse = float(np.abs(to_numpy(lse) - ref_lse).max())
-    assert np.isfinite(to_numpy(out)).all()
-    assert e_out <= bar_out and e_lse <= lse_bar, (e_out, bar_out, e_lse, lse_bar)
+    ref = fp8_reference(qkv_np, w, theta, interleaved)
+    worst, bars, _ = check_against_e4m3_oracle(to_numpy(out), to_numpy(lse), ref, range(T), w.hd)
+    assert_bar_is_tight(bars)
     assert lib.attn_device_status() == 0
 
 
@@ -102,12 +126,12 @@ def test_fp8_forward_rejects_unsupported_shapes(lib):
 
 @pytest.mark.parametrize("name", ["gqa_block", "long_context_gqa"])
 def test_fp8_forward_full_size_sampled(lib, name):
-    """Full-size call as bench.py --fp8 makes it (caller workspace); the
-    oracle is evaluated on seeded query rows of every head."""
+    """Full-size call as bench.py --fp8 makes it (caller workspace, RoPE
+    1e6); the e4m3 oracle is evaluated on seeded query rows of every head."""
     import torch
     from causal_attention_gqa_gb300 import binding
     w = WORKLOADS[name]
-    qkv_np, dout_np = make_inputs(w, "bf16")
+    qkv_np, _ = make_inputs(w, "bf16")
     qkv = to_device(qkv_np, "bf16")
     out = torch.empty((w.B, w.T, w.C), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((w.B, w.NH, w.T), dtype=torch.float32, device="cuda")
@@ -116,12 +140,7 @@ def test_fp8_forward_full_size_sampled(lib, name):
     binding.attn_fwd_fp8(out, lse, qkv, w.B, w.T, w.C, w.NH, w.NKV, w.rope_theta, binding.DTYPE_BF16, ws, nb)
     torch.cuda.synchronize()
     qr = sample_rows(w.T, 48, w.seed + 11)
-    ref = oracle.attention_sampled(qkv_np, dout_np, w.C, w.NH, w.NKV, w.rope_theta, qr, [], qr)
-    _, _, V = oracle.split_qkv(qkv_np, w.C, w.NH, w.NKV)
-    got_out = to_numpy(out)[:, qr]
-    got_lse = to_numpy(lse)[:, :, qr]
-    assert np.isfinite(got_out).all() and np.isfinite(got_lse).all()
-    e_out = float(np.abs(got_out - ref["out_rows"]).max()) / float(np.abs(V).max())
-    e_lse = float(np.abs(got_lse - ref["lse_rows"]).max()) / max(1.0, float(np.abs(ref["lse_rows"]).max()))
-    assert e_out <= out_bar(w.T) and e_lse <= LSE_BAR, (e_out, e_lse)
+    ref = fp8_reference(qkv_np, w, w.rope_theta, rows=qr)
+    worst, bars, _ = check_against_e4m3_oracle(to_numpy(out), to_numpy(lse), ref, qr, w.hd)
+    assert_bar_is_tight(bars)
     assert lib.attn_device_status() == 0
