@@ -65,6 +65,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "fwd_tc05": "attn_fwd2_sm103.cu", "bwd_dkdv_tc05": "attn_bwd_sm103.cu", "bwd_dq_tc05": "attn_bwd_sm103.cu",
     "bwd_row_dot": "attn_prep.cu", "rope_qk": "attn_prep.cu", "bwd_prologue": "attn_prep.cu",
+    "fwd_split": "attn_split_sm103.cu", "bwd_dkdv_split": "attn_split_sm103.cu", "bwd_dq_split": "attn_split_sm103.cu",
 }
 
 
@@ -78,6 +79,8 @@ def parse_args():
     ap.add_argument("--also", default="long_context_gqa",
                     help="second workload timed in the same run and reported under per_config ('' for none)")
     ap.add_argument("--also-steps", type=int, default=200)
+    ap.add_argument("--dtype", choices=["bf16", "tf32"], default="bf16",
+                    help="tf32: float32 tensors through ATTN_DTYPE_TF32 (the split tensor-core path at head size 64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", default=None, metavar="B,L,NH,NKV,hd")
     ap.add_argument("--proj", default=None, metavar="B,T,Cm,NH,NKV,hd")
@@ -216,7 +219,8 @@ def kernel_algorithmic_flops(name, w):
     dK/dV kernel covers 4 (S, dP, dV, dK); the dQ kernel 1 (dQ; its S and dP
     recomputation is extra work, not counted)."""
     unit = 2.0 * w.B * w.NH * w.hd * w.causal_pairs
-    return {"fwd_tc05": 2 * unit, "bwd_dkdv_tc05": 4 * unit, "bwd_dq_tc05": 1 * unit}.get(name)
+    return {"fwd_tc05": 2 * unit, "bwd_dkdv_tc05": 4 * unit, "bwd_dq_tc05": 1 * unit,
+            "fwd_split": 2 * unit, "bwd_dkdv_split": 4 * unit, "bwd_dq_split": 1 * unit}.get(name)
 
 
 # --------------------------------------------------------------------------- arms
@@ -262,15 +266,24 @@ def max_over_ranks(values, device):
 SUSTAINED_AFTER_S = 2.0     # a timed region at least this long is priced against the sustained peak
 
 
-def choose_peak(peaks, peak_src, timed_seconds):
-    """The bf16 peak a timed region is priced against: the burst figure (a
-    short cuBLAS loop at full clocks) unless the region lasted long enough
-    for the power cap to pull the clocks down, then the sustained one."""
+TF32_PER_BF16 = 1.1 / 2.25   # nominal dense TF32 / bf16 tensor rates of a GB300
+
+
+def choose_peak(peaks, peak_src, timed_seconds, dtype="bf16"):
+    """The peak a timed region is priced against: the measured bf16 burst
+    figure (a short cuBLAS loop at full clocks) unless the region lasted long
+    enough for the power cap to pull the clocks down, then the sustained one;
+    for float32 tensors on the TF32 dtype, that figure times the nominal
+    TF32/bf16 ratio."""
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     if timed_seconds >= SUSTAINED_AFTER_S:
-        return sustained, f"{peak_src} bf16_tflops_sustained ({timed_seconds:.2f} s timed region)"
-    return burst, f"{peak_src} bf16_tflops (burst: {timed_seconds:.3f} s timed region < {SUSTAINED_AFTER_S} s)"
+        tf, desc = sustained, f"{peak_src} bf16_tflops_sustained ({timed_seconds:.2f} s timed region)"
+    else:
+        tf, desc = burst, f"{peak_src} bf16_tflops (burst: {timed_seconds:.3f} s timed region < {SUSTAINED_AFTER_S} s)"
+    if dtype == "tf32":
+        return tf * TF32_PER_BF16, desc + " x 1.1/2.25 (nominal dense TF32/bf16)"
+    return tf, desc
 
 
 def roofline_of(prof, w, peak_tf, peak_desc):
@@ -288,7 +301,7 @@ def roofline_of(prof, w, peak_tf, peak_desc):
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": traffic_for(dom), "peak_source": peak_desc,
                 "avg_launch_ms": tot_ms / n_launch, "algorithmic_flop_per_launch": kfl}
-    bwd = [k for k in ("bwd_dkdv_tc05", "bwd_dq_tc05") if k in prof]
+    bwd = [k for k in ("bwd_dkdv_tc05", "bwd_dq_tc05", "bwd_dkdv_split", "bwd_dq_split") if k in prof]
     combined = None
     if bwd:
         t = sum(prof[k][1] / prof[k][0] for k in bwd)
@@ -308,24 +321,27 @@ def time_workload(args, w, dev, world, steps, e2e):
     from causal_attention_gqa_gb300.workloads import make_inputs
 
     B, T, C, NH, NKV = w.B, w.T, w.C, w.NH, w.NKV
-    qkv_np, dout_np = make_inputs(w, "bf16")
-    qkv_host = torch.from_numpy(qkv_np).to(torch.bfloat16).pin_memory()
-    dout_host = torch.from_numpy(dout_np).to(torch.bfloat16).pin_memory()
+    tf32 = args.dtype == "tf32"
+    tdt, esz = (torch.float32, 4) if tf32 else (torch.bfloat16, 2)
+    qkv_np, dout_np = make_inputs(w, "f32" if tf32 else "bf16")
+    qkv_host = torch.from_numpy(qkv_np).to(tdt).pin_memory()
+    dout_host = torch.from_numpy(dout_np).to(tdt).pin_memory()
     del qkv_np, dout_np
     qkv = qkv_host.to(dev)
     dout = dout_host.to(dev)
-    out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, T, C), dtype=tdt, device=dev)
     lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
     dqkv = torch.empty_like(qkv)
-    dqkv_host = torch.empty(dqkv.shape, dtype=torch.bfloat16).pin_memory()
-    ws_bytes = binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16)
+    dqkv_host = torch.empty(dqkv.shape, dtype=tdt).pin_memory()
+    base = binding.DTYPE_TF32 if tf32 else binding.DTYPE_BF16
+    ws_bytes = binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, base)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    fws_bytes = binding.attn_fwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16)
+    fws_bytes = binding.attn_fwd_workspace_bytes(B, T, C, NH, NKV, base)
     fws = torch.empty(max(fws_bytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
-    code = binding.DTYPE_BF16 | (binding.FLAG_ROPE_INTERLEAVED if args.rope_interleaved else 0)
+    code = base | (binding.FLAG_ROPE_INTERLEAVED if args.rope_interleaved else 0)
 
     def step(qkv=qkv, dout=dout, dqkv=dqkv):
         binding.attn_fwd_ws(out, lse, qkv, B, T, C, NH, NKV, w.rope_theta, code, fws, fws_bytes, sptr)
@@ -419,22 +435,22 @@ def time_workload(args, w, dev, world, steps, e2e):
     e_end.record(stream)
     barrier()
     res.update({"e2e_ms": e_start.elapsed_time(e_end) / e2e_steps, "e2e_steps": e2e_steps,
-                "h2d_bytes": qkv_host.numel() * 2 + dout_host.numel() * 2, "d2h_bytes": dqkv_host.numel() * 2})
+                "h2d_bytes": (qkv_host.numel() + dout_host.numel()) * esz, "d2h_bytes": dqkv_host.numel() * esz})
     return res
 
 
-def summarise(w, world, r, peaks, peak_src):
+def summarise(w, world, r, peaks, peak_src, dtype="bf16"):
     """Whole-job throughput, peak fraction, kernel table and roofline of one
     timed workload (r from time_workload, times already max-reduced)."""
     prof = r["prof"]
     fl = flops_per_step(w)
     value = world * fl / (r["ms_per_step"] * 1e-3) / 1e12
-    peak_tf, peak_desc = choose_peak(peaks, peak_src, r["timed_s"])
+    peak_tf, peak_desc = choose_peak(peaks, peak_src, r["timed_s"], dtype)
     roof, combined = roofline_of(prof, w, peak_tf, peak_desc)
     kernel_ms = {k: v[1] for k, v in prof.items()}
     return {
         "value": value, "ms_per_step": r["ms_per_step"], "steps": r["steps"],
-        "peak_bf16_frac": value / world / peak_tf, "peak_bf16_tflops": peak_tf, "peak_source": peak_desc,
+        f"peak_{dtype}_frac": value / world / peak_tf, f"peak_{dtype}_tflops": peak_tf, "peak_source": peak_desc,
         "wall_s_timed_region": r["wall"], "clocks": r["clocks"],
         "kernels": {k: {"launches": v[0], "avg_ms": v[1] / v[0], "share": v[1] / sum(kernel_ms.values())}
                     for k, v in prof.items()},
@@ -465,7 +481,7 @@ def run_ours(args, w):
     ws = rank_shard(w, rank, world)     # this rank's batch rows of the global batch
     head = time_workload(args, ws, dev, world, args.steps, e2e=True)
     extra = {}
-    if args.also and args.also != w.name:
+    if args.also and args.also != w.name and args.dtype == "bf16":
         wa = WORKLOADS[args.also]
         extra[wa.name] = (wa, time_workload(args, rank_shard(wa, rank, world), dev, world,
                                             min(args.steps, args.also_steps), e2e=False))
@@ -479,20 +495,22 @@ def run_ours(args, w):
         return 0
 
     peaks, peak_src = load_peaks()
-    s = summarise(ws, world, head, peaks, peak_src)
+    s = summarise(ws, world, head, peaks, peak_src, args.dtype)
     fl = flops_per_step(ws)
     e2e_value = world * fl / (head["e2e_ms"] * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": s["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": s["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32 (TF32 path: three bf16 products per float32 product)"
+        if args.dtype == "tf32" else "bf16", "data": "synthetic",
         "config": config_of(ws, {"parallelism": f"batch rows sharded over {world} ranks, no collective"
                                  if world > 1 else "single GPU", "global_batch": world * ws.B,
                                  "rope_pairs": "interleaved (GPT-J)" if args.rope_interleaved else "NEOX",
                                  "l2": "flushed between timed steps (256 MiB write outside the timed events)",
                                  "kernel_breakdown": f"separate pass of {head['n_prof']} steps with per-kernel "
                                                      "events",
-                                 "peak_bf16_frac": s["peak_bf16_frac"], "peak_bf16_tflops": s["peak_bf16_tflops"],
+                                 f"peak_{args.dtype}_frac": s[f"peak_{args.dtype}_frac"],
+                                 f"peak_{args.dtype}_tflops": s[f"peak_{args.dtype}_tflops"],
                                  "peak_source": s["peak_source"],
                                  "measured_peaks": {k: peaks.get(k) for k in
                                                     ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs")},

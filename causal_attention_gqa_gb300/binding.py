@@ -280,7 +280,7 @@ def attn_selftest_wait_timeout(limit_ns: int) -> int:
     return v.value
 
 
-N_KERNEL_IDS = 13
+N_KERNEL_IDS = 17
 
 
 def attn_profile_start() -> None:

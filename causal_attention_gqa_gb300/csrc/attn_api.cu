@@ -162,10 +162,32 @@ size_t row_part_bytes(const Geometry& g, int dtype) {
 // kernel's work-item counter.
 size_t rot_part_bytes(const Geometry& g) { return align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2); }
 
+// dtype TF32 on tensor cores (head size 64): bf16 hi/lo parts of qkv (and,
+// for the backward, of dout), each array rounded up to 256 bytes.
+bool split_path(const Geometry& g, int dtype) { return dtype == ATTN_DTYPE_TF32 && split_supported(g); }
+size_t split_part_bytes(const Geometry& g, int width) { return align256((size_t)g.B * g.T * width * 2); }
+size_t split_table_bytes(const Geometry& g) { return align256((size_t)g.B * g.NH * row_table_rows(g.T) * 2 * 4); }
+
 size_t workspace_bytes(const Geometry& g, int dtype) {
+  if (split_path(g, dtype))
+    return split_table_bytes(g) + 2 * split_part_bytes(g, g.W) + 2 * split_part_bytes(g, g.C);
   size_t bytes = row_part_bytes(g, dtype);
   if (dtype == ATTN_DTYPE_BF16) bytes += rot_part_bytes(g) + 256;
   return bytes;
+}
+
+// Tensor maps of the split path over the hi/lo arrays carved from `ws`
+// (qkv parts first, then dout parts when `dout` is set).
+bool split_maps(SplitArgs* a, uint8_t* ws, bool dout) {
+  const Geometry& g = a->g;
+  a->qkv_hi = reinterpret_cast<__nv_bfloat16*>(ws);
+  a->qkv_lo = reinterpret_cast<__nv_bfloat16*>(ws + split_part_bytes(g, g.W));
+  if (!make_tmap(&a->tm_hi, a->qkv_hi, g.W, g.T, g.B) || !make_tmap(&a->tm_lo, a->qkv_lo, g.W, g.T, g.B))
+    return false;
+  if (!dout) return true;
+  a->dout_hi = reinterpret_cast<__nv_bfloat16*>(ws + 2 * split_part_bytes(g, g.W));
+  a->dout_lo = reinterpret_cast<__nv_bfloat16*>(ws + 2 * split_part_bytes(g, g.W) + split_part_bytes(g, g.C));
+  return make_tmap(&a->tm_dohi, a->dout_hi, g.C, g.T, g.B) && make_tmap(&a->tm_dolo, a->dout_lo, g.C, g.T, g.B);
 }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
@@ -220,6 +242,20 @@ int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH
   if (st != ATTN_OK) return st;
   if (!out || !lse || !qkv) return ATTN_ERR_NULL_POINTER;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (split_path(g, dtype) && workspace != nullptr) {
+    // float32 tensors on the tensor cores: hi/lo parts in the workspace.
+    if (!aligned16(out) || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return ATTN_ERR_MISALIGNED;
+    SplitArgs a{};
+    a.g = g;
+    a.qkv = qkv;
+    a.out = out;
+    a.lse = lse;
+    a.status = status_word();
+    if (!a.status || !split_maps(&a, static_cast<uint8_t*>(workspace), false)) return ATTN_ERR_CUDA;
+    return from_cuda(split_fwd_launch(a, s));
+  }
   if (dtype == ATTN_DTYPE_F32 || dtype == ATTN_DTYPE_TF32) {
     if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(qkv)) & 3u)
       return ATTN_ERR_MISALIGNED;
@@ -267,6 +303,7 @@ extern "C" int attn_fwd(void* out, float* lse, const void* qkv, int B, int T, in
 extern "C" size_t attn_fwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype) {
   Geometry g;
   if (check_shape(B, T, C, NH, NKV, 0.f, dtype, &g) != ATTN_OK) return 0;
+  if (split_path(g, dtype)) return 2 * split_part_bytes(g, g.W);
   if (dtype != ATTN_DTYPE_BF16) return 0;
   return align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2);
 }
@@ -305,6 +342,25 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* Drow = static_cast<float*>(workspace);
+  if (split_path(g, dtype)) {
+    // float32 tensors on the tensor cores; qk_rot is not used (the hi/lo
+    // parts of the rotated Q/K are formed again from qkv).
+    if (!aligned16(dqkv) || !aligned16(qkv) || !aligned16(out) || !aligned16(dout) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+      return ATTN_ERR_MISALIGNED;
+    SplitArgs a{};
+    a.g = g;
+    a.qkv = qkv;
+    a.dout = dout;
+    a.out = const_cast<void*>(out);
+    a.lse = const_cast<float*>(lse);
+    a.dqkv = dqkv;
+    a.LD = static_cast<float*>(workspace);
+    a.status = status_word();
+    if (!a.status || !split_maps(&a, static_cast<uint8_t*>(workspace) + split_table_bytes(g), true))
+      return ATTN_ERR_CUDA;
+    return from_cuda(split_bwd_launch(a, s));
+  }
   if (dtype == ATTN_DTYPE_F32 || dtype == ATTN_DTYPE_TF32) {
     if ((reinterpret_cast<uintptr_t>(dqkv) | reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(out) |
          reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(lse)) & 3u)

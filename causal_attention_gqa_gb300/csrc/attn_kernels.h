@@ -48,6 +48,31 @@ bool simt_tiled_supported(const SimtArgs& a);
 cudaError_t simt_tiled_launch(const SimtArgs& a, cudaStream_t stream);
 size_t simt_max_smem_bytes(int hd);
 
+// ------------------------------------------------------------ float32 on tensor cores
+// dtype TF32, head size 64: every product of float32 operands as three bf16
+// products of hi/lo parts (attn_split_sm103.cu).  The parts of Q, K, V (Q and
+// K rotated when RoPE is on) and of dO live in the workspace in the column
+// layout of qkv / dout.
+struct SplitArgs {
+  Geometry g;
+  CUtensorMap tm_hi, tm_lo;       // over qkv_hi / qkv_lo [B, T, W] bf16 (64-column, 128-row boxes)
+  CUtensorMap tm_dohi, tm_dolo;   // over dout_hi / dout_lo [B, T, C] bf16 (backward)
+  const void* qkv;                // float32 [B, T, W]
+  const void* dout;               // float32 [B, T, C] (backward)
+  void* out;                      // float32 [B, T, C]: forward writes it, backward reads it
+  float* lse;                     // float32 [B, NH, T]: forward writes it, backward reads it
+  void* dqkv;                     // float32 [B, T, W] (backward)
+  __nv_bfloat16* qkv_hi;
+  __nv_bfloat16* qkv_lo;
+  __nv_bfloat16* dout_hi;
+  __nv_bfloat16* dout_lo;
+  float* LD;                      // backward row tables: -lse log2(e) and -D over T rounded up to 128
+  int* status;
+};
+bool split_supported(const Geometry& g);
+cudaError_t split_fwd_launch(const SplitArgs& a, cudaStream_t stream);
+cudaError_t split_bwd_launch(const SplitArgs& a, cudaStream_t stream);
+
 // ------------------------------------------------------------ FP8 forward
 // e4m3 operands with per-tile (Q, K) and per-head (V) scales; head size 128,
 // an even number of query heads per kv head.

@@ -35,7 +35,7 @@ cudaEvent_t take_event() {
 const char* kNames[kKernelCount] = {
     "fwd_tc05", "bwd_dkdv_tc05", "bwd_dq_tc05", "bwd_row_dot",
     "rope_qk", "fwd_simt", "bwd_dkdv_simt", "bwd_dq_simt", "bwd_prologue", "decode", "qkv_proj",
-    "fp8_prep", "fwd_fp8",
+    "fp8_prep", "fwd_fp8", "split_prep", "fwd_split", "bwd_dkdv_split", "bwd_dq_split",
 };
 
 }  // namespace

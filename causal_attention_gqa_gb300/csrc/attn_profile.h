@@ -21,7 +21,11 @@ enum KernelId {
   kKernelProj = 10,
   kKernelFp8Prep = 11,
   kKernelFwdFp8 = 12,
-  kKernelCount = 13
+  kKernelSplitPrep = 13,
+  kKernelFwdSplit = 14,
+  kKernelBwdDkdvSplit = 15,
+  kKernelBwdDqSplit = 16,
+  kKernelCount = 17
 };
 
 // Record the start / end of a launch of kernel `id` on `stream` (no-ops while

@@ -64,9 +64,14 @@ extern "C" {
 typedef enum {
   /* float32 tensors, exact float32 arithmetic on CUDA cores. */
   ATTN_DTYPE_F32 = 0,
-  /* float32 tensors held to the same 1e-4 bar as ATTN_DTYPE_F32; the library
-     runs it on the exact float32 kernels (no reduced-precision tensor-core
-     variant is built), so results equal those of ATTN_DTYPE_F32. */
+  /* float32 tensors held to the same 1e-4 bar as ATTN_DTYPE_F32, computed on
+     the tensor cores where it can be: with head size 64, attn_fwd_ws,
+     attn_bwd and attn_bwd_rot split every float32 operand into bf16 parts
+     hi + lo in the workspace and take each product as hi*hi + hi*lo + lo*hi
+     on tcgen05 MMAs with float32 accumulation (~1e-5 of the float64 result;
+     the softmax weights and dS are split the same way).  Elsewhere (attn_fwd,
+     which has no workspace, and other head sizes) it runs the exact float32
+     kernels, with results equal to ATTN_DTYPE_F32's. */
   ATTN_DTYPE_TF32 = 1,
   /* bf16 tensors, tcgen05 tensor-core MMAs with float32 accumulation. */
   ATTN_DTYPE_BF16 = 2
@@ -114,8 +119,10 @@ ATTN_API int attn_fwd(void* out, float* lse, const void* qkv,
 /*
  * attn_fwd_workspace_bytes -- size in bytes of the scratch attn_fwd_ws
  * uses for this shape and dtype: room for a RoPE-rotated copy of Q and K,
- * [B,T,(NH+NKV)*hd] of dtype, for BF16; 0 for F32 (which needs none) and
- * for invalid arguments.
+ * [B,T,(NH+NKV)*hd] of dtype, for BF16; for TF32 with head size 64 the bf16
+ * hi and lo parts of qkv (2 x [B,T,(NH+2*NKV)*hd] bf16, Q and K rotated);
+ * 0 for F32 and other TF32 head sizes (which need none) and for invalid
+ * arguments.
  *
  * attn_fwd_ws -- attn_fwd with caller-provided scratch.  Same arguments,
  * results and supported shapes as attn_fwd, plus
@@ -130,7 +137,10 @@ ATTN_API int attn_fwd(void* out, float* lse, const void* qkv,
  * inside the attention kernel, once per use, which costs more for long
  * sequences because each K tile is used by many query tiles.  Without RoPE,
  * or for F32, it is attn_fwd.  The two give the same results up to the
- * rounding of the rotated values to dtype (both round them once).
+ * rounding of the rotated values to dtype (both round them once).  With TF32
+ * and head size 64 it runs the tensor-core path (see ATTN_DTYPE_TF32) on the
+ * parts it writes into the workspace; float32 tensors must then be 16-byte
+ * aligned (ATTN_ERR_MISALIGNED otherwise).
  */
 ATTN_API size_t attn_fwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype);
 ATTN_API int attn_fwd_ws(void* out, float* lse, const void* qkv,
@@ -142,7 +152,9 @@ ATTN_API int attn_fwd_ws(void* out, float* lse, const void* qkv,
  * for this shape and dtype: the row dots D = rowsum(dO * O) (float32
  * [B,NH,T]; for BF16 stored next to the rescaled lse as float pairs over T
  * rounded up to 64 rows), plus, for BF16, room for a RoPE-rotated bf16 copy
- * of Q and K (used only when rope_theta > 0).  Returns 0 for invalid
+ * of Q and K (used only when rope_theta > 0); for TF32 with head size 64 the
+ * row tables over T rounded up to 128 rows and the bf16 hi/lo parts of qkv
+ * and dout (the tensor-core path; 16-byte aligned tensors).  Returns 0 for invalid
  * arguments.
  */
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int T, int C, int NH, int NKV, int dtype);

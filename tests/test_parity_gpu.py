@@ -94,27 +94,24 @@ def test_f32_head64_unaligned_tensors(lib):
     assert all(v <= TOL["f32"] for v in errs.values()), errs
 
 
-def test_tf32_dtype_runs_the_float32_kernels(lib):
-    """ATTN_DTYPE_TF32 (float32 tensors, 1e-4 bar) is computed by the exact
-    float32 kernels: bit-identical to ATTN_DTYPE_F32, and within the bar."""
+def test_tf32_forward_without_workspace_runs_the_float32_kernels(lib):
+    """attn_fwd takes no workspace, so with ATTN_DTYPE_TF32 it runs the exact
+    float32 kernels (the tensor-core path needs scratch for its bf16 parts):
+    bit-identical to ATTN_DTYPE_F32, and within the float32 bar."""
     import torch
     from helpers import to_device, to_numpy
     w = shape_workload(2, 70, 128, 2, 1, 1e6, seed=31)
-    qkv_np, dout_np = make_inputs(w, "f32")
-    qkv, dout = to_device(qkv_np, "f32"), to_device(dout_np, "f32")
+    qkv_np, _ = make_inputs(w, "f32")
+    qkv = to_device(qkv_np, "f32")
     res = {}
     for code in (lib.DTYPE_F32, lib.DTYPE_TF32):
-        out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta, dtype=code)
-        dqkv = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta, dtype=code)
-        torch.cuda.synchronize()
-        res[code] = (out, lse, dqkv)
+        res[code] = lib.forward(qkv, w.NH, w.NKV, w.rope_theta, dtype=code)
+    torch.cuda.synchronize()
     for a, b in zip(res[lib.DTYPE_F32], res[lib.DTYPE_TF32]):
         assert torch.equal(a, b)
-    out, lse, dqkv = res[lib.DTYPE_TF32]
-    ref_dqkv, aux = oracle.attention_backward(qkv_np, dout_np, w.C, w.NH, w.NKV, w.rope_theta, return_aux=True)
-    errs = {"out": rel_err(to_numpy(out), aux["out"]), "lse": rel_err(to_numpy(lse), aux["lse"]),
-            "dqkv": rel_err(to_numpy(dqkv), ref_dqkv)}
-    assert all(v <= TOL["f32"] for v in errs.values()), errs
+    out, lse = res[lib.DTYPE_TF32]
+    ref_out, ref_lse = oracle.attention_forward(qkv_np, w.C, w.NH, w.NKV, w.rope_theta)
+    assert rel_err(to_numpy(out), ref_out) <= TOL["f32"] and rel_err(to_numpy(lse), ref_lse) <= TOL["f32"]
 
 
 # ------------------------------------------------------------------ bf16 forward
