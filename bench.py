@@ -194,16 +194,18 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def traffic_for(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source is unchanged since the capture; else None."""
+def traffic_for(kernel, workload=None):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if the kernel's source is unchanged since the capture;
+    else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel)
+            table = json.load(f)
     except (OSError, ValueError):
         return None
-    if not rec:
+    rec = table.get(f"{kernel}@{workload}") or table.get(kernel)
+    if not rec or (workload is not None and rec.get("workload") != workload):
         return None
     src = os.path.join(ROOT, "causal_attention_gqa_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
     try:
@@ -299,7 +301,7 @@ def roofline_of(prof, w, peak_tf, peak_desc):
     if kfl is not None:
         achieved = kfl / (tot_ms / n_launch * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "traffic": traffic_for(dom), "peak_source": peak_desc,
+                "frac": achieved / peak_tf, "traffic": traffic_for(dom, w.name), "peak_source": peak_desc,
                 "avg_launch_ms": tot_ms / n_launch, "algorithmic_flop_per_launch": kfl}
     bwd = [k for k in ("bwd_dkdv_tc05", "bwd_dq_tc05", "bwd_dkdv_split", "bwd_dq_split") if k in prof]
     combined = None

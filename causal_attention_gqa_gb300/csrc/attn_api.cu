@@ -176,17 +176,17 @@ size_t workspace_bytes(const Geometry& g, int dtype) {
   return bytes;
 }
 
-// Tensor maps of the split path over the hi/lo arrays carved from `ws`
-// (qkv parts first, then dout parts when `dout` is set).
-bool split_maps(SplitArgs* a, uint8_t* ws, bool dout) {
+// Tensor maps of the split path: the qkv parts at `qkv_parts` (hi, then lo),
+// and, when `dout_parts` is set, the dout parts there (hi, then lo).
+bool split_maps(SplitArgs* a, uint8_t* qkv_parts, uint8_t* dout_parts) {
   const Geometry& g = a->g;
-  a->qkv_hi = reinterpret_cast<__nv_bfloat16*>(ws);
-  a->qkv_lo = reinterpret_cast<__nv_bfloat16*>(ws + split_part_bytes(g, g.W));
+  a->qkv_hi = reinterpret_cast<__nv_bfloat16*>(qkv_parts);
+  a->qkv_lo = reinterpret_cast<__nv_bfloat16*>(qkv_parts + split_part_bytes(g, g.W));
   if (!make_tmap(&a->tm_hi, a->qkv_hi, g.W, g.T, g.B) || !make_tmap(&a->tm_lo, a->qkv_lo, g.W, g.T, g.B))
     return false;
-  if (!dout) return true;
-  a->dout_hi = reinterpret_cast<__nv_bfloat16*>(ws + 2 * split_part_bytes(g, g.W));
-  a->dout_lo = reinterpret_cast<__nv_bfloat16*>(ws + 2 * split_part_bytes(g, g.W) + split_part_bytes(g, g.C));
+  if (!dout_parts) return true;
+  a->dout_hi = reinterpret_cast<__nv_bfloat16*>(dout_parts);
+  a->dout_lo = reinterpret_cast<__nv_bfloat16*>(dout_parts + split_part_bytes(g, g.C));
   return make_tmap(&a->tm_dohi, a->dout_hi, g.C, g.T, g.B) && make_tmap(&a->tm_dolo, a->dout_lo, g.C, g.T, g.B);
 }
 
@@ -253,7 +253,7 @@ int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH
     a.out = out;
     a.lse = lse;
     a.status = status_word();
-    if (!a.status || !split_maps(&a, static_cast<uint8_t*>(workspace), false)) return ATTN_ERR_CUDA;
+    if (!a.status || !split_maps(&a, static_cast<uint8_t*>(workspace), nullptr)) return ATTN_ERR_CUDA;
     return from_cuda(split_fwd_launch(a, s));
   }
   if (dtype == ATTN_DTYPE_F32 || dtype == ATTN_DTYPE_TF32) {
@@ -269,9 +269,6 @@ int fwd_impl(void* out, float* lse, const void* qkv, int B, int T, int C, int NH
   }
   if (!aligned16(out) || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
   const bool pre_rotate = workspace != nullptr && g.rope_theta > 0.f;
-  // The attention kernel's own rotation (attn_fwd, bf16) pairs NEOX columns
-  // only; the interleaved pairing goes through the rotation pass of attn_fwd_ws.
-  if (g.rope_interleaved && !pre_rotate) return ATTN_ERR_UNSUPPORTED;
   if (pre_rotate && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
   Tc05FwdArgs a{};
   a.g = g;
@@ -343,10 +340,11 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* Drow = static_cast<float*>(workspace);
   if (split_path(g, dtype)) {
-    // float32 tensors on the tensor cores; qk_rot is not used (the hi/lo
-    // parts of the rotated Q/K are formed again from qkv).
+    // float32 tensors on the tensor cores; with qk_rot (the workspace of the
+    // attn_fwd_ws call, which holds the hi/lo parts of this qkv) the parts are
+    // not formed again.
     if (!aligned16(dqkv) || !aligned16(qkv) || !aligned16(out) || !aligned16(dout) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(qk_rot) & 255u))
       return ATTN_ERR_MISALIGNED;
     SplitArgs a{};
     a.g = g;
@@ -357,8 +355,11 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
     a.dqkv = dqkv;
     a.LD = static_cast<float*>(workspace);
     a.status = status_word();
-    if (!a.status || !split_maps(&a, static_cast<uint8_t*>(workspace) + split_table_bytes(g), true))
-      return ATTN_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace) + split_table_bytes(g);
+    uint8_t* dout_parts = ws + 2 * split_part_bytes(g, g.W);
+    a.qkv_given = qk_rot != nullptr;
+    uint8_t* qkv_parts = a.qkv_given ? static_cast<uint8_t*>(const_cast<void*>(qk_rot)) : ws;
+    if (!a.status || !split_maps(&a, qkv_parts, dout_parts)) return ATTN_ERR_CUDA;
     return from_cuda(split_bwd_launch(a, s));
   }
   if (dtype == ATTN_DTYPE_F32 || dtype == ATTN_DTYPE_TF32) {

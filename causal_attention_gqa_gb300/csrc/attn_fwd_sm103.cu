@@ -188,6 +188,55 @@ struct TileRotator {
       }
     }
   }
+
+  // Interleaved (GPT-J) pairs (2i, 2i+1) of "nanoeuler -- CUDA kernels",
+  // rope_kernel: each bf16x2 word of the tile is one pair, rotated in place
+  // (scores q . k do not depend on the element order Q and K share).  Thread
+  // p owns the sixteen columns 16p .. 16p + 15, i.e. pairs 8p .. 8p + 7, the
+  // same pairs (and angles) as in the NEOX layout.
+  __device__ void rotate_interleaved(uint8_t* tile, int pos0) {
+    float2 c[4], sn[4];   // pair 8p + e: component e & 1 of entry e >> 1
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float s0, c0, s1, c1;
+      __sincosf(rope_angle(pos0 + r0, f_hi[2 * q], f_lo[2 * q]), &s0, &c0);
+      __sincosf(rope_angle(pos0 + r0, f_hi[2 * q + 1], f_lo[2 * q + 1]), &s1, &c1);
+      c[q] = make_float2(c0, c1);
+      sn[q] = make_float2(s0, s1);
+    }
+#pragma unroll 1
+    for (int k = 0; k < ROWS; ++k) {
+      const int r = r0 + k * RS;
+      uint4* a_ptr = reinterpret_cast<uint4*>(tile + sw128_offset(r, 16 * p));
+      uint4* b_ptr = reinterpret_cast<uint4*>(tile + sw128_offset(r, 16 * p + 8));
+      const uint4 a = *a_ptr, b = *b_ptr;
+      uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float cs = (e & 1) ? c[e >> 1].y : c[e >> 1].x;
+        const float ss = (e & 1) ? sn[e >> 1].y : sn[e >> 1].x;
+        float y0, y1;
+        rope_pair(bf16_lo(w[e]), bf16_hi(w[e]), cs, ss, y0, y1);
+        w[e] = pack_bf16x2(y0, y1);
+      }
+      *a_ptr = make_uint4(w[0], w[1], w[2], w[3]);
+      *b_ptr = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // advance the angles by RS positions
+        const float2 nss = make_float2(-step_s[q].x, -step_s[q].y);
+        const float2 cn = __ffma2_rn(c[q], step_c[q], __fmul2_rn(sn[q], nss));
+        sn[q] = __ffma2_rn(sn[q], step_c[q], __fmul2_rn(c[q], step_s[q]));
+        c[q] = cn;
+      }
+    }
+  }
+
+  __device__ void rotate_tile(uint8_t* tile, int pos0, bool interleaved) {
+    if (interleaved)
+      rotate_interleaved(tile, pos0);
+    else
+      rotate(tile, pos0);
+  }
 };
 
 template <int HD, bool ROPE>
@@ -585,7 +634,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->q_full[qb]), (it >> 1) & 1, abort_flag,
                                                     kWaitLimitNs));
       if (!ok) break;
-      rot.rotate(sQ + qb * Cfg::kTileBytes, item.qt * kBM);
+      rot.rotate_tile(sQ + qb * Cfg::kTileBytes, item.qt * kBM, g.rope_interleaved != 0);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->q_ready[qb]));
@@ -594,7 +643,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->k_full[s]), (gi / NK) & 1, abort_flag,
                                                       kWaitLimitNs));
         if (!ok) break;
-        rot.rotate(sK + s * Cfg::kTileBytes, j * kBN);
+        rot.rotate_tile(sK + s * Cfg::kTileBytes, j * kBN, g.rope_interleaved != 0);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->k_ready[s]));

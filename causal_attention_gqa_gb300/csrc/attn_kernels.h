@@ -67,6 +67,7 @@ struct SplitArgs {
   __nv_bfloat16* dout_hi;
   __nv_bfloat16* dout_lo;
   float* LD;                      // backward row tables: -lse log2(e) and -D over T rounded up to 128
+  bool qkv_given;                 // backward: qkv_hi / qkv_lo already hold the forward's parts
   int* status;
 };
 bool split_supported(const Geometry& g);

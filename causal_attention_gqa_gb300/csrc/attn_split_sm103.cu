@@ -958,6 +958,11 @@ cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream, bool with_dout
   const long long rows = (long long)g.B * g.T;
   const bool rope = g.rope_theta > 0.f;
   const int qk_cols = (g.NH + g.NKV) * g.hd;
+  if (a.qkv_given) {   // the forward's parts of this qkv: only dO is split
+    split_plain_kernel<<<grid_for(rows * (g.C / 8), 256), 256, 0, stream>>>(
+        static_cast<const float*>(a.dout), g.C, 0, g.C, a.dout_hi, a.dout_lo, g.C, rows);
+    return cudaGetLastError();
+  }
   // Q and K (rotated when RoPE is on), then V, then dO.
   if (rope) {
     split_rope_kernel<<<grid_for(rows * (g.NH + g.NKV) * (g.hd / 16), 256), 256, 0, stream>>>(

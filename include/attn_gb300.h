@@ -78,15 +78,15 @@ typedef enum {
 } attn_dtype_t;
 
 /*
- * ATTN_FLAG_ROPE_INTERLEAVED -- OR-ed into the dtype argument of attn_fwd_ws,
- * attn_bwd, attn_bwd_rot, attn_bwd_noalloc (and, for the float32 dtypes,
- * attn_fwd) to use the interleaved (GPT-J) RoPE pairing of "nanoeuler -- CUDA
+ * ATTN_FLAG_ROPE_INTERLEAVED -- OR-ed into the dtype argument of attn_fwd,
+ * attn_fwd_ws, attn_fwd_fp8, attn_bwd, attn_bwd_rot and attn_bwd_noalloc to
+ * use the interleaved (GPT-J) RoPE pairing of "nanoeuler -- CUDA
  * kernels", rope_kernel -- pair (2i, 2i+1) of each head turns by t*theta^(-2i/hd):
  *   y[2i] = x[2i] cos - x[2i+1] sin,   y[2i+1] = x[2i] sin + x[2i+1] cos
  * -- instead of the NEOX pairing (i, i + hd/2).  Ignored when rope_theta <= 0.
- * attn_fwd with ATTN_DTYPE_BF16 rotates inside its attention kernel, which
- * pairs NEOX columns only, and returns ATTN_ERR_UNSUPPORTED with this flag
- * (use attn_fwd_ws).  The *_workspace_bytes() functions accept and ignore it.
+ * attn_fwd with ATTN_DTYPE_BF16 rotates inside its attention kernel, turning
+ * each interleaved pair of the Q and K tiles in place.  The
+ * *_workspace_bytes() functions accept and ignore the flag.
  * A forward and its backward must use the same pairing.
  */
 #define ATTN_FLAG_ROPE_INTERLEAVED 0x100
@@ -184,7 +184,9 @@ ATTN_API int attn_bwd(void* dqkv, const void* qkv, const void* out, const void* 
  *          RoPE, [B,T,(NH+NKV)*hd] of dtype; 256-byte aligned).
  * With BF16 and rope_theta > 0 the backward then reads Q and K from qk_rot
  * instead of rotating them again into its own workspace (one HBM pass fewer);
- * otherwise qk_rot is ignored and it is attn_bwd.  A qk_rot that does not
+ * with TF32 at head size 64 it reads the bf16 hi/lo parts of qkv that
+ * attn_fwd_ws left there instead of forming them again; otherwise qk_rot is
+ * ignored and it is attn_bwd.  A qk_rot that does not
  * hold the rotation of this qkv gives wrong gradients: the library cannot
  * check it.
  */

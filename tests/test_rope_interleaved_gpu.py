@@ -1,7 +1,8 @@
 """GPU parity with the interleaved (GPT-J) RoPE pairing (ATTN_FLAG_ROPE_INTERLEAVED)
 against the float64 oracle: the bf16 path through attn_fwd_ws + attn_bwd_rot
-(paired-head and single-head forward kernels) and through attn_bwd's own
-rotation, and the float32 path (row-per-warp and tiled kernels)."""
+(paired-head and single-head forward kernels), through attn_bwd's own
+rotation, and through attn_fwd's rotation inside the attention kernel; the
+float32 path (row-per-warp and tiled kernels)."""
 import numpy as np
 import pytest
 
@@ -12,11 +13,14 @@ from helpers import TOL, rel_err, to_device, to_numpy
 pytestmark = pytest.mark.gpu
 
 
-def check(lib, w, dtype, use_rot=True):
+def check(lib, w, dtype, use_rot=True, in_kernel=False):
     import torch
     qkv_np, dout_np = make_inputs(w, dtype)
     qkv, dout = to_device(qkv_np, dtype), to_device(dout_np, dtype)
-    if dtype == "bf16":
+    if dtype == "bf16" and in_kernel:
+        out, lse = lib.forward(qkv, w.NH, w.NKV, w.rope_theta, rope_interleaved=True)   # attn_fwd
+        dqkv = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta, rope_interleaved=True)
+    elif dtype == "bf16":
         out, lse, fws = lib.forward_ws(qkv, w.NH, w.NKV, w.rope_theta, rope_interleaved=True)
         dqkv = lib.backward(qkv, out, dout, lse, w.NH, w.NKV, w.rope_theta, qk_rot=fws if use_rot else None,
                             rope_interleaved=True)
@@ -54,15 +58,12 @@ def test_f32_interleaved(lib, B, T, C, NH, NKV, theta):
     check(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 100 + T + 63), "f32")
 
 
-def test_bf16_attn_fwd_rejects_interleaved(lib):
-    """attn_fwd (bf16) rotates inside its attention kernel, NEOX pairs only."""
-    import torch
-    from causal_attention_gqa_gb300.binding import AttnError
-    qkv = torch.zeros((1, 128, 3 * 128), dtype=torch.bfloat16, device="cuda")
-    out = torch.empty((1, 128, 128), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
-    with pytest.raises(AttnError) as ei:
-        lib.attn_fwd(out, lse, qkv, 1, 128, 128, 1, 1, 1e4, lib.DTYPE_BF16 | lib.FLAG_ROPE_INTERLEAVED)
-    assert ei.value.status == -3
-    lib.attn_fwd(out, lse, qkv, 1, 128, 128, 1, 1, 0.0, lib.DTYPE_BF16 | lib.FLAG_ROPE_INTERLEAVED)  # no RoPE: ignored
-    torch.cuda.synchronize()
+@pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
+    (2, 300, 512, 8, 2, 1e4),      # head size 64
+    (1, 257, 1024, 8, 4, 1e6),     # head size 128
+    (1, 1, 256, 2, 1, 1e4),        # one token
+])
+def test_bf16_interleaved_rotated_inside_the_forward_kernel(lib, B, T, C, NH, NKV, theta):
+    """attn_fwd (bf16) rotates each Q tile and every landed K tile in shared
+    memory: with the flag it turns each bf16 pair (2i, 2i+1) in place."""
+    check(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 100 + T + 64), "bf16", in_kernel=True)
