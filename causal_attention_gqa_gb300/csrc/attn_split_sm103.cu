@@ -218,15 +218,18 @@ __global__ void split_tables_kernel(float* __restrict__ LD, const float* __restr
 // ===========================================================================
 // Per key tile j: S = Qh Kh^T + Qh Kl^T + Ql Kh^T; online softmax over S's row
 // (exact rescale of O whenever the row maximum grows); P split into hi/lo in
-// TMEM; O += Ph Vh + Ph Vl + Pl Vh.  TMEM: S [0, 128), Ph [128, 192),
-// Pl [192, 256), O [256, 320).  Shared memory: Qh, Ql, and two stages of
-// (Kh, Kl, Vh, Vl).
+// TMEM; O += Ph Vh + Ph Vl + Pl Vh.  S is double-buffered and the issuer runs
+// two score tiles ahead of the PV products (S(j+2) right after PV(j)), so the
+// softmax of tile j+1 overlaps PV(j).  TMEM: S0 [0, 128), S1 [128, 256),
+// Ph [256, 320), Pl [320, 384), O [384, 448).  Shared memory: Qh, Ql, then a
+// K ring and a V ring of two stages of (hi, lo) each: K(j) is released as soon
+// as S(j) has read it, V(j) once PV(j) has.
 constexpr int kFwdThreads = 192;   // producer, issuer, four softmax warps
-constexpr int kFwdSmem = 2 * kTile + 2 * 4 * kTile + 256 + 1024;
-constexpr uint32_t kFS = 0, kFPh = 128, kFPl = 192, kFO = 256;
+constexpr int kFwdSmem = 2 * kTile + 2 * 2 * kTile + 2 * 2 * kTile + 256 + 1024;
+constexpr uint32_t kFPh = 256, kFPl = 320, kFO = 384;
 
 struct SplitFwdBars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_full, pv_done, drain;
+  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, pv_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -237,7 +240,8 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;                          // Qh, Ql
-  uint8_t* sKV = smem + 2 * kTile;             // stage s: Kh, Kl, Vh, Vl at sKV + (4 s + k) kTile
+  uint8_t* sK = smem + 2 * kTile;              // stage s: Kh, Kl at sK + 2 s kTile
+  uint8_t* sV = smem + 6 * kTile;              // stage s: Vh, Vl at sV + 2 s kTile
   SplitFwdBars* bars = reinterpret_cast<SplitFwdBars*>(smem + 10 * kTile);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -249,10 +253,12 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->p_full), 4);
     ptx::mbar_init(ptx::smem_u32(&bars->pv_done), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
@@ -271,7 +277,7 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
     *abort_flag = 1;
     record_status(status, kErrDeviceTimeout);
   };
-  int kv_issued = 0;
+  int k_issued = 0, v_issued = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -283,18 +289,26 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
       for (int j = 0; j <= qt; ++j) {
         const int st = j & 1;
         if (j >= 2 &&
-            !ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[st]), ((j >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+            !ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[st]), ((j >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
           fail();
           break;
         }
-        const uint32_t kf = ptx::smem_u32(&bars->kv_full[st]);
-        uint8_t* s4 = sKV + 4 * st * kTile;
-        ptx::mbar_arrive_expect_tx(kf, 4 * kTile);
-        ptx::tma_load_3d(ptx::smem_u32(s4), &tm_hi, g.C + kh * kHD, j * 128, b, kf);
-        ptx::tma_load_3d(ptx::smem_u32(s4 + kTile), &tm_lo, g.C + kh * kHD, j * 128, b, kf);
-        ptx::tma_load_3d(ptx::smem_u32(s4 + 2 * kTile), &tm_hi, g.C + g.NKV * kHD + kh * kHD, j * 128, b, kf);
-        ptx::tma_load_3d(ptx::smem_u32(s4 + 3 * kTile), &tm_lo, g.C + g.NKV * kHD + kh * kHD, j * 128, b, kf);
-        kv_issued = j + 1;
+        const uint32_t kf = ptx::smem_u32(&bars->k_full[st]);
+        ptx::mbar_arrive_expect_tx(kf, 2 * kTile);
+        ptx::tma_load_3d(ptx::smem_u32(sK + 2 * st * kTile), &tm_hi, g.C + kh * kHD, j * 128, b, kf);
+        ptx::tma_load_3d(ptx::smem_u32(sK + (2 * st + 1) * kTile), &tm_lo, g.C + kh * kHD, j * 128, b, kf);
+        k_issued = j + 1;
+        if (j >= 2 &&
+            !ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), ((j >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
+        ptx::mbar_arrive_expect_tx(vf, 2 * kTile);
+        ptx::tma_load_3d(ptx::smem_u32(sV + 2 * st * kTile), &tm_hi, g.C + g.NKV * kHD + kh * kHD, j * 128, b, vf);
+        ptx::tma_load_3d(ptx::smem_u32(sV + (2 * st + 1) * kTile), &tm_lo, g.C + g.NKV * kHD + kh * kHD, j * 128,
+                         b, vf);
+        v_issued = j + 1;
       }
     }
   } else if (warp == 1) {
@@ -304,31 +318,37 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
       constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, kHD, false, true);
       const uint64_t dQh = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
       const uint64_t dQl = ptx::sw128_desc(ptx::smem_u32(sQ + kTile), 16, 1024);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
-      for (int j = 0; j <= qt && ok; ++j) {
+      // S(j) into buffer j & 1 (free: the softmax read S(j-2) before it
+      // signalled p_full(j-2), which this thread waited for before PV(j-2)).
+      auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        uint8_t* s4 = sKV + 4 * st * kTile;
-        const uint64_t dKh = ptx::sw128_desc(ptx::smem_u32(s4), 16, 1024);
-        const uint64_t dKl = ptx::sw128_desc(ptx::smem_u32(s4 + kTile), 16, 1024);
-        const uint64_t dVh = ptx::sw128_desc(ptx::smem_u32(s4 + 2 * kTile), kTile, 1024);
-        const uint64_t dVl = ptx::sw128_desc(ptx::smem_u32(s4 + 3 * kTile), kTile, 1024);
-        // S(j) overwrites S(j-1), which the softmax read before it signalled
-        // p_full(j-1), waited for before PV(j-1).
+        const uint64_t dKh = ptx::sw128_desc(ptx::smem_u32(sK + 2 * st * kTile), 16, 1024);
+        const uint64_t dKl = ptx::sw128_desc(ptx::smem_u32(sK + (2 * st + 1) * kTile), 16, 1024);
+        const uint32_t d_s = tmem + 128u * (uint32_t)st;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(tmem + kFS, ptx::desc_advance(dQh, off), ptx::desc_advance(dKh, off), idesc_s,
-                           kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(tmem + kFS, ptx::desc_advance(dQh, off), ptx::desc_advance(dKl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(tmem + kFS, ptx::desc_advance(dQl, off), ptx::desc_advance(dKh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(dKh, off), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(dKl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQl, off), ptx::desc_advance(dKh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[st]));
+        return true;
+      };
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
+      if (ok) ok = issue_s(0);
+      if (ok && qt >= 1) ok = issue_s(1);
+      for (int j = 0; j <= qt && ok; ++j) {
+        const int st = j & 1;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), j & 1, abort_flag, kWaitLimitNs);
+        if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
+        const uint64_t dVh = ptx::sw128_desc(ptx::smem_u32(sV + 2 * st * kTile), kTile, 1024);
+        const uint64_t dVl = ptx::sw128_desc(ptx::smem_u32(sV + (2 * st + 1) * kTile), kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           ptx::mma_bf16_ts(tmem + kFO, tmem + kFPh + kk * 8, ptx::desc_advance(dVh, kk * 2048), idesc_o,
@@ -337,7 +357,8 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
           ptx::mma_bf16_ts(tmem + kFO, tmem + kFPl + kk * 8, ptx::desc_advance(dVh, kk * 2048), idesc_o, 1u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->pv_done));
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[st]));
+        if (j + 2 <= qt) ok = issue_s(j + 2);
       }
       if (!ok) fail();
       ptx::mma_commit(ptx::smem_u32(&bars->drain));
@@ -352,14 +373,16 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
     float m = -INFINITY, l = 0.f;                      // log2 units
     bool ok = true;
     for (int j = 0; j <= qt; ++j) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), j & 1, abort_flag, kWaitLimitNs));
+      const int sb = j & 1;
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sb]), (j >> 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       float s[128];
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t r[32];
-        ptx::tmem_ld32(t_lane + kFS + c0, r);
+        ptx::tmem_ld32(t_lane + 128u * (uint32_t)sb + c0, r);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(r[c]);
@@ -441,8 +464,10 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
   __syncthreads();
   if (warp == 0 && lane == 0) {
     // Every copy issued has landed before shared memory is released.
-    for (int st = 0; st < 2 && st < kv_issued; ++st)
-      ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((kv_issued - 1 - st) / 2) & 1, nullptr, kWaitLimitNs);
+    for (int st = 0; st < 2 && st < k_issued; ++st)
+      ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / 2) & 1, nullptr, kWaitLimitNs);
+    for (int st = 0; st < 2 && st < v_issued; ++st)
+      ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / 2) & 1, nullptr, kWaitLimitNs);
     ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, nullptr, kWaitLimitNs);
   }
   if (warp == 1) {
@@ -504,18 +529,20 @@ __device__ __forceinline__ void split_grad_row(uint32_t acc, float s, bool rope,
 // Per step (query head h of the group, query tile i >= j): S^T = K Q^T and
 // dP^T = V dO^T (three products each); P^T = exp2(S^T scale log2e - lse
 // log2e) split into TMEM over S^T; dV += P^T dO; dS^T = P^T (dP^T - D) split
-// into TMEM over dP^T; dK += dS^T Q.  Elementwise group w owns queries
-// 64 w .. 64 w + 63: its hi parts at columns 64 w .. + 31, lo parts at
-// 64 w + 32 .. + 63 of each 128-column block.  TMEM: S^T [0, 128), dP^T
-// [128, 256), dK [256, 320), dV [320, 384).  Shared memory: Kh, Kl, Vh, Vl,
-// then two ring stages of (Qh, Ql, dOh, dOl, row tables).
+// into TMEM over dP^T; dK += dS^T Q.  S^T is double-buffered and issued one
+// step ahead (dP^T(n), dV(n), S^T(n+1), dK(n)), so that the elementwise warps
+// form P^T(n+1) while the tensor core runs dK(n).  Elementwise group w owns
+// queries 64 w .. 64 w + 63: its hi parts at columns 64 w .. + 31, lo parts at
+// 64 w + 32 .. + 63 of each 128-column block.  TMEM: S^T buffers [0, 128) and
+// [128, 256), dP^T [256, 384), dK [384, 448), dV [448, 512).  Shared memory:
+// Kh, Kl, Vh, Vl, then two ring stages of (Qh, Ql, dOh, dOl, row tables).
 constexpr int kBwdThreads = 320;
 constexpr int kDkvStage = 4 * kTile + 1024;
 constexpr int kDkvSmem = 4 * kTile + 2 * kDkvStage + 256 + 1024;
-constexpr uint32_t kBS = 0, kBDP = 128, kBDK = 256, kBDV = 320;
+constexpr uint32_t kBDP = 256, kBDK = 384, kBDV = 448;   // S^T buffers at 0 and 128
 
 struct SplitDkvBars {
-  uint64_t kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_full, ds_full, acc_done, drain;
+  uint64_t kv_full, qdo_full[2], qdo_empty[2], s_full[2], dp_full, p_full, ds_full, acc_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -545,7 +572,8 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->p_full), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
@@ -609,27 +637,34 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       const uint64_t dKl = ptx::sw128_desc(ptx::smem_u32(sKV + kTile), 16, 1024);
       const uint64_t dVh = ptx::sw128_desc(ptx::smem_u32(sKV + 2 * kTile), 16, 1024);
       const uint64_t dVl = ptx::sw128_desc(ptx::smem_u32(sKV + 3 * kTile), 16, 1024);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
-      for (int n = 0; n < n_steps && ok; ++n) {
+      // S^T(n) = K Q(n)^T into buffer n & 1 (free: P^T(n-2) there was read by
+      // dV(n-2), issued before).
+      auto issue_s = [&](int n) -> bool {
         const int st = n & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), (n >> 1) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), (n >> 1) & 1, abort_flag, kWaitLimitNs))
+          return false;
         ptx::tc_fence_after();
-        uint8_t* s5 = sRing + st * kDkvStage;
-        const uint32_t aQh = ptx::smem_u32(s5), aQl = aQh + kTile, aDh = aQh + 2 * kTile, aDl = aQh + 3 * kTile;
-        const uint64_t kQh = ptx::sw128_desc(aQh, 16, 1024), kQl = ptx::sw128_desc(aQl, 16, 1024);
-        const uint64_t kDh = ptx::sw128_desc(aDh, 16, 1024), kDl = ptx::sw128_desc(aDl, 16, 1024);
-        // S^T = K Q^T and dP^T = V dO^T (over P^T / dS^T of the previous
-        // step, read by its dV / dK MMAs issued before: MMAs run in order).
+        const uint32_t aQh = ptx::smem_u32(sRing + st * kDkvStage);
+        const uint64_t kQh = ptx::sw128_desc(aQh, 16, 1024), kQl = ptx::sw128_desc(aQh + kTile, 16, 1024);
+        const uint32_t d_s = tmem + 128u * (uint32_t)st;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(tmem + kBS, ptx::desc_advance(dKh, off), ptx::desc_advance(kQh, off), idesc_s,
-                           kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(tmem + kBS, ptx::desc_advance(dKh, off), ptx::desc_advance(kQl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(tmem + kBS, ptx::desc_advance(dKl, off), ptx::desc_advance(kQh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dKh, off), ptx::desc_advance(kQh, off), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dKh, off), ptx::desc_advance(kQl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dKl, off), ptx::desc_advance(kQh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
+        return true;
+      };
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
+      if (ok && n_steps > 0) ok = issue_s(0);
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n & 1;
+        const uint32_t aQh = ptx::smem_u32(sRing + st * kDkvStage), aQl = aQh + kTile;
+        const uint32_t aDh = aQh + 2 * kTile, aDl = aQh + 3 * kTile;
+        const uint64_t kDh = ptx::sw128_desc(aDh, 16, 1024), kDl = ptx::sw128_desc(aDl, 16, 1024);
+        // dP^T = V dO^T (over dS^T(n-1), read by dK(n-1) issued before).
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
@@ -644,13 +679,16 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t mDh = ptx::sw128_desc(aDh, kTile, 1024), mDl = ptx::sw128_desc(aDl, kTile, 1024);
+        const uint32_t t_p = tmem + 128u * (uint32_t)st;
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          const uint32_t ph = tmem + kBS + hi_col(kk), pl = ph + 32;
+          const uint32_t ph = t_p + hi_col(kk), pl = ph + 32;
           ptx::mma_bf16_ts(tmem + kBDV, ph, ptx::desc_advance(mDh, kk * 2048), idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_bf16_ts(tmem + kBDV, ph, ptx::desc_advance(mDl, kk * 2048), idesc_g, 1u);
           ptx::mma_bf16_ts(tmem + kBDV, pl, ptx::desc_advance(mDh, kk * 2048), idesc_g, 1u);
         }
+        // The next step's scores, into the other S^T buffer.
+        if (n + 1 < n_steps && !(ok = issue_s(n + 1))) break;
         // dK += dS^T Q (B: Q MN-major).
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
@@ -684,17 +722,19 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       const int qi = j + n % nqj;
       const bool diag = qi == j;
       const float* tab = reinterpret_cast<const float*>(sRing + (n & 1) * kDkvStage + 4 * kTile);
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, abort_flag, kWaitLimitNs));
+      const uint32_t t_s = t_lane + 128u * (uint32_t)(n & 1);
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (n >> 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       float p[64];
-      load64(t_lane + kBS + q0, p);
+      load64(t_s + q0, p);
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float e = ptx::ex2_approx(fmaf(p[c], sl2, tab[q0 + c]));
         p[c] = (diag && q0 + c < row) ? 0.f : e;        // query q0 + c comes before key `row`
       }
-      store_split64(t_lane + kBS + q0, p);
+      store_split64(t_s + q0, p);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -743,14 +783,17 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
 // ===========================================================================
 // Per key tile j <= i: S = Q K^T and dP = dO V^T (three products each),
 // P = exp2(S scale log2e - lse log2e), dS = P (dP - D) split into TMEM over
-// dP, dQ += dS K.  Elementwise group w owns keys 64 w .. 64 w + 63.  TMEM: S
-// [0, 128), dP [128, 256), dQ [256, 320).  Shared memory: Qh, Ql, dOh, dOl,
-// then two ring stages of (Kh, Kl, Vh, Vl).
-constexpr int kDqSmem = 4 * kTile + 2 * 4 * kTile + 256 + 1024;
-constexpr uint32_t kQS = 0, kQDP = 128, kQDQ = 256;
+// dP, dQ += dS K.  S is double-buffered and issued one tile ahead (dP(j),
+// S(j+1), dQ(j)), so that P(j+1) is formed while the tensor core runs dQ(j).
+// Elementwise group w owns keys 64 w .. 64 w + 63.  TMEM: S buffers [0, 128)
+// and [128, 256), dP [256, 384), dQ [384, 448).  Shared memory: Qh, Ql, dOh,
+// dOl, a K ring of three stages (K(j) is read by S(j) and by dQ(j), which
+// trails S(j+1)) and a V ring of two stages (V(j) is read by dP(j) only).
+constexpr int kDqSmem = 4 * kTile + 3 * 2 * kTile + 2 * 2 * kTile + 256 + 1024;
+constexpr uint32_t kQDP = 256, kQDQ = 384;
 
 struct SplitDqBars {
-  uint64_t qdo_full, kv_full[2], kv_empty[2], s_full, dp_full, ds_full, acc_done, drain;
+  uint64_t qdo_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full, ds_full, acc_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -763,8 +806,9 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQD = smem;                                    // Qh, Ql, dOh, dOl
-  uint8_t* sKV = smem + 4 * kTile;                        // stage s at sKV + 4 s kTile: Kh, Kl, Vh, Vl
-  SplitDqBars* bars = reinterpret_cast<SplitDqBars*>(smem + 12 * kTile);
+  uint8_t* sK = smem + 4 * kTile;                         // stage s at sK + 2 s kTile: Kh, Kl
+  uint8_t* sV = smem + 10 * kTile;                        // stage s at sV + 2 s kTile: Vh, Vl
+  SplitDqBars* bars = reinterpret_cast<SplitDqBars*>(smem + 14 * kTile);
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nq = (g.T + 127) / 128, bh_count = g.B * g.NH;
@@ -775,11 +819,15 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bars->qdo_full), 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+    for (int s = 0; s < 3; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->k_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->v_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
+    }
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->acc_done), 1);
@@ -800,7 +848,7 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
     *abort_flag = 1;
     record_status(status, kErrDeviceTimeout);
   };
-  int kv_issued = 0;
+  int k_issued = 0, v_issued = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -812,20 +860,28 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
       ptx::tma_load_3d(ptx::smem_u32(sQD + 2 * kTile), &tm_dohi, h * kHD, qt * 128, b, qf);
       ptx::tma_load_3d(ptx::smem_u32(sQD + 3 * kTile), &tm_dolo, h * kHD, qt * 128, b, qf);
       for (int jj = 0; jj <= qt; ++jj) {
-        const int st = jj & 1;
-        if (jj >= 2 &&
-            !ptx::mbar_wait(ptx::smem_u32(&bars->kv_empty[st]), ((jj >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+        const int ks = jj % 3, vs = jj & 1;
+        if (jj >= 3 &&
+            !ptx::mbar_wait(ptx::smem_u32(&bars->k_empty[ks]), (jj / 3 - 1) & 1, abort_flag, kWaitLimitNs)) {
           fail();
           break;
         }
-        uint8_t* s4 = sKV + 4 * st * kTile;
-        const uint32_t kf = ptx::smem_u32(&bars->kv_full[st]);
-        ptx::mbar_arrive_expect_tx(kf, 4 * kTile);
-        ptx::tma_load_3d(ptx::smem_u32(s4), &tm_hi, g.C + kh * kHD, jj * 128, b, kf);
-        ptx::tma_load_3d(ptx::smem_u32(s4 + kTile), &tm_lo, g.C + kh * kHD, jj * 128, b, kf);
-        ptx::tma_load_3d(ptx::smem_u32(s4 + 2 * kTile), &tm_hi, g.C + g.NKV * kHD + kh * kHD, jj * 128, b, kf);
-        ptx::tma_load_3d(ptx::smem_u32(s4 + 3 * kTile), &tm_lo, g.C + g.NKV * kHD + kh * kHD, jj * 128, b, kf);
-        kv_issued = jj + 1;
+        const uint32_t kf = ptx::smem_u32(&bars->k_full[ks]);
+        ptx::mbar_arrive_expect_tx(kf, 2 * kTile);
+        ptx::tma_load_3d(ptx::smem_u32(sK + 2 * ks * kTile), &tm_hi, g.C + kh * kHD, jj * 128, b, kf);
+        ptx::tma_load_3d(ptx::smem_u32(sK + (2 * ks + 1) * kTile), &tm_lo, g.C + kh * kHD, jj * 128, b, kf);
+        k_issued = jj + 1;
+        if (jj >= 2 &&
+            !ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), ((jj >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        const uint32_t vf = ptx::smem_u32(&bars->v_full[vs]);
+        ptx::mbar_arrive_expect_tx(vf, 2 * kTile);
+        ptx::tma_load_3d(ptx::smem_u32(sV + 2 * vs * kTile), &tm_hi, g.C + g.NKV * kHD + kh * kHD, jj * 128, b, vf);
+        ptx::tma_load_3d(ptx::smem_u32(sV + (2 * vs + 1) * kTile), &tm_lo, g.C + g.NKV * kHD + kh * kHD, jj * 128,
+                         b, vf);
+        v_issued = jj + 1;
       }
     }
   } else if (warp == 1) {
@@ -837,27 +893,35 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
       const uint64_t dQl = ptx::sw128_desc(ptx::smem_u32(sQD + kTile), 16, 1024);
       const uint64_t dDh = ptx::sw128_desc(ptx::smem_u32(sQD + 2 * kTile), 16, 1024);
       const uint64_t dDl = ptx::sw128_desc(ptx::smem_u32(sQD + 3 * kTile), 16, 1024);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full), 0, abort_flag, kWaitLimitNs);
-      for (int jj = 0; jj <= qt && ok; ++jj) {
-        const int st = jj & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), (jj >> 1) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
+      // S(j) = Q K(j)^T into buffer j & 1 (free: the elementwise warps read
+      // S(j-2) before they signalled ds_full(j-2), waited for before dQ(j-2)).
+      auto issue_s = [&](int jj) -> bool {
+        const int ks = jj % 3;
+        if (!ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), (jj / 3) & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        uint8_t* s4 = sKV + 4 * st * kTile;
-        const uint32_t aKh = ptx::smem_u32(s4), aKl = aKh + kTile;
-        const uint64_t kKh = ptx::sw128_desc(aKh, 16, 1024), kKl = ptx::sw128_desc(aKl, 16, 1024);
-        const uint64_t kVh = ptx::sw128_desc(aKh + 2 * kTile, 16, 1024), kVl = ptx::sw128_desc(aKh + 3 * kTile, 16, 1024);
-        // S = Q K^T, dP = dO V^T (over dS of the previous step, read by its
-        // dQ MMAs issued before).
+        const uint32_t aKh = ptx::smem_u32(sK + 2 * ks * kTile);
+        const uint64_t kKh = ptx::sw128_desc(aKh, 16, 1024), kKl = ptx::sw128_desc(aKh + kTile, 16, 1024);
+        const uint32_t d_s = tmem + 128u * (uint32_t)(jj & 1);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(tmem + kQS, ptx::desc_advance(dQh, off), ptx::desc_advance(kKh, off), idesc_s,
-                           kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(tmem + kQS, ptx::desc_advance(dQh, off), ptx::desc_advance(kKl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(tmem + kQS, ptx::desc_advance(dQl, off), ptx::desc_advance(kKh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(kKh, off), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(kKl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQl, off), ptx::desc_advance(kKh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+        ptx::mma_commit(ptx::smem_u32(&bars->s_full[jj & 1]));
+        return true;
+      };
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full), 0, abort_flag, kWaitLimitNs);
+      if (ok) ok = issue_s(0);
+      for (int jj = 0; jj <= qt && ok; ++jj) {
+        const int ks = jj % 3, vs = jj & 1;
+        // dP = dO V^T (over dS(j-1), read by dQ(j-1) issued before).
+        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[vs]), (jj >> 1) & 1, abort_flag, kWaitLimitNs)))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t aVh = ptx::smem_u32(sV + 2 * vs * kTile);
+        const uint64_t kVh = ptx::sw128_desc(aVh, 16, 1024), kVl = ptx::sw128_desc(aVh + kTile, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
@@ -867,11 +931,15 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
           ptx::mma_bf16_ss(tmem + kQDP, ptx::desc_advance(dDl, off), ptx::desc_advance(kVh, off), idesc_s, 1u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
+        // The next tile's scores, into the other S buffer.
+        if (jj + 1 <= qt && !(ok = issue_s(jj + 1))) break;
         // dQ += dS K (B: K MN-major, 16 keys per K step).
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), jj & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint64_t mKh = ptx::sw128_desc(aKh, kTile, 1024), mKl = ptx::sw128_desc(aKl, kTile, 1024);
+        const uint32_t aKh = ptx::smem_u32(sK + 2 * ks * kTile);
+        const uint64_t mKh = ptx::sw128_desc(aKh, kTile, 1024), mKl = ptx::sw128_desc(aKh + kTile, kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t dh = tmem + kQDP + hi_col(kk), dl = dh + 32;
@@ -879,7 +947,7 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
           ptx::mma_bf16_ts(tmem + kQDQ, dh, ptx::desc_advance(mKl, kk * 2048), idesc_g, 1u);
           ptx::mma_bf16_ts(tmem + kQDQ, dl, ptx::desc_advance(mKh, kk * 2048), idesc_g, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[st]));
+        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
       }
       if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
       else fail();
@@ -900,11 +968,12 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
     bool ok = true;
     for (int jj = 0; jj <= qt; ++jj) {
       const bool diag = jj == qt;
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), jj & 1, abort_flag, kWaitLimitNs));
+      ok = __all_sync(0xffffffffu,
+                      ptx::mbar_wait(ptx::smem_u32(&bars->s_full[jj & 1]), (jj >> 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       float p[64];
-      load64(t_lane + kQS + k0, p);
+      load64(t_lane + 128u * (uint32_t)(jj & 1) + k0, p);
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float e = ptx::ex2_approx(fmaf(p[c], sl2, nl));
@@ -938,8 +1007,10 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
   __syncthreads();
   if (warp == 0 && lane == 0) {
     ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full), 0, nullptr, kWaitLimitNs);
-    for (int st = 0; st < 2 && st < kv_issued; ++st)
-      ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[st]), ((kv_issued - 1 - st) / 2) & 1, nullptr, kWaitLimitNs);
+    for (int st = 0; st < 3 && st < k_issued; ++st)
+      ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / 3) & 1, nullptr, kWaitLimitNs);
+    for (int st = 0; st < 2 && st < v_issued; ++st)
+      ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / 2) & 1, nullptr, kWaitLimitNs);
   }
   if (warp == 1) {
     __syncwarp();
