@@ -218,10 +218,15 @@ __global__ void split_tables_kernel(float* __restrict__ LD, const float* __restr
 // ===========================================================================
 // Per key tile j: S = Qh Kh^T + Qh Kl^T + Ql Kh^T; online softmax over S's row
 // (exact rescale of O whenever the row maximum grows); P split into hi/lo in
-// TMEM; O += Ph Vh + Ph Vl + Pl Vh.  S is double-buffered and the issuer runs
-// two score tiles ahead of the PV products (S(j+2) right after PV(j)), so the
-// softmax of tile j+1 overlaps PV(j).  TMEM: S0 [0, 128), S1 [128, 256),
-// Ph [256, 320), Pl [320, 384), O [384, 448).  Shared memory: Qh, Ql, then a
+// TMEM; O += Ph Vh + Ph Vl + Pl Vh, as one N = 128 product Ph [Vh | Vl] (Vh and
+// Vl sit side by side in shared memory: the accumulator's first 64 columns
+// get Ph Vh, the next 64 Ph Vl) and one N = 64 product Pl Vh into the first
+// half; the epilogue adds the halves.  Sixteen MMAs a tile instead of 24 of
+// N = 64 (the issue of the PV products sits on the tile's critical path).  S
+// is double-buffered and the issuer runs two score tiles ahead of the PV
+// products (S(j+2) right after PV(j)), so the softmax of tile j+1 overlaps
+// PV(j).  TMEM: S0 [0, 128), S1 [128, 256), Ph [256, 320), Pl [320, 384),
+// O [384, 512).  Shared memory: Qh, Ql, then a
 // K ring and a V ring of two stages of (hi, lo) each: K(j) is released as soon
 // as S(j) has read it, V(j) once PV(j) has.
 constexpr int kFwdThreads = 192;   // producer, issuer, four softmax warps
@@ -316,6 +321,7 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, kHD, false, true);
+      constexpr uint32_t idesc_o2 = ptx::idesc_bf16_f32(128, 2 * kHD, false, true);
       const uint64_t dQh = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
       const uint64_t dQl = ptx::sw128_desc(ptx::smem_u32(sQ + kTile), 16, 1024);
       // S(j) into buffer j & 1 (free: the softmax read S(j-2) before it
@@ -347,14 +353,13 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
         if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint64_t dVh = ptx::sw128_desc(ptx::smem_u32(sV + 2 * st * kTile), kTile, 1024);
-        const uint64_t dVl = ptx::sw128_desc(ptx::smem_u32(sV + (2 * st + 1) * kTile), kTile, 1024);
+        // B: [Vh | Vl] MN-major, the two 64-column atoms kTile apart.
+        const uint64_t dV2 = ptx::sw128_desc(ptx::smem_u32(sV + 2 * st * kTile), kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPh + kk * 8, ptx::desc_advance(dVh, kk * 2048), idesc_o,
+          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPh + kk * 8, ptx::desc_advance(dV2, kk * 2048), idesc_o2,
                            (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPh + kk * 8, ptx::desc_advance(dVl, kk * 2048), idesc_o, 1u);
-          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPl + kk * 8, ptx::desc_advance(dVh, kk * 2048), idesc_o, 1u);
+          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPl + kk * 8, ptx::desc_advance(dV2, kk * 2048), idesc_o, 1u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->pv_done));
         ptx::mma_commit(ptx::smem_u32(&bars->v_empty[st]));
@@ -411,14 +416,15 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
         if (!ok) break;
         ptx::tc_fence_after();
         if (__any_sync(0xffffffffu, m_new > m)) {
-          uint32_t o[64];
-          ptx::tmem_ld32(t_lane + kFO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-          ptx::tmem_ld32(t_lane + kFO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-          ptx::tmem_wait_ld();
+#pragma unroll 1
+          for (int c0 = 0; c0 < 2 * kHD; c0 += 32) {
+            uint32_t o[32];
+            ptx::tmem_ld32(t_lane + kFO + c0, o);
+            ptx::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 64; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
-          ptx::tmem_st32(t_lane + kFO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-          ptx::tmem_st32(t_lane + kFO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+            ptx::tmem_st32(t_lane + kFO + c0, o);
+          }
         }
       }
       m = m_new;
@@ -440,10 +446,18 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->pv_done), qt & 1, abort_flag, kWaitLimitNs));
     if (ok) {
       ptx::tc_fence_after();
-      uint32_t o[64];
-      ptx::tmem_ld32(t_lane + kFO, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-      ptx::tmem_ld32(t_lane + kFO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-      ptx::tmem_wait_ld();
+      float o[64];
+      {
+        uint32_t a[32], b2[32];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          ptx::tmem_ld32(t_lane + kFO + 32 * h2, a);
+          ptx::tmem_ld32(t_lane + kFO + kHD + 32 * h2, b2);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[32 * h2 + c] = __uint_as_float(a[c]) + __uint_as_float(b2[c]);
+        }
+      }
       const int t = qt * 128 + row;
       if (t < g.T) {
         const float inv_l = 1.f / l;
@@ -451,8 +465,7 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
 #pragma unroll
         for (int q = 0; q < 16; ++q)
           *reinterpret_cast<float4*>(dst + 4 * q) =
-              make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                          __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+              make_float4(o[4 * q] * inv_l, o[4 * q + 1] * inv_l, o[4 * q + 2] * inv_l, o[4 * q + 3] * inv_l);
         lse[((size_t)b * g.NH + h) * g.T + t] = (m + log2f(l)) * kLn2;
       }
     } else {
@@ -477,43 +490,54 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
   }
 }
 
-// Float32 epilogue of one gradient row held in TMEM (kHD columns at `acc`):
-// scaled by `s`, the RoPE rotation at position `t` undone if `rope`, written
-// to `dst` (interleaved pairs back to columns 2i, 2i+1).  The row is shared
-// by `nparts` callers: this one takes 16 of the 32 pairs (RoPE) or 32 of the
-// 64 columns (no RoPE) when nparts = 2.  Warp-collective.
-__device__ __forceinline__ void split_grad_row(uint32_t acc, float s, bool rope, int t, const Geometry& g,
-                                               float* dst, bool valid, int part, int nparts) {
+// Float32 epilogue of one gradient row held in TMEM (kHD columns at `acc`,
+// plus the kHD columns after them when `two`: an accumulator kept as two
+// halves that add up to the row): scaled by `s`, the RoPE rotation at
+// position `t` undone if `rope`, written to `dst` (interleaved pairs back to
+// columns 2i, 2i+1).  The row is shared by `nparts` callers: this one takes
+// 16 of the 32 pairs (RoPE) or 32 of the 64 columns (no RoPE) when
+// nparts = 2.  Warp-collective.
+__device__ __forceinline__ void split_grad_row(uint32_t acc, bool two, float s, bool rope, int t,
+                                               const Geometry& g, float* dst, bool valid, int part, int nparts) {
   constexpr int HALF = kHD / 2;
   if (!rope) {
     const int n = kHD / nparts, c0 = part * n;
 #pragma unroll 1
     for (int c = c0; c < c0 + n; c += 16) {
-      uint32_t v[16];
+      uint32_t v[16], w[16];
       ptx::tmem_ld16(acc + c, v);
+      if (two) ptx::tmem_ld16(acc + kHD + c, w);
       ptx::tmem_wait_ld();
+      float x[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = two ? __uint_as_float(v[e]) + __uint_as_float(w[e]) : __uint_as_float(v[e]);
       if (valid) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           *reinterpret_cast<float4*>(dst + c + 4 * q) =
-              make_float4(__uint_as_float(v[4 * q]) * s, __uint_as_float(v[4 * q + 1]) * s,
-                          __uint_as_float(v[4 * q + 2]) * s, __uint_as_float(v[4 * q + 3]) * s);
+              make_float4(x[4 * q] * s, x[4 * q + 1] * s, x[4 * q + 2] * s, x[4 * q + 3] * s);
       }
     }
     return;
   }
   const int n = HALF / nparts, i0 = part * n;
-  uint32_t a[16], c[16];
+  uint32_t a[16], c[16], a2[16], c2[16];
   ptx::tmem_ld16(acc + i0, a);
   ptx::tmem_ld16(acc + HALF + i0, c);
+  if (two) {
+    ptx::tmem_ld16(acc + kHD + i0, a2);
+    ptx::tmem_ld16(acc + kHD + HALF + i0, c2);
+  }
   ptx::tmem_wait_ld();
   if (!valid) return;
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     const int i = i0 + e;
+    const float xa = two ? __uint_as_float(a[e]) + __uint_as_float(a2[e]) : __uint_as_float(a[e]);
+    const float xc = two ? __uint_as_float(c[e]) + __uint_as_float(c2[e]) : __uint_as_float(c[e]);
     float sn, cs, y0, y1;
     __sincosf(rope_angle(t, g.rope_f_hi[i], g.rope_f_lo[i]), &sn, &cs);
-    rope_pair_transpose(__uint_as_float(a[e]) * s, __uint_as_float(c[e]) * s, cs, sn, y0, y1);
+    rope_pair_transpose(xa * s, xc * s, cs, sn, y0, y1);
     if (!g.rope_interleaved) {
       dst[i] = y0;
       dst[HALF + i] = y1;
@@ -529,17 +553,22 @@ __device__ __forceinline__ void split_grad_row(uint32_t acc, float s, bool rope,
 // Per step (query head h of the group, query tile i >= j): S^T = K Q^T and
 // dP^T = V dO^T (three products each); P^T = exp2(S^T scale log2e - lse
 // log2e) split into TMEM over S^T; dV += P^T dO; dS^T = P^T (dP^T - D) split
-// into TMEM over dP^T; dK += dS^T Q.  S^T is double-buffered and issued one
-// step ahead (dP^T(n), dV(n), S^T(n+1), dK(n)), so that the elementwise warps
-// form P^T(n+1) while the tensor core runs dK(n).  Elementwise group w owns
-// queries 64 w .. 64 w + 63: its hi parts at columns 64 w .. + 31, lo parts at
-// 64 w + 32 .. + 63 of each 128-column block.  TMEM: S^T buffers [0, 128) and
-// [128, 256), dP^T [256, 384), dK [384, 448), dV [448, 512).  Shared memory:
+// into TMEM over dP^T; dK += dS^T Q.  The gradient products take the hi and
+// lo parts of dO (of Q) as one N = 128 B operand [dOh | dOl] (they sit side
+// by side in shared memory): P^Th [dOh | dOl] at N = 128 and P^Tl dOh at
+// N = 64 into the first half of a two-half accumulator that the epilogue
+// adds up, 16 MMAs a product instead of 24 of N = 64.  S^T(n+1) is issued
+// one step ahead (dP^T(n), dV(n), S^T(n+1), dK(n)), so that the elementwise
+// warps form P^T(n+1) while the tensor core runs dK(n); it goes over P^T(n)
+// in the one S^T buffer after dV(n) has read it (MMAs from one thread run in
+// order).  Elementwise group w owns queries 64 w .. 64 w + 63: its hi parts at
+// columns 64 w .. + 31, lo parts at 64 w + 32 .. + 63 of each 128-column
+// block.  TMEM: S^T [0, 128), dP^T [128, 256), dK [256, 384), dV [384, 512).  Shared memory:
 // Kh, Kl, Vh, Vl, then two ring stages of (Qh, Ql, dOh, dOl, row tables).
 constexpr int kBwdThreads = 320;
 constexpr int kDkvStage = 4 * kTile + 1024;
 constexpr int kDkvSmem = 4 * kTile + 2 * kDkvStage + 256 + 1024;
-constexpr uint32_t kBDP = 256, kBDK = 384, kBDV = 448;   // S^T buffers at 0 and 128
+constexpr uint32_t kBS = 0, kBDP = 128, kBDK = 256, kBDV = 384;
 
 struct SplitDkvBars {
   uint64_t kv_full, qdo_full[2], qdo_empty[2], s_full[2], dp_full, p_full, ds_full, acc_done, drain;
@@ -633,12 +662,12 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, kHD, false, true);
+      constexpr uint32_t idesc_g2 = ptx::idesc_bf16_f32(128, 2 * kHD, false, true);
       const uint64_t dKh = ptx::sw128_desc(ptx::smem_u32(sKV), 16, 1024);
       const uint64_t dKl = ptx::sw128_desc(ptx::smem_u32(sKV + kTile), 16, 1024);
       const uint64_t dVh = ptx::sw128_desc(ptx::smem_u32(sKV + 2 * kTile), 16, 1024);
       const uint64_t dVl = ptx::sw128_desc(ptx::smem_u32(sKV + 3 * kTile), 16, 1024);
-      // S^T(n) = K Q(n)^T into buffer n & 1 (free: P^T(n-2) there was read by
-      // dV(n-2), issued before).
+      // S^T(n) = K Q(n)^T over P^T(n-1), read by dV(n-1) issued before.
       auto issue_s = [&](int n) -> bool {
         const int st = n & 1;
         if (!ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), (n >> 1) & 1, abort_flag, kWaitLimitNs))
@@ -646,7 +675,7 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
         ptx::tc_fence_after();
         const uint32_t aQh = ptx::smem_u32(sRing + st * kDkvStage);
         const uint64_t kQh = ptx::sw128_desc(aQh, 16, 1024), kQl = ptx::sw128_desc(aQh + kTile, 16, 1024);
-        const uint32_t d_s = tmem + 128u * (uint32_t)st;
+        const uint32_t d_s = tmem + kBS;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
@@ -661,7 +690,7 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       if (ok && n_steps > 0) ok = issue_s(0);
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n & 1;
-        const uint32_t aQh = ptx::smem_u32(sRing + st * kDkvStage), aQl = aQh + kTile;
+        const uint32_t aQh = ptx::smem_u32(sRing + st * kDkvStage);
         const uint32_t aDh = aQh + 2 * kTile, aDl = aQh + 3 * kTile;
         const uint64_t kDh = ptx::sw128_desc(aDh, 16, 1024), kDl = ptx::sw128_desc(aDl, 16, 1024);
         // dP^T = V dO^T (over dS^T(n-1), read by dK(n-1) issued before).
@@ -674,32 +703,30 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
           ptx::mma_bf16_ss(tmem + kBDP, ptx::desc_advance(dVl, off), ptx::desc_advance(kDh, off), idesc_s, 1u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-        // dV += P^T dO (B: dO MN-major, 16 queries per K step).
+        // dV += P^T dO (B: [dOh | dOl] MN-major, 16 queries per K step).
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint64_t mDh = ptx::sw128_desc(aDh, kTile, 1024), mDl = ptx::sw128_desc(aDl, kTile, 1024);
-        const uint32_t t_p = tmem + 128u * (uint32_t)st;
+        const uint64_t mD2 = ptx::sw128_desc(aDh, kTile, 1024);
+        const uint32_t t_p = tmem + kBS;
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t ph = t_p + hi_col(kk), pl = ph + 32;
-          ptx::mma_bf16_ts(tmem + kBDV, ph, ptx::desc_advance(mDh, kk * 2048), idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kBDV, ph, ptx::desc_advance(mDl, kk * 2048), idesc_g, 1u);
-          ptx::mma_bf16_ts(tmem + kBDV, pl, ptx::desc_advance(mDh, kk * 2048), idesc_g, 1u);
+          ptx::mma_bf16_ts(tmem + kBDV, ph, ptx::desc_advance(mD2, kk * 2048), idesc_g2, (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + kBDV, pl, ptx::desc_advance(mD2, kk * 2048), idesc_g, 1u);
         }
-        // The next step's scores, into the other S^T buffer.
+        // The next step's scores, over P^T(n) (dV(n) above read it).
         if (n + 1 < n_steps && !(ok = issue_s(n + 1))) break;
-        // dK += dS^T Q (B: Q MN-major).
+        // dK += dS^T Q (B: [Qh | Ql] MN-major).
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
-        const uint64_t mQh = ptx::sw128_desc(aQh, kTile, 1024), mQl = ptx::sw128_desc(aQl, kTile, 1024);
+        const uint64_t mQ2 = ptx::sw128_desc(aQh, kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t dh = tmem + kBDP + hi_col(kk), dl = dh + 32;
-          ptx::mma_bf16_ts(tmem + kBDK, dh, ptx::desc_advance(mQh, kk * 2048), idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kBDK, dh, ptx::desc_advance(mQl, kk * 2048), idesc_g, 1u);
-          ptx::mma_bf16_ts(tmem + kBDK, dl, ptx::desc_advance(mQh, kk * 2048), idesc_g, 1u);
+          ptx::mma_bf16_ts(tmem + kBDK, dh, ptx::desc_advance(mQ2, kk * 2048), idesc_g2, (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + kBDK, dl, ptx::desc_advance(mQ2, kk * 2048), idesc_g, 1u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[st]));
       }
@@ -722,7 +749,7 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       const int qi = j + n % nqj;
       const bool diag = qi == j;
       const float* tab = reinterpret_cast<const float*>(sRing + (n & 1) * kDkvStage + 4 * kTile);
-      const uint32_t t_s = t_lane + 128u * (uint32_t)(n & 1);
+      const uint32_t t_s = t_lane + kBS;
       ok = __all_sync(0xffffffffu,
                       ptx::mbar_wait(ptx::smem_u32(&bars->s_full[n & 1]), (n >> 1) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
@@ -757,8 +784,8 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       ptx::tc_fence_after();
       const bool valid = ks < g.T;
       float* drow = dqkv + ((size_t)b * g.T + (valid ? ks : 0)) * g.W;
-      split_grad_row(t_lane + kBDV, 1.f, false, ks, g, drow + g.C + g.NKV * kHD + kh * kHD, valid, wg, 2);
-      split_grad_row(t_lane + kBDK, g.scale, ROPE, ks, g, drow + g.C + kh * kHD, valid, wg, 2);
+      split_grad_row(t_lane + kBDV, true, 1.f, false, ks, g, drow + g.C + g.NKV * kHD + kh * kHD, valid, wg, 2);
+      split_grad_row(t_lane + kBDK, true, g.scale, ROPE, ks, g, drow + g.C + kh * kHD, valid, wg, 2);
     } else {
       fail();
     }
@@ -783,10 +810,12 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
 // ===========================================================================
 // Per key tile j <= i: S = Q K^T and dP = dO V^T (three products each),
 // P = exp2(S scale log2e - lse log2e), dS = P (dP - D) split into TMEM over
-// dP, dQ += dS K.  S is double-buffered and issued one tile ahead (dP(j),
+// dP, dQ += dSh Kh + dSh Kl + dSl Kh as one N = 128 product dSh [Kh | Kl]
+// and one N = 64 product dSl Kh into the accumulator's first half (the
+// epilogue adds the halves).  S is double-buffered and issued one tile ahead (dP(j),
 // S(j+1), dQ(j)), so that P(j+1) is formed while the tensor core runs dQ(j).
 // Elementwise group w owns keys 64 w .. 64 w + 63.  TMEM: S buffers [0, 128)
-// and [128, 256), dP [256, 384), dQ [384, 448).  Shared memory: Qh, Ql, dOh,
+// and [128, 256), dP [256, 384), dQ [384, 512) as two halves.  Shared memory: Qh, Ql, dOh,
 // dOl, a K ring of three stages (K(j) is read by S(j) and by dQ(j), which
 // trails S(j+1)) and a V ring of two stages (V(j) is read by dP(j) only).
 constexpr int kDqSmem = 4 * kTile + 3 * 2 * kTile + 2 * 2 * kTile + 256 + 1024;
@@ -889,6 +918,7 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
     if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, kHD, false, true);
+      constexpr uint32_t idesc_g2 = ptx::idesc_bf16_f32(128, 2 * kHD, false, true);
       const uint64_t dQh = ptx::sw128_desc(ptx::smem_u32(sQD), 16, 1024);
       const uint64_t dQl = ptx::sw128_desc(ptx::smem_u32(sQD + kTile), 16, 1024);
       const uint64_t dDh = ptx::sw128_desc(ptx::smem_u32(sQD + 2 * kTile), 16, 1024);
@@ -934,18 +964,19 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
         ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
         // The next tile's scores, into the other S buffer.
         if (jj + 1 <= qt && !(ok = issue_s(jj + 1))) break;
-        // dQ += dS K (B: K MN-major, 16 keys per K step).
+        // dQ += dS K (B: [Kh | Kl] MN-major, the two 64-column atoms kTile
+        // apart; 16 keys per K step).
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), jj & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t aKh = ptx::smem_u32(sK + 2 * ks * kTile);
-        const uint64_t mKh = ptx::sw128_desc(aKh, kTile, 1024), mKl = ptx::sw128_desc(aKh + kTile, kTile, 1024);
+        const uint64_t mK2 = ptx::sw128_desc(aKh, kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t dh = tmem + kQDP + hi_col(kk), dl = dh + 32;
-          ptx::mma_bf16_ts(tmem + kQDQ, dh, ptx::desc_advance(mKh, kk * 2048), idesc_g, (jj > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kQDQ, dh, ptx::desc_advance(mKl, kk * 2048), idesc_g, 1u);
-          ptx::mma_bf16_ts(tmem + kQDQ, dl, ptx::desc_advance(mKh, kk * 2048), idesc_g, 1u);
+          ptx::mma_bf16_ts(tmem + kQDQ, dh, ptx::desc_advance(mK2, kk * 2048), idesc_g2,
+                           (jj > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + kQDQ, dl, ptx::desc_advance(mK2, kk * 2048), idesc_g, 1u);
         }
         ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
       }
@@ -997,7 +1028,7 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
       ptx::tc_fence_after();
       const bool valid = tq < g.T;
       float* drow = dqkv + ((size_t)b * g.T + (valid ? tq : 0)) * g.W + h * kHD;
-      split_grad_row(t_lane + kQDQ, g.scale, ROPE, tq, g, drow, valid, wg, 2);
+      split_grad_row(t_lane + kQDQ, true, g.scale, ROPE, tq, g, drow, valid, wg, 2);
     } else {
       fail();
     }
