@@ -263,8 +263,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), ((issued - 1 - st) / NQS) & 1, nullptr, kWaitLimitNs);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (the whole warp
+    // runs the loop; one elected lane issues each MMA and commit)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
@@ -273,19 +274,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       const uint64_t dDOk = ptx::sw128_desc(ptx::smem_u32(sDO), 16, 1024);
       const uint64_t dQm = ptx::sw128_desc(ptx::smem_u32(sQ), Cfg::kAtom, 1024);
       const uint64_t dDOm = ptx::sw128_desc(ptx::smem_u32(sDO), Cfg::kAtom, 1024);
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
+      bool ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
       // dK += dS^T Q of step m once both groups wrote dS^T(m); frees the
       // step's ring slot.
       auto issue_dk = [&](int m) -> bool {
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), m & 1, abort_flag, kWaitLimitNs)) return false;
+        if (!ptx::mbar_wait_all(ptx::smem_u32(&bars->ds_full), m & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
         const int ms = m % NQS;
         const uint64_t gq = ptx::desc_advance(dQm, ms * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(gq, kk * 2048),
+          ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDK, tmem + Cfg::kTmemDP + pair_col(kk), ptx::desc_advance(gq, kk * 2048),
                            idesc_g, (m > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[ms]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->qdo_empty[ms]));
         return true;
       };
       // Issue order S^T(n), dK(n-1), dP^T(n), dV(n): the tensor core works on
@@ -295,40 +296,40 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // overwrites P^T(n) after dV(n): MMAs from one thread run in order.
       for (int n = 0; n < n_steps && ok; ++n) {
         const int qs = n % NQS;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t bq = ptx::desc_advance(dQk, qs * Cfg::kQTile), bdo = ptx::desc_advance(dDOk, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemS, ptx::desc_advance(dK, off), ptx::desc_advance(bq, off), idesc_s,
+          ptx::mma_bf16_ss_w(tmem + Cfg::kTmemS, ptx::desc_advance(dK, off), ptx::desc_advance(bq, off), idesc_s,
                            kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full));
         if (n > 0 && !(ok = issue_dk(n - 1))) break;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-          ptx::mma_bf16_ss(tmem + Cfg::kTmemDP, ptx::desc_advance(dV, off), ptx::desc_advance(bdo, off), idesc_s,
+          ptx::mma_bf16_ss_w(tmem + Cfg::kTmemDP, ptx::desc_advance(dV, off), ptx::desc_advance(bdo, off), idesc_s,
                            kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
         // dV += P^T dO once both groups wrote P^T.
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t gdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk), ptx::desc_advance(gdo, kk * 2048),
+          ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk), ptx::desc_advance(gdo, kk * 2048),
                            idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
       }
       if (ok && n_steps > 0) ok = issue_dk(n_steps - 1);
-      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (ok) ptx::mma_commit_w(ptx::smem_u32(&bars->acc_done));
       if (!ok) fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
@@ -680,8 +681,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (the whole warp
+    // runs the loop; one elected lane issues each MMA and commit)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, HD, false, true);
       const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
@@ -695,64 +697,65 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int p_g = -1, p_it = 0;
       bool p_first = false, p_last = false;
       auto issue_dq = [&]() -> bool {
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), p_g & 1, abort_flag, kWaitLimitNs)) return false;
+        if (!ptx::mbar_wait_all(ptx::smem_u32(&bars->ds_full), p_g & 1, abort_flag, kWaitLimitNs)) return false;
         const int db = p_it & 1;
         // The item's first dQ MMA overwrites accumulator db: the epilogue of
         // the item two before must have read it.
         if (p_first && p_it >= 2 &&
-            !ptx::mbar_wait(ptx::smem_u32(&bars->dq_free[db]), ((p_it >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
+            !ptx::mbar_wait_all(ptx::smem_u32(&bars->dq_free[db]), ((p_it >> 1) - 1) & 1, abort_flag, kWaitLimitNs))
           return false;
         ptx::tc_fence_after();
         const int ms = p_g % NKS;
         const uint64_t bk = ptx::desc_advance(dKm, ms * Cfg::kKTile);
 #pragma unroll
         for (int kk = 0; kk < Cfg::kKeys / 16; ++kk)
-          ptx::mma_bf16_ts(tmem + Cfg::kTmemDQ + 128 * db, tmem + Cfg::kTmemDP + pair_col(kk),
+          ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDQ + 128 * db, tmem + Cfg::kTmemDP + pair_col(kk),
                            ptx::desc_advance(bk, kk * 2048), idesc_g, (!p_first || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ms]));
-        if (p_last) ptx::mma_commit(ptx::smem_u32(&bars->acc_done[db]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->k_empty[ms]));
+        if (p_last) ptx::mma_commit_w(ptx::smem_u32(&bars->acc_done[db]));
         return true;
       };
       int gs = 0;
       for (int it = 0; ok; ++it) {
         const int w = next_item(it, &ok);
-        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[it % NIS]));
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[it % NIS]));
         if (!ok || w < 0) break;
         const DqItem item = dq_item(w, g);
         const int n_steps = item.qt + 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs);
         for (int n = 0; n < n_steps && ok; ++n) {
           const int gi = gs + n, ks = gi % NKS, u = gi / NKS;
           // K landed; the groups have read the previous S out of TMEM.
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), u & 1, abort_flag, kWaitLimitNs);
-          if (ok && gi > 0) ok = ptx::mbar_wait(ptx::smem_u32(&bars->s_free), (gi - 1) & 1, abort_flag, kWaitLimitNs);
+          ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->k_full[ks]), u & 1, abort_flag, kWaitLimitNs);
+          if (ok && gi > 0) ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->s_free), (gi - 1) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, ks * Cfg::kKTile);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-            ptx::mma_bf16_ss(tmem + Cfg::kTmemS, ptx::desc_advance(dQ, off), ptx::desc_advance(bk, off), idesc_s,
+            ptx::mma_bf16_ss_w(tmem + Cfg::kTmemS, ptx::desc_advance(dQ, off), ptx::desc_advance(bk, off), idesc_s,
                              kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(ptx::smem_u32(&bars->s_full));
-          if (n == n_steps - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->s_full));
+          if (n == n_steps - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->q_empty));
           // The previous step's dQ reads its dS in the dP columns: issued
           // before dP overwrites them (MMAs from one thread run in order).
           if (p_g >= 0 && !(ok = issue_dq())) break;
-          if (n == 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->do_full), it & 1, abort_flag, kWaitLimitNs)))
+          if (n == 0 && !(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->do_full), it & 1, abort_flag, kWaitLimitNs)))
             break;
-          if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[ks]), u & 1, abort_flag, kWaitLimitNs))) break;
+          if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->v_full[ks]), u & 1, abort_flag, kWaitLimitNs))) break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-            ptx::mma_bf16_ss(tmem + Cfg::kTmemDP, ptx::desc_advance(dDO, off), ptx::desc_advance(bv, off), idesc_s,
+            ptx::mma_bf16_ss_w(tmem + Cfg::kTmemDP, ptx::desc_advance(dDO, off), ptx::desc_advance(bv, off), idesc_s,
                              kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[ks]));
-          if (n == n_steps - 1) ptx::mma_commit(ptx::smem_u32(&bars->do_empty));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[ks]));
+          if (n == n_steps - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->do_empty));
           p_g = gi;
           p_it = it;
           p_first = n == 0;
@@ -762,8 +765,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       if (ok && p_g >= 0) ok = issue_dq();
       if (!ok) fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue

@@ -103,6 +103,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
   }
 }
 
+// Warp-collective form: every lane of a converged warp polls, and the warp
+// leaves together with one result.
+__device__ __forceinline__ bool mbar_wait_all(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                              uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
+}
+
 // ----------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -224,6 +231,45 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// Forms issued by one elected lane of a converged warp: the whole warp runs
+// the issue loop, so that its descriptor and address arithmetic stays
+// warp-uniform, and one lane issues the instruction.
+__device__ __forceinline__ void mma_bf16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e, p;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e, p;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar)
+      : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
