@@ -184,7 +184,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_e4m3_f32(128, 128);
       constexpr uint32_t idesc_o = ptx::idesc_e4m3_f32(128, kHD);
       const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
@@ -197,29 +199,29 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
         const uint64_t aq = ptx::desc_advance(dQ, x * Cfg::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kHD / 32; ++kk)
-          ptx::mma_e4m3_ss(tmem + tmem_s(x), ptx::desc_advance(aq, kk * 32), ptx::desc_advance(bk, kk * 32), idesc_s,
+          ptx::mma_e4m3_ss_w(tmem + tmem_s(x), ptx::desc_advance(aq, kk * 32), ptx::desc_advance(bk, kk * 32), idesc_s,
                            kk > 0 ? 1u : 0u);
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[x]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full[x]));
       };
       // O_x += P8_x(g) V8_g with P from TMEM (four e4m3 per column).
       auto issue_pv = [&](int x, int gk, bool first) {
         const uint64_t bv = ptx::desc_advance(dV, (gk % 2) * Cfg::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 128 / 32; ++kk)
-          ptx::mma_e4m3_ts(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, ptx::desc_advance(bv, kk * 32), idesc_o,
+          ptx::mma_e4m3_ts_w(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, ptx::desc_advance(bv, kk * 32), idesc_o,
                            (!first || kk > 0) ? 1u : 0u);
       };
       int g0 = 0;   // global index of the item's first key tile
       for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake(it, w0, dw)) {
         const Fp8Item item = fp8_item(w, g);
         const int n_kv = item.qt + 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs) &&
-             ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[g0 % 2]), (g0 >> 1) & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs) &&
+             ptx::mbar_wait_all(ptx::smem_u32(&bars->kv_full[g0 % 2]), (g0 >> 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_s(0, g0);
         issue_s(1, g0);
-        if (n_kv == 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+        if (n_kv == 1) ptx::mma_commit_w(ptx::smem_u32(&bars->q_empty));
         for (int j = 0; j < n_kv && ok; ++j) {
           const int gk = g0 + j;
 #pragma unroll
@@ -228,23 +230,23 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
             // first PV overwrites O_x, which the previous item's epilogue
             // must have read.
             // (V_j landed with K_j, checked before the score MMAs.)
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full[x]), gk & 1, abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full[x]), gk & 1, abort_flag, kWaitLimitNs);
             if (ok && j == 0 && it >= 1)
-              ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_free[x]), (it - 1) & 1, abort_flag, kWaitLimitNs);
+              ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->o_free[x]), (it - 1) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv(x, gk, j == 0);
-            if (x == 1) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[gk % 2]));   // last reader of K_j, V_j
-            if (j == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->o_done[x]));
+            if (x == 1) ptx::mma_commit_w(ptx::smem_u32(&bars->kv_empty[gk % 2]));   // last reader of K_j, V_j
+            if (j == n_kv - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->o_done[x]));
             // S_x(j+1) after PV_x(j): it overwrites P_x(j).
             if (j + 1 < n_kv) {
               if (x == 0 &&
-                  !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full[(gk + 1) % 2]), ((gk + 1) >> 1) & 1,
+                  !(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->kv_full[(gk + 1) % 2]), ((gk + 1) >> 1) & 1,
                                         abort_flag, kWaitLimitNs)))
                 break;
               ptx::tc_fence_after();
               issue_s(x, gk + 1);
-              if (x == 1 && j + 1 == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+              if (x == 1 && j + 1 == n_kv - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->q_empty));
             }
           }
         }
@@ -252,8 +254,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant_
       }
       if (!ok) fail();
       // Drain: every MMA this thread issued has finished before TMEM is freed.
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue

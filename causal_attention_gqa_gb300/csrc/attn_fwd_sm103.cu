@@ -372,7 +372,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ score-MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kBM, kBN, false, false);
       const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
@@ -381,7 +383,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
       for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake_item(it, w0, dw)) {
         const FwdItem item = fwd_item(w, g);
         const int n_kv = item.qt + 1, qb = it & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(ROPE ? &bars->q_ready[qb] : &bars->q_full[qb]), (it >> 1) & 1, abort_flag,
+        ok = ptx::mbar_wait_all(ptx::smem_u32(ROPE ? &bars->q_ready[qb] : &bars->q_full[qb]), (it >> 1) & 1, abort_flag,
                             kWaitLimitNs);
         for (int j = 0; j < n_kv && ok; ++j, ++gi) {
           const int s = gi % NK, sb = gi & 1;
@@ -389,8 +391,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
           const uint32_t fb = ptx::smem_u32(&bars->s_free[sb]);
           // K_j landed (and rotated); score buffer sb read out by the softmax of tile gi-2.
           if (!(ptx::mbar_ready(kb, (gi / NK) & 1) & (gi < 2 ? 1u : ptx::mbar_ready(fb, ((gi >> 1) - 1) & 1)))) {
-            ok = ptx::mbar_wait(kb, (gi / NK) & 1, abort_flag, kWaitLimitNs);
-            if (ok && gi >= 2) ok = ptx::mbar_wait(fb, ((gi >> 1) - 1) & 1, abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait_all(kb, (gi / NK) & 1, abort_flag, kWaitLimitNs);
+            if (ok && gi >= 2) ok = ptx::mbar_wait_all(fb, ((gi >> 1) - 1) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
           }
           ptx::tc_fence_after();
@@ -400,21 +402,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kAtomBytes + (kk & 3) * 32;
-            ptx::mma_bf16_ss(d_s, ptx::desc_advance(aq, off), ptx::desc_advance(bk, off), idesc_s, kk > 0 ? 1u : 0u);
+            ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(aq, off), ptx::desc_advance(bk, off), idesc_s, kk > 0 ? 1u : 0u);
           }
-          ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
-          ptx::mma_commit(ptx::smem_u32(&bars->k_empty[s]));
-          if (j == n_kv - 1) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qb]));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->s_full[sb]));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->k_empty[s]));
+          if (j == n_kv - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->q_empty[qb]));
         }
       }
       if (!ok) fail();
       // Drain: every MMA this thread issued has finished before TMEM is freed.
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV-MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kBM, HD, false, true);
       const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), Cfg::kAtomBytes, 1024);
       bool ok = true;
@@ -425,13 +429,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
         // The first PV of an item overwrites its O buffer: the epilogue of the
         // item that last used it must have read it out.
         if (it >= NO)
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->o_free[ob]), (((it - NO) / NO)) & 1, abort_flag, kWaitLimitNs);
+          ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->o_free[ob]), (((it - NO) / NO)) & 1, abort_flag, kWaitLimitNs);
         for (int j = 0; j < n_kv && ok; ++j, ++gi) {
           const int pb = gi & 1, sp = gi % NV;
           const uint32_t pf = ptx::smem_u32(&bars->p_full[pb]), vf = ptx::smem_u32(&bars->v_full[sp]);
           if (!(ptx::mbar_ready(pf, (gi >> 1) & 1) & ptx::mbar_ready(vf, (gi / NV) & 1))) {
-            ok = ptx::mbar_wait(pf, (gi >> 1) & 1, abort_flag, kWaitLimitNs);
-            if (ok) ok = ptx::mbar_wait(vf, (gi / NV) & 1, abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait_all(pf, (gi >> 1) & 1, abort_flag, kWaitLimitNs);
+            if (ok) ok = ptx::mbar_wait_all(vf, (gi / NV) & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
           }
           ptx::tc_fence_after();
@@ -440,14 +444,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CU
           const uint32_t a_p = tmem + (pb ? Cfg::kTmemP1 : Cfg::kTmemP0);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            ptx::mma_bf16_ts(d_o, a_p + kk * 8, ptx::desc_advance(bv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_u32(&bars->pv_done[pb]));
-          ptx::mma_commit(ptx::smem_u32(&bars->v_empty[sp]));
+            ptx::mma_bf16_ts_w(d_o, a_p + kk * 8, ptx::desc_advance(bv, kk * 2048), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit_w(ptx::smem_u32(&bars->pv_done[pb]));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[sp]));
         }
       }
       if (!ok) fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain2));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain2), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain2));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain2), 0, nullptr, kWaitLimitNs);
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ------------------------------------------------------------ softmax + epilogue

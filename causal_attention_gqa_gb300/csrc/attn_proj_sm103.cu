@@ -127,7 +127,9 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, false, false);
       const uint64_t d0 = ptx::sw128_desc(ptx::smem_u32(smem), 16, 1024);
       bool ok = true;
@@ -136,35 +138,36 @@ proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int buf = lt & 1;
         // The accumulator's previous tile (two back) has been read out.
         if (lt >= 2 &&
-            !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[buf]), ((lt >> 1) - 1) & 1, abort_flag,
+            !(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->acc_empty[buf]), ((lt >> 1) - 1) & 1, abort_flag,
                                   kWaitLimitNs)))
           break;
         ptx::tc_fence_after();
         // Each stage's barrier is checked (non-blocking) one k-block ahead.
-        uint32_t ready = ptx::mbar_test(ptx::smem_u32(&bars->full[it % kStages]), (it / kStages) & 1);
+        uint32_t ready =
+            __all_sync(0xffffffffu, ptx::mbar_test(ptx::smem_u32(&bars->full[it % kStages]), (it / kStages) & 1) != 0);
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int st = it % kStages, u = it / kStages;
-          if (!ready && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full[st]), u & 1, abort_flag, kWaitLimitNs)))
+          if (!ready && !(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->full[st]), u & 1, abort_flag, kWaitLimitNs)))
             break;
           ptx::tc_fence_after();
-          ready = (kb + 1 < n_kb) ? ptx::mbar_test(ptx::smem_u32(&bars->full[(it + 1) % kStages]),
-                                                   ((it + 1) / kStages) & 1)
+          ready = (kb + 1 < n_kb) ? __all_sync(0xffffffffu, ptx::mbar_test(ptx::smem_u32(&bars->full[(it + 1) % kStages]),
+                                                                            ((it + 1) / kStages) & 1) != 0)
                                   : 1u;
           const uint64_t da = ptx::desc_advance(d0, st * kStageBytes);
           const uint64_t db = ptx::desc_advance(d0, st * kStageBytes + kATile);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            ptx::mma_bf16_ss(tmem + buf * kBN, ptx::desc_advance(da, (kk >> 2) * kAAtom + (kk & 3) * 32),
+            ptx::mma_bf16_ss_w(tmem + buf * kBN, ptx::desc_advance(da, (kk >> 2) * kAAtom + (kk & 3) * 32),
                              ptx::desc_advance(db, (kk >> 2) * kBAtom + (kk & 3) * 32), idesc,
                              (kb > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_u32(&bars->empty[st]));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->empty[st]));
         }
         if (!ok) break;
-        ptx::mma_commit(ptx::smem_u32(&bars->acc_full[buf]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->acc_full[buf]));
       }
       if (!ok) fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ epilogue

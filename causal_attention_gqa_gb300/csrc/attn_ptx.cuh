@@ -387,6 +387,34 @@ __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The e4m3 forms issued by one elected lane of a converged warp (see
+// mma_bf16_ss_w).
+__device__ __forceinline__ void mma_e4m3_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e, p;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_e4m3_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e, p;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Two floats to two e4m3 bytes (round to nearest even, saturating at +-448):
 // `lo` in bits 0..7, `hi` in bits 8..15.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {

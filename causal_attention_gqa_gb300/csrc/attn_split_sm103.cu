@@ -318,7 +318,9 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, kHD, false, true);
       constexpr uint32_t idesc_o2 = ptx::idesc_bf16_f32(128, 2 * kHD, false, true);
@@ -328,7 +330,7 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
       // signalled p_full(j-2), which this thread waited for before PV(j-2)).
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
+        if (!ptx::mbar_wait_all(ptx::smem_u32(&bars->k_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
         const uint64_t dKh = ptx::sw128_desc(ptx::smem_u32(sK + 2 * st * kTile), 16, 1024);
         const uint64_t dKl = ptx::sw128_desc(ptx::smem_u32(sK + (2 * st + 1) * kTile), 16, 1024);
@@ -336,38 +338,38 @@ split_fwd_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constan
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(dKh, off), idesc_s, kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(dKl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQl, off), ptx::desc_advance(dKh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(dKh, off), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(dKl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dQl, off), ptx::desc_advance(dKh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
-        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[st]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full[st]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->k_empty[st]));
         return true;
       };
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
+      bool ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->q_full), 0, abort_flag, kWaitLimitNs);
       if (ok) ok = issue_s(0);
       if (ok && qt >= 1) ok = issue_s(1);
       for (int j = 0; j <= qt && ok; ++j) {
         const int st = j & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), j & 1, abort_flag, kWaitLimitNs);
-        if (ok) ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full), j & 1, abort_flag, kWaitLimitNs);
+        if (ok) ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->v_full[st]), (j >> 1) & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         // B: [Vh | Vl] MN-major, the two 64-column atoms kTile apart.
         const uint64_t dV2 = ptx::sw128_desc(ptx::smem_u32(sV + 2 * st * kTile), kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPh + kk * 8, ptx::desc_advance(dV2, kk * 2048), idesc_o2,
+          ptx::mma_bf16_ts_w(tmem + kFO, tmem + kFPh + kk * 8, ptx::desc_advance(dV2, kk * 2048), idesc_o2,
                            (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kFO, tmem + kFPl + kk * 8, ptx::desc_advance(dV2, kk * 2048), idesc_o, 1u);
+          ptx::mma_bf16_ts_w(tmem + kFO, tmem + kFPl + kk * 8, ptx::desc_advance(dV2, kk * 2048), idesc_o, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->pv_done));
-        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[st]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->pv_done));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[st]));
         if (j + 2 <= qt) ok = issue_s(j + 2);
       }
       if (!ok) fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -659,7 +661,9 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, kHD, false, true);
       constexpr uint32_t idesc_g2 = ptx::idesc_bf16_f32(128, 2 * kHD, false, true);
@@ -670,7 +674,7 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
       // S^T(n) = K Q(n)^T over P^T(n-1), read by dV(n-1) issued before.
       auto issue_s = [&](int n) -> bool {
         const int st = n & 1;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full[st]), (n >> 1) & 1, abort_flag, kWaitLimitNs))
+        if (!ptx::mbar_wait_all(ptx::smem_u32(&bars->qdo_full[st]), (n >> 1) & 1, abort_flag, kWaitLimitNs))
           return false;
         ptx::tc_fence_after();
         const uint32_t aQh = ptx::smem_u32(sRing + st * kDkvStage);
@@ -679,14 +683,14 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dKh, off), ptx::desc_advance(kQh, off), idesc_s, kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dKh, off), ptx::desc_advance(kQl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dKl, off), ptx::desc_advance(kQh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dKh, off), ptx::desc_advance(kQh, off), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dKh, off), ptx::desc_advance(kQl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dKl, off), ptx::desc_advance(kQh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[st]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full[st]));
         return true;
       };
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
+      bool ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->kv_full), 0, abort_flag, kWaitLimitNs);
       if (ok && n_steps > 0) ok = issue_s(0);
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n & 1;
@@ -697,14 +701,14 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(tmem + kBDP, ptx::desc_advance(dVh, off), ptx::desc_advance(kDh, off), idesc_s,
+          ptx::mma_bf16_ss_w(tmem + kBDP, ptx::desc_advance(dVh, off), ptx::desc_advance(kDh, off), idesc_s,
                            kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(tmem + kBDP, ptx::desc_advance(dVh, off), ptx::desc_advance(kDl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(tmem + kBDP, ptx::desc_advance(dVl, off), ptx::desc_advance(kDh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(tmem + kBDP, ptx::desc_advance(dVh, off), ptx::desc_advance(kDl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(tmem + kBDP, ptx::desc_advance(dVl, off), ptx::desc_advance(kDh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
         // dV += P^T dO (B: [dOh | dOl] MN-major, 16 queries per K step).
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t mD2 = ptx::sw128_desc(aDh, kTile, 1024);
@@ -712,28 +716,28 @@ split_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_co
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t ph = t_p + hi_col(kk), pl = ph + 32;
-          ptx::mma_bf16_ts(tmem + kBDV, ph, ptx::desc_advance(mD2, kk * 2048), idesc_g2, (n > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kBDV, pl, ptx::desc_advance(mD2, kk * 2048), idesc_g, 1u);
+          ptx::mma_bf16_ts_w(tmem + kBDV, ph, ptx::desc_advance(mD2, kk * 2048), idesc_g2, (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts_w(tmem + kBDV, pl, ptx::desc_advance(mD2, kk * 2048), idesc_g, 1u);
         }
         // The next step's scores, over P^T(n) (dV(n) above read it).
         if (n + 1 < n_steps && !(ok = issue_s(n + 1))) break;
         // dK += dS^T Q (B: [Qh | Ql] MN-major).
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), n & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->ds_full), n & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint64_t mQ2 = ptx::sw128_desc(aQh, kTile, 1024);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t dh = tmem + kBDP + hi_col(kk), dl = dh + 32;
-          ptx::mma_bf16_ts(tmem + kBDK, dh, ptx::desc_advance(mQ2, kk * 2048), idesc_g2, (n > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kBDK, dl, ptx::desc_advance(mQ2, kk * 2048), idesc_g, 1u);
+          ptx::mma_bf16_ts_w(tmem + kBDK, dh, ptx::desc_advance(mQ2, kk * 2048), idesc_g2, (n > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts_w(tmem + kBDK, dl, ptx::desc_advance(mQ2, kk * 2048), idesc_g, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->qdo_empty[st]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->qdo_empty[st]));
       }
-      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (ok) ptx::mma_commit_w(ptx::smem_u32(&bars->acc_done));
       else fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
@@ -915,7 +919,9 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp runs the issue loop; one elected lane issues each MMA
+    // and commit, and every wait is warp-collective)
+    {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_g = ptx::idesc_bf16_f32(128, kHD, false, true);
       constexpr uint32_t idesc_g2 = ptx::idesc_bf16_f32(128, 2 * kHD, false, true);
@@ -927,7 +933,7 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
       // S(j-2) before they signalled ds_full(j-2), waited for before dQ(j-2)).
       auto issue_s = [&](int jj) -> bool {
         const int ks = jj % 3;
-        if (!ptx::mbar_wait(ptx::smem_u32(&bars->k_full[ks]), (jj / 3) & 1, abort_flag, kWaitLimitNs)) return false;
+        if (!ptx::mbar_wait_all(ptx::smem_u32(&bars->k_full[ks]), (jj / 3) & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
         const uint32_t aKh = ptx::smem_u32(sK + 2 * ks * kTile);
         const uint64_t kKh = ptx::sw128_desc(aKh, 16, 1024), kKl = ptx::sw128_desc(aKh + kTile, 16, 1024);
@@ -935,19 +941,19 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(kKh, off), idesc_s, kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(kKl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(d_s, ptx::desc_advance(dQl, off), ptx::desc_advance(kKh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(kKh, off), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dQh, off), ptx::desc_advance(kKl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(d_s, ptx::desc_advance(dQl, off), ptx::desc_advance(kKh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->s_full[jj & 1]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full[jj & 1]));
         return true;
       };
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->qdo_full), 0, abort_flag, kWaitLimitNs);
+      bool ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->qdo_full), 0, abort_flag, kWaitLimitNs);
       if (ok) ok = issue_s(0);
       for (int jj = 0; jj <= qt && ok; ++jj) {
         const int ks = jj % 3, vs = jj & 1;
         // dP = dO V^T (over dS(j-1), read by dQ(j-1) issued before).
-        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_full[vs]), (jj >> 1) & 1, abort_flag, kWaitLimitNs)))
+        if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->v_full[vs]), (jj >> 1) & 1, abort_flag, kWaitLimitNs)))
           break;
         ptx::tc_fence_after();
         const uint32_t aVh = ptx::smem_u32(sV + 2 * vs * kTile);
@@ -955,18 +961,18 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = kk * 32;
-          ptx::mma_bf16_ss(tmem + kQDP, ptx::desc_advance(dDh, off), ptx::desc_advance(kVh, off), idesc_s,
+          ptx::mma_bf16_ss_w(tmem + kQDP, ptx::desc_advance(dDh, off), ptx::desc_advance(kVh, off), idesc_s,
                            kk > 0 ? 1u : 0u);
-          ptx::mma_bf16_ss(tmem + kQDP, ptx::desc_advance(dDh, off), ptx::desc_advance(kVl, off), idesc_s, 1u);
-          ptx::mma_bf16_ss(tmem + kQDP, ptx::desc_advance(dDl, off), ptx::desc_advance(kVh, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(tmem + kQDP, ptx::desc_advance(dDh, off), ptx::desc_advance(kVl, off), idesc_s, 1u);
+          ptx::mma_bf16_ss_w(tmem + kQDP, ptx::desc_advance(dDl, off), ptx::desc_advance(kVh, off), idesc_s, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->dp_full));
-        ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[vs]));
         // The next tile's scores, into the other S buffer.
         if (jj + 1 <= qt && !(ok = issue_s(jj + 1))) break;
         // dQ += dS K (B: [Kh | Kl] MN-major, the two 64-column atoms kTile
         // apart; 16 keys per K step).
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->ds_full), jj & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->ds_full), jj & 1, abort_flag, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t aKh = ptx::smem_u32(sK + 2 * ks * kTile);
@@ -974,16 +980,16 @@ split_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
           const uint32_t dh = tmem + kQDP + hi_col(kk), dl = dh + 32;
-          ptx::mma_bf16_ts(tmem + kQDQ, dh, ptx::desc_advance(mK2, kk * 2048), idesc_g2,
+          ptx::mma_bf16_ts_w(tmem + kQDQ, dh, ptx::desc_advance(mK2, kk * 2048), idesc_g2,
                            (jj > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_bf16_ts(tmem + kQDQ, dl, ptx::desc_advance(mK2, kk * 2048), idesc_g, 1u);
+          ptx::mma_bf16_ts_w(tmem + kQDQ, dl, ptx::desc_advance(mK2, kk * 2048), idesc_g, 1u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->k_empty[ks]));
       }
-      if (ok) ptx::mma_commit(ptx::smem_u32(&bars->acc_done));
+      if (ok) ptx::mma_commit_w(ptx::smem_u32(&bars->acc_done));
       else fail();
-      ptx::mma_commit(ptx::smem_u32(&bars->drain));
-      ptx::mbar_wait(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
+      ptx::mma_commit_w(ptx::smem_u32(&bars->drain));
+      ptx::mbar_wait_all(ptx::smem_u32(&bars->drain), 0, nullptr, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
