@@ -7,6 +7,7 @@ into one shared library next to this file.  The C ABI is declared in
 from __future__ import annotations
 
 import concurrent.futures
+import fcntl
 import glob
 import os
 import shutil
@@ -49,11 +50,25 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the path of the shared library."""
+    """Compile (if needed) and return the path of the shared library.
+
+    Concurrent callers (parallel test workers) serialise on a lock file in
+    the build folder: one compiles, the others then find the library fresh."""
     if not force and not _stale():
         return LIB_PATH
-    nvcc = nvcc_path()
     os.makedirs(BUILD_DIR, exist_ok=True)
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not _stale():
+                return LIB_PATH
+            return _build_locked(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool) -> str:
+    nvcc = nvcc_path()
     srcs = _sources()
 
     def compile_one(src):
