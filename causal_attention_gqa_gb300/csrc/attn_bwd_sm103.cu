@@ -488,13 +488,17 @@ struct DqCfg {
   static constexpr int kQTile = kQ * HD * 2;           // Q_i, dO_i or the staged dQ tile
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kAtom = 128 * 128;              // one 64-column atom column of a 128-row tile
-  static constexpr int kKStages = (HD == 128) ? 2 : 4; // K ring and V ring depth
+  // K(t) is read by S(t) and by dQ(t), which is issued a step later, so its
+  // ring needs a stage more than V's (read by dP(t) only) to keep each load
+  // a step ahead of its use.
+  static constexpr int kKStages = (HD == 128) ? 3 : 4; // K ring depth
+  static constexpr int kVStages = (HD == 128) ? 1 : 4; // V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kQOff + kQTile;
   static constexpr int kStOff = kDOOff + kQTile;       // dQ staging tile (TMA store source)
   static constexpr int kKOff = kStOff + kQTile;
   static constexpr int kVOff = kKOff + kKStages * kKTile;
-  static constexpr int kBarOff = kVOff + kKStages * kKTile;
+  static constexpr int kBarOff = kVOff + kVStages * kKTile;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 256, kTmemCols = 512;
   static constexpr int kItemSlots = 4;                 // claimed-item queue depth
@@ -533,7 +537,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const __grid_constant__ CUtensorMap tm_dqkv, const float* __restrict__ LD,
               int* __restrict__ item_counter, int n_items, int* __restrict__ status, Geometry g) {
   using Cfg = DqCfg<HD>;
-  constexpr int NKS = Cfg::kKStages, NIS = Cfg::kItemSlots;
+  constexpr int NKS = Cfg::kKStages, NVS = Cfg::kVStages, NIS = Cfg::kItemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
@@ -554,6 +558,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; i < NKS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->k_empty[i]), 1);
+    }
+    for (int i = 0; i < NVS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->v_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->v_empty[i]), 1);
     }
@@ -654,14 +660,15 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                item.b, df);
             do_loaded = true;
           }
-          if (u > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[st]), (u - 1) & 1, abort_flag,
-                                             kWaitLimitNs)))
+          const int vs = gi % NVS, vu = gi / NVS;
+          if (vu > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), (vu - 1) & 1, abort_flag,
+                                              kWaitLimitNs)))
             break;
-          const uint32_t vf = ptx::smem_u32(&bars->v_full[st]);
+          const uint32_t vf = ptx::smem_u32(&bars->v_full[vs]);
           ptx::mbar_arrive_expect_tx(vf, Cfg::kKTile);
 #pragma unroll
           for (int a = 0; a < HD / 64; ++a)
-            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kKTile + a * Cfg::kAtom), &tm_v,
+            ptx::tma_load_3d(ptx::smem_u32(sV + vs * Cfg::kKTile + a * Cfg::kAtom), &tm_v,
                              g.C + g.NKV * HD + kh * HD + 64 * a, n * 128, item.b, vf);
           v_issued = gi + 1;
         }
@@ -676,8 +683,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         for (int st = 0; st < NKS && st < k_issued; ++st)
           ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
-        for (int st = 0; st < NKS && st < v_issued; ++st)
-          ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
+        for (int st = 0; st < NVS && st < v_issued; ++st)
+          ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / NVS) & 1, nullptr, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -725,13 +732,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int n_steps = item.qt + 1;
         ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs);
         for (int n = 0; n < n_steps && ok; ++n) {
-          const int gi = gs + n, ks = gi % NKS, u = gi / NKS;
+          const int gi = gs + n, ks = gi % NKS, u = gi / NKS, vs = gi % NVS, vu = gi / NVS;
           // K landed; the groups have read the previous S out of TMEM.
           ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->k_full[ks]), u & 1, abort_flag, kWaitLimitNs);
           if (ok && gi > 0) ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->s_free), (gi - 1) & 1, abort_flag, kWaitLimitNs);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, ks * Cfg::kKTile);
+          const uint64_t bk = ptx::desc_advance(dK, ks * Cfg::kKTile), bv = ptx::desc_advance(dV, vs * Cfg::kKTile);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
@@ -745,7 +752,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (p_g >= 0 && !(ok = issue_dq())) break;
           if (n == 0 && !(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->do_full), it & 1, abort_flag, kWaitLimitNs)))
             break;
-          if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->v_full[ks]), u & 1, abort_flag, kWaitLimitNs))) break;
+          if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->v_full[vs]), vu & 1, abort_flag, kWaitLimitNs))) break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
@@ -754,7 +761,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                              kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
-          ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[ks]));
+          ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[vs]));
           if (n == n_steps - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->do_empty));
           p_g = gi;
           p_it = it;
