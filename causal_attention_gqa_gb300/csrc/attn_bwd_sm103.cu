@@ -142,7 +142,7 @@ struct DkdvCfg {
 struct DkdvBarriers {
   uint64_t kv_full, acc_done, drain, staged;
   uint64_t qdo_full[4], qdo_empty[4];
-  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t s_full, dp_full, p_full[2], ds_full;
   uint32_t tmem_base;
   int abort;
 };
@@ -191,7 +191,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->p_full), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->p_full[0]), 8);
+    ptx::mbar_init(ptx::smem_u32(&bars->p_full[1]), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -316,14 +317,21 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
         ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
         // dV += P^T dO once both groups wrote P^T.
-        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full), n & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
-        ptx::tc_fence_after();
+        // P^T arrives in halves: queries 0-31 and 64-95 (K steps 0, 1, 4,
+        // 5), then 32-63 and 96-127, so dV starts before it is complete.
         const uint64_t gdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile);
 #pragma unroll
-        for (int kk = 0; kk < Cfg::kQ / 16; ++kk)
-          ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk), ptx::desc_advance(gdo, kk * 2048),
-                           idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full[hh]), n & 1, abort_flag, kWaitLimitNs))) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kk = (i >> 1) * 4 + hh * 2 + (i & 1);
+            ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk),
+                               ptx::desc_advance(gdo, kk * 2048), idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
       }
       if (ok && n_steps > 0) ok = issue_dk(n_steps - 1);
       if (ok) ptx::mma_commit_w(ptx::smem_u32(&bars->acc_done));
@@ -387,11 +395,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           pw[(c >> 1) + 1] = pack_bf16x2(e[2], e[3]);
         }
         ptx::tmem_st16(t_s + 16 * half, pw);
+        // Each half of this group's queries is signalled once it is in TMEM.
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[half]));
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full));
       // ---- dS^T = P^T * (dP^T - D), while dV is accumulated.
       Lw[0] = d4[0];
       Lw[1] = d4[1];
