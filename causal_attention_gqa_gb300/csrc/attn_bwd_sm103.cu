@@ -37,7 +37,7 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kThreadsDkdv = 320;   // producer, MMA issuer, two elementwise warpgroups
-constexpr int kThreadsDq = 320;     // producer, MMA issuer, two elementwise warpgroups
+constexpr int kThreadsDq = 352;     // producer, MMA issuer, two elementwise warpgroups, Q producer
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint4 pack8(const uint32_t* f, float s) {
@@ -482,9 +482,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // the workspace that the prologue clears: CTAs that become resident early
 // (the kernel starts while the dK/dV kernel drains) take more items.  Per
 // item, Q_i and dO_i stay in shared memory and the CTA walks the 128-key
-// tiles 0..i (every MMA N = 128).  The next item's Q and dO are loaded as
-// soon as the current item's last score MMAs have read them, and its first
-// MMAs overlap the current item's epilogue.
+// tiles 0..i (every MMA N = 128).  A Q producer warp loads the next item's Q
+// into the other of two Q buffers while the current item runs (an item's dQ
+// tile is staged in its own Q buffer for the TMA store); its dO follows as
+// soon as the current item's last dP MMA has read the one dO buffer, and its
+// first MMAs overlap the current item's epilogue.
 // TMEM: S [0, 128), dP [128, 256), two dQ accumulators from 256 (items
 // alternate).  The elementwise groups turn S into P (kept in registers) while
 // dP is computed, then dP into dS, written (bf16 pairs) into TMEM over the dP
@@ -494,7 +496,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 template <int HD>
 struct DqCfg {
   static constexpr int kQ = 128, kKeys = 128;
-  static constexpr int kQTile = kQ * HD * 2;           // Q_i, dO_i or the staged dQ tile
+  static constexpr int kQTile = kQ * HD * 2;           // Q_i, dO_i or a staged dQ tile
   static constexpr int kKTile = kKeys * HD * 2;        // K_j or V_j
   static constexpr int kAtom = 128 * 128;              // one 64-column atom column of a 128-row tile
   // K(t) is read by S(t) and by dQ(t), which is issued a step later, so its
@@ -502,10 +504,11 @@ struct DqCfg {
   // a step ahead of its use.
   static constexpr int kKStages = (HD == 128) ? 3 : 4; // K ring depth
   static constexpr int kVStages = (HD == 128) ? 1 : 4; // V ring depth
+  // Two Q buffers (items alternate; an item's dQ tile is staged for its TMA
+  // store in the item's own Q buffer once its last score MMA has read it).
   static constexpr int kQOff = 0;
-  static constexpr int kDOOff = kQOff + kQTile;
-  static constexpr int kStOff = kDOOff + kQTile;       // dQ staging tile (TMA store source)
-  static constexpr int kKOff = kStOff + kQTile;
+  static constexpr int kDOOff = kQOff + 2 * kQTile;
+  static constexpr int kKOff = kDOOff + kQTile;
   static constexpr int kVOff = kKOff + kKStages * kKTile;
   static constexpr int kBarOff = kVOff + kVStages * kKTile;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;
@@ -515,10 +518,10 @@ struct DqCfg {
 };
 
 struct DqBarriers {
-  uint64_t q_full, q_empty, do_full, do_empty, drain;
+  uint64_t q_full[2], do_full, do_empty, drain;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, ds_full;
-  uint64_t acc_done[2], dq_free[2], staged, stage_free;
+  uint64_t acc_done[2], dq_free[2], staged, stage_free[2];
   uint64_t item_full[4], item_empty[4];
   int item[4];
   uint32_t tmem_base;
@@ -551,7 +554,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
   uint8_t* sDO = smem + Cfg::kDOOff;
-  uint8_t* sSt = smem + Cfg::kStOff;
   uint8_t* sK = smem + Cfg::kKOff;
   uint8_t* sV = smem + Cfg::kVOff;
   DqBarriers* bars = reinterpret_cast<DqBarriers*>(smem + Cfg::kBarOff);
@@ -559,8 +561,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->q_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->q_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->do_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->do_empty), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
@@ -581,10 +583,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ptx::mbar_init(ptx::smem_u32(&bars->dq_free[i]), 8);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->staged), 8);
-    ptx::mbar_init(ptx::smem_u32(&bars->stage_free), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->stage_free[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->stage_free[1]), 1);
     for (int i = 0; i < NIS; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars->item_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->item_empty[i]), 9);   // MMA issuer + 8 elementwise warps
+      ptx::mbar_init(ptx::smem_u32(&bars->item_empty[i]), 10);  // MMA issuer, 8 elementwise warps, Q producer
     }
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -619,7 +622,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int k_issued = 0, v_issued = 0, q_issued = 0;  // global sequence counters
+      int k_issued = 0, v_issued = 0, do_issued = 0;  // global sequence counters
       int gs = 0;                                    // global index of the item's first key step
       bool ok = true;
       for (int it = 0; ok; ++it) {
@@ -635,15 +638,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (w < 0) break;
         const DqItem item = dq_item(w, g);
         const int kh = item.h / g.grp, n_steps = item.qt + 1;
-        // Q and dO of this item once the previous item's last score MMAs read them.
-        if (it > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty), (it - 1) & 1, abort_flag, kWaitLimitNs)))
-          break;
-        const uint32_t qf = ptx::smem_u32(&bars->q_full);
-        ptx::mbar_arrive_expect_tx(qf, Cfg::kQTile);
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          ptx::tma_load_3d(ptx::smem_u32(sQ + a * Cfg::kAtom), &tm_q, item.h * HD + 64 * a, item.qt * 128, item.b, qf);
-        q_issued = it + 1;
+        // K, V and dO of this item (Q comes from the Q producer warp); dO once
+        // the previous item's last dP MMA has read it.
         bool do_loaded = false;
         for (int n = 0; n < n_steps && ok; ++n) {
           const int gi = gs + n, st = gi % NKS, u = gi / NKS;
@@ -668,6 +664,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               ptx::tma_load_3d(ptx::smem_u32(sDO + a * Cfg::kAtom), &tm_do, item.h * HD + 64 * a, item.qt * 128,
                                item.b, df);
             do_loaded = true;
+            do_issued = it + 1;
           }
           const int vs = gi % NVS, vu = gi / NVS;
           if (vu > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), (vu - 1) & 1, abort_flag,
@@ -686,15 +683,43 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!ok) fail();
       if (*abort_flag) {
         // Let every copy already in flight land before shared memory is released.
-        if (q_issued > 0) {
-          ptx::mbar_wait(ptx::smem_u32(&bars->q_full), (q_issued - 1) & 1, nullptr, kWaitLimitNs);
-          ptx::mbar_wait(ptx::smem_u32(&bars->do_full), (q_issued - 1) & 1, nullptr, kWaitLimitNs);
-        }
+        if (do_issued > 0)
+          ptx::mbar_wait(ptx::smem_u32(&bars->do_full), (do_issued - 1) & 1, nullptr, kWaitLimitNs);
         for (int st = 0; st < NKS && st < k_issued; ++st)
           ptx::mbar_wait(ptx::smem_u32(&bars->k_full[st]), ((k_issued - 1 - st) / NKS) & 1, nullptr, kWaitLimitNs);
         for (int st = 0; st < NVS && st < v_issued; ++st)
           ptx::mbar_wait(ptx::smem_u32(&bars->v_full[st]), ((v_issued - 1 - st) / NVS) & 1, nullptr, kWaitLimitNs);
       }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ Q producer
+    // Q of item it into buffer it & 1 as soon as the TMA store of item it-2's
+    // dQ tile, staged there, has read it (which also means item it-2's score
+    // MMAs have completed): the next item's Q lands while this one runs.
+    if (lane == 0) {
+      int q_issued = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int w = next_item(it, &ok);
+        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[it % NIS]));
+        if (!ok || w < 0) break;
+        const DqItem item = dq_item(w, g);
+        const int qb = it & 1;
+        if (it >= 2 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->stage_free[qb]), ((it >> 1) - 1) & 1, abort_flag,
+                                             kWaitLimitNs)))
+          break;
+        const uint32_t qf = ptx::smem_u32(&bars->q_full[qb]);
+        ptx::mbar_arrive_expect_tx(qf, Cfg::kQTile);
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a)
+          ptx::tma_load_3d(ptx::smem_u32(sQ + qb * Cfg::kQTile + a * Cfg::kAtom), &tm_q, item.h * HD + 64 * a,
+                           item.qt * 128, item.b, qf);
+        q_issued = it + 1;
+      }
+      if (!ok) fail();
+      // Let the Q loads already in flight land before shared memory is released.
+      for (int i = q_issued - 2 > 0 ? q_issued - 2 : 0; i < q_issued; ++i)
+        ptx::mbar_wait(ptx::smem_u32(&bars->q_full[i & 1]), (i >> 1) & 1, nullptr, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the whole warp
@@ -739,7 +764,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!ok || w < 0) break;
         const DqItem item = dq_item(w, g);
         const int n_steps = item.qt + 1;
-        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->q_full), it & 1, abort_flag, kWaitLimitNs);
+        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->q_full[it & 1]), (it >> 1) & 1, abort_flag, kWaitLimitNs);
+        const uint64_t dQb = ptx::desc_advance(dQ, (it & 1) * Cfg::kQTile);
         for (int n = 0; n < n_steps && ok; ++n) {
           const int gi = gs + n, ks = gi % NKS, u = gi / NKS, vs = gi % NVS, vu = gi / NVS;
           // K landed; the groups have read the previous S out of TMEM.
@@ -751,11 +777,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-            ptx::mma_bf16_ss_w(tmem + Cfg::kTmemS, ptx::desc_advance(dQ, off), ptx::desc_advance(bk, off), idesc_s,
+            ptx::mma_bf16_ss_w(tmem + Cfg::kTmemS, ptx::desc_advance(dQb, off), ptx::desc_advance(bk, off), idesc_s,
                              kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit_w(ptx::smem_u32(&bars->s_full));
-          if (n == n_steps - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->q_empty));
           // The previous step's dQ reads its dS in the dP columns: issued
           // before dP overwrites them (MMAs from one thread run in order).
           if (p_g >= 0 && !(ok = issue_dq())) break;
@@ -797,6 +822,55 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float2 sl2x2 = make_float2(sl2, sl2);
     const int Tp = row_table_rows(g.T);
     const int k0 = 64 * wg;                        // first key (within a tile) of this group
+    // Warp 2's store in flight (the Q buffer it reads, -1: none): released
+    // once the store has read it, at warp 2's next dS arrival or at the start
+    // of the next item, whichever comes first (never later: the Q producer
+    // waits for the release before loading the item after next).
+    int store_db = -1;
+    auto release_store = [&]() {
+      if (warp == 2 && lane == 0 && store_db >= 0) {
+        ptx::bulk_wait_read();
+        ptx::mbar_arrive(ptx::smem_u32(&bars->stage_free[store_db]));   // the Q producer may reload it
+        store_db = -1;
+      }
+    };
+    // dQ of a finished item: staged in the item's Q buffer (its last score
+    // MMA, which precedes its last dQ MMA, has read it) and written with TMA
+    // stores (rows past T are clipped).  It runs after the next item's first
+    // dS is out (the RoPE undo in it takes about as long as a step), so that
+    // the tensor core works on that item's first MMAs meanwhile.
+    auto epilogue = [&](int pit, const DqItem& pitem) -> bool {
+      const int db = pit & 1;
+      const int ptq = pitem.qt * 128 + row;
+      uint8_t* sSt = sQ + db * Cfg::kQTile;
+      if (!__all_sync(0xffffffffu,
+                      ptx::mbar_wait(ptx::smem_u32(&bars->acc_done[db]), (pit >> 1) & 1, abort_flag, kWaitLimitNs)))
+        return false;
+      ptx::tc_fence_after();
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ + 128 * db, g.scale, ROPE, ptq, g, sSt, row, wg, 2);
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free[db]));
+        ptx::mbar_arrive(ptx::smem_u32(&bars->staged));
+      }
+      bool sok = true;
+      if (warp == 2 && lane == 0) {
+        sok = ptx::mbar_wait(ptx::smem_u32(&bars->staged), pit & 1, abort_flag, kWaitLimitNs);
+        if (sok) {
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(sSt + a * Cfg::kAtom), pitem.h * HD + 64 * a, pitem.qt * 128,
+                              pitem.b);
+          ptx::bulk_commit();
+          store_db = db;                           // released by release_store()
+        }
+      }
+      return __shfl_sync(0xffffffffu, sok ? 1 : 0, 0) != 0;
+    };
+    int pend_it = -1;                              // finished item whose epilogue is due
+    DqItem pend_item{};
     bool ok = true;
     int gs = 0;
     for (int it = 0; ok; ++it) {
@@ -805,6 +879,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[it % NIS]));
       if (!ok || w < 0) break;
+      release_store();
       const DqItem item = dq_item(w, g);
       const int n_steps = item.qt + 1;
       const int tq = item.qt * 128 + row;
@@ -864,42 +939,18 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->ds_full));
+        release_store();
+        if (n == 0 && pend_it >= 0) {
+          if (!(ok = epilogue(pend_it, pend_item))) break;
+          pend_it = -1;
+        }
       }
       if (!ok) break;
       gs += n_steps;
-      // ---- Epilogue: dQ of this item, staged and written with TMA stores
-      // (rows past T are clipped) while the next item's MMAs start.
-      const int db = it & 1;
-      ok = __all_sync(0xffffffffu,
-                      ptx::mbar_wait(ptx::smem_u32(&bars->acc_done[db]), (it >> 1) & 1, abort_flag, kWaitLimitNs));
-      // The staging tile is free once the previous item's stores have read it.
-      if (ok && it > 0)
-        ok = __all_sync(0xffffffffu,
-                        ptx::mbar_wait(ptx::smem_u32(&bars->stage_free), (it - 1) & 1, abort_flag, kWaitLimitNs));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ + 128 * db, g.scale, ROPE, tq, g, sSt, row, wg, 2);
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(ptx::smem_u32(&bars->dq_free[db]));
-        ptx::mbar_arrive(ptx::smem_u32(&bars->staged));
-      }
-      if (warp == 2 && lane == 0) {
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->staged), it & 1, abort_flag, kWaitLimitNs);
-        if (ok) {
-#pragma unroll
-          for (int a = 0; a < HD / 64; ++a)
-            ptx::tma_store_3d(&tm_dqkv, ptx::smem_u32(sSt + a * Cfg::kAtom), item.h * HD + 64 * a, item.qt * 128,
-                              item.b);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read();
-          ptx::mbar_arrive(ptx::smem_u32(&bars->stage_free));
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      pend_it = it;
+      pend_item = item;
     }
+    if (ok && pend_it >= 0) ok = epilogue(pend_it, pend_item);
     if (!ok) fail();
     // Every tile store has landed in global memory before the CTA exits.
     if (warp == 2 && lane == 0) ptx::bulk_wait();
