@@ -207,7 +207,9 @@ def traffic_for(kernel, workload=None):
     rec = table.get(f"{kernel}@{workload}") or table.get(kernel)
     if not rec or (workload is not None and rec.get("workload") != workload):
         return None
-    src = os.path.join(ROOT, "causal_attention_gqa_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    # A record may name its own source file (the same event name covers
+    # different kernels at different head sizes).
+    src = os.path.join(ROOT, "causal_attention_gqa_gb300", "csrc", rec.get("source") or KERNEL_SOURCES.get(kernel, ""))
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
