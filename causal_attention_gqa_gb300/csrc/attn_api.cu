@@ -162,6 +162,11 @@ size_t row_part_bytes(const Geometry& g, int dtype) {
 // kernel's work-item counter.
 size_t rot_part_bytes(const Geometry& g) { return align256((size_t)g.B * g.T * (g.NH + g.NKV) * g.hd * 2); }
 
+// bf16: after the counter, the RoPE angle table [hd/2][T] of (cos, sin) float
+// pairs the prologue writes for the gradient epilogues (reserved whether or
+// not RoPE is on: the size query takes no rope_theta).
+size_t rope_table_bytes(const Geometry& g) { return align256((size_t)g.T * g.hd * sizeof(float)); }
+
 // dtype TF32 on tensor cores (head size 64): bf16 hi/lo parts of qkv (and,
 // for the backward, of dout), each array rounded up to 256 bytes.
 bool split_path(const Geometry& g, int dtype) { return dtype == ATTN_DTYPE_TF32 && split_supported(g); }
@@ -172,7 +177,7 @@ size_t workspace_bytes(const Geometry& g, int dtype) {
   if (split_path(g, dtype))
     return split_table_bytes(g) + 2 * split_part_bytes(g, g.W) + 2 * split_part_bytes(g, g.C);
   size_t bytes = row_part_bytes(g, dtype);
-  if (dtype == ATTN_DTYPE_BF16) bytes += rot_part_bytes(g) + 256;
+  if (dtype == ATTN_DTYPE_BF16) bytes += rot_part_bytes(g) + 256 + rope_table_bytes(g);
   return bytes;
 }
 
@@ -396,6 +401,8 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
   // column h*hd and kv head kh at C + kh*hd.
   void* rot = static_cast<uint8_t*>(workspace) + row_part_bytes(g, dtype);
   a.item_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(rot) + rot_part_bytes(g));
+  float* rope_cs = reinterpret_cast<float*>(static_cast<uint8_t*>(rot) + rot_part_bytes(g) + 256);
+  a.rope_cs = rope_cs;
   const void* qk_src = !rope ? qkv : (reuse ? qk_rot : rot);
   const int qk_width = rope ? (g.NH + g.NKV) * g.hd : g.W;
   for (int r = 0; r < 2; ++r) {
@@ -406,7 +413,7 @@ int bwd_impl(void* dqkv, const void* qkv, const void* out, const void* dout, con
   }
   if (!make_tmap(&a.tm_dqkv, dqkv, g.W, g.T, g.B, 128)) return ATTN_ERR_CUDA;
   cudaError_t e = launch_bwd_prologue_bf16(static_cast<float*>(workspace), rope && !reuse ? rot : nullptr,
-                                           a.item_counter, out, dout, lse, qkv, g, s);
+                                           a.item_counter, rope ? rope_cs : nullptr, out, dout, lse, qkv, g, s);
   if (e == cudaSuccess) e = tc05_bwd_launch(a, s);
   return from_cuda(e);
 }

@@ -55,7 +55,10 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int col) {
 }
 
 // Epilogue of one gradient row held in TMEM (HD float32 columns at `acc`):
-// multiply by `s`, undo the RoPE rotation at position `t` if `rope`, round to
+// multiply by `s`, undo the RoPE rotation at position `t` if `rope` (cos and
+// sin of each pair's angle from the prologue's table `cs` when given: in the
+// dQ kernel, where the epilogue overlaps the next item's MMAs, forming them
+// per pair took as long as a step), round to
 // bf16 and write row `row` of the swizzled staging tile `stile` (HD columns),
 // from which one thread then writes the whole tile with TMA stores (coalesced;
 // one 16-byte store per thread and row would not be).  Every lane of the warp
@@ -64,7 +67,8 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int col) {
 // handles part `part`.
 template <int HD>
 __device__ __forceinline__ void stage_grad_row(uint32_t acc, float s, bool rope, int t, const Geometry& g,
-                                               uint8_t* stile, int row, int part, int nparts) {
+                                               const float* __restrict__ cs, uint8_t* stile, int row, int part,
+                                               int nparts) {
   if (!rope) {
 #pragma unroll 1
     for (int c0 = 32 * part; c0 < HD; c0 += 32 * nparts) {
@@ -80,15 +84,26 @@ __device__ __forceinline__ void stage_grad_row(uint32_t acc, float s, bool rope,
 #pragma unroll 1
   for (int c0 = 32 * part; c0 < HALF; c0 += 32 * nparts) {
     uint32_t lo[32], hi[32];
+    // Pair i of position t at cs[2 (i T + t)]: the warp's 32 consecutive rows
+    // read one contiguous run per pair.  Rows past T (clipped by the TMA
+    // store) read the last row's angles.  Without a table (cs == NULL) the
+    // angles are formed here.
+    float2 a[32];
+    if (cs != nullptr) {
+      const float2* cs2 = reinterpret_cast<const float2*>(cs) + (size_t)c0 * g.T + (t < g.T ? t : g.T - 1);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) a[e] = __ldg(cs2 + (size_t)e * g.T);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) __sincosf(rope_angle(t, g.rope_f_hi[c0 + e], g.rope_f_lo[c0 + e]), &a[e].y, &a[e].x);
+    }
     ptx::tmem_ld32(acc + c0, lo);
     ptx::tmem_ld32(acc + HALF + c0, hi);
     ptx::tmem_wait_ld();
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      const int i = c0 + e;
-      float sn, cs, y0, y1;
-      __sincosf(rope_angle(t, g.rope_f_hi[i], g.rope_f_lo[i]), &sn, &cs);
-      rope_pair_transpose(__uint_as_float(lo[e]) * s, __uint_as_float(hi[e]) * s, cs, sn, y0, y1);
+      float y0, y1;
+      rope_pair_transpose(__uint_as_float(lo[e]) * s, __uint_as_float(hi[e]) * s, a[e].x, a[e].y, y0, y1);
       lo[e] = __float_as_uint(y0);
       hi[e] = __float_as_uint(y1);
     }
@@ -440,8 +455,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     uint8_t* stK = sDO;
     if (ok) {
       ptx::tc_fence_after();
-      stage_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, stV, row, wg, 2);
-      stage_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, stK, row, wg, 2);
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDV, 1.f, false, ks, g, nullptr, stV, row, wg, 2);
+      // The angles are formed here: at the CTA's end nothing overlaps the
+      // epilogue, and the table reads measured slower than forming them.
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDK, g.scale, ROPE, ks, g, nullptr, stK, row, wg, 2);
     } else {
       fail();
     }
@@ -547,7 +564,8 @@ __global__ void __launch_bounds__(kThreadsDq, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_dqkv, const float* __restrict__ LD,
-              int* __restrict__ item_counter, int n_items, int* __restrict__ status, Geometry g) {
+              const float* __restrict__ rope_cs, int* __restrict__ item_counter, int n_items,
+              int* __restrict__ status, Geometry g) {
   using Cfg = DqCfg<HD>;
   constexpr int NKS = Cfg::kKStages, NVS = Cfg::kVStages, NIS = Cfg::kItemSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -847,7 +865,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                       ptx::mbar_wait(ptx::smem_u32(&bars->acc_done[db]), (pit >> 1) & 1, abort_flag, kWaitLimitNs)))
         return false;
       ptx::tc_fence_after();
-      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ + 128 * db, g.scale, ROPE, ptq, g, sSt, row, wg, 2);
+      stage_grad_row<HD>(t_lane + Cfg::kTmemDQ + 128 * db, g.scale, ROPE, ptq, g, rope_cs, sSt, row, wg, 2);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
@@ -988,7 +1006,7 @@ cudaError_t launch_bwd(const Tc05BwdArgs& a, cudaStream_t stream) {
   const unsigned grid2 = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelBwdDqTc05, stream);
   e = launch_pdl(k2, dim3(grid2), dim3(kThreadsDq), DqCfg<HD>::kSmemBytes, stream, a.tm_qk[1], a.tm_do[1],
-                 a.tm_qk[1], a.tm_v[1], a.tm_dqkv, a.LD, a.item_counter, n_items, a.status, g);
+                 a.tm_qk[1], a.tm_v[1], a.tm_dqkv, a.LD, a.rope_cs, a.item_counter, n_items, a.status, g);
   prof_end(kKernelBwdDqTc05, stream);
   return e;
 }

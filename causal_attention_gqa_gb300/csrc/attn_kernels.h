@@ -147,10 +147,13 @@ __host__ __device__ inline int row_table_rows(int T) { return (T + 127) / 128 * 
 // bf16 (hd a multiple of 16): the row tables, two float arrays of Tp rows per
 // (b, h): LD[(2*(b*NH + h))*Tp + t] = -lse * log2(e) and
 // LD[(2*(b*NH + h) + 1)*Tp + t] = -D with D = dO . O (zeros for t >= T); and,
-// when `rot` is not NULL, the RoPE-rotated Q/K copy; it also clears
-// *item_counter; in one launch.
-cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, const void* out, const void* dout,
-                                     const float* lse, const void* qkv, const Geometry& g, cudaStream_t stream);
+// when `rot` is not NULL, the RoPE-rotated Q/K copy; when `rope_cs` is not
+// NULL, the table rope_cs[2(i*T + t)], [2(i*T + t) + 1] = cos, sin of the RoPE
+// angle of position t and pair i that the gradient epilogues read; it also
+// clears *item_counter; in one launch.
+cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, float* rope_cs, const void* out,
+                                     const void* dout, const float* lse, const void* qkv, const Geometry& g,
+                                     cudaStream_t stream);
 
 // ------------------------------------------------------------ tcgen05 bf16 path
 struct Tc05FwdArgs {
@@ -188,6 +191,7 @@ struct Tc05BwdArgs {
   void* dqkv;            // [B,T,W] bf16
   const float* LD;       // row tables: -lse * log2(e) and -D per (b, h), see launch_bwd_prologue_bf16
   int* item_counter;     // dQ work-item counter (workspace), cleared by the prologue
+  const float* rope_cs;  // RoPE (cos, sin) table [hd/2][T] written by the prologue (RoPE only)
   int* status;
   int num_sms;           // persistent grid size
 };

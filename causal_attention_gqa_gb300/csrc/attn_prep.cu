@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
                                                                  const float* __restrict__ lse,
                                                                  __nv_bfloat16* __restrict__ rot,
                                                                  int* __restrict__ item_counter,
+                                                                 float* __restrict__ rope_cs,
                                                                  const __nv_bfloat16* __restrict__ qkv, Geometry g,
                                                                  int vph_log2) {
   // out is written by the forward that may still be finishing (programmatic
@@ -233,12 +234,25 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
       LD[(size_t)(2 * bh + 1) * Tp + t] = 0.f;
     }
   }
+  // The (cos, sin) of every RoPE angle, for the gradient epilogues: pair i,
+  // position t at rope_cs[2 (i T + t)], so that the 32 consecutive rows of a
+  // warp read one contiguous run per pair.
+  if (rope_cs != nullptr) {
+    const int half = g.hd >> 1, n_cs = g.T * half;
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n_cs; k += gridDim.x * blockDim.x) {
+      const int i = k / g.T, t = k - i * g.T;
+      float sn, cs;
+      __sincosf(rope_angle(t, g.rope_f_hi[i], g.rope_f_lo[i]), &sn, &cs);
+      *reinterpret_cast<float2*>(rope_cs + 2 * (size_t)k) = make_float2(cs, sn);
+    }
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, const void* out, const void* dout,
-                                     const float* lse, const void* qkv, const Geometry& g, cudaStream_t stream) {
+cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, float* rope_cs, const void* out,
+                                     const void* dout, const float* lse, const void* qkv, const Geometry& g,
+                                     cudaStream_t stream) {
   const int vph = g.hd / 8;  // 8 or 16
   int vph_log2 = 0;
   while ((1 << vph_log2) < vph) ++vph_log2;
@@ -248,10 +262,10 @@ cudaError_t launch_bwd_prologue_bf16(float* LD, void* rot, int* item_counter, co
   prof_begin(kKernelBwdPrologue, stream);
   cudaError_t e = rot != nullptr
                       ? launch_pdl(bwd_prologue_bf16_kernel<true>, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
-                                   (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter,
+                                   (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter, rope_cs,
                                    (const __nv_bfloat16*)qkv, g, vph_log2)
                       : launch_pdl(bwd_prologue_bf16_kernel<false>, dim3((unsigned)blocks), dim3(256), 0, stream, LD,
-                                   (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter,
+                                   (const uint4*)out, (const uint4*)dout, lse, (__nv_bfloat16*)rot, item_counter, rope_cs,
                                    (const __nv_bfloat16*)qkv, g, vph_log2);
   prof_end(kKernelBwdPrologue, stream);
   return e;

@@ -150,9 +150,11 @@ ATTN_API int attn_fwd_ws(void* out, float* lse, const void* qkv,
 /*
  * attn_bwd_workspace_bytes -- size in bytes of the scratch attn_bwd needs
  * for this shape and dtype: the row dots D = rowsum(dO * O) (float32
- * [B,NH,T]; for BF16 stored next to the rescaled lse as float pairs over T
- * rounded up to 64 rows), plus, for BF16, room for a RoPE-rotated bf16 copy
- * of Q and K (used only when rope_theta > 0); for TF32 with head size 64 the
+ * [B,NH,T]; for BF16 stored next to the rescaled lse as two float tables of
+ * T rounded up to 128 rows per (b, h)), plus, for BF16, room for a
+ * RoPE-rotated bf16 copy of Q and K, 256 bytes for a work-item counter and a
+ * float (cos, sin) table of the RoPE angles [hd/2][T] (the copy and the table
+ * are used only when rope_theta > 0); for TF32 with head size 64 the
  * row tables over T rounded up to 128 rows and the bf16 hi/lo parts of qkv
  * and dout (the tensor-core path; 16-byte aligned tensors).  Returns 0 for invalid
  * arguments.
@@ -214,8 +216,8 @@ ATTN_API int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const vo
  *    loaded holds ATTN_NOALLOC_SCRATCH_BYTES until the process exits.
  *  - Problems whose attn_bwd_workspace_bytes() exceeds that size are
  *    rejected with ATTN_ERR_WORKSPACE before anything is launched (e.g. the
- *    bf16 B=4, T=2048, NH=16, NKV=4, hd=128 case needs about 42.5 MB and
- *    fits; B=1, T=8192, NH=32, NKV=8, hd=128 needs about 85 MB and does not).
+ *    bf16 B=4, T=2048, NH=16, NKV=4, hd=128 case needs about 44 MB and
+ *    fits; B=1, T=8192, NH=32, NKV=8, hd=128 needs about 90 MB and does not).
  *  - The first call on a device (with that device current) looks up the
  *    buffer's device address; make that first call before any stream
  *    capture on that device.  The address is then kept for the life of the

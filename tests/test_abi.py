@@ -50,14 +50,19 @@ def test_strerror_and_version(cdll):
 def test_workspace_size(cdll):
     from causal_attention_gqa_gb300 import binding
     B, T, C, NH, NKV = 4, 2048, 2048, 16, 4
-    # bf16: (lse, D) float pairs per (b, h) row over T rounded up to 64, then
-    # the rotated Q/K copy; each part rounded up to 256 bytes.
+    # bf16: (lse, D) float tables per (b, h) over T rounded up to 128, then
+    # the rotated Q/K copy, the dQ kernel's work-item counter and the RoPE
+    # (cos, sin) table [hd/2][T]; each part rounded up to 256 bytes.
+    def up(n):
+        return (n + 255) // 256 * 256
     row_bytes = B * NH * T * 8
     rot_bytes = B * T * (NH + NKV) * (C // NH) * 2
-    cnt_bytes = 256   # the dQ kernel's work-item counter
-    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == row_bytes + rot_bytes + cnt_bytes
+    cnt_bytes = 256
+    cs_bytes = T * (C // NH) * 4
+    assert binding.attn_bwd_workspace_bytes(B, T, C, NH, NKV, binding.DTYPE_BF16) == \
+        row_bytes + rot_bytes + cnt_bytes + cs_bytes
     ragged = binding.attn_bwd_workspace_bytes(1, 100, 256, 2, 1, binding.DTYPE_BF16)
-    assert ragged == 2 * 128 * 8 + 100 * 3 * 128 * 2 + (256 - (100 * 3 * 128 * 2) % 256) % 256 + 256
+    assert ragged == 2 * 128 * 8 + up(100 * 3 * 128 * 2) + 256 + up(100 * 128 * 4)
     assert binding.attn_bwd_workspace_bytes(1, 16, 16, 4, 4, binding.DTYPE_F32) == 256
     assert binding.attn_bwd_workspace_bytes(1, 16, 16, 3, 4, binding.DTYPE_F32) == 0
 
