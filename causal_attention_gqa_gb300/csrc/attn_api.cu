@@ -527,7 +527,7 @@ extern "C" int attn_qkv_proj(void* qkv, void* qk_rot, const void* x, const void*
   a.status = status_word();
   a.num_sms = num_sms();
   if (!a.status || a.num_sms <= 0) return ATTN_ERR_CUDA;
-  if (!make_tmap(&a.tm_x, x, Cm, (int)M, 1, 128) || !make_tmap(&a.tm_w, w, Cm, (int)N, 1, 256)) return ATTN_ERR_CUDA;
+  if (!make_tmap(&a.tm_x, x, Cm, (int)M, 1, 128) || !make_tmap(&a.tm_w, w, Cm, (int)N, 1, 128)) return ATTN_ERR_CUDA;
   return from_cuda(proj_launch(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -165,6 +165,19 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory whose completion is signalled
+// on an mbarrier of either CTA of the pair (address from cluster_addr):
+// the second CTA of a pair loads its operand halves against the first CTA's
+// stage barrier.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(cluster_bar)
+      : "memory");
+}
+
 // 3-D tiled load (coordinates innermost first) completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2,
                                             uint32_t bar) {
@@ -173,6 +186,100 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// ----------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs running tcgen05 with .cta_group::2: one MMA issued by
+// the first CTA (rank 0) reads operands from both CTAs' shared memory and
+// writes both CTAs' tensor memory.  Every tcgen05 instruction of such a
+// kernel uses .cta_group::2.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address, in the cluster's shared window, of the object at shared::cta
+// address `smem_addr` in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// cluster_addr).  CTA-scope release: the arrival only signals (what it
+// guards is ordered by TMA completion and the tcgen05 fences); a
+// cluster-scope release costs ~1,500 cycles per arrive on this GPU.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_address) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_address) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_address, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_address), "r"(v) : "memory");
+}
+
+// Every thread of both CTAs: arrive and wait (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;\n" ::
+          : "memory");
+}
+
+// Waits and tests with cluster-scope acquire, for barriers that other CTAs
+// of the cluster arrive on (remote arrives, multicast commits).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t mbar_test_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// mbar_wait with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                             uint64_t limit_ns) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_cl_all(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                                 uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_cl(bar, parity, abort, limit_ns));
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -269,6 +376,52 @@ __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
       "  elect.sync _|e, 0xffffffff;\n"
       "  @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
       "}\n" ::"r"(bar)
+      : "memory");
+}
+
+// .cta_group::2 forms (CTA pairs).  Allocation and release are collective:
+// one warp of each CTA of the pair executes them.
+__device__ __forceinline__ void tmem_alloc2(uint32_t holder_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[256 x N] (+)= A B over the pair: rows 0-127 of A from the first CTA's
+// shared memory, rows 128-255 from the second's (same address), B's N rows
+// half from each; each CTA's TMEM receives its 128 rows.  Issued by the
+// first CTA, whole warp, one elected lane.
+__device__ __forceinline__ void mma2_bf16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e, p;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  @e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Commit the issuing thread's MMAs to the mbarrier at shared::cta address
+// `bar` in every CTA of `cta_mask` (bit i: cluster rank i).
+__device__ __forceinline__ void mma2_commit_mc_w(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  elect.sync _|e, 0xffffffff;\n"
+      "  @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
+      "}\n" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 

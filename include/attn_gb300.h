@@ -219,9 +219,9 @@ ATTN_API int attn_bwd_rot(void* dqkv, const void* qkv, const void* out, const vo
  *    bf16 B=4, T=2048, NH=16, NKV=4, hd=128 case needs about 44 MB and
  *    fits; B=1, T=8192, NH=32, NKV=8, hd=128 needs about 90 MB and does not).
  *  - The first call on a device (with that device current) looks up the
- *    buffer's device address; make that first call before any stream
- *    capture on that device.  The address is then kept for the life of the
- *    process: after cudaDeviceReset() on a device the buffer lives in a new
+ *    buffer's device address with cudaGetSymbolAddress.  The address is then
+ *    kept for the life of the process: after cudaDeviceReset() on a device
+ *    the buffer lives in a new
  *    context at an address this library does not look up again, so do not
  *    call attn_bwd_noalloc on that device after a reset.
  *  - All calls share the one buffer, which keeps the last call's contents.

@@ -201,4 +201,7 @@ def test_bf16_gqa_block_full_sampled_in_kernel_rope(lib):
 
 
 def test_bf16_long_context_full_sampled(lib):
-    check_sampled(lib, WORKLOADS["long_context_gqa"], "bf16", kv_groups=[(0, 0), (0, 7)], fwd_ws=True)
+    # dK/dV on every kv group (each needs every query row of its four heads
+    # in the oracle, a few seconds per group).
+    w = WORKLOADS["long_context_gqa"]
+    check_sampled(lib, w, "bf16", kv_groups=[(0, kh) for kh in range(w.NKV)], fwd_ws=True)

@@ -32,6 +32,7 @@ def run_proj(lib, B, T, Cm, NH, NKV, hd, theta, interleaved):
     (2, 77, 200, 3, 1, 64, 1e4, True),         # K tail (Cm = 200), N tail (N = 320)
     (1, 129, 512, 4, 4, 128, 1e4, True),
     (1, 64, 128, 2, 1, 128, 0.0, False),       # no RoPE: no copy
+    (4, 2048, 2048, 16, 4, 128, 1e6, False),   # the GQA block's projection: several tiles per CTA pair
 ])
 def test_qkv_projection_matches_oracle(lib, B, T, Cm, NH, NKV, hd, theta, interleaved):
     x_np, w_np, qkv, rot = run_proj(lib, B, T, Cm, NH, NKV, hd, theta, interleaved)
