@@ -648,7 +648,9 @@ def run_proj(args):
                    "l2": "flushed between calls (256 MiB write outside the timed events)"},
         "variants": res,
         "roofline": {"bound": "tensor", "achieved": v, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": v / peaks["bf16_tflops"], "traffic": None, "peak_source": f"{src} bf16_tflops (burst)"},
+                     "frac": v / peaks["bf16_tflops"],
+                     "traffic": traffic_for("proj", "qkv_projection_" + args.proj.replace(",", "_")),
+                     "peak_source": f"{src} bf16_tflops (burst)"},
     }
     print(json.dumps(line), flush=True)
     return 0
