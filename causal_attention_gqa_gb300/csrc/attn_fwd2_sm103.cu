@@ -1,17 +1,21 @@
 // Causal GQA attention forward on sm_103a tensor cores for two query heads
-// that share a kv head (bf16 in, f32 accumulation), head size 128.
+// per work item (bf16 in, f32 accumulation): head size 128 with two query
+// heads of one kv head (they read the same K/V tiles), or head size 64 with
+// any two query heads (sharing K/V tiles when they share a kv head, else
+// each brings its own K/V tiles into the same ring stage).
 //
 // Persistent kernel: one CTA per SM walks its share of a list of work items
 // (dealt back and forth across the CTAs), one item = a 128-query tile of two
-// query heads 2p, 2p+1 of one batch row (they read the same K/V tiles, so
-// every K/V tile loaded feeds two score and two PV MMAs), heaviest (longest
-// causal key range) first.  Two softmax warpgroups, one per query head, work
+// query heads 2p, 2p+1 of one batch row (with a shared kv head every K/V
+// tile loaded feeds two score and two PV MMAs), heaviest (longest causal key
+// range) first.  Two softmax warpgroups, one per query head, work
 // in ping-pong: while group A turns S_A(j) into P_A(j), the tensor core runs
 // PV_B(j-1) and S_B(j), and the other way round, so neither the tensor core
 // nor the softmax waits for the other as long as one tile's softmax takes
 // less than two tiles' MMAs.  Warp roles:
-//   warp 0      TMA producer: both Q tiles of an item, then K_j and V_j
-//               together into a two-stage ring (one barrier per key tile).
+//   warp 0      TMA producer: both Q tiles of an item, then K_j and V_j (of
+//               one kv head, or of both heads' kv heads) together into a
+//               two-stage ring (one barrier per key tile).
 //   warp 1      TMEM owner and the single MMA issuer, in the order
 //               S_A(0), S_B(0), then per key tile PV_A(j), S_A(j+1), PV_B(j),
 //               S_B(j+1).
@@ -22,7 +26,8 @@
 //               grows past a threshold (exact: l and O share the stale max),
 //               and at the end of an item writes out = O / l (staged in shared
 //               memory, TMA store) and lse = m + ln l.
-// TMEM columns: S_A, S_B (128 each), O_A, O_B (128 each).  P(j) overwrites
+// TMEM columns: S_A, S_B (128 each), O_A, O_B (128 each, of which the head
+// size is used).  P(j) overwrites
 // S(j) and the next score MMA into the same columns is issued after the PV
 // MMA that reads P(j): MMAs issued by one thread execute in order.
 // The math is that of "nanoeuler -- CUDA kernels", attention_forward_kernel
@@ -41,19 +46,23 @@
 namespace attn {
 namespace {
 
-constexpr int kHD = 128;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: P may reach 2^8 before O is rescaled
 constexpr int kThreads = 320;
 
+// SHARED: the two heads of an item read one kv head's K/V tiles; else each
+// ring stage holds K_A, K_B (and V_A, V_B).
+template <int HD, bool SHARED>
 struct Fwd2Cfg {
   static constexpr int kAtom = 128 * 128;               // 128 rows x one 128-byte swizzle-atom column
-  static constexpr int kTileBytes = 128 * kHD * 2;      // Q / K / V / output tile
+  static constexpr int kTileBytes = 128 * HD * 2;       // Q / K / V / output tile
+  static constexpr int kKT = SHARED ? 1 : 2;            // K (and V) tiles per ring stage
+  static constexpr int kStageBytes = kKT * kTileBytes;
   static constexpr int kKStages = 2, kVStages = 2;
   static constexpr int kQOff = 0;                       // Q_A, Q_B
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kStOff = kVOff + kVStages * kTileBytes;   // output staging tile
+  static constexpr int kVOff = kKOff + kKStages * kStageBytes;
+  static constexpr int kStOff = kVOff + kVStages * kStageBytes;   // output staging tile
   static constexpr int kBarOff = kStOff + kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;
   static_assert(kSmemBytes <= 232448, "paired forward kernel exceeds the 227 KB shared-memory limit");
@@ -97,11 +106,12 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int col) {
   return (uint32_t)((col >> 6) * (128 * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
 }
 
+template <int HD, bool SHARED>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_out, float* __restrict__ lse, int* __restrict__ status, Geometry g,
             int n_items) {
-  using Cfg = Fwd2Cfg;
+  using Cfg = Fwd2Cfg<HD, SHARED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Cfg::kQOff;
@@ -161,7 +171,8 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
       for (int it = 0, w = w0; w < n_items && ok; ++it, w = snake(it, w0, dw)) {
         const Fwd2Item item = fwd2_item(w, g);
         const int n_kv = item.qt + 1;
-        const int k_col = g.C + item.kh * kHD, v_col = g.C + g.NKV * kHD + item.kh * kHD;
+        // kv heads of the item's two query heads (the same one when SHARED)
+        const int kh2[2] = {item.h0 / g.grp, (item.h0 + 1) / g.grp};
         if (it >= 1 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->q_empty), (it - 1) & 1, abort_flag, kWaitLimitNs)))
           break;
         const uint32_t qf = ptx::smem_u32(&bars->q_full);
@@ -169,9 +180,9 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
 #pragma unroll
         for (int x = 0; x < 2; ++x)
 #pragma unroll
-          for (int a = 0; a < kHD / 64; ++a)
+          for (int a = 0; a < HD / 64; ++a)
             ptx::tma_load_3d(ptx::smem_u32(sQ + x * Cfg::kTileBytes + a * Cfg::kAtom), &tm_qk,
-                             (item.h0 + x) * kHD + 64 * a, item.qt * 128, item.b, qf);
+                             (item.h0 + x) * HD + 64 * a, item.qt * 128, item.b, qf);
         q_issued = it + 1;
         // K_j and V_j into one ring stage with one barrier (each barrier the
         // MMA issuer checks stalls the tensor pipe).
@@ -181,13 +192,18 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
                                                kWaitLimitNs)))
             break;
           const uint32_t kvf = ptx::smem_u32(&bars->kv_full[st]);
-          ptx::mbar_arrive_expect_tx(kvf, 2 * Cfg::kTileBytes);
+          ptx::mbar_arrive_expect_tx(kvf, 2 * Cfg::kStageBytes);
 #pragma unroll
-          for (int a = 0; a < kHD / 64; ++a) {
-            ptx::tma_load_3d(ptx::smem_u32(sK + st * Cfg::kTileBytes + a * Cfg::kAtom), &tm_qk, k_col + 64 * a,
-                             j * 128, item.b, kvf);
-            ptx::tma_load_3d(ptx::smem_u32(sV + st * Cfg::kTileBytes + a * Cfg::kAtom), &tm_v, v_col + 64 * a,
-                             j * 128, item.b, kvf);
+          for (int y = 0; y < Cfg::kKT; ++y) {
+            const int k_col = g.C + kh2[y] * HD, v_col = g.C + g.NKV * HD + kh2[y] * HD;
+            const int off = st * Cfg::kStageBytes + y * Cfg::kTileBytes;
+#pragma unroll
+            for (int a = 0; a < HD / 64; ++a) {
+              ptx::tma_load_3d(ptx::smem_u32(sK + off + a * Cfg::kAtom), &tm_qk, k_col + 64 * a, j * 128, item.b,
+                               kvf);
+              ptx::tma_load_3d(ptx::smem_u32(sV + off + a * Cfg::kAtom), &tm_v, v_col + 64 * a, j * 128, item.b,
+                               kvf);
+            }
           }
           kv_issued = gk + 1;
         }
@@ -206,17 +222,17 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
     // and commit, and every wait is warp-collective)
     {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, kHD, false, true);
+      constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(128, HD, false, true);
       const uint64_t dQ = ptx::sw128_desc(ptx::smem_u32(sQ), 16, 1024);
       const uint64_t dK = ptx::sw128_desc(ptx::smem_u32(sK), 16, 1024);
       const uint64_t dV = ptx::sw128_desc(ptx::smem_u32(sV), Cfg::kAtom, 1024);
       bool ok = true;
       // S_x(g) = Q_x K_g^T into the score columns of group x.
       auto issue_s = [&](int x, int gk) {
-        const uint64_t bk = ptx::desc_advance(dK, (gk % 2) * Cfg::kTileBytes);
+        const uint64_t bk = ptx::desc_advance(dK, (gk % 2) * Cfg::kStageBytes + (SHARED ? 0 : x) * Cfg::kTileBytes);
         const uint64_t aq = ptx::desc_advance(dQ, x * Cfg::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
+        for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
           ptx::mma_bf16_ss_w(tmem + tmem_s(x), ptx::desc_advance(aq, off), ptx::desc_advance(bk, off), idesc_s,
                            kk > 0 ? 1u : 0u);
@@ -225,7 +241,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
       };
       // O_x += P_x(g) V_g with P from TMEM.
       auto issue_pv = [&](int x, int gk, bool first) {
-        const uint64_t bv = ptx::desc_advance(dV, (gk % 2) * Cfg::kTileBytes);
+        const uint64_t bv = ptx::desc_advance(dV, (gk % 2) * Cfg::kStageBytes + (SHARED ? 0 : x) * Cfg::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)
           ptx::mma_bf16_ts_w(tmem + tmem_o(x), tmem + tmem_s(x) + kk * 8, ptx::desc_advance(bv, kk * 2048), idesc_o,
@@ -346,7 +362,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
         // completion this group waited for.
         if ((j >= 1) && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < kHD; c0 += 32) {
+          for (int c0 = 0; c0 < HD; c0 += 32) {
             uint32_t o[32];
             ptx::tmem_ld32(o_addr + c0, o);
             ptx::tmem_wait_ld();
@@ -373,7 +389,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
       ptx::tc_fence_after();
       const float inv_l = 1.f / l;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHD; c0 += 32) {
+      for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t o[32];
         ptx::tmem_ld32(o_addr + c0, o);
         ptx::tmem_wait_ld();
@@ -402,8 +418,8 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->staged[x]), it & 1, abort_flag, kWaitLimitNs);
         if (ok) {
 #pragma unroll
-          for (int a = 0; a < kHD / 64; ++a)
-            ptx::tma_store_3d(&tm_out, ptx::smem_u32(sSt + a * Cfg::kAtom), (item.h0 + x) * kHD + 64 * a,
+          for (int a = 0; a < HD / 64; ++a)
+            ptx::tma_store_3d(&tm_out, ptx::smem_u32(sSt + a * Cfg::kAtom), (item.h0 + x) * HD + 64 * a,
                               item.qt * 128, item.b);
           ptx::bulk_commit();
           ptx::bulk_wait_read();
@@ -428,19 +444,32 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_qk, const __grid_constant__ C
 
 }  // namespace
 
-bool tc05_fwd2_supported(const Geometry& g) { return g.hd == kHD && g.grp % 2 == 0; }
+bool tc05_fwd2_supported(const Geometry& g) {
+  return (g.hd == 128 && g.grp % 2 == 0) || (g.hd == 64 && g.NH % 2 == 0);
+}
 
-cudaError_t tc05_fwd2_launch(const Tc05FwdArgs& a, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(fwd2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Fwd2Cfg::kSmemBytes);
+namespace {
+template <int HD, bool SHARED>
+cudaError_t launch_fwd2(const Tc05FwdArgs& a, cudaStream_t stream) {
+  using Cfg = Fwd2Cfg<HD, SHARED>;
+  auto kern = fwd2_kernel<HD, SHARED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_qt = (a.g.T + 127) / 128;
   const int n_items = n_qt * a.g.B * (a.g.NH / 2);
   const unsigned grid = (unsigned)(n_items < a.num_sms ? n_items : a.num_sms);
   prof_begin(kKernelFwdTc05, stream);
-  e = launch_pdl(fwd2_kernel, dim3(grid), dim3(kThreads), Fwd2Cfg::kSmemBytes, stream, a.tm_qk, a.tm_v, a.tm_out,
-                 a.lse, a.status, a.g, n_items);
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream, a.tm_qk, a.tm_v, a.tm_out, a.lse,
+                 a.status, a.g, n_items);
   prof_end(kKernelFwdTc05, stream);
   return e;
+}
+}  // namespace
+
+cudaError_t tc05_fwd2_launch(const Tc05FwdArgs& a, cudaStream_t stream) {
+  if (a.g.hd == 128 && a.g.grp % 2 == 0) return launch_fwd2<128, true>(a, stream);
+  if (a.g.hd == 64) return a.g.grp % 2 == 0 ? launch_fwd2<64, true>(a, stream) : launch_fwd2<64, false>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

@@ -128,6 +128,11 @@ def test_bf16_forward_shapes(lib, B, T, C, NH, NKV, theta):
     # paired-head forward kernel (ragged T, T = 1, one tile, several items)
     (2, 385, 1024, 8, 2, 0.0), (1, 1, 256, 2, 1, 0.0), (1, 128, 256, 2, 1, 0.0), (3, 200, 1024, 8, 4, 0.0),
     (1, 700, 2048, 16, 2, 0.0),
+    # head size 64, an even number of query heads: heads sharing a kv head,
+    # one kv head per query head, and groups of three (a pair can straddle
+    # two kv heads)
+    (2, 300, 512, 8, 4, 0.0), (1, 200, 256, 4, 4, 0.0), (1, 1, 128, 2, 2, 0.0), (2, 385, 384, 6, 2, 0.0),
+    (1, 640, 768, 12, 12, 0.0),
 ])
 def test_bf16_forward_paired_heads(lib, B, T, C, NH, NKV, theta):
     check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 13), "bf16", backward=False)
