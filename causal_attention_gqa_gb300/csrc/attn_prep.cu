@@ -118,17 +118,20 @@ __global__ void __launch_bounds__(256, 3) rope_qk_bf16_kernel(__nv_bfloat16* __r
   }
 }
 
-// bf16 backward prologue, one launch.  Block-stride over groups of four
-// token rows of the flattened B*T rows; for each group:
-//  * threads 0..C/8-1 each multiply one 16-byte chunk of out and dout of the
-//    four rows; the hd/8 lanes of a head sum their partials with shuffles and
-//    one of them writes -D[b,h,t] with D = dO . O into the second row table
-//    of (b, h);
-//  * (RoPE only) threads 0..(NH+NKV)*hd/16-1 each rotate 8 NEOX pairs of one
-//    Q or K head of the four rows into the workspace copy.
-// Every load of a group is issued before the first of them is used, so that
-// each thread keeps several 16-byte loads in flight (the kernel is bound by
-// HBM latency and bandwidth, not arithmetic).
+// bf16 backward prologue, one launch.
+//  * -D[b,h,t] with D = dO . O, into the second row table of (b, h): each
+//    thread multiplies 16-byte chunks of out and dout, the hd/8 lanes of a
+//    head (aligned: C/8 is a multiple of hd/8) sum their partials with
+//    shuffles and one of them writes the table entry.  Rows of at least 256
+//    chunks: block-stride over groups of four token rows, threads over the
+//    chunks of the group's rows.  Narrower rows: the chunks of all B*T rows
+//    flattened, four per thread and pass (a block per group of rows would
+//    leave most of a block idle).  All loads of a pass are issued before the
+//    first of them is used.
+//  * (RoPE only) block-stride over groups of four token rows: threads
+//    0..(NH+NKV)*hd/16-1 each rotate 8 NEOX pairs of one Q or K head of the
+//    four rows into the workspace copy.
+// The kernel is bound by HBM latency and bandwidth, not arithmetic.
 // Afterwards the first row table, -lse[b,h,t] * log2(e), is written from lse
 // along t, and the rows T..Tp-1 of both tables are cleared, so that whole
 // 64-row tiles of the tables can be copied.  The two tables hold the per-row
@@ -152,17 +155,55 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
   constexpr int R = 4;                            // token rows per iteration
   const int vph = 1 << vph_log2;                  // 16-byte chunks per head (hd / 8)
   const int dot_units = g.C >> 3;                 // chunks per token row
-  const int dot_threads = (dot_units + 31) & ~31;  // whole warps take part in the shuffles
+  const int dot_threads = (dot_units + 31) & ~31;  // rounded to whole warps
   const int gph_log2 = vph_log2 - 1;              // 8-pair groups per head (hd / 16), log2
   const int heads = g.NH + g.NKV, half = g.hd >> 1;
   const int rope_units = ROPE ? heads << gph_log2 : 0;
   const int rows = g.B * g.T, Tp = row_table_rows(g.T);
   const int rot_w = heads * g.hd;
   const int n_groups = (rows + R - 1) / R;
+  if (dot_units < (int)blockDim.x) {
+    // Rows narrower than a block (C/8 < 256 chunks): flattened chunks.
+    constexpr int U = 4;
+    const long long n_units = (long long)rows * dot_units;
+    const int lane = threadIdx.x & 31;
+    for (long long base = ((long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31)) * U; base < n_units;
+         base += (long long)gridDim.x * blockDim.x * U) {
+      uint4 a[U], d[U];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const long long u = base + 32 * i + lane;
+        a[i] = make_uint4(0u, 0u, 0u, 0u);
+        d[i] = a[i];
+        if (u < n_units) {
+          a[i] = out[u];
+          d[i] = dout[u];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        float acc = bf16_lo(a[i].x) * bf16_lo(d[i].x) + bf16_hi(a[i].x) * bf16_hi(d[i].x) +
+                    bf16_lo(a[i].y) * bf16_lo(d[i].y) + bf16_hi(a[i].y) * bf16_hi(d[i].y) +
+                    bf16_lo(a[i].z) * bf16_lo(d[i].z) + bf16_hi(a[i].z) * bf16_hi(d[i].z) +
+                    bf16_lo(a[i].w) * bf16_lo(d[i].w) + bf16_hi(a[i].w) * bf16_hi(d[i].w);
+        for (int off = vph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long u = base + 32 * i + lane;
+        if (u < n_units && (lane & (vph - 1)) == 0) {
+          const int row = (int)(u / dot_units), c = (int)(u - (long long)row * dot_units);
+          const int b = row / g.T, t = row - b * g.T;
+          LD[(size_t)(2 * (b * g.NH + (c >> vph_log2)) + 1) * Tp + t] = -acc;
+        }
+      }
+    }
+  }
+  const bool dot_by_group = dot_units >= (int)blockDim.x;
   for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
     const int row0 = grp * R;
     const int nr = min(R, rows - row0);
-    for (int c = threadIdx.x; c < dot_threads; c += blockDim.x) {
+    // Rows at least a block wide: the block's threads take the chunks of the
+    // group's four rows (eight loads in flight per chunk column); whole
+    // warps take part in the shuffles.
+    for (int c = threadIdx.x; dot_by_group && c < dot_threads; c += blockDim.x) {
       uint4 a[R], d[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -183,8 +224,7 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
         if (c < dot_units && r < nr && (c & (vph - 1)) == 0) {
           const int row = row0 + r;
           const int b = row / g.T, t = row - b * g.T;
-          const int bh = b * g.NH + (c >> vph_log2);
-          LD[(size_t)(2 * bh + 1) * Tp + t] = -acc;
+          LD[(size_t)(2 * (b * g.NH + (c >> vph_log2)) + 1) * Tp + t] = -acc;
         }
       }
     }
