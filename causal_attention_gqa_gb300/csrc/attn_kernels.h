@@ -106,7 +106,7 @@ struct ProjGeometry {
   float rope_f_lo[64];
 };
 struct ProjArgs {
-  CUtensorMap tm_x, tm_w;
+  CUtensorMap tm_x, tm_w;   // x [M, Cm] and w [N, Cm] bf16: 64-column, 128-row boxes, 128-byte swizzle
   void* qkv;
   void* rot;         // may be null
   ProjGeometry pg;
@@ -172,9 +172,10 @@ struct Tc05FwdArgs {
   int num_sms;        // persistent grid size
 };
 cudaError_t tc05_fwd_launch(const Tc05FwdArgs& a, cudaStream_t stream);
-// Paired-head forward (two query heads of one kv group per work item): head
-// size 128, an even number of query heads per kv head, Q/K not rotated in
-// the kernel.
+// Paired-head forward (two query heads per work item), Q/K not rotated in
+// the kernel: head size 128 with an even number of query heads per kv head
+// (the pair shares its K/V tiles), or head size 64 with an even number of
+// query heads (sharing K/V tiles when the pair shares a kv head).
 bool tc05_fwd2_supported(const Geometry& g);
 cudaError_t tc05_fwd2_launch(const Tc05FwdArgs& a, cudaStream_t stream);
 
