@@ -151,13 +151,22 @@ struct DkdvCfg {
   static constexpr int kBarOff = kLDOff + kQStages * kQ * 8;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDK = 256, kTmemDV = 256 + HD, kTmemCols = 512;
+  // Head size 64 leaves TMEM columns 384-511 free: S^T is double-buffered
+  // there and issued a step ahead (see the issuer).
+  static constexpr bool kDblS = (HD == 64);
+  static constexpr uint32_t kTmemS2 = 384;
+  static_assert(!kDblS || kTmemDV + HD <= kTmemS2, "second score buffer overlaps the gradient accumulators");
   static_assert(kSmemBytes <= 232448, "dK/dV kernel exceeds the 227 KB shared-memory limit");
 };
 
 struct DkdvBarriers {
   uint64_t kv_full, acc_done, drain, staged;
   uint64_t qdo_full[4], qdo_empty[4];
-  uint64_t s_full, dp_full, p_full[2], ds_full;
+  // p_full[2 * b + h]: half h of P^T of the steps using score buffer b
+  // (head size 128: b = 0 only).  With the scores a step ahead, the
+  // elementwise groups can finish P^T(n+1) before the issuer has waited for
+  // P^T(n); one barrier per buffer keeps each wait within one phase.
+  uint64_t s_full[2], dp_full, p_full[4], ds_full;
   uint32_t tmem_base;
   int abort;
 };
@@ -204,10 +213,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->qdo_empty[i]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->s_full[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->dp_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->p_full[0]), 8);
-    ptx::mbar_init(ptx::smem_u32(&bars->p_full[1]), 8);
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(ptx::smem_u32(&bars->p_full[i]), 8);
     ptx::mbar_init(ptx::smem_u32(&bars->ds_full), 8);
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -305,24 +314,37 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ptx::mma_commit_w(ptx::smem_u32(&bars->qdo_empty[ms]));
         return true;
       };
-      // Issue order S^T(n), dK(n-1), dP^T(n), dV(n): the tensor core works on
-      // dK(n-1) and dP^T(n) while the elementwise groups turn S^T(n) into
-      // P^T(n), and on dV(n) and S^T(n+1) while they form dS^T(n).  dP^T(n)
-      // overwrites dS^T(n-1) after dK(n-1) has been issued, S^T(n+1)
-      // overwrites P^T(n) after dV(n): MMAs from one thread run in order.
-      for (int n = 0; n < n_steps && ok; ++n) {
+      // S^T(n) into its score buffer, once Q_n landed.
+      auto sbuf = [&](int n) -> uint32_t { return (Cfg::kDblS && (n & 1)) ? Cfg::kTmemS2 : Cfg::kTmemS; };
+      auto issue_s = [&](int n) -> bool {
         const int qs = n % NQS;
-        ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs);
-        if (!ok) break;
+        if (!ptx::mbar_wait_all(ptx::smem_u32(&bars->qdo_full[qs]), (n / NQS) & 1, abort_flag, kWaitLimitNs))
+          return false;
         ptx::tc_fence_after();
-        const uint64_t bq = ptx::desc_advance(dQk, qs * Cfg::kQTile), bdo = ptx::desc_advance(dDOk, qs * Cfg::kQTile);
+        const uint64_t bq = ptx::desc_advance(dQk, qs * Cfg::kQTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * Cfg::kAtom + (kk & 3) * 32;
-          ptx::mma_bf16_ss_w(tmem + Cfg::kTmemS, ptx::desc_advance(dK, off), ptx::desc_advance(bq, off), idesc_s,
-                           kk > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss_w(tmem + sbuf(n), ptx::desc_advance(dK, off), ptx::desc_advance(bq, off), idesc_s,
+                             kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full));
+        ptx::mma_commit_w(ptx::smem_u32(&bars->s_full[Cfg::kDblS ? (n & 1) : 0]));
+        return true;
+      };
+      // Issue order S^T(n), dK(n-1), dP^T(n), dV(n) (head size 128), or with
+      // the scores a step ahead in two buffers S^T(n+1), dK(n-1), dP^T(n),
+      // dV(n) (head size 64, whose shorter MMAs would leave the tensor core
+      // idle while P^T(n) is formed): the tensor core works on dK(n-1) and
+      // dP^T(n) while the elementwise groups turn S^T(n) into P^T(n), and on
+      // dV(n) and the next scores while they form dS^T(n).  dP^T(n)
+      // overwrites dS^T(n-1) after dK(n-1) has been issued, and a score MMA
+      // overwrites P^T of the step that last used its buffer after that
+      // step's dV: MMAs from one thread run in order.
+      if (Cfg::kDblS) ok = ok && issue_s(0);
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int qs = n % NQS;
+        if (!(ok = Cfg::kDblS ? (n + 1 >= n_steps || issue_s(n + 1)) : issue_s(n))) break;
+        const uint64_t bdo = ptx::desc_advance(dDOk, qs * Cfg::kQTile);
         if (n > 0 && !(ok = issue_dk(n - 1))) break;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -337,12 +359,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         const uint64_t gdo = ptx::desc_advance(dDOm, qs * Cfg::kQTile);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full[hh]), n & 1, abort_flag, kWaitLimitNs))) break;
+          const int pb = Cfg::kDblS ? (n & 1) : 0;
+          if (!(ok = ptx::mbar_wait_all(ptx::smem_u32(&bars->p_full[2 * pb + hh]), Cfg::kDblS ? (n >> 1) & 1 : n & 1,
+                                        abort_flag, kWaitLimitNs)))
+            break;
           ptx::tc_fence_after();
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int kk = (i >> 1) * 4 + hh * 2 + (i & 1);
-            ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDV, tmem + Cfg::kTmemS + pair_col(kk),
+            ptx::mma_bf16_ts_w(tmem + Cfg::kTmemDV, tmem + sbuf(n) + pair_col(kk),
                                ptx::desc_advance(gdo, kk * 2048), idesc_g, (n > 0 || kk > 0) ? 1u : 0u);
           }
         }
@@ -363,7 +388,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int row = quarter * 32 + lane;           // key row within the tile
     const int ks = j * 128 + row;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t t_s = t_lane + Cfg::kTmemS + 64 * wg, t_dp = t_lane + Cfg::kTmemDP + 64 * wg;
+    const uint32_t t_dp = t_lane + Cfg::kTmemDP + 64 * wg;
     const float sl2 = g.scale * kLog2e;
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
@@ -379,7 +404,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       float4 Lw[2];
       // s_full(n) also means the step's loads (table included) have landed:
       // the issuer waited for them before the score MMAs.
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full), n & 1, abort_flag, kWaitLimitNs));
+      const int sb = Cfg::kDblS ? (n & 1) : 0;
+      const uint32_t t_s = t_lane + (sb ? Cfg::kTmemS2 : Cfg::kTmemS) + 64 * wg;
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&bars->s_full[sb]), Cfg::kDblS ? (n >> 1) & 1 : n & 1,
+                                                  abort_flag, kWaitLimitNs));
       if (!ok) break;
       ptx::tc_fence_after();
       Lw[0] = lse4[0];
@@ -414,7 +442,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[half]));
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[2 * sb + half]));
       }
       // ---- dS^T = P^T * (dP^T - D), while dV is accumulated.
       Lw[0] = d4[0];
