@@ -564,6 +564,8 @@ struct DqCfg {
 
 struct DqBarriers {
   uint64_t q_full[2], do_full, do_empty, drain;
+  // v_empty: V stage free (a ring of more than one stage; with one stage the
+  // producer waits for dp_full instead, dP being V's only reader).
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, ds_full;
   uint64_t acc_done[2], dq_free[2], staged, stage_free[2];
@@ -713,8 +715,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             do_issued = it + 1;
           }
           const int vs = gi % NVS, vu = gi / NVS;
-          if (vu > 0 && !(ok = ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), (vu - 1) & 1, abort_flag,
-                                              kWaitLimitNs)))
+          // One V stage: dP(gi-1), its only reader, has completed once
+          // dp_full has (dP(gi) cannot complete before V(gi) is loaded).
+          if (vu > 0 && !(ok = (NVS == 1 ? ptx::mbar_wait(ptx::smem_u32(&bars->dp_full), (gi - 1) & 1, abort_flag,
+                                                          kWaitLimitNs)
+                                         : ptx::mbar_wait(ptx::smem_u32(&bars->v_empty[vs]), (vu - 1) & 1, abort_flag,
+                                                          kWaitLimitNs))))
             break;
           const uint32_t vf = ptx::smem_u32(&bars->v_full[vs]);
           ptx::mbar_arrive_expect_tx(vf, Cfg::kKTile);
@@ -841,7 +847,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                              kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit_w(ptx::smem_u32(&bars->dp_full));
-          ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[vs]));
+          if (NVS > 1) ptx::mma_commit_w(ptx::smem_u32(&bars->v_empty[vs]));
           if (n == n_steps - 1) ptx::mma_commit_w(ptx::smem_u32(&bars->do_empty));
           p_g = gi;
           p_it = it;
