@@ -1,0 +1,309 @@
+"""Discrete-event model of the mbarrier protocols of the tcgen05 backward
+kernels (csrc/attn_bwd_sm103.cu), used by test_barrier_protocols.py.
+
+Each role of a CTA (TMA producer, MMA issuer, elementwise warps) is a
+generator that yields requests; a seeded scheduler interleaves them at
+random, the tensor pipe executes queued MMAs in issue order, TMA copies land
+in any order.  Hazard assertions check every read against the writes it
+depends on, and every barrier wait is checked the way the hardware performs
+it: a wait for a barrier's n-th completion is a parity test, which is only
+exact when the barrier has completed n-1 or n times so far.
+
+Requests:
+  ('wait', bar, n)      block until bar has completed n+1 phases
+  ('arrive', bar)       one arrival
+  ('mma', label, fn)    queue work on the in-order tensor pipe (fn runs then)
+  ('commit', bar)       queue one arrival behind the queued MMAs
+  ('tma', bar, fn)      a copy: fn runs when it lands, then one arrival on bar
+"""
+import random
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.phase = name, count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, f"over-arrival on {self.name}"
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+
+class Deadlock(Exception):
+    pass
+
+
+class Sim:
+    def __init__(self, seed):
+        self.rng = random.Random(seed)
+        self.roles, self.pipe, self.tma = {}, [], []
+
+    def add(self, name, gen):
+        self.roles[name] = [gen, None]
+
+    @staticmethod
+    def _ready(req):
+        _, bar, n = req
+        assert bar.phase <= n + 1, f"{bar.name}: wait for completion {n} sees {bar.phase} (parity ambiguous)"
+        assert bar.phase >= n, f"{bar.name}: wait for completion {n} sees {bar.phase} (parity wait passes early)"
+        return bar.phase > n
+
+    def _step(self, name):
+        st = self.roles[name]
+        gen, req = st
+        if req is not None:
+            if not self._ready(req):
+                return False
+            st[1] = None
+        while True:
+            try:
+                r = next(gen)
+            except StopIteration:
+                del self.roles[name]
+                return True
+            if r[0] == 'wait':
+                if self._ready(r):
+                    continue
+                st[1] = r
+                return True
+            if r[0] == 'arrive':
+                r[1].arrive()
+            elif r[0] in ('mma', 'commit'):
+                self.pipe.append(r)
+            elif r[0] == 'tma':
+                self.tma.append(r)
+            if self.rng.random() < 0.3:
+                return True
+
+    def run(self, max_iter=10 ** 6):
+        for _ in range(max_iter):
+            opts = list(self.roles) + (['@pipe'] if self.pipe else []) + (['@tma'] if self.tma else [])
+            if not opts:
+                return
+            self.rng.shuffle(opts)
+            progressed = False
+            for o in opts:
+                if o == '@pipe':
+                    r = self.pipe.pop(0)
+                    if r[0] == 'mma':
+                        r[2]()
+                    else:
+                        r[1].arrive()
+                    progressed = True
+                elif o == '@tma':
+                    r = self.tma.pop(self.rng.randrange(len(self.tma)))
+                    r[2]()
+                    r[1].arrive()
+                    progressed = True
+                elif self._step(o):
+                    progressed = True
+                if progressed:
+                    break
+            if not progressed:
+                raise Deadlock({n: (r[1][1].name, r[1][2]) for n, r in self.roles.items() if r[1]})
+        raise RuntimeError("no termination")
+
+
+def dkdv_cta(seed, n_steps, double_scores=True, n_stages=4, p_barrier_per_buffer=True, release_by_dp=False):
+    """One CTA of bwd_dkdv_kernel: K/V once, then n_steps steps of a Q/dO ring
+    of n_stages stages.  double_scores: head size 64, S^T issued a step ahead
+    into two TMEM buffers (issue order S^T(n+1), dK(n-1), dP^T(n), dV(n));
+    else head size 128 (S^T(n), dK(n-1), dP^T(n), dV(n)).  The two flags after
+    it select variants that are not in the library (for the planted-mistake
+    checks): one P^T barrier pair for both buffers, and ring stages reloaded
+    on dp_full instead of their own release barrier."""
+    dbl = double_scores
+    sim = Sim(seed)
+    kv_full = Bar("kv_full", 1)
+    qdo_full = [Bar(f"qdo_full{i}", 1) for i in range(n_stages)]
+    qdo_empty = [Bar(f"qdo_empty{i}", 1) for i in range(n_stages)]
+    s_full = [Bar("s_full0", 1), Bar("s_full1", 1)]
+    dp_full, ds_full, acc_done = Bar("dp_full", 1), Bar("ds_full", 8), Bar("acc_done", 1)
+    nb = 2 if (dbl and p_barrier_per_buffer) else 1
+    p_full = [[Bar(f"p_full{b}{h}", 8) for h in range(2)] for b in range(nb)]
+    st = dict(q_land=[-1] * n_stages, s_exec=-1, dp_exec=-1, dv_exec=-1, dk_exec=-1,
+              s_read={w: -1 for w in range(8)}, p_wr={(w, h): -1 for w in range(8) for h in range(2)},
+              ds_wr={w: -1 for w in range(8)}, dp_read={w: -1 for w in range(8)})
+
+    def pbar(n, h):
+        b = (n & 1) if nb == 2 else 0
+        return p_full[b][h], ((n >> 1) if nb == 2 else n)
+
+    def producer():
+        yield ('tma', kv_full, lambda: None)
+        for n in range(n_steps):
+            s = n % n_stages
+            if n >= n_stages:
+                yield ('wait', dp_full, n - 1) if release_by_dp else ('wait', qdo_empty[s], n // n_stages - 1)
+
+            def land(n=n, s=s):
+                assert st['dk_exec'] >= n - n_stages, "ring stage reloaded before dK read it"
+                st['q_land'][s] = n
+            yield ('tma', qdo_full[s], land)
+
+    def issuer():
+        yield ('wait', kv_full, 0)
+
+        def issue_s(n):
+            s = n % n_stages
+            yield ('wait', qdo_full[s], n // n_stages)
+
+            def ex(n=n, s=s):
+                assert st['q_land'][s] == n
+                if dbl and n >= 2:
+                    assert st['dv_exec'] >= n - 2, "S^T overwrote P^T(n-2) before dV read it"
+                    assert all(v >= n - 2 for v in st['s_read'].values())
+                if not dbl and n >= 1:
+                    assert st['dv_exec'] >= n - 1, "S^T overwrote P^T(n-1) before dV read it"
+                st['s_exec'] = n
+            yield ('mma', 'S', ex)
+            yield ('commit', s_full[n & 1 if dbl else 0])
+
+        def issue_dk(m):
+            yield ('wait', ds_full, m)
+
+            def ex(m=m):
+                assert all(v >= m for v in st['ds_wr'].values()), "dK before dS^T written"
+                assert st['q_land'][m % n_stages] == m, "dK read a reloaded stage"
+                st['dk_exec'] = m
+            yield ('mma', 'dK', ex)
+            if not release_by_dp:
+                yield ('commit', qdo_empty[m % n_stages])
+
+        if dbl:
+            yield from issue_s(0)
+        for n in range(n_steps):
+            if dbl:
+                if n + 1 < n_steps:
+                    yield from issue_s(n + 1)
+            else:
+                yield from issue_s(n)
+            if n > 0:
+                yield from issue_dk(n - 1)
+
+            def exdp(n=n):
+                assert st['dk_exec'] >= n - 1, "dP^T overwrote dS^T(n-1) before dK read it"
+                assert all(v >= n - 1 for v in st['dp_read'].values())
+                assert st['q_land'][n % n_stages] == n
+                st['dp_exec'] = n
+            yield ('mma', 'dP', exdp)
+            yield ('commit', dp_full)
+            for h in range(2):
+                bar, k = pbar(n, h)
+                yield ('wait', bar, k)
+
+                def exdv(n=n, h=h):
+                    assert all(st['p_wr'][(w, h)] >= n for w in range(8)), "dV before P^T written"
+                    assert st['q_land'][n % n_stages] == n
+                    if h == 1:
+                        st['dv_exec'] = n
+                yield ('mma', 'dV', exdv)
+        yield from issue_dk(n_steps - 1)
+        yield ('commit', acc_done)
+
+    def elementwise(w):
+        for n in range(n_steps):
+            yield ('wait', s_full[n & 1 if dbl else 0], (n >> 1) if dbl else n)
+            assert st['s_exec'] >= n
+            st['s_read'][w] = n
+            for h in range(2):
+                st['p_wr'][(w, h)] = n
+                yield ('arrive', pbar(n, h)[0])
+            yield ('wait', dp_full, n)
+            assert st['dp_exec'] >= n
+            st['dp_read'][w] = n
+            st['ds_wr'][w] = n
+            yield ('arrive', ds_full)
+        yield ('wait', acc_done, 0)
+        assert st['dk_exec'] == n_steps - 1 and st['dv_exec'] == n_steps - 1
+
+    sim.add('producer', producer())
+    sim.add('issuer', issuer())
+    for w in range(8):
+        sim.add(f'ew{w}', elementwise(w))
+    sim.run()
+
+
+def dq_rings(seed, steps, k_stages=3):
+    """The K and V rings of bwd_dq_kernel at head size 128 for one item: K in
+    k_stages stages released after the dQ MMA that reads it last; V in one
+    stage, reloaded once dp_full shows dP (V's only reader) complete."""
+    sim = Sim(seed)
+    k_full = [Bar(f"k_full{i}", 1) for i in range(k_stages)]
+    k_empty = [Bar(f"k_empty{i}", 1) for i in range(k_stages)]
+    v_full = Bar("v_full", 1)
+    s_full, s_free, dp_full, ds_full = Bar("s_full", 1), Bar("s_free", 8), Bar("dp_full", 1), Bar("ds_full", 8)
+    st = dict(k_land=[-1] * k_stages, v_land=-1, s_exec=-1, dp_exec=-1, dq_exec=-1,
+              s_read={w: -1 for w in range(8)}, ds_wr={w: -1 for w in range(8)})
+
+    def producer():
+        for g in range(steps):
+            s = g % k_stages
+            if g >= k_stages:
+                yield ('wait', k_empty[s], g // k_stages - 1)
+
+            def lk(g=g, s=s):
+                assert st['dq_exec'] >= g - k_stages, "K stage reloaded before dQ read it"
+                st['k_land'][s] = g
+            yield ('tma', k_full[s], lk)
+            if g >= 1:
+                yield ('wait', dp_full, g - 1)
+
+            def lv(g=g):
+                assert st['dp_exec'] >= g - 1, "V reloaded before dP read it"
+                st['v_land'] = g
+            yield ('tma', v_full, lv)
+
+    def issuer():
+        def dq(m):
+            yield ('wait', ds_full, m)
+
+            def ex(m=m):
+                assert all(v >= m for v in st['ds_wr'].values())
+                assert st['k_land'][m % k_stages] == m
+                st['dq_exec'] = m
+            yield ('mma', 'dQ', ex)
+            yield ('commit', k_empty[m % k_stages])
+
+        for g in range(steps):
+            s = g % k_stages
+            yield ('wait', k_full[s], g // k_stages)
+            if g > 0:
+                yield ('wait', s_free, g - 1)
+
+            def exs(g=g, s=s):
+                assert st['k_land'][s] == g
+                assert all(v >= g - 1 for v in st['s_read'].values())
+                st['s_exec'] = g
+            yield ('mma', 'S', exs)
+            yield ('commit', s_full)
+            if g > 0:
+                yield from dq(g - 1)
+            yield ('wait', v_full, g)
+
+            def exdp(g=g):
+                assert st['v_land'] == g
+                assert st['dq_exec'] >= g - 1, "dP overwrote dS before dQ read it"
+                st['dp_exec'] = g
+            yield ('mma', 'dP', exdp)
+            yield ('commit', dp_full)
+        yield from dq(steps - 1)
+
+    def elementwise(w):
+        for g in range(steps):
+            yield ('wait', s_full, g)
+            assert st['s_exec'] >= g
+            st['s_read'][w] = g
+            yield ('arrive', s_free)
+            yield ('wait', dp_full, g)
+            assert st['dp_exec'] >= g
+            st['ds_wr'][w] = g
+            yield ('arrive', ds_full)
+
+    sim.add('producer', producer())
+    sim.add('issuer', issuer())
+    for w in range(8):
+        sim.add(f'ew{w}', elementwise(w))
+    sim.run()
