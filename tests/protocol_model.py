@@ -1,5 +1,6 @@
-"""Discrete-event model of the mbarrier protocols of the tcgen05 backward
-kernels (csrc/attn_bwd_sm103.cu), used by test_barrier_protocols.py.
+"""Discrete-event model of the mbarrier protocols of the tcgen05 kernels
+(csrc/attn_fwd2_sm103.cu, csrc/attn_bwd_sm103.cu), used by
+test_barrier_protocols.py.
 
 Each role of a CTA (TMA producer, MMA issuer, elementwise warps) is a
 generator that yields requests; a seeded scheduler interleaves them at
@@ -306,4 +307,148 @@ def dq_rings(seed, steps, k_stages=3):
     sim.add('issuer', issuer())
     for w in range(8):
         sim.add(f'ew{w}', elementwise(w))
+    sim.run()
+
+
+def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
+    """One CTA of the paired-head forward (fwd2_kernel, two query heads
+    sharing each K/V tile): `items` lists the key tiles of each work item.
+    Roles: producer (Q of an item after the previous item's last score MMA;
+    K and V of a tile into a two-stage ring), issuer (S_A(0), S_B(0), then per
+    tile PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)), four softmax warps per head
+    (P written over the scores; O rescaled between PVs) and each head's
+    epilogue through the one staging tile.  The two flags drop waits of the
+    library's protocol (planted-mistake checks).  The model shows the o_free
+    wait to be implied by p_full: a head's softmax warps read O in the
+    epilogue before they arrive on p_full for the next item's first tile,
+    and that first PV waits for p_full."""
+    sim = Sim(seed)
+    q_full, q_empty = Bar("q_full", 1), Bar("q_empty", 1)
+    kv_full = [Bar("kv_full0", 1), Bar("kv_full1", 1)]
+    kv_empty = [Bar("kv_empty0", 1), Bar("kv_empty1", 1)]
+    s_full = [Bar("s_full0", 1), Bar("s_full1", 1)]
+    p_full = [Bar("p_full0", 4), Bar("p_full1", 4)]
+    o_done = [Bar("o_done0", 1), Bar("o_done1", 1)]
+    o_free = [Bar("o_free0", 4), Bar("o_free1", 4)]
+    staged = [Bar("staged0", 4), Bar("staged1", 4)]
+    stage_free = Bar("stage_free", 1)
+    store_read = [Bar("store_read0", 1), Bar("store_read1", 1)]   # a storer's own wait on its copy
+    tiles = [(it, j, n) for it, n in enumerate(items) for j in range(n)]
+    first = {}
+    for gk, (it, j, n) in enumerate(tiles):
+        first.setdefault(it, gk)
+    st = dict(q_land=-1, kv_land=[-1, -1], s_exec=[-1, -1], pv_exec=[-1, -1], s_read={}, p_wr={},
+              o_read={}, stage_use=-1, store_read=-1)
+    for x in range(2):
+        for w in range(4):
+            st['s_read'][(x, w)] = -1
+            st['p_wr'][(x, w)] = -1
+            st['o_read'][(x, w)] = -1
+
+    def producer():
+        gk = 0
+        for it, n in enumerate(items):
+            if it >= 1:
+                yield ('wait', q_empty, it - 1)
+
+            def lq(it=it):
+                assert all(v >= first[it - 1] + items[it - 1] - 1 for v in st['s_exec']) if it >= 1 else True, \
+                    "Q reloaded before the last score MMAs read it"
+                st['q_land'] = it
+            yield ('tma', q_full, lq)
+            for j in range(n):
+                s = gk % 2
+                if gk >= 2:
+                    yield ('wait', kv_empty[s], (gk >> 1) - 1)
+
+                def lkv(gk=gk, s=s):
+                    assert min(st['pv_exec']) >= gk - 2, "K/V stage reloaded before the PVs read it"
+                    st['kv_land'][s] = gk
+                yield ('tma', kv_full[s], lkv)
+                gk += 1
+
+    def issuer():
+        def issue_s(x, gk, it):
+            def ex(x=x, gk=gk, it=it):
+                assert st['q_land'] == it and st['kv_land'][gk % 2] == gk
+                assert st['pv_exec'][x] >= gk - 1, "S overwrote P before the PV read it"
+                assert all(st['s_read'][(x, w)] >= gk - 1 for w in range(4))
+                st['s_exec'][x] = gk
+            yield ('mma', f'S{x}', ex)
+            yield ('commit', s_full[x])
+
+        g0 = 0
+        for it, n in enumerate(items):
+            yield ('wait', q_full, it)
+            yield ('wait', kv_full[g0 % 2], g0 >> 1)
+            yield from issue_s(0, g0, it)
+            yield from issue_s(1, g0, it)
+            if n == 1:
+                yield ('commit', q_empty)
+            for j in range(n):
+                gk = g0 + j
+                for x in range(2):
+                    yield ('wait', p_full[x], gk)
+                    if j == 0 and it >= 1 and wait_o_free:
+                        yield ('wait', o_free[x], it - 1)
+
+                    def expv(x=x, gk=gk, j=j, it=it):
+                        assert all(st['p_wr'][(x, w)] >= gk for w in range(4)), "PV before P written"
+                        assert st['kv_land'][gk % 2] == gk
+                        if j == 0 and it >= 1:
+                            assert all(st['o_read'][(x, w)] >= it - 1 for w in range(4)), \
+                                "PV overwrote O before the epilogue read it"
+                        st['pv_exec'][x] = gk
+                    yield ('mma', f'PV{x}', expv)
+                    if x == 1:
+                        yield ('commit', kv_empty[gk % 2])
+                    if j == n - 1:
+                        yield ('commit', o_done[x])
+                    if j + 1 < n:
+                        if x == 0:
+                            yield ('wait', kv_full[(gk + 1) % 2], (gk + 1) >> 1)
+                        yield from issue_s(x, gk + 1, it)
+                        if x == 1 and j + 1 == n - 1:
+                            yield ('commit', q_empty)
+            g0 += n
+
+    def softmax(x, w):
+        gk = 0
+        for it, n in enumerate(items):
+            for j in range(n):
+                yield ('wait', s_full[x], gk)
+                assert st['s_exec'][x] >= gk
+                # the O rescale of tile j: PV_x(j-1) has completed, PV_x(j) waits for this warp
+                assert st['pv_exec'][x] == gk - 1 or (j == 0 and st['pv_exec'][x] < gk), "O rescaled under a PV"
+                st['s_read'][(x, w)] = gk
+                st['p_wr'][(x, w)] = gk
+                yield ('arrive', p_full[x])
+                gk += 1
+            use = 2 * it + x
+            yield ('wait', o_done[x], it)
+            if use > 0 and wait_stage_free:
+                yield ('wait', stage_free, use - 1)
+            assert st['pv_exec'][x] >= gk - 1
+            assert st['store_read'] >= use - 1, "staging tile rewritten before its store read it"
+            st['o_read'][(x, w)] = it
+            st['stage_use'] = use
+            yield ('arrive', o_free[x])
+            yield ('arrive', staged[x])
+            if w == 0:
+                # The group's first warp stores the tile and waits until the
+                # copy engine has read it (bulk wait_group.read) before
+                # releasing the staging tile.
+                yield ('wait', staged[x], it)
+
+                def read(use=use):
+                    st['store_read'] = use
+                yield ('tma', store_read[x], read)
+                yield ('wait', store_read[x], it)
+                yield ('arrive', stage_free)
+
+    sim.add('producer', producer())
+    sim.add('issuer', issuer())
+    for x in range(2):
+        for w in range(4):
+            sim.add(f'sm{x}{w}', softmax(x, w))
     sim.run()

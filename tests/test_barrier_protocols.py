@@ -1,5 +1,6 @@
 """The barrier protocols of the tcgen05 backward kernels, checked in a
-discrete-event model (protocol_model.py) over randomised interleavings: the
+discrete-event model (protocol_model.py) over randomised interleavings (the
+paired-head forward and the backward kernels): the
 committed issue orders pass every hazard and parity check, and the planted
 mistakes (protocol variants that are not in the library) are caught."""
 import pytest
@@ -46,3 +47,20 @@ def test_planted_ring_release_on_dp_full():
     dp_full's second completion before its first can be seen (the order that
     faulted the GPU)."""
     assert all(_fails(lambda s=s: dkdv_cta(s, 6, False, 2, release_by_dp=True)) for s in range(20))
+
+
+def test_paired_forward_protocol():
+    import random
+
+    from protocol_model import fwd_pair_cta
+    for seed in range(150):
+        rng = random.Random(seed)
+        items = [rng.randint(1, 5) for _ in range(rng.randint(1, 4))]
+        fwd_pair_cta(seed, items)
+
+
+def test_planted_forward_staging_without_release_wait():
+    """The two heads share one staging tile: without the wait for the previous
+    store to have read it, a head overwrites the tile under the copy."""
+    from protocol_model import fwd_pair_cta
+    assert any(_fails(lambda s=s: fwd_pair_cta(s, [2, 2, 3, 1], wait_stage_free=False)) for s in range(100))
