@@ -1,8 +1,8 @@
-"""The barrier protocols of the tcgen05 backward kernels, checked in a
-discrete-event model (protocol_model.py) over randomised interleavings (the
-paired-head forward and the backward kernels): the
-committed issue orders pass every hazard and parity check, and the planted
-mistakes (protocol variants that are not in the library) are caught."""
+"""The barrier protocols of the tcgen05 kernels (the paired-head forward, the
+dK/dV and dQ kernels), checked in a discrete-event model (protocol_model.py)
+over randomised interleavings: the committed issue orders pass every hazard
+and parity check, and the planted mistakes (protocol variants that are not in
+the library) are caught."""
 import pytest
 
 from protocol_model import dkdv_cta, dq_rings
