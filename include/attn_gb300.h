@@ -295,7 +295,9 @@ ATTN_API int attn_decode(void* out, float* lse, const void* q, const void* k_cac
  *   qkv [B*T, (NH+2*NKV)*hd] bf16, written.
  * hd must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).  All pointers
  * 16-byte aligned; a copy handed to attn_fwd_rot / attn_bwd_rot must be
- * 256-byte aligned.  Asynchronous on `stream`; deterministic.
+ * 256-byte aligned.  Asynchronous on `stream`; deterministic.  The kernel
+ * runs on clusters of two CTAs (one per SM); ATTN_ERR_CUDA if the device
+ * cannot hold such a cluster.
  *
  * attn_fwd_rot -- attn_fwd (bf16 with RoPE) reading the rotated Q/K from
  * qk_rot (made by attn_qkv_proj or attn_fwd_ws on the same qkv) instead of
