@@ -152,8 +152,9 @@ def test_no_device_errors_recorded(lib):
 @pytest.mark.parametrize("dtype,theta,fwd_ws", [("bf16", 1e6, True), ("bf16", 0.0, False), ("f32", 1e6, False)])
 def test_cuda_graph_capture_replays_identically(lib, dtype, theta, fwd_ws):
     """A forward + backward captured into a CUDA graph (the launch-overhead
-    remedy for small problems) replays bit-identically to eager calls: no
-    entry point synchronises, allocates or reads host state on the stream."""
+    remedy for small problems) replays bit-identically to eager calls: none of
+    these four entry points synchronises, allocates or reads host state on the
+    stream."""
     import torch
     w = shape_workload(2, 200, 1024 if dtype == "bf16" else 128, 8, 2, theta, seed=51)
     qkv_np, dout_np = make_inputs(w, dtype)
