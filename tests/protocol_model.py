@@ -16,6 +16,10 @@ Requests:
   ('mma', label, fn)    queue work on the in-order tensor pipe (fn runs then)
   ('commit', bar)       queue one arrival behind the queued MMAs
   ('tma', bar, fn)      a copy: fn runs when it lands, then one arrival on bar
+  ('tma', bar, fn, b)   a copy that completes b bytes of bar's transaction count
+  ('arrive_tx', bar, b) one arrival that first expects b more bytes
+A commit may name a tuple of barriers (a multicast commit: one arrival on
+each).
 """
 import random
 
@@ -30,6 +34,33 @@ class Bar:
         if self.pending == 0:
             self.phase += 1
             self.pending = self.count
+
+
+class TxBar(Bar):
+    """A barrier whose phase also waits for a transaction count (bytes
+    expected by arrive_tx, completed by copies) to return to zero; copies may
+    complete bytes before they are expected (the count goes negative)."""
+
+    def __init__(self, name, count):
+        super().__init__(name, count)
+        self.tx = 0
+
+    def _flip(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, f"over-arrival on {self.name}"
+        self._flip()
+
+    def expect(self, nbytes):
+        self.tx += nbytes
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        self._flip()
 
 
 class Deadlock(Exception):
@@ -71,6 +102,9 @@ class Sim:
                 return True
             if r[0] == 'arrive':
                 r[1].arrive()
+            elif r[0] == 'arrive_tx':
+                r[1].expect(r[2])
+                r[1].arrive()
             elif r[0] in ('mma', 'commit'):
                 self.pipe.append(r)
             elif r[0] == 'tma':
@@ -91,12 +125,16 @@ class Sim:
                     if r[0] == 'mma':
                         r[2]()
                     else:
-                        r[1].arrive()
+                        for b in (r[1] if isinstance(r[1], tuple) else (r[1],)):
+                            b.arrive()
                     progressed = True
                 elif o == '@tma':
                     r = self.tma.pop(self.rng.randrange(len(self.tma)))
                     r[2]()
-                    r[1].arrive()
+                    if len(r) == 4:
+                        r[1].complete_tx(r[3])
+                    else:
+                        r[1].arrive()
                     progressed = True
                 elif self._step(o):
                     progressed = True
@@ -451,4 +489,108 @@ def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
     for x in range(2):
         for w in range(4):
             sim.add(f'sm{x}{w}', softmax(x, w))
+    sim.run()
+
+
+def proj_pair(seed, n_tiles, n_kb, n_stages=3, expect_both=True, acc_empty_wait=True, peer_empty_wait=True):
+    """One CTA pair of the QKV projection (proj_kernel, tcgen05.mma.cta_group::2):
+    n_tiles output tiles of n_kb k-blocks each, a ring of n_stages stages in
+    each CTA.  Each CTA's producer copies its half of a stage (two copies of
+    16 KB) and signals the first CTA's stage barrier, on which the first
+    CTA's producer also expects the bytes of both halves; the first CTA's
+    issuer runs the MMAs (reading both CTAs' stages, writing both CTAs'
+    accumulators) and commits stage release, accumulator full and the final
+    drain to both CTAs' barriers at once; both CTAs' four epilogue warps
+    release an accumulator on the first CTA's barrier (count 8).  The issuer
+    tests the next stage's barrier one k-block ahead (the same parity check,
+    without blocking).  After every role has finished (the final cluster
+    barrier) no MMA or copy may still be in flight.  The flags drop parts of
+    the protocol (planted-mistake checks): the first CTA expecting one CTA's
+    bytes, the issuer not waiting for the accumulator's release, the second
+    CTA's producer not waiting for its stage's release."""
+    sim = Sim(seed)
+    half = 2 * 16384
+    full = [TxBar(f"full{i}", 1) for i in range(n_stages)]             # first CTA's
+    empty = [[Bar(f"empty{r}{i}", 1) for i in range(n_stages)] for r in range(2)]
+    acc_full = [[Bar(f"acc_full{r}{b}", 1) for b in range(2)] for r in range(2)]
+    acc_empty = [Bar(f"acc_empty{b}", 8) for b in range(2)]           # first CTA's
+    drain = [Bar(f"drain{r}", 1) for r in range(2)]
+    done = Bar("done", 2 + 1 + 1 + 8)
+    st = dict(land=[[-1] * n_stages for _ in range(2)], mma_exec=-1,
+              acc_tile=[-1, -1], acc_read={(r, w): -1 for r in range(2) for w in range(4)})
+
+    def producer(r):
+        for it in range(n_tiles * n_kb):
+            s, u = it % n_stages, it // n_stages
+            if u > 0 and (r == 0 or peer_empty_wait):
+                yield ('wait', empty[r][s], u - 1)
+            if r == 0:
+                yield ('arrive_tx', full[s], 2 * half if expect_both else half)
+
+            def land(it=it, s=s, r=r):
+                assert st['mma_exec'] >= it - n_stages, "stage overwritten before the MMAs read it"
+                st['land'][r][s] = it
+            # The two copies (x rows, w rows) of this CTA's half; the first
+            # one's landing is folded into the second's bytes.
+            yield ('tma', full[s], lambda: None, half // 2)
+            yield ('tma', full[s], land, half // 2)
+        yield ('arrive', done)
+
+    def issuer():
+        def test(bar, n):
+            return Sim._ready(('wait', bar, n))
+        it = 0
+        for lt in range(n_tiles):
+            b = lt & 1
+            if lt >= 2 and acc_empty_wait:
+                yield ('wait', acc_empty[b], (lt >> 1) - 1)
+            ready = test(full[it % n_stages], it // n_stages)
+            for kb in range(n_kb):
+                s, u = it % n_stages, it // n_stages
+                if not ready:
+                    yield ('wait', full[s], u)
+                ready = test(full[(it + 1) % n_stages], (it + 1) // n_stages) if kb + 1 < n_kb else True
+
+                def ex(it=it, s=s, lt=lt, kb=kb, b=b):
+                    assert st['land'][0][s] == it and st['land'][1][s] == it, "MMA before both halves landed"
+                    if kb == 0:
+                        assert all(v >= lt - 2 for v in st['acc_read'].values()), \
+                            "accumulator overwritten before both epilogues read it"
+                    st['mma_exec'] = it
+                    if kb == n_kb - 1:
+                        st['acc_tile'][b] = lt
+                yield ('mma', 'MMA', ex)
+                yield ('commit', (empty[0][s], empty[1][s]))
+                it += 1
+            yield ('commit', (acc_full[0][b], acc_full[1][b]))
+        yield ('commit', (drain[0], drain[1]))
+        yield ('wait', drain[0], 0)
+        yield ('arrive', done)
+
+    def tmem_warp_peer():
+        yield ('wait', drain[1], 0)
+        yield ('arrive', done)
+
+    def epilogue(r, w):
+        for lt in range(n_tiles):
+            b = lt & 1
+            yield ('wait', acc_full[r][b], lt >> 1)
+            assert st['acc_tile'][b] == lt, "epilogue read an accumulator the MMAs had not finished"
+            st['acc_read'][(r, w)] = lt
+            yield ('arrive', acc_empty[b])
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "pair released its memory with MMAs or copies in flight"
+        assert st['mma_exec'] == n_tiles * n_kb - 1
+
+    for r in range(2):
+        sim.add(f'producer{r}', producer(r))
+    sim.add('issuer', issuer())
+    sim.add('tmem1', tmem_warp_peer())
+    for r in range(2):
+        for w in range(4):
+            sim.add(f'epi{r}{w}', epilogue(r, w))
+    sim.add('teardown', teardown())
     sim.run()

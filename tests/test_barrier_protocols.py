@@ -1,5 +1,5 @@
 """The barrier protocols of the tcgen05 kernels (the paired-head forward, the
-dK/dV and dQ kernels), checked in a discrete-event model (protocol_model.py)
+dK/dV and dQ kernels, the QKV projection on CTA pairs), checked in a discrete-event model (protocol_model.py)
 over randomised interleavings: the committed issue orders pass every hazard
 and parity check, and the planted mistakes (protocol variants that are not in
 the library) are caught."""
@@ -64,3 +64,31 @@ def test_planted_forward_staging_without_release_wait():
     store to have read it, a head overwrites the tile under the copy."""
     from protocol_model import fwd_pair_cta
     assert any(_fails(lambda s=s: fwd_pair_cta(s, [2, 2, 3, 1], wait_stage_free=False)) for s in range(100))
+
+
+@pytest.mark.parametrize("n_tiles,n_kb,n_stages", [(1, 1, 2), (2, 3, 2), (3, 4, 3), (5, 2, 6), (6, 1, 6), (4, 7, 6)])
+def test_projection_pair_protocol(n_tiles, n_kb, n_stages):
+    from protocol_model import proj_pair
+    for seed in SEEDS:
+        proj_pair(seed, n_tiles, n_kb, n_stages)
+
+
+def test_planted_projection_expects_one_half():
+    """A stage barrier that expects one CTA's bytes completes on the first
+    half to land: the pair's MMA then reads the other CTA's stale half."""
+    from protocol_model import proj_pair
+    assert any(_fails(lambda s=s: proj_pair(s, 4, 3, 2, expect_both=False)) for s in range(100))
+
+
+def test_planted_projection_accumulator_not_released():
+    """Without the wait for both CTAs' epilogues, the MMAs of tile n+2 write
+    the accumulator that tile n is still being read from."""
+    from protocol_model import proj_pair
+    assert any(_fails(lambda s=s: proj_pair(s, 6, 1, 6, acc_empty_wait=False)) for s in range(100))
+
+
+def test_planted_projection_peer_ignores_stage_release():
+    """The second CTA's copies must wait for the multicast stage release too:
+    its half is read by MMAs that the first CTA issues."""
+    from protocol_model import proj_pair
+    assert any(_fails(lambda s=s: proj_pair(s, 4, 3, 2, peer_empty_wait=False)) for s in range(100))
