@@ -1,6 +1,6 @@
 """Discrete-event model of the mbarrier protocols of the tcgen05 kernels
-(csrc/attn_fwd2_sm103.cu, csrc/attn_bwd_sm103.cu), used by
-test_barrier_protocols.py.
+(csrc/attn_fwd2_sm103.cu, csrc/attn_bwd_sm103.cu, csrc/attn_proj_sm103.cu),
+used by test_barrier_protocols.py.
 
 Each role of a CTA (TMA producer, MMA issuer, elementwise warps) is a
 generator that yields requests; a seeded scheduler interleaves them at
@@ -18,6 +18,8 @@ Requests:
   ('tma', bar, fn)      a copy: fn runs when it lands, then one arrival on bar
   ('tma', bar, fn, b)   a copy that completes b bytes of bar's transaction count
   ('arrive_tx', bar, b) one arrival that first expects b more bytes
+  ('until', pred)       block until pred() holds (a wait that is not a
+                        barrier's, e.g. for every bulk store to have read)
 A commit may name a tuple of barriers (a multicast commit: one arrival on
 each).
 """
@@ -77,6 +79,8 @@ class Sim:
 
     @staticmethod
     def _ready(req):
+        if req[0] == 'until':
+            return req[1]()
         _, bar, n = req
         assert bar.phase <= n + 1, f"{bar.name}: wait for completion {n} sees {bar.phase} (parity ambiguous)"
         assert bar.phase >= n, f"{bar.name}: wait for completion {n} sees {bar.phase} (parity wait passes early)"
@@ -95,7 +99,7 @@ class Sim:
             except StopIteration:
                 del self.roles[name]
                 return True
-            if r[0] == 'wait':
+            if r[0] in ('wait', 'until'):
                 if self._ready(r):
                     continue
                 st[1] = r
@@ -592,5 +596,253 @@ def proj_pair(seed, n_tiles, n_kb, n_stages=3, expect_both=True, acc_empty_wait=
     for r in range(2):
         for w in range(4):
             sim.add(f'epi{r}{w}', epilogue(r, w))
+    sim.add('teardown', teardown())
+    sim.run()
+
+
+def dq_cta(seed, items, k_stages=3, v_stages=1, item_slots=4, wait_stage_free=True, wait_dq_free=True,
+           k_release_on_s=False):
+    """One persistent CTA of bwd_dq_kernel (head size 128: a 3-stage K ring and
+    a one-stage V ring; head size 64: 4 and 4): `items` lists the key steps of
+    each item the CTA claims.  Roles: the producer (claims items into a queue
+    of item_slots slots; K, V and the item's dO), the Q producer (Q of item
+    it into buffer it & 1 once the store of item it-2's dQ tile, staged in
+    that buffer, has read it), the MMA issuer (order S(n), dQ(n-1), dP(n);
+    two dQ accumulators, items alternating), and eight elementwise warps
+    (P from S, dS over dP in TMEM; the epilogue of an item after the next
+    item's first dS, staging dQ in the item's Q buffer; the first warp issues
+    the tile store and releases the buffer once the store has read it, at
+    its next dS arrival or the next item's start).  The flags change the
+    protocol (planted-mistake checks): the Q reload without the wait for the
+    store's read; the first dQ MMA of an item without the wait for the
+    epilogue two items back (which the model shows to be implied: every
+    elementwise warp runs that epilogue before its first dS arrival of the
+    next item but one, and the dQ MMA waits for that dS); the K stage
+    released after its score MMA instead of after its dQ MMA."""
+    sim = Sim(seed)
+    NKS, NVS, NIS = k_stages, v_stages, item_slots
+    q_full = [Bar("q_full0", 1), Bar("q_full1", 1)]
+    do_full, do_empty, drain = Bar("do_full", 1), Bar("do_empty", 1), Bar("drain", 1)
+    k_full = [Bar(f"k_full{i}", 1) for i in range(NKS)]
+    k_empty = [Bar(f"k_empty{i}", 1) for i in range(NKS)]
+    v_full = [Bar(f"v_full{i}", 1) for i in range(NVS)]
+    v_empty = [Bar(f"v_empty{i}", 1) for i in range(NVS)]
+    s_full, s_free, dp_full, ds_full = Bar("s_full", 1), Bar("s_free", 8), Bar("dp_full", 1), Bar("ds_full", 8)
+    acc_done = [Bar("acc_done0", 1), Bar("acc_done1", 1)]
+    dq_free = [Bar("dq_free0", 8), Bar("dq_free1", 8)]
+    staged = Bar("staged", 8)
+    stage_free = [Bar("stage_free0", 1), Bar("stage_free1", 1)]
+    store_read = Bar("store_read", 1)          # counts the stores' reads (waited on by 'until')
+    item_full = [Bar(f"item_full{i}", 1) for i in range(NIS)]
+    item_empty = [Bar(f"item_empty{i}", 10) for i in range(NIS)]
+    done = Bar("done", 1 + 1 + 1 + 8)
+    slot_val = [None] * NIS
+    first_g = []
+    g = 0
+    for n in items:
+        first_g.append(g)
+        g += n
+    last_g = [first_g[i] + items[i] - 1 for i in range(len(items))]
+    W = range(8)
+    st = dict(q_land=[-1, -1], do_land=-1, k_land=[-1] * NKS, v_land=[-1] * NVS, s_exec=-1, dp_exec=-1,
+              dq_exec=-1, acc_item=[-1, -1], s_read={w: -1 for w in W}, dp_read={w: -1 for w in W},
+              ds_wr={w: -1 for w in W}, acc_read={w: -1 for w in W}, staged_item=[-1, -1],
+              store_read=[-1, -1], stores_pending=0)
+
+    def next_item(it):
+        slot = it % NIS
+        yield ('wait', item_full[slot], it // NIS)
+        yield ('arrive', item_empty[slot])
+
+    def producer():
+        for it in range(len(items) + 1):
+            slot = it % NIS
+            if it >= NIS:
+                yield ('wait', item_empty[slot], it // NIS - 1)
+            slot_val[slot] = it if it < len(items) else -1
+            yield ('arrive', item_full[slot])
+            if it == len(items):
+                break
+            for n in range(items[it]):
+                gi = first_g[it] + n
+                ks, u = gi % NKS, gi // NKS
+                if u > 0:
+                    yield ('wait', k_empty[ks], u - 1)
+
+                def lk(gi=gi, ks=ks):
+                    assert st['dq_exec'] >= gi - NKS and st['s_exec'] >= gi - NKS, "K stage reloaded under a reader"
+                    st['k_land'][ks] = gi
+                yield ('tma', k_full[ks], lk)
+                if n == 0:
+                    if it > 0:
+                        yield ('wait', do_empty, it - 1)
+
+                    def ld(it=it):
+                        assert it == 0 or st['dp_exec'] >= last_g[it - 1], "dO reloaded before the last dP read it"
+                        st['do_land'] = it
+                    yield ('tma', do_full, ld)
+                vs, vu = gi % NVS, gi // NVS
+                if vu > 0:
+                    yield ('wait', dp_full, gi - 1) if NVS == 1 else ('wait', v_empty[vs], vu - 1)
+
+                def lv(gi=gi, vs=vs):
+                    assert st['dp_exec'] >= gi - NVS, "V stage reloaded before dP read it"
+                    st['v_land'][vs] = gi
+                yield ('tma', v_full[vs], lv)
+        yield ('arrive', done)
+
+    def q_producer():
+        for it in range(len(items) + 1):
+            yield from next_item(it)
+            if slot_val[it % NIS] < 0:
+                break
+            qb = it & 1
+            if it >= 2 and wait_stage_free:
+                yield ('wait', stage_free[qb], (it >> 1) - 1)
+
+            def lq(it=it, qb=qb):
+                if it >= 2:
+                    assert st['s_exec'] >= last_g[it - 2], "Q reloaded before the last score MMA read it"
+                    assert st['store_read'][qb] >= it - 2, "Q reloaded over a dQ tile its store had not read"
+                st['q_land'][qb] = it
+            yield ('tma', q_full[qb], lq)
+        yield ('arrive', done)
+
+    def issuer():
+        pend = [None]
+
+        def issue_dq():
+            pg, pit, pfirst, plast = pend[0]
+            yield ('wait', ds_full, pg)
+            db = pit & 1
+            if pfirst and pit >= 2 and wait_dq_free:
+                yield ('wait', dq_free[db], (pit >> 1) - 1)
+
+            def ex(pg=pg, pit=pit, pfirst=pfirst, db=db):
+                assert all(v >= pg for v in st['ds_wr'].values()), "dQ before dS written"
+                assert st['k_land'][pg % NKS] == pg
+                if pfirst:
+                    assert all(v >= pit - 2 for v in st['acc_read'].values()), \
+                        "dQ accumulator overwritten before the epilogue read it"
+                    st['acc_item'][db] = pit
+                st['dq_exec'] = pg
+            yield ('mma', 'dQ', ex)
+            if not k_release_on_s:
+                yield ('commit', k_empty[pg % NKS])
+            if plast:
+                yield ('commit', acc_done[db])
+
+        for it in range(len(items) + 1):
+            yield from next_item(it)
+            if slot_val[it % NIS] < 0:
+                break
+            yield ('wait', q_full[it & 1], it >> 1)
+            for n in range(items[it]):
+                gi = first_g[it] + n
+                ks, vs = gi % NKS, gi % NVS
+                yield ('wait', k_full[ks], gi // NKS)
+                if gi > 0:
+                    yield ('wait', s_free, gi - 1)
+
+                def exs(gi=gi, ks=ks, it=it):
+                    assert st['q_land'][it & 1] == it and st['k_land'][ks] == gi
+                    assert all(v >= gi - 1 for v in st['s_read'].values()), "S overwritten before it was read"
+                    st['s_exec'] = gi
+                yield ('mma', 'S', exs)
+                yield ('commit', s_full)
+                if k_release_on_s:
+                    yield ('commit', k_empty[ks])
+                if pend[0] is not None:
+                    yield from issue_dq()
+                if n == 0:
+                    yield ('wait', do_full, it)
+                yield ('wait', v_full[vs], gi // NVS)
+
+                def exdp(gi=gi, vs=vs, it=it):
+                    assert st['do_land'] == it and st['v_land'][vs] == gi
+                    assert st['dq_exec'] >= gi - 1, "dP overwrote dS before dQ read it"
+                    assert all(v >= gi - 1 for v in st['dp_read'].values())
+                    st['dp_exec'] = gi
+                yield ('mma', 'dP', exdp)
+                yield ('commit', dp_full)
+                if NVS > 1:
+                    yield ('commit', v_empty[vs])
+                if n == items[it] - 1:
+                    yield ('commit', do_empty)
+                pend[0] = (gi, it, n == 0, n == items[it] - 1)
+        if pend[0] is not None:
+            yield from issue_dq()
+        yield ('commit', drain)
+        yield ('wait', drain, 0)
+        yield ('arrive', done)
+
+    def elementwise(w):
+        store_db = [-1]
+
+        def release_store():
+            if w == 0 and store_db[0] >= 0:
+                yield ('until', lambda: st['reads_done'] == st['stores_issued'])
+                yield ('arrive', stage_free[store_db[0]])
+                store_db[0] = -1
+
+        def epilogue(pit):
+            db = pit & 1
+            yield ('wait', acc_done[db], pit >> 1)
+            assert st['dq_exec'] >= last_g[pit] and st['acc_item'][db] == pit, "epilogue read an unfinished dQ"
+            assert st['s_exec'] >= last_g[pit], "dQ staged over a Q tile a score MMA still reads"
+            assert st['store_read'][db] >= pit - 2, "dQ staged over a tile its store had not read"
+            st['acc_read'][w] = pit
+            yield ('arrive', dq_free[db])
+            yield ('arrive', staged)
+            if w == 0:
+                yield ('wait', staged, pit)
+                st['staged_item'][db] = pit
+                st['stores_issued'] += 1
+
+                def read(pit=pit, db=db):
+                    assert st['staged_item'][db] == pit
+                    st['store_read'][db] = pit
+                    st['reads_done'] += 1
+                yield ('tma', store_read, read)
+                store_db[0] = db
+
+        pend = -1
+        for it in range(len(items) + 1):
+            yield from next_item(it)
+            if slot_val[it % NIS] < 0:
+                break
+            yield from release_store()
+            for n in range(items[it]):
+                gi = first_g[it] + n
+                yield ('wait', s_full, gi)
+                assert st['s_exec'] == gi
+                st['s_read'][w] = gi
+                yield ('arrive', s_free)
+                yield ('wait', dp_full, gi)
+                assert st['dp_exec'] == gi
+                st['dp_read'][w] = gi
+                st['ds_wr'][w] = gi
+                yield ('arrive', ds_full)
+                yield from release_store()
+                if n == 0 and pend >= 0:
+                    yield from epilogue(pend)
+                    pend = -1
+            pend = it
+        if pend >= 0:
+            yield from epilogue(pend)
+        if w == 0:
+            yield ('until', lambda: st['reads_done'] == st['stores_issued'])     # the final bulk wait
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "CTA exits with MMAs, copies or stores in flight"
+
+    st['stores_issued'] = st['reads_done'] = 0
+    sim.add('producer', producer())
+    sim.add('qproducer', q_producer())
+    sim.add('issuer', issuer())
+    for w in W:
+        sim.add(f'ew{w}', elementwise(w))
     sim.add('teardown', teardown())
     sim.run()

@@ -1,8 +1,8 @@
 """The barrier protocols of the tcgen05 kernels (the paired-head forward, the
-dK/dV and dQ kernels, the QKV projection on CTA pairs), checked in a discrete-event model (protocol_model.py)
-over randomised interleavings: the committed issue orders pass every hazard
-and parity check, and the planted mistakes (protocol variants that are not in
-the library) are caught."""
+dK/dV kernel, the whole dQ CTA, the QKV projection on CTA pairs), checked in
+a discrete-event model (protocol_model.py) over randomised interleavings: the
+committed issue orders pass every hazard and parity check, and the planted
+mistakes (protocol variants that are not in the library) are caught."""
 import pytest
 
 from protocol_model import dkdv_cta, dq_rings
@@ -92,3 +92,46 @@ def test_planted_projection_peer_ignores_stage_release():
     its half is read by MMAs that the first CTA issues."""
     from protocol_model import proj_pair
     assert any(_fails(lambda s=s: proj_pair(s, 4, 3, 2, peer_empty_wait=False)) for s in range(100))
+
+
+@pytest.mark.parametrize("k_stages,v_stages", [(3, 1), (4, 4)])
+def test_dq_cta_protocol(k_stages, v_stages):
+    """The dQ kernel's whole CTA (item queue, two Q buffers, deferred
+    epilogues and their tile stores) at both head sizes' ring depths."""
+    import random
+
+    from protocol_model import dq_cta
+    for seed in range(150):
+        rng = random.Random(seed)
+        items = [rng.randint(1, 5) for _ in range(rng.randint(1, 7))]
+        dq_cta(seed, items, k_stages=k_stages, v_stages=v_stages)
+
+
+def test_dq_accumulator_release_is_implied():
+    """Dropping the wait for the epilogue two items back still passes: every
+    elementwise warp reads the accumulator before its first dS arrival of the
+    item that overwrites it."""
+    import random
+
+    from protocol_model import dq_cta
+    for seed in range(100):
+        rng = random.Random(seed)
+        dq_cta(seed, [rng.randint(1, 3) for _ in range(rng.randint(3, 6))], wait_dq_free=False)
+
+
+def test_planted_dq_q_reload_before_store_read():
+    """The Q producer reloading a buffer before the dQ tile staged in it has
+    been read by its store."""
+    from protocol_model import dq_cta
+    assert any(_fails(lambda s=s: dq_cta(s, [2, 1, 3, 1, 2], wait_stage_free=False)) for s in range(100))
+
+
+def test_planted_dq_k_released_after_score():
+    """Releasing a K stage after its score MMA (its dQ MMA still reads it):
+    caught with the head-64 rings; with the head-128 rings (three K stages,
+    one V stage) the V reload's wait for the previous dP already orders the
+    K reload after that dQ MMA."""
+    from protocol_model import dq_cta
+    assert any(_fails(lambda s=s: dq_cta(s, [3, 2, 4], 4, 4, k_release_on_s=True)) for s in range(100))
+    for s in range(100):
+        dq_cta(s, [3, 2, 4], 3, 1, k_release_on_s=True)
