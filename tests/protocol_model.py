@@ -359,8 +359,11 @@ def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
     K and V of a tile into a two-stage ring), issuer (S_A(0), S_B(0), then per
     tile PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)), four softmax warps per head
     (P written over the scores; O rescaled between PVs) and each head's
-    epilogue through the one staging tile.  The two flags drop waits of the
-    library's protocol (planted-mistake checks).  The model shows the o_free
+    epilogue through the one staging tile; after every role has finished
+    (the issuer having waited for its drain commit) no MMA or copy may still
+    be in flight.  The FP8 forward (fwd_fp8_kernel) runs the same protocol.
+    The two flags drop waits of the library's protocol (planted-mistake
+    checks).  The model shows the o_free
     wait to be implied by p_full: a head's softmax warps read O in the
     epilogue before they arrive on p_full for the next item's first tile,
     and that first PV waits for p_full."""
@@ -375,6 +378,8 @@ def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
     staged = [Bar("staged0", 4), Bar("staged1", 4)]
     stage_free = Bar("stage_free", 1)
     store_read = [Bar("store_read0", 1), Bar("store_read1", 1)]   # a storer's own wait on its copy
+    drain = Bar("drain", 1)
+    done = Bar("done", 1 + 1 + 8)
     tiles = [(it, j, n) for it, n in enumerate(items) for j in range(n)]
     first = {}
     for gk, (it, j, n) in enumerate(tiles):
@@ -408,6 +413,7 @@ def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
                     st['kv_land'][s] = gk
                 yield ('tma', kv_full[s], lkv)
                 gk += 1
+        yield ('arrive', done)
 
     def issuer():
         def issue_s(x, gk, it):
@@ -453,6 +459,9 @@ def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
                         if x == 1 and j + 1 == n - 1:
                             yield ('commit', q_empty)
             g0 += n
+        yield ('commit', drain)
+        yield ('wait', drain, 0)
+        yield ('arrive', done)
 
     def softmax(x, w):
         gk = 0
@@ -487,12 +496,19 @@ def fwd_pair_cta(seed, items, wait_o_free=True, wait_stage_free=True):
                 yield ('tma', store_read[x], read)
                 yield ('wait', store_read[x], it)
                 yield ('arrive', stage_free)
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "CTA exits with MMAs or copies in flight"
+        assert st['store_read'] == 2 * len(items) - 1
 
     sim.add('producer', producer())
     sim.add('issuer', issuer())
     for x in range(2):
         for w in range(4):
             sim.add(f'sm{x}{w}', softmax(x, w))
+    sim.add('teardown', teardown())
     sim.run()
 
 

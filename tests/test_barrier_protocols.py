@@ -50,6 +50,8 @@ def test_planted_ring_release_on_dp_full():
 
 
 def test_paired_forward_protocol():
+    """The paired-head forward's protocol (the bf16 and the FP8 kernels issue
+    and wait in the same order), random item lengths."""
     import random
 
     from protocol_model import fwd_pair_cta
