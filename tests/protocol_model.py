@@ -261,6 +261,8 @@ def dkdv_cta(seed, n_steps, double_scores=True, n_stages=4, p_barrier_per_buffer
             yield ('arrive', ds_full)
         yield ('wait', acc_done, 0)
         assert st['dk_exec'] == n_steps - 1 and st['dv_exec'] == n_steps - 1
+        # The epilogue stages dV and dK in the first Q and dO ring stages.
+        assert not sim.tma, "gradient tiles staged over a ring stage a copy still fills"
 
     sim.add('producer', producer())
     sim.add('issuer', issuer())
