@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
   for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
     const int row0 = grp * R;
     const int nr = min(R, rows - row0);
+    const int b0 = row0 / g.T, t0 = row0 - b0 * g.T;  // the group's first row; the others follow in t
     // Rows at least a block wide: the block's threads take the chunks of the
     // group's four rows (eight loads in flight per chunk column); whole
     // warps take part in the shuffles.
@@ -222,8 +223,11 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
                     bf16_lo(a[r].w) * bf16_lo(d[r].w) + bf16_hi(a[r].w) * bf16_hi(d[r].w);
         for (int off = vph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (c < dot_units && r < nr && (c & (vph - 1)) == 0) {
-          const int row = row0 + r;
-          const int b = row / g.T, t = row - b * g.T;
+          int t = t0 + r, b = b0;
+          while (t >= g.T) {                          // the group runs into the next batch row
+            t -= g.T;
+            ++b;
+          }
           LD[(size_t)(2 * (b * g.NH + (c >> vph_log2)) + 1) * Tp + t] = -acc;
         }
       }

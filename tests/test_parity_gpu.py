@@ -141,6 +141,9 @@ def test_bf16_forward_paired_heads(lib, B, T, C, NH, NKV, theta):
 @pytest.mark.parametrize("B,T,C,NH,NKV,theta", [
     (1, 1, 128, 1, 1, 1e6), (1, 129, 256, 2, 1, 1e6), (2, 300, 512, 8, 2, 1e6), (1, 256, 256, 4, 1, 1e4),
     (1, 1000, 512, 4, 1, 1e6), (1, 77, 512, 4, 4, 0.0), (3, 200, 1024, 8, 4, 1e6),
+    # rows a block wide (the prologue's per-group row dot) in four-row groups
+    # that run from one batch row into the next
+    (3, 101, 2048, 16, 4, 1e6),
 ])
 def test_bf16_forward_workspace_shapes(lib, B, T, C, NH, NKV, theta):
     """attn_fwd_ws (Q/K rotated once into the workspace, then attention) and
@@ -154,6 +157,8 @@ def test_bf16_forward_workspace_shapes(lib, B, T, C, NH, NKV, theta):
     # rows of at least 256 16-byte chunks whose count is not a multiple of 32
     # (the prologue's per-group row dot with a partial last warp)
     (1, 100, 2112, 33, 11, 1e6), (1, 70, 2176, 17, 17, 0.0),
+    # the same with four-row groups running into the next batch row
+    (2, 70, 2112, 33, 11, 1e6),
 ])
 def test_bf16_backward_shapes(lib, B, T, C, NH, NKV, theta):
     check_full(lib, shape_workload(B, T, C, NH, NKV, theta, seed=B * 1000 + T + 11), "bf16")
