@@ -1,6 +1,6 @@
 """Discrete-event model of the mbarrier protocols of the tcgen05 kernels
-(csrc/attn_fwd2_sm103.cu, csrc/attn_bwd_sm103.cu, csrc/attn_proj_sm103.cu),
-used by test_barrier_protocols.py.
+(csrc/attn_fwd2_sm103.cu, csrc/attn_bwd_sm103.cu, csrc/attn_proj_sm103.cu,
+csrc/attn_split_sm103.cu), used by test_barrier_protocols.py.
 
 Each role of a CTA (TMA producer, MMA issuer, elementwise warps) is a
 generator that yields requests; a seeded scheduler interleaves them at
@@ -859,6 +859,348 @@ def dq_cta(seed, items, k_stages=3, v_stages=1, item_slots=4, wait_stage_free=Tr
     st['stores_issued'] = st['reads_done'] = 0
     sim.add('producer', producer())
     sim.add('qproducer', q_producer())
+    sim.add('issuer', issuer())
+    for w in W:
+        sim.add(f'ew{w}', elementwise(w))
+    sim.add('teardown', teardown())
+    sim.run()
+
+
+def split_fwd_cta(seed, n, pv_wait=True, v_release=True):
+    """One CTA of split_fwd_kernel (float32 tensors as bf16 hi/lo parts, one
+    128-query tile, key tiles 0..n-1): the producer loads Q once and each key
+    tile's K and V parts into two-stage rings (K released once its score
+    product has read it, V once its PV product has); the issuer runs the
+    score products two tiles ahead into two score buffers (S(0), S(1), then
+    per tile PV(j), S(j+2)); four softmax warps turn S(j) into P(j) (written
+    over P(j-1) in TMEM) and rescale O, both after PV(j-1) has completed.
+    The flags drop parts of the protocol (planted-mistake checks): the
+    softmax warps not waiting for PV(j-1), and V stages reloaded without
+    waiting for their PV."""
+    sim = Sim(seed)
+    q_full = Bar("q_full", 1)
+    k_full = [Bar(f"k_full{s}", 1) for s in range(2)]
+    k_empty = [Bar(f"k_empty{s}", 1) for s in range(2)]
+    v_full = [Bar(f"v_full{s}", 1) for s in range(2)]
+    v_empty = [Bar(f"v_empty{s}", 1) for s in range(2)]
+    s_full = [Bar(f"s_full{s}", 1) for s in range(2)]
+    p_full, pv_done, drain = Bar("p_full", 4), Bar("pv_done", 1), Bar("drain", 1)
+    done = Bar("done", 1 + 1 + 4)
+    W = range(4)
+    st = dict(q_land=False, k_land=[-1, -1], v_land=[-1, -1], s_exec=-1, pv_exec=-1,
+              s_read={w: -1 for w in W}, p_wr={w: -1 for w in W}, o_scaled={w: -1 for w in W})
+
+    def producer():
+        def lq():
+            st['q_land'] = True
+        yield ('tma', q_full, lq)
+        for j in range(n):
+            s = j & 1
+            if j >= 2:
+                yield ('wait', k_empty[s], (j >> 1) - 1)
+
+            def lk(j=j, s=s):
+                assert st['s_exec'] >= j - 2, "K stage reloaded before its score product read it"
+                st['k_land'][s] = j
+            yield ('tma', k_full[s], lk)
+            if j >= 2 and v_release:
+                yield ('wait', v_empty[s], (j >> 1) - 1)
+
+            def lv(j=j, s=s):
+                assert st['pv_exec'] >= j - 2, "V stage reloaded before its PV product read it"
+                st['v_land'][s] = j
+            yield ('tma', v_full[s], lv)
+        yield ('arrive', done)
+
+    def issuer():
+        def issue_s(j):
+            s = j & 1
+            yield ('wait', k_full[s], j >> 1)
+
+            def ex(j=j, s=s):
+                assert st['q_land'] and st['k_land'][s] == j
+                assert all(v >= j - 2 for v in st['s_read'].values()), "S overwritten before the softmax read it"
+                st['s_exec'] = j
+            yield ('mma', 'S', ex)
+            yield ('commit', s_full[s])
+            yield ('commit', k_empty[s])
+
+        yield ('wait', q_full, 0)
+        yield from issue_s(0)
+        if n >= 2:
+            yield from issue_s(1)
+        for j in range(n):
+            s = j & 1
+            yield ('wait', p_full, j)
+            yield ('wait', v_full[s], j >> 1)
+
+            def expv(j=j, s=s):
+                assert all(v >= j for v in st['p_wr'].values()), "PV before P written"
+                assert all(v >= j for v in st['o_scaled'].values()), "PV before O rescaled"
+                assert st['v_land'][s] == j
+                st['pv_exec'] = j
+            yield ('mma', 'PV', expv)
+            yield ('commit', pv_done)
+            yield ('commit', v_empty[s])
+            if j + 2 < n:
+                yield from issue_s(j + 2)
+        yield ('commit', drain)
+        yield ('wait', drain, 0)
+        yield ('arrive', done)
+
+    def softmax(w):
+        for j in range(n):
+            yield ('wait', s_full[j & 1], j >> 1)
+            assert st['s_exec'] >= j
+            st['s_read'][w] = j
+            if j > 0 and pv_wait:
+                yield ('wait', pv_done, j - 1)
+            assert st['pv_exec'] >= j - 1, "P or O written under the previous PV product"
+            st['o_scaled'][w] = j
+            st['p_wr'][w] = j
+            yield ('arrive', p_full)
+        yield ('wait', pv_done, n - 1)
+        assert st['pv_exec'] == n - 1
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "CTA exits with MMAs or copies in flight"
+
+    sim.add('producer', producer())
+    sim.add('issuer', issuer())
+    for w in W:
+        sim.add(f'sm{w}', softmax(w))
+    sim.add('teardown', teardown())
+    sim.run()
+
+
+def split_dkdv_cta(seed, n_steps, s_before_p=False, release_after_dp=False):
+    """One CTA of split_dkdv_kernel (float32 tensors as bf16 hi/lo parts; key
+    tile stationary): K and V once, then per step a two-stage ring of Q, dO
+    and row tables.  Issue order per step: dP^T(n) over dS^T(n-1) (read by
+    dK(n-1), issued before), dV(n) once the elementwise warps wrote P^T(n)
+    over S^T(n), S^T(n+1) over P^T(n) (read by dV(n), issued before), dK(n)
+    once they wrote dS^T(n) over dP^T(n); the ring stage is released after
+    dK(n).  The flags change the protocol (planted-mistake checks): S^T(n+1)
+    issued before the wait for P^T(n), and the ring stage released after
+    dP^T(n) instead of after dK(n)."""
+    sim = Sim(seed)
+    kv_full = Bar("kv_full", 1)
+    qdo_full = [Bar(f"qdo_full{s}", 1) for s in range(2)]
+    qdo_empty = [Bar(f"qdo_empty{s}", 1) for s in range(2)]
+    s_full = [Bar(f"s_full{s}", 1) for s in range(2)]
+    dp_full, p_full, ds_full = Bar("dp_full", 1), Bar("p_full", 8), Bar("ds_full", 8)
+    acc_done, drain = Bar("acc_done", 1), Bar("drain", 1)
+    done = Bar("done", 1 + 1 + 8)
+    W = range(8)
+    # TMEM S/P buffer and dP/dS buffer: what they hold ('S', n) / ('P', n) ...
+    st = dict(land=[-1, -1], sbuf=None, dpbuf=None, dk_exec=-1, dv_exec=-1)
+
+    def producer():
+        yield ('tma', kv_full, lambda: None)
+        for n in range(n_steps):
+            s = n & 1
+            if n >= 2:
+                yield ('wait', qdo_empty[s], (n >> 1) - 1)
+
+            def land(n=n, s=s):
+                assert st['dk_exec'] >= n - 2 and st['dv_exec'] >= n - 2, "ring stage reloaded under a reader"
+                st['land'][s] = n
+            yield ('tma', qdo_full[s], land)
+        yield ('arrive', done)
+
+    def issuer():
+        def issue_s(n):
+            s = n & 1
+            yield ('wait', qdo_full[s], n >> 1)
+
+            def ex(n=n, s=s):
+                assert st['land'][s] == n
+                assert n == 0 or st['dv_exec'] >= n - 1, "S^T overwrote P^T before dV read it"
+                st['sbuf'] = ('S', n)
+            yield ('mma', 'S', ex)
+            yield ('commit', s_full[s])
+
+        yield ('wait', kv_full, 0)
+        if n_steps > 0:
+            yield from issue_s(0)
+        for n in range(n_steps):
+            s = n & 1
+
+            def exdp(n=n, s=s):
+                assert st['land'][s] == n
+                assert n == 0 or st['dk_exec'] >= n - 1, "dP^T overwrote dS^T before dK read it"
+                st['dpbuf'] = ('dP', n)
+            yield ('mma', 'dP', exdp)
+            yield ('commit', dp_full)
+            if release_after_dp:
+                yield ('commit', qdo_empty[s])
+            if s_before_p and n + 1 < n_steps:
+                yield from issue_s(n + 1)
+            yield ('wait', p_full, n)
+
+            def exdv(n=n, s=s):
+                assert st['sbuf'] == ('P', n) and st['land'][s] == n, "dV read something other than P^T(n)"
+                st['dv_exec'] = n
+            yield ('mma', 'dV', exdv)
+            if not s_before_p and n + 1 < n_steps:
+                yield from issue_s(n + 1)
+            yield ('wait', ds_full, n)
+
+            def exdk(n=n, s=s):
+                assert st['dpbuf'] == ('dS', n) and st['land'][s] == n, "dK read something other than dS^T(n)"
+                st['dk_exec'] = n
+            yield ('mma', 'dK', exdk)
+            if not release_after_dp:
+                yield ('commit', qdo_empty[s])
+        yield ('commit', acc_done)
+        yield ('commit', drain)
+        yield ('wait', drain, 0)
+        yield ('arrive', done)
+
+    pw = {w: 0 for w in W}
+    dw = {w: 0 for w in W}
+
+    def elementwise(w):
+        for n in range(n_steps):
+            yield ('wait', s_full[n & 1], n >> 1)
+            assert st['sbuf'] in (('S', n), ('P', n)), "elementwise read a score tile other than S^T(n)"
+            pw[w] = n + 1
+            if all(v == n + 1 for v in pw.values()):
+                st['sbuf'] = ('P', n)
+            yield ('arrive', p_full)
+            yield ('wait', dp_full, n)
+            assert st['dpbuf'] in (('dP', n), ('dS', n)), "elementwise read a dP^T tile other than dP^T(n)"
+            dw[w] = n + 1
+            if all(v == n + 1 for v in dw.values()):
+                st['dpbuf'] = ('dS', n)
+            yield ('arrive', ds_full)
+        yield ('wait', acc_done, 0)
+        assert st['dk_exec'] == n_steps - 1 and st['dv_exec'] == n_steps - 1
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "CTA exits with MMAs or copies in flight"
+
+    sim.add('producer', producer())
+    sim.add('issuer', issuer())
+    for w in W:
+        sim.add(f'ew{w}', elementwise(w))
+    sim.add('teardown', teardown())
+    sim.run()
+
+
+def split_dq_cta(seed, n, k_release_after_s=False, one_s_buffer=False):
+    """One CTA of split_dq_kernel (float32 tensors as bf16 hi/lo parts; query
+    tile stationary, key tiles 0..n-1): Q and dO once, K in a three-stage ring
+    (read by S(j) and dQ(j)), V in a two-stage ring (read by dP(j)).  Issue
+    order per tile: dP(j) over dS(j-1) (read by dQ(j-1), issued before), S(j+1)
+    into the other score buffer (its previous tile S(j-1) was read before the
+    elementwise warps signalled dS(j-1), waited for before dQ(j-1)), dQ(j) once
+    dS(j) is written.  The flags change the protocol (planted-mistake
+    checks): K stages released after their score product, and one score
+    buffer for all tiles."""
+    sim = Sim(seed)
+    qdo_full = Bar("qdo_full", 1)
+    k_full = [Bar(f"k_full{s}", 1) for s in range(3)]
+    k_empty = [Bar(f"k_empty{s}", 1) for s in range(3)]
+    v_full = [Bar(f"v_full{s}", 1) for s in range(2)]
+    v_empty = [Bar(f"v_empty{s}", 1) for s in range(2)]
+    s_full = [Bar(f"s_full{s}", 1) for s in range(2)]
+    dp_full, ds_full, acc_done, drain = Bar("dp_full", 1), Bar("ds_full", 8), Bar("acc_done", 1), Bar("drain", 1)
+    done = Bar("done", 1 + 1 + 8)
+    W = range(8)
+    st = dict(k_land=[-1] * 3, v_land=[-1] * 2, sbuf=[-1, -1], s_exec=-1, dp_exec=-1, dq_exec=-1,
+              s_read={w: -1 for w in W}, ds_wr={w: -1 for w in W})
+
+    def sb(j):
+        return 0 if one_s_buffer else (j & 1)
+
+    def producer():
+        yield ('tma', qdo_full, lambda: None)
+        for j in range(n):
+            ks, vs = j % 3, j & 1
+            if j >= 3:
+                yield ('wait', k_empty[ks], j // 3 - 1)
+
+            def lk(j=j, ks=ks):
+                assert st['dq_exec'] >= j - 3 and st['s_exec'] >= j - 3, "K stage reloaded under a reader"
+                st['k_land'][ks] = j
+            yield ('tma', k_full[ks], lk)
+            if j >= 2:
+                yield ('wait', v_empty[vs], (j >> 1) - 1)
+
+            def lv(j=j, vs=vs):
+                assert st['dp_exec'] >= j - 2, "V stage reloaded before dP read it"
+                st['v_land'][vs] = j
+            yield ('tma', v_full[vs], lv)
+        yield ('arrive', done)
+
+    def issuer():
+        def issue_s(j):
+            ks = j % 3
+            yield ('wait', k_full[ks], j // 3)
+
+            def ex(j=j, ks=ks):
+                assert st['k_land'][ks] == j
+                assert all(v >= j - (1 if one_s_buffer else 2) for v in st['s_read'].values()), \
+                    "S overwritten before the elementwise warps read it"
+                st['sbuf'][sb(j)] = j
+                st['s_exec'] = j
+            yield ('mma', 'S', ex)
+            yield ('commit', s_full[j & 1])
+            if k_release_after_s:
+                yield ('commit', k_empty[ks])
+
+        yield ('wait', qdo_full, 0)
+        yield from issue_s(0)
+        for j in range(n):
+            vs = j & 1
+            yield ('wait', v_full[vs], j >> 1)
+
+            def exdp(j=j, vs=vs):
+                assert st['v_land'][vs] == j
+                assert st['dq_exec'] >= j - 1, "dP overwrote dS before dQ read it"
+                st['dp_exec'] = j
+            yield ('mma', 'dP', exdp)
+            yield ('commit', dp_full)
+            yield ('commit', v_empty[vs])
+            if j + 1 < n:
+                yield from issue_s(j + 1)
+            yield ('wait', ds_full, j)
+
+            def exdq(j=j):
+                assert all(v >= j for v in st['ds_wr'].values()), "dQ before dS written"
+                assert st['k_land'][j % 3] == j, "dQ read a reloaded K stage"
+                st['dq_exec'] = j
+            yield ('mma', 'dQ', exdq)
+            if not k_release_after_s:
+                yield ('commit', k_empty[j % 3])
+        yield ('commit', acc_done)
+        yield ('commit', drain)
+        yield ('wait', drain, 0)
+        yield ('arrive', done)
+
+    def elementwise(w):
+        for j in range(n):
+            yield ('wait', s_full[j & 1], j >> 1)
+            assert st['sbuf'][sb(j)] == j, "elementwise read a score tile other than S(j)"
+            st['s_read'][w] = j
+            yield ('wait', dp_full, j)
+            assert st['dp_exec'] == j
+            st['ds_wr'][w] = j
+            yield ('arrive', ds_full)
+        yield ('wait', acc_done, 0)
+        assert st['dq_exec'] == n - 1
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "CTA exits with MMAs or copies in flight"
+
+    sim.add('producer', producer())
     sim.add('issuer', issuer())
     for w in W:
         sim.add(f'ew{w}', elementwise(w))

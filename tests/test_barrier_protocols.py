@@ -1,5 +1,6 @@
 """The barrier protocols of the tcgen05 kernels (the paired-head forward, the
-dK/dV kernel, the whole dQ CTA, the QKV projection on CTA pairs), checked in
+dK/dV kernel, the whole dQ CTA, the QKV projection on CTA pairs, the three
+kernels of the float32 split path), checked in
 a discrete-event model (protocol_model.py) over randomised interleavings: the
 committed issue orders pass every hazard and parity check, and the planted
 mistakes (protocol variants that are not in the library) are caught."""
@@ -137,3 +138,27 @@ def test_planted_dq_k_released_after_score():
     assert any(_fails(lambda s=s: dq_cta(s, [3, 2, 4], 4, 4, k_release_on_s=True)) for s in range(100))
     for s in range(100):
         dq_cta(s, [3, 2, 4], 3, 1, k_release_on_s=True)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 12])
+def test_split_kernels_protocols(n):
+    """The float32 split path's forward, dK/dV and dQ kernels."""
+    from protocol_model import split_dkdv_cta, split_dq_cta, split_fwd_cta
+    for seed in range(60):
+        split_fwd_cta(seed, n)
+        split_dkdv_cta(seed, n)
+        split_dq_cta(seed, n)
+
+
+def test_planted_split_variants():
+    """Each dropped or moved step of the split kernels' protocols is caught:
+    the softmax writing P over the previous PV's operand, a V stage reloaded
+    before its PV, S^T(n+1) issued before dV(n) read P^T(n), the Q/dO stage
+    released before dK read it, K stages released after their score product,
+    and one score buffer for all key tiles of the dQ kernel."""
+    from protocol_model import split_dkdv_cta, split_dq_cta, split_fwd_cta
+    cases = [(split_fwd_cta, dict(pv_wait=False)), (split_fwd_cta, dict(v_release=False)),
+             (split_dkdv_cta, dict(s_before_p=True)), (split_dkdv_cta, dict(release_after_dp=True)),
+             (split_dq_cta, dict(k_release_after_s=True)), (split_dq_cta, dict(one_s_buffer=True))]
+    for fn, kw in cases:
+        assert any(_fails(lambda s=s: fn(s, 6, **kw)) for s in range(100)), (fn.__name__, kw)
