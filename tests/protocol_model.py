@@ -1206,3 +1206,220 @@ def split_dq_cta(seed, n, k_release_after_s=False, one_s_buffer=False):
         sim.add(f'ew{w}', elementwise(w))
     sim.add('teardown', teardown())
     sim.run()
+
+
+def fwd_one_cta(seed, items, nk=3, nv=2, no=1, rope=False, store_release=True, rescale_wait=True,
+                wait_rotated_k=True):
+    """One CTA of the one-head forward (fwd_kernel): `items` lists the key
+    tiles of each work item.  Roles: the producer (Q of item it into buffer
+    it & 1 once item it-2's last score MMA and its output store have both
+    released it; K in nk stages two tiles ahead of V in nv stages), the score
+    issuer (S(g) into buffer g & 1 once the softmax read S(g-2)), the PV
+    issuer (PV(g) from P buffer g & 1 into O buffer it % no, an item's first
+    PV once the epilogue no items back read that O buffer), four softmax
+    warps (P(g) over P(g-2) once PV(g-2) completed; O rescaled, when the row
+    maximum grows, once PV(g-1) completed; the epilogue stages out in the
+    item's Q buffer and the first warp stores it), and with RoPE four
+    rotating warps (Q and every landed K tile rotated in place before the
+    score MMA may read them).  The flags change the protocol
+    (planted-mistake checks): the Q buffer released by the score MMAs alone,
+    the O rescale without its wait, and the score issuer reading a K tile
+    that has only landed."""
+    sim = Sim(seed)
+    rng = __import__("random").Random(seed * 7919 + 1)
+    q_full = [Bar(f"q_full{i}", 1) for i in range(2)]
+    q_ready = [Bar(f"q_ready{i}", 4) for i in range(2)]
+    q_empty = [Bar(f"q_empty{i}", 2 if store_release else 1) for i in range(2)]
+    o_free = [Bar(f"o_free{i}", 4) for i in range(no)]
+    s_full = [Bar(f"s_full{i}", 1) for i in range(2)]
+    s_free = [Bar(f"s_free{i}", 4) for i in range(2)]
+    p_full = [Bar(f"p_full{i}", 4) for i in range(2)]
+    pv_done = [Bar(f"pv_done{i}", 1) for i in range(2)]
+    k_full = [Bar(f"k_full{i}", 1) for i in range(nk)]
+    k_ready = [Bar(f"k_ready{i}", 4) for i in range(nk)]
+    k_empty = [Bar(f"k_empty{i}", 1) for i in range(nk)]
+    v_full = [Bar(f"v_full{i}", 1) for i in range(nv)]
+    v_empty = [Bar(f"v_empty{i}", 1) for i in range(nv)]
+    o_staged, drain, drain2 = Bar("o_staged", 4), Bar("drain", 1), Bar("drain2", 1)
+    done = Bar("done", 1 + 1 + 1 + 4 + (4 if rope else 0))
+    first, last = [], []
+    g = 0
+    for n in items:
+        first.append(g)
+        last.append(g + n - 1)
+        g += n
+    W = range(4)
+    st = dict(q_item=[-1, -1], q_rot=[-1, -1], q_staged=[-1, -1], store_read=[-1, -1], k_land=[-1] * nk,
+              k_rot=[-1] * nk, v_land=[-1] * nv, s_exec=-1, pv_exec=-1, o_item=[-1] * no,
+              s_read={w: -1 for w in W}, p_wr={w: -1 for w in W}, o_read={w: -1 for w in W},
+              o_scaled={w: -1 for w in W})
+
+    def producer():
+        kg = vg = 0
+        for it, n in enumerate(items):
+            qb = it & 1
+            if it >= 2:
+                yield ('wait', q_empty[qb], (it >> 1) - 1)
+
+            def lq(it=it, qb=qb):
+                if it >= 2:
+                    assert st['s_exec'] >= last[it - 2], "Q reloaded before the last score MMA read it"
+                    assert st['store_read'][qb] >= it - 2, "Q reloaded over an output tile its store had not read"
+                st['q_item'][qb] = it
+            yield ('tma', q_full[qb], lq)
+
+            def load_k(gi):
+                s, u = gi % nk, gi // nk
+                if u > 0:
+                    yield ('wait', k_empty[s], u - 1)
+
+                def lk(gi=gi, s=s):
+                    assert st['s_exec'] >= gi - nk, "K stage reloaded before its score MMA read it"
+                    st['k_land'][s] = gi
+                yield ('tma', k_full[s], lk)
+
+            def load_v(gi):
+                s, u = gi % nv, gi // nv
+                if u > 0:
+                    yield ('wait', v_empty[s], u - 1)
+
+                def lv(gi=gi, s=s):
+                    assert st['pv_exec'] >= gi - nv, "V stage reloaded before its PV read it"
+                    st['v_land'][s] = gi
+                yield ('tma', v_full[s], lv)
+            base = first[it]
+            for j in range(min(2, n)):
+                yield from load_k(base + j)
+            for j in range(n):
+                yield from load_v(base + j)
+                if j + 2 < n:
+                    yield from load_k(base + j + 2)
+        yield ('arrive', done)
+
+    def score_issuer():
+        for it, n in enumerate(items):
+            qb = it & 1
+            yield ('wait', (q_ready if rope else q_full)[qb], it >> 1)
+            for j in range(n):
+                gi = first[it] + j
+                s, sb = gi % nk, gi & 1
+                yield ('wait', (k_ready if rope and wait_rotated_k else k_full)[s], gi // nk)
+                if gi >= 2:
+                    yield ('wait', s_free[sb], (gi >> 1) - 1)
+
+                def ex(gi=gi, s=s, it=it, qb=qb):
+                    assert st['q_item'][qb] == it and st['k_land'][s] == gi
+                    if rope:
+                        assert st['q_rot'][qb] == it, "score MMA read an unrotated Q"
+                        assert st['k_rot'][s] == gi, "score MMA read an unrotated K"
+                    assert all(v >= gi - 2 for v in st['s_read'].values()), "S overwritten before it was read"
+                    st['s_exec'] = gi
+                yield ('mma', 'S', ex)
+                yield ('commit', s_full[sb])
+                yield ('commit', k_empty[s])
+                if j == n - 1:
+                    yield ('commit', q_empty[qb])
+        yield ('commit', drain)
+        yield ('wait', drain, 0)
+        yield ('arrive', done)
+
+    def pv_issuer():
+        for it, n in enumerate(items):
+            ob = it % no
+            if it >= no:
+                yield ('wait', o_free[ob], (it - no) // no)
+            for j in range(n):
+                gi = first[it] + j
+                pb, sp = gi & 1, gi % nv
+                yield ('wait', p_full[pb], gi >> 1)
+                yield ('wait', v_full[sp], gi // nv)
+
+                def ex(gi=gi, sp=sp, it=it, ob=ob, j=j):
+                    assert all(v >= gi for v in st['p_wr'].values()), "PV before P written"
+                    assert all(v >= gi for v in st['o_scaled'].values()), "PV before O rescaled"
+                    assert st['v_land'][sp] == gi
+                    if j == 0:
+                        assert all(v >= it - no for v in st['o_read'].values()), \
+                            "PV overwrote O before the epilogue read it"
+                        st['o_item'][ob] = it
+                    st['pv_exec'] = gi
+                yield ('mma', 'PV', ex)
+                yield ('commit', pv_done[pb])
+                yield ('commit', v_empty[sp])
+        yield ('commit', drain2)
+        yield ('wait', drain2, 0)
+        yield ('arrive', done)
+
+    def softmax(w):
+        for it, n in enumerate(items):
+            ob, qb = it % no, it & 1
+            for j in range(n):
+                gi = first[it] + j
+                sb = pb = gi & 1
+                yield ('wait', s_full[sb], gi >> 1)
+                assert st['s_exec'] >= gi
+                st['s_read'][w] = gi
+                yield ('arrive', s_free[sb])
+                if gi >= 2:
+                    yield ('wait', pv_done[pb], (gi - 2) >> 1)
+                assert st['pv_exec'] >= gi - 2, "P written over a P the PV had not read"
+                st['p_wr'][w] = gi
+                if j >= 1 and rng.random() < 0.5:
+                    if rescale_wait:
+                        yield ('wait', pv_done[pb ^ 1], (gi - 1) >> 1)
+                    assert st['pv_exec'] >= gi - 1, "O rescaled under a PV"
+                st['o_scaled'][w] = gi
+                yield ('arrive', p_full[pb])
+            lg = last[it]
+            yield ('wait', pv_done[lg & 1], lg >> 1)
+            assert st['pv_exec'] >= lg and st['o_item'][ob] == it
+            assert st['s_exec'] >= lg, "output staged over a Q tile a score MMA still reads"
+            assert st['q_item'][qb] == it
+            st['o_read'][w] = it
+            st['q_staged'][qb] = it
+            yield ('arrive', o_free[ob])
+            yield ('arrive', o_staged)
+            if w == 0:
+                yield ('wait', o_staged, it)
+
+                def read(it=it, qb=qb):
+                    assert st['q_staged'][qb] == it and st['q_item'][qb] == it
+                    st['store_read'][qb] = it
+                yield ('tma', Bar("store", 1), read)
+                yield ('until', lambda it=it, qb=qb: st['store_read'][qb] == it)
+                if store_release:
+                    yield ('arrive', q_empty[qb])
+        yield ('arrive', done)
+
+    def rotator(w):
+        for it, n in enumerate(items):
+            qb = it & 1
+            yield ('wait', q_full[qb], it >> 1)
+            assert st['q_item'][qb] == it
+            if w == 0:
+                st['q_rot'][qb] = it
+            yield ('arrive', q_ready[qb])
+            for j in range(n):
+                gi = first[it] + j
+                s = gi % nk
+                yield ('wait', k_full[s], gi // nk)
+                assert st['k_land'][s] == gi
+                if w == 0:
+                    st['k_rot'][s] = gi
+                yield ('arrive', k_ready[s])
+        yield ('arrive', done)
+
+    def teardown():
+        yield ('wait', done, 0)
+        assert not sim.pipe and not sim.tma, "CTA exits with MMAs or copies in flight"
+
+    sim.add('producer', producer())
+    sim.add('score', score_issuer())
+    sim.add('pv', pv_issuer())
+    for w in W:
+        sim.add(f'sm{w}', softmax(w))
+    if rope:
+        for w in W:
+            sim.add(f'rot{w}', rotator(w))
+    sim.add('teardown', teardown())
+    sim.run()

@@ -1,6 +1,6 @@
-"""The barrier protocols of the tcgen05 kernels (the paired-head forward, the
-dK/dV kernel, the whole dQ CTA, the QKV projection on CTA pairs, the three
-kernels of the float32 split path), checked in
+"""The barrier protocols of the tcgen05 kernels (the paired-head and one-head
+forwards, the dK/dV kernel, the whole dQ CTA, the QKV projection on CTA
+pairs, the three kernels of the float32 split path), checked in
 a discrete-event model (protocol_model.py) over randomised interleavings: the
 committed issue orders pass every hazard and parity check, and the planted
 mistakes (protocol variants that are not in the library) are caught."""
@@ -162,3 +162,29 @@ def test_planted_split_variants():
              (split_dq_cta, dict(k_release_after_s=True)), (split_dq_cta, dict(one_s_buffer=True))]
     for fn, kw in cases:
         assert any(_fails(lambda s=s: fn(s, 6, **kw)) for s in range(100)), (fn.__name__, kw)
+
+
+@pytest.mark.parametrize("hd", [128, 64])
+@pytest.mark.parametrize("rope", [False, True])
+def test_one_head_forward_protocol(hd, rope):
+    """The one-head forward at both head sizes' ring depths (K 3 / V 2 / one
+    O buffer at 128; 4 / 4 / two at 64), with and without the rotating
+    warps."""
+    import random
+
+    from protocol_model import fwd_one_cta
+    nk, nv, no = (3, 2, 1) if hd == 128 else (4, 4, 2)
+    for seed in range(100):
+        rng = random.Random(seed)
+        items = [rng.randint(1, 5) for _ in range(rng.randint(1, 5))]
+        fwd_one_cta(seed, items, nk=nk, nv=nv, no=no, rope=rope)
+
+
+def test_planted_one_head_forward_variants():
+    """The Q buffer released by the score MMAs alone (the output tile staged in
+    it could be overwritten under its store), the O rescale without the wait
+    for the previous PV, and the score MMA waiting for a K tile to land rather
+    than to be rotated."""
+    from protocol_model import fwd_one_cta
+    for kw in (dict(store_release=False), dict(rescale_wait=False), dict(wait_rotated_k=False, rope=True)):
+        assert any(_fails(lambda s=s: fwd_one_cta(s, [3, 2, 4, 1], **kw)) for s in range(100)), kw
