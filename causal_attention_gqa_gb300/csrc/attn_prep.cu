@@ -180,6 +180,12 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
           d[i] = dout[u];
         }
       }
+      // Row (b, t) and chunk c of the thread's first unit of the pass from
+      // one division; its other units, 32, 64 and 96 chunks on, by carrying.
+      const long long u0 = base + lane;
+      const int row0 = n_units < 0x7fff0000LL ? (int)u0 / dot_units : (int)(u0 / dot_units);
+      int c = (int)(u0 - (long long)row0 * dot_units);
+      int b = row0 / g.T, t = row0 - b * g.T;
 #pragma unroll
       for (int i = 0; i < U; ++i) {
         float acc = bf16_lo(a[i].x) * bf16_lo(d[i].x) + bf16_hi(a[i].x) * bf16_hi(d[i].x) +
@@ -188,10 +194,13 @@ __global__ void __launch_bounds__(256, ROPE ? 3 : 4) bwd_prologue_bf16_kernel(fl
                     bf16_lo(a[i].w) * bf16_lo(d[i].w) + bf16_hi(a[i].w) * bf16_hi(d[i].w);
         for (int off = vph >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         const long long u = base + 32 * i + lane;
-        if (u < n_units && (lane & (vph - 1)) == 0) {
-          const int row = (int)(u / dot_units), c = (int)(u - (long long)row * dot_units);
-          const int b = row / g.T, t = row - b * g.T;
+        if (u < n_units && (lane & (vph - 1)) == 0)
           LD[(size_t)(2 * (b * g.NH + (c >> vph_log2)) + 1) * Tp + t] = -acc;
+        for (c += 32; c >= dot_units; c -= dot_units) {
+          if (++t == g.T) {
+            t = 0;
+            ++b;
+          }
         }
       }
     }
